@@ -1,0 +1,83 @@
+"""Small builders for hand-made workload dictionaries used by the tests."""
+import numpy as np
+
+from speculative_verification_gb300 import workloads as W
+
+
+def sample_workload(logits, dtype="f32", temperature=1.0, top_k=None, top_p=None, min_p=None,
+                    repetition=None, frequency=None, presence=None, history=None, bias=None,
+                    mask_words=None, use_mask=None, seed=0, position=None, row_stride=None):
+    """logits: [rows, V] float array.  Scalars broadcast over rows; history is a
+    list of id lists; bias a list of (ids, vals); mask_words [rows, W] int32."""
+    z = np.atleast_2d(np.asarray(logits, np.float32))
+    n, V = z.shape
+    def col(v, dt):
+        if v is None:
+            return None
+        a = np.asarray(v, dt)
+        return np.full(n, a, dt) if a.ndim == 0 else a
+    w = dict(kind="sample", num_rows=n, vocab=V, dtype=dtype,
+             logits=(W.to_bf16_bits(z) if dtype == "bf16" else z),
+             row_stride=V if row_stride is None else row_stride,
+             temperature=col(temperature, np.float32), top_k=col(top_k, np.int32),
+             top_p=col(top_p, np.float32), min_p=col(min_p, np.float32),
+             repetition=col(repetition, np.float32), frequency=col(frequency, np.float32),
+             presence=col(presence, np.float32),
+             seed=col(seed, np.uint64),
+             position=(np.arange(n, dtype=np.int64) if position is None else col(position, np.int64)))
+    if history is not None:
+        off = np.zeros(n + 1, np.int32)
+        off[1:] = np.cumsum([len(h) for h in history])
+        w["hist_offsets"] = off
+        w["hist_ids"] = (np.concatenate([np.asarray(h, np.int32) for h in history])
+                         if off[-1] else np.zeros(0, np.int32))
+    if bias is not None:
+        off = np.zeros(n + 1, np.int32)
+        off[1:] = np.cumsum([len(b[0]) for b in bias])
+        w["bias_offsets"] = off
+        w["bias_ids"] = (np.concatenate([np.asarray(b[0], np.int32) for b in bias])
+                         if off[-1] else np.zeros(0, np.int32))
+        w["bias_vals"] = (np.concatenate([np.asarray(b[1], np.float32) for b in bias])
+                          if off[-1] else np.zeros(0, np.float32))
+    if mask_words is not None:
+        m = np.atleast_2d(np.asarray(mask_words).astype(np.uint32).view(np.int32))
+        w["bitmask"] = m
+        w["bitmask_stride"] = m.shape[1]
+        if use_mask is not None:
+            w["use_bitmask"] = col(use_mask, np.uint8)
+    return w
+
+
+def verify_workload(target_logits, ks, drafts, draft_probs, dtype="f32", temperature=1.0, top_k=None,
+                    top_p=None, min_p=None, seed=0, position=0, max_draft=None, history=None,
+                    repetition=None, frequency=None, presence=None):
+    """target_logits: [sum(k+1), V]; ks: per-request draft counts; drafts: [sum k];
+    draft_probs: [sum k, V]."""
+    z = np.atleast_2d(np.asarray(target_logits, np.float32))
+    V = z.shape[1]
+    ks = np.asarray(ks, np.int32)
+    R = ks.size
+    def col(v, dt):
+        if v is None:
+            return None
+        a = np.asarray(v, dt)
+        return np.full(R, a, dt) if a.ndim == 0 else a
+    off = np.zeros(R + 1, np.int32)
+    off[1:] = np.cumsum(ks)
+    q = np.asarray(draft_probs, np.float32).reshape(-1, V) if int(ks.sum()) else np.zeros((0, V), np.float32)
+    w = dict(kind="verify", num_requests=R, vocab=V, max_draft=int(ks.max() if max_draft is None else max_draft),
+             dtype=dtype, target_logits=(W.to_bf16_bits(z) if dtype == "bf16" else z), row_stride=V,
+             draft_offsets=off, draft_tokens=np.asarray(drafts, np.int32).reshape(-1),
+             draft_probs=q, draft_stride=V,
+             temperature=col(temperature, np.float32), top_k=col(top_k, np.int32),
+             top_p=col(top_p, np.float32), min_p=col(min_p, np.float32),
+             repetition=col(repetition, np.float32), frequency=col(frequency, np.float32),
+             presence=col(presence, np.float32),
+             seed=col(seed, np.uint64), position=col(position, np.int64))
+    if history is not None:
+        hoff = np.zeros(R + 1, np.int32)
+        hoff[1:] = np.cumsum([len(h) for h in history])
+        w["hist_offsets"] = hoff
+        w["hist_ids"] = (np.concatenate([np.asarray(h, np.int32) for h in history])
+                         if hoff[-1] else np.zeros(0, np.int32))
+    return w
