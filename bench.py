@@ -1,0 +1,481 @@
+#!/usr/bin/env python
+"""Benchmark of batched heterogeneous sampling (+ speculative verification).
+
+Headline: sampled rows/s and logits-read HBM GB/s on the heterogeneous-decode
+workload (64 rows x V = 128256, bf16 logits, every row with penalties over a
+512-id history, 16 bias entries, mixed greedy / top-k / top-p / min-p).
+
+A step is one ss_process_sample call on one 64-row batch.  Steps cycle through
+a ring of input sets whose total size exceeds twice the L2 cache, so every
+step reads its logits from HBM.  The K timed steps are replayed from CUDA
+graphs (a graph of `ring * 8` calls, replayed) and timed with CUDA events on
+the launching stream, between barriers and device synchronisations; the
+maximum over ranks is reported.  Multi-GPU runs are data-parallel replicas
+(weak scaling: every rank samples its own batches; no collective on the data
+path).
+
+--impl reference times the CPU oracle (the plain single-threaded C program
+under oracle/) on the same workload and metric, as the reference arm.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_verification_gb300 import workloads as W  # noqa: E402
+
+METRIC = "sampled rows/s and logits HBM GB/s (% of peak) at V=128k B=64; spec-verify rows/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_NAME = "ss_row_kernel"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_verification_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    with open(os.path.join(ROOT, "include", "ss.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload_key):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "ss_row_kernel_traffic.md")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    cur = {}
+    for line in open(path):
+        line = line.strip().strip("`")
+        if ":" in line:
+            k, v = line.split(":", 1)
+            cur[k.strip().lstrip("- ")] = v.strip()
+    if cur.get("kernel_sha256") != want or cur.get("workload") != workload_key:
+        return None
+    try:
+        return int(cur["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.15)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def workload_for(cfg, rank, idx):
+    return W.make(cfg, seed=cfg + 7919 * (rank * 1000 + idx))
+
+
+# --------------------------------------------------------------- our arm --
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    from speculative_verification_gb300 import build as ss_build
+    from speculative_verification_gb300 import ss
+
+    ss_build.build()
+    ss.load()
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    cfg = args.config
+    ring_host = [workload_for(cfg, rank, i) for i in range(args.ring)]
+    bytes_per_call = W.algorithmic_bytes(ring_host[0])
+    rows_per_call = int(ring_host[0]["num_rows"]) if ring_host[0]["kind"] == "sample" else int(
+        ring_host[0]["draft_offsets"][-1]) + int(ring_host[0]["num_requests"])
+    ring = [ss.to_device(w, dev) for w in ring_host]
+    out = ss.alloc_outputs(ring[0], dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(i):
+        ss.run(ring[i % args.ring], out, stream=stream)
+
+    # graphs: one of `per_graph` calls (replayed), one for the remainder
+    per_graph = min(args.steps, args.ring * 8)
+    with torch.cuda.stream(stream):
+        for i in range(args.ring):  # warm the launch path before capture
+            call(i)
+    stream.synchronize()
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    call(i)
+        return g
+
+    g_main = capture(per_graph) if per_graph > 0 else None
+    reps, rem = divmod(args.steps, per_graph) if per_graph > 0 else (0, 0)
+    g_rem = capture(rem) if rem else None
+
+    def replay_steps(n_steps):
+        r, m = divmod(n_steps, per_graph)
+        with torch.cuda.stream(stream):
+            for _ in range(r):
+                g_main.replay()
+            if m:
+                (g_rem if m == rem else capture(m)).replay()
+
+    # warm-up (untimed)
+    replay_steps(max(args.warmup, 3))
+    stream.synchronize()
+
+    # timed region
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    ms = start.elapsed_time(stop)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    per_call_s = ms / 1e3 / args.steps
+    value = rows_per_call * args.steps * world / (ms / 1e3)
+
+    # end-to-end through the public API with host buffers (pinned)
+    e2e = run_e2e(args, ss, ring_host, dev, stream, rows_per_call, dist)
+
+    # speculative-verify throughput (secondary metric), same protocol
+    spec = run_spec(args, ss, rank, dev, stream) if args.spec_steps > 0 else None
+
+    peak, peak_kind = measured_peak()
+    achieved = bytes_per_call / per_call_s / 1e9
+    res = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded numpy PCG64: bf16 N(0,3) logits + 1-5 spikes, mixed per-row params)",
+        "config": {
+            "workload": W.CONFIG_NAMES[cfg],
+            "rows_per_step": rows_per_call,
+            "vocab": int(ring_host[0]["vocab"]),
+            "input_dtype": ring_host[0]["dtype"],
+            "l2": "ring of %d input sets, %.0f MB > 2x L2" % (args.ring, args.ring * bytes_per_call / 1e6),
+            "launch": "CUDA graph of %d calls, replayed" % per_graph,
+            "parallelism": "dp%d replicas" % world,
+            "cluster_ctas_per_row": ss.ss_cluster_size(int(ring_host[0]["vocab"]), ring_host[0]["dtype"]),
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured" else "fallback",
+            "algorithmic_bytes_per_launch": bytes_per_call,
+            "traffic": recorded_traffic(W.CONFIG_NAMES[cfg]),
+            "kernel": KERNEL_NAME,
+            "kernel_sha256": kernel_source_hash(),
+        },
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if spec is not None:
+        res["spec_verify"] = spec
+    return res
+
+
+def run_e2e(args, ss, ring_host, dev, stream, rows_per_call, dist):
+    """Same metric through ss_process_sample with the step's inputs copied from
+    pinned host memory and the results copied back, every step."""
+    import torch
+    n_steps = max(1, min(args.e2e_steps, args.steps))
+    pinned = [ss.to_device(w, pin=True) for w in ring_host[: min(4, len(ring_host))]]
+    staging = ss.to_device(ring_host[0], dev)
+    out = ss.alloc_outputs(staging, dev)
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()
+                if k in ("token", "status", "kept", "out_tokens", "num_accepted")}
+    h2d = sum(v.numel() * v.element_size() for k, v in pinned[0].items() if isinstance(v, torch.Tensor))
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def step(i):
+        src = pinned[i % len(pinned)]
+        with torch.cuda.stream(stream):
+            for k, v in src.items():
+                if isinstance(v, torch.Tensor):
+                    staging[k].copy_(v, non_blocking=True)
+            ss.run(staging, out, stream=stream)
+            for k, v in host_out.items():
+                v.copy_(out[k], non_blocking=True)
+
+    for i in range(3):
+        step(i)
+    stream.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(n_steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    world = dist.get_world_size() if dist else 1
+    return {"value": rows_per_call * n_steps * world / (ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n_steps}
+
+
+def run_spec(args, ss, rank, dev, stream):
+    """Verification throughput on the linear-draft workload (32 requests, k=4)."""
+    import torch
+    ring_host = [workload_for(4, rank, i) for i in range(max(2, args.ring // 2))]
+    ring = [ss.to_device(w, dev) for w in ring_host]
+    out = ss.alloc_outputs(ring[0], dev)
+    rows = int(ring_host[0]["draft_offsets"][-1]) + int(ring_host[0]["num_requests"])
+    with torch.cuda.stream(stream):
+        ss.ss_workspace_init(out["workspace"], stream=stream)
+        for i in range(len(ring)):
+            ss.run(ring[i], out, stream=stream)
+    stream.synchronize()
+    n = args.spec_steps
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(len(ring)):
+                ss.run(ring[i], out, stream=stream)
+    reps = max(1, n // len(ring))
+    for _ in range(3):
+        g.replay()
+    stream.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    calls = reps * len(ring)
+    return {"workload": W.CONFIG_NAMES[4], "target_rows_per_s": rows * calls / (ms / 1e3),
+            "requests_per_s": int(ring_host[0]["num_requests"]) * calls / (ms / 1e3),
+            "ms_per_call": ms / calls, "calls": calls,
+            "logits_GBps": W.algorithmic_bytes(ring_host[0]) * calls / (ms / 1e3) / 1e9}
+
+
+# -------------------------------------------------------- oracle timing --
+
+
+def time_oracle(cfg, seconds, max_steps=None):
+    """Rows/s of the CPU oracle on rows of the same workload (1 thread)."""
+    from oracle import oracle as O
+    sample = W.make(cfg, seed=cfg + 424242, rows=8) if cfg != 4 else None
+    if sample is None:
+        raise ValueError("oracle timing uses sampling workloads")
+    rows = 0
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        O.process_sample(sample)
+        rows += int(sample["num_rows"])
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_steps and steps >= max_steps):
+            break
+    return rows / el, rows, el
+
+
+def cpu_baseline_block(cfg, seconds):
+    v, rows, el = time_oracle(cfg, seconds)
+    return {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": "%d rows of the %s workload (8-row batches) in %.1f s, one thread" % (rows, W.CONFIG_NAMES[cfg], el)}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step samples one 8-row batch of
+    the same workload; at most as many steps as fit in ~90 s are timed."""
+    from oracle import oracle as O
+    cfg = args.config
+    sample = W.make(cfg, seed=cfg + 424242, rows=8)
+    for _ in range(max(0, min(args.warmup, 2))):
+        O.process_sample(sample)
+    t0 = time.perf_counter()
+    steps = 0
+    budget = 90.0
+    while steps < args.steps:
+        O.process_sample(sample)
+        steps += 1
+        if time.perf_counter() - t0 > budget:
+            break
+    el = time.perf_counter() - t0
+    rows = steps * int(sample["num_rows"])
+    value = rows / el
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": 1,
+        "steps": steps,
+        "steps_requested": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded numpy PCG64)",
+        "config": {"workload": W.CONFIG_NAMES[cfg], "rows_per_step": int(sample["num_rows"]),
+                   "vocab": int(sample["vocab"])},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d steps x 8 rows of the %s workload, one thread" % (steps, W.CONFIG_NAMES[cfg])},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, help="workload 2 (headline) or 1/3")
+    ap.add_argument("--ring", type=int, default=16)
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--spec-steps", type=int, default=4000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)))
+        return 0
+
+    # the oracle runs before any CUDA work (no fork after the first GPU call)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_block(args.config, args.cpu_seconds)
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    res = run_ours(args, rank, world, dist)
+    if cpu is not None:
+        res["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(res))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

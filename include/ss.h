@@ -1,0 +1,199 @@
+/*
+ * ss.h -- C ABI of the GB300 (sm_103a) batched sampling and speculative
+ * verification library (libss.so).
+ *
+ * What is computed (all citations are to the pages this library implements):
+ *   - SonicSampler: Unified Tile-Aware Kernels for LLM Sampling and Speculative
+ *     Verification (abstract): one batched kernel applies, per request,
+ *     grammar-constrained decoding, repetition / frequency / presence
+ *     penalties, logit bias, temperature, top-k / top-p / min-p filtering and
+ *     speculative verification, with a hierarchical two-stage top-k, and stays
+ *     CUDA-Graph compatible.
+ *   - FlashSampling (meineki.news), paragraphs 2-3: exact sampling as the argmax
+ *     of logits plus Gumbel noise, reduced per vocabulary tile and then across
+ *     tiles; the argmax decomposes over vocabulary partitions.
+ *   - Accelerating Sonar through speculation (Perplexity blog), sections
+ *     "Speculative decoding" and "Draft-target": drafts are accepted by
+ *     comparing the full draft and target distributions, the longest accepted
+ *     prefix is kept, and the target's logits after it give one more token
+ *     (n drafts -> up to n+1 tokens).  The accept rule min(1, p/q) and the
+ *     residual max(p - q, 0) are those of the post's first reference, "Fast
+ *     inference from transformers via speculative decoding".
+ *
+ * Per row, in this order (the pages name the steps; the order and rounding are
+ * this library's stated convention):
+ *   z = logits row (fp32 or bf16, upcast exactly)
+ *   penalties for each token seen c > 0 times in the row's history (and, for a
+ *     verification target position j, in the drafts before j):
+ *       z = z > 0 ? z / repetition : z * repetition
+ *       z = z - frequency * c
+ *       z = z - presence
+ *   z = z + bias                        (bias ids of a row must be distinct)
+ *   z = -inf where the grammar mask bit is 0
+ *       (bit t & 31 of 32-bit word t >> 5, least significant bit first)
+ *   temperature 0: greedy, token = lowest index of max z
+ *   otherwise y = z * fp32(1 / temperature); order tokens by (y desc, index
+ *   asc); K = shortest of the top-k prefix, the top-p prefix (mass in the
+ *   top-k-renormalised distribution reaches top_p) and the min-p prefix
+ *   (exp(y - y_max) >= min_p); token = argmax over K of y + g, with Gumbel
+ *   noise g = -log(-log u) from Philox4x32-10:
+ *     key (seed lo32, seed hi32), counter (t >> 2, position, row, stream),
+ *     lane t & 3, u = (2 * (x >> 9) + 1) * 2^-24.
+ *   stream 0 = draw / bonus token, 1 = accept uniform (t = 0), 2 = residual.
+ * Verification of request i with k_i drafts x_0..x_{k_i-1}: for j = 0.. k_i-1
+ *   accept x_j iff u_j * q_j(x_j) < P_j(x_j) (P_j = the distribution above at
+ *   target position j); at the first rejection draw from max(P_j - q_j, 0)
+ *   by argmax of log(P_j - q_j) + g (stream 2) over tokens with P_j > q_j; if
+ *   all drafts are accepted, draw the bonus token from position k_i.
+ *
+ * Conventions of every entry point:
+ *   - Pointers inside the argument structs are DEVICE pointers owned by the
+ *     caller; the library keeps none of them after the call returns.
+ *   - Calls are asynchronous on `stream`; results are valid once the stream
+ *     reaches them.  They never synchronise, allocate or copy device to host,
+ *     and launch a fixed number of kernels, so a call can be captured into a
+ *     CUDA graph (the launch shape depends only on the host-side counts).
+ *   - Host-detectable errors (NULL required pointer, bad sizes, misalignment,
+ *     unsupported dtype, workspace too small) return an SS_ERR_* code and
+ *     launch nothing.
+ *   - Data-dependent errors are reported per row in out_status (SS_ROW_*),
+ *     with token -1; a kernel never traps.
+ *   - The logits pointer must be aligned to its element size.  Vocabulary
+ *     slices that start on a 16-byte boundary (16-byte aligned pointer and
+ *     row_stride * element size a multiple of 16) are staged with bulk TMA
+ *     copies; others with plain loads, which is slower.
+ */
+#ifndef SS_H
+#define SS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* ss_stream_t;
+
+typedef enum {
+  SS_OK = 0,
+  SS_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size or stride, misaligned ptr */
+  SS_ERR_UNSUPPORTED = 2,  /* vocabulary too large for one thread-block cluster */
+  SS_ERR_CUDA = 3,         /* a CUDA runtime call failed; ss_last_cuda_error() */
+  SS_ERR_WORKSPACE = 4     /* workspace NULL or smaller than ss_workspace_size */
+} ss_status;
+
+typedef enum { SS_DTYPE_F32 = 0, SS_DTYPE_BF16 = 1 } ss_dtype;
+
+/* Per-row status written to out_status; when several apply the larger wins. */
+enum {
+  SS_ROW_OK = 0,
+  SS_ROW_EMPTY_SET = 1,  /* every token is masked out                               */
+  SS_ROW_NONFINITE = 2,  /* an allowed processed logit is NaN or +inf               */
+  SS_ROW_BAD_INDEX = 3,  /* history / draft / bias id outside [0, V) or duplicate bias id */
+  SS_ROW_BAD_PARAM = 4,  /* temperature < 0 or non-finite, top_k < 0, top_p <= 0 or NaN,
+                            min_p outside [0, 1], repetition <= 0 or non-finite,
+                            frequency / presence / bias value non-finite, negative list
+                            length, position outside [0, 2^32 - 1 - k], k > max_draft */
+  SS_ROW_TIMEOUT = 5,    /* a bounded wait for an asynchronous copy gave up         */
+  SS_ROW_LIMIT = 6       /* more distinct penalised/biased tokens in one vocabulary
+                            slice than the slice's table holds (SS_MAX_PATCHED)     */
+};
+
+/* Distinct penalised or biased tokens one vocabulary slice can hold. */
+#define SS_MAX_PATCHED 1024
+
+/* Per-row (process_sample) or per-request (spec_verify) parameters.  Arrays
+ * have one entry per row/request; an optional array left NULL switches the
+ * feature off for every row. */
+typedef struct {
+  const float* temperature;     /* required; 0 = greedy                          */
+  const int32_t* top_k;         /* NULL or <= 0 or >= allowed count: off         */
+  const float* top_p;           /* NULL or >= 1: off                             */
+  const float* min_p;           /* NULL or 0: off                                */
+  const float* repetition;      /* NULL: 1 (off)                                 */
+  const float* frequency;       /* NULL: 0 (off)                                 */
+  const float* presence;        /* NULL: 0 (off)                                 */
+  const int32_t* hist_offsets;  /* [n+1] CSR offsets into hist_ids, or NULL      */
+  const int32_t* hist_ids;      /* token history used by the three penalties     */
+  const int32_t* bias_offsets;  /* [n+1] CSR offsets into bias_ids/vals, or NULL */
+  const int32_t* bias_ids;
+  const float* bias_vals;
+  const int32_t* bitmask;       /* [n, bitmask_stride] allow bits, or NULL       */
+  int64_t bitmask_stride;       /* words per row, >= ceil(V / 32)                */
+  const uint8_t* use_bitmask;   /* NULL: every row uses its mask row             */
+  const uint64_t* seed;         /* required: Philox key                          */
+  const int64_t* position;      /* required: Philox counter word 1               */
+} ss_params;
+
+/* ss_process_sample: one token per row.  Row r is logits + r * row_stride. */
+typedef struct {
+  int32_t num_rows;
+  int32_t vocab;                /* V >= 1                                         */
+  int64_t row_stride;           /* elements; 0 (all rows alias row 0) or >= V     */
+  int32_t dtype;                /* ss_dtype                                       */
+  const void* logits;
+  ss_params params;             /* indexed by row                                 */
+  int32_t* out_token;           /* [num_rows], -1 when out_status != SS_ROW_OK    */
+  int32_t* out_status;          /* [num_rows]                                     */
+  int32_t* out_kept;            /* [num_rows] |K| (1 greedy, 0 error), or NULL    */
+  float* debug_processed;       /* [num_rows, V] processed logits y (z for greedy
+                                   rows, -inf where masked), or NULL              */
+} ss_sample_args;
+
+/* ss_spec_verify: request i owns target rows draft_offsets[i] + i + j,
+ * j = 0..k_i, k_i = draft_offsets[i+1] - draft_offsets[i] (0 allowed: then the
+ * call returns exactly the ss_process_sample draw of that row). */
+typedef struct {
+  int32_t num_requests;
+  int32_t vocab;
+  int32_t max_draft;            /* upper bound of every k_i                       */
+  int64_t row_stride;           /* elements between target rows (>= V)            */
+  int32_t dtype;
+  const void* target_logits;    /* [sum(k_i + 1), row_stride]                      */
+  const int32_t* draft_offsets; /* [R+1], non-decreasing, draft_offsets[0] = 0    */
+  const int32_t* draft_tokens;  /* [sum k_i]                                      */
+  const float* draft_probs;     /* [sum k_i, draft_stride] q_j over the vocabulary */
+  int64_t draft_stride;         /* elements, >= V                                 */
+  ss_params params;             /* indexed by request                             */
+  int32_t* out_tokens;          /* [R, max_draft + 1]: accepted drafts, then the
+                                   residual or bonus token, then -1              */
+  int32_t* out_num_accepted;    /* [R] in [0, k_i]; tokens emitted = this + 1     */
+  int32_t* out_status;          /* [R] worst row status of the request            */
+  int32_t* out_kept;            /* [sum(k_i + 1)] |K| per target row, or NULL     */
+  float* debug_processed;       /* [sum(k_i + 1), V], or NULL                     */
+} ss_verify_args;
+
+/* Bytes of caller-owned device workspace ss_spec_verify needs for up to
+ * `max_requests` requests with up to `max_draft` drafts each (per-position
+ * results and one arrival counter per request). */
+size_t ss_workspace_size(int32_t max_requests, int32_t max_draft);
+
+/* Zero a workspace before its first use (cudaMemsetAsync on `stream`).  Every
+ * ss_spec_verify call leaves the counters at zero again, so this is needed
+ * once per buffer.  Calls sharing one workspace must not overlap in time. */
+ss_status ss_workspace_init(void* workspace, size_t workspace_bytes, ss_stream_t stream);
+
+/* Batched sampling; one kernel launch. */
+ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream);
+
+/* Batched speculative verification; one kernel launch.  The workspace must
+ * have been zeroed once (ss_workspace_init). */
+ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t workspace_bytes,
+                         ss_stream_t stream);
+
+/* Cluster size (CTAs per vocabulary row) the kernels use for this vocabulary
+ * and dtype, or 0 if unsupported. */
+int32_t ss_cluster_size(int32_t vocab, int32_t dtype);
+
+/* The cudaError_t of the last SS_ERR_CUDA on this thread. */
+int32_t ss_last_cuda_error(void);
+
+const char* ss_status_string(ss_status status);
+const char* ss_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SS_H */

@@ -1,0 +1,45 @@
+"""Compile libss.so (the sm_103a CUDA kernels + C ABI) in-tree with nvcc.
+
+One translation unit, one -gencode (sm_103a), no cmake; the output goes to
+speculative_verification_gb300/_build/libss.so.
+"""
+import os
+import subprocess
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+OUT_DIR = os.path.join(HERE, "_build")
+LIB = os.path.join(OUT_DIR, "libss.so")
+SOURCES = ["ss_kernel.cu"]
+DEPS = ["ss_kernel.cu", "ss_philox.cuh", "ss_ptx.cuh"]
+
+NVCC_FLAGS = [
+    "-std=c++17", "-O3", "-lineinfo",
+    "-gencode", "arch=compute_103a,code=sm_103a",
+    "-Xcompiler", "-fPIC", "-shared",
+]
+
+
+def nvcc():
+    cand = os.environ.get("NVCC") or os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    os.makedirs(OUT_DIR, exist_ok=True)
+    inputs = [os.path.join(CSRC, d) for d in DEPS] + [os.path.join(INCLUDE, "ss.h")]
+    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= max(map(os.path.getmtime, inputs)):
+        return LIB
+    tmp = LIB + ".tmp%d" % os.getpid()
+    cmd = [nvcc()] + NVCC_FLAGS + ["-I" + INCLUDE, "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    subprocess.check_call(cmd)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force=True, verbose=True))

@@ -1,0 +1,290 @@
+"""Thin ctypes binding of libss (include/ss.h).
+
+Argument marshalling only: every step of sampling and verification runs in
+the CUDA kernels of libss.so.  PyTorch supplies device memory and the current
+stream.  There is no CPU fallback: if the library is missing or no GPU is
+present, the calls raise.
+"""
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libss.so")
+
+SS_OK = 0
+SS_DTYPE = {"f32": 0, "bf16": 1}
+ROW_STATUS = {0: "ok", 1: "empty_set", 2: "nonfinite", 3: "bad_index", 4: "bad_param", 5: "timeout", 6: "limit"}
+
+
+class SSError(RuntimeError):
+    pass
+
+
+class ss_params(C.Structure):
+    _fields_ = [
+        ("temperature", C.c_void_p),
+        ("top_k", C.c_void_p),
+        ("top_p", C.c_void_p),
+        ("min_p", C.c_void_p),
+        ("repetition", C.c_void_p),
+        ("frequency", C.c_void_p),
+        ("presence", C.c_void_p),
+        ("hist_offsets", C.c_void_p),
+        ("hist_ids", C.c_void_p),
+        ("bias_offsets", C.c_void_p),
+        ("bias_ids", C.c_void_p),
+        ("bias_vals", C.c_void_p),
+        ("bitmask", C.c_void_p),
+        ("bitmask_stride", C.c_int64),
+        ("use_bitmask", C.c_void_p),
+        ("seed", C.c_void_p),
+        ("position", C.c_void_p),
+    ]
+
+
+class ss_sample_args(C.Structure):
+    _fields_ = [
+        ("num_rows", C.c_int32),
+        ("vocab", C.c_int32),
+        ("row_stride", C.c_int64),
+        ("dtype", C.c_int32),
+        ("logits", C.c_void_p),
+        ("params", ss_params),
+        ("out_token", C.c_void_p),
+        ("out_status", C.c_void_p),
+        ("out_kept", C.c_void_p),
+        ("debug_processed", C.c_void_p),
+    ]
+
+
+class ss_verify_args(C.Structure):
+    _fields_ = [
+        ("num_requests", C.c_int32),
+        ("vocab", C.c_int32),
+        ("max_draft", C.c_int32),
+        ("row_stride", C.c_int64),
+        ("dtype", C.c_int32),
+        ("target_logits", C.c_void_p),
+        ("draft_offsets", C.c_void_p),
+        ("draft_tokens", C.c_void_p),
+        ("draft_probs", C.c_void_p),
+        ("draft_stride", C.c_int64),
+        ("params", ss_params),
+        ("out_tokens", C.c_void_p),
+        ("out_num_accepted", C.c_void_p),
+        ("out_status", C.c_void_p),
+        ("out_kept", C.c_void_p),
+        ("debug_processed", C.c_void_p),
+    ]
+
+
+# Every symbol include/ss.h declares, with its ctypes signature.
+SIGNATURES = {
+    "ss_workspace_size": ([C.c_int32, C.c_int32], C.c_size_t),
+    "ss_workspace_init": ([C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "ss_process_sample": ([C.POINTER(ss_sample_args), C.c_void_p], C.c_int),
+    "ss_spec_verify": ([C.POINTER(ss_verify_args), C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "ss_cluster_size": ([C.c_int32, C.c_int32], C.c_int32),
+    "ss_last_cuda_error": ([], C.c_int32),
+    "ss_status_string": ([C.c_int], C.c_char_p),
+    "ss_version": ([], C.c_char_p),
+}
+
+_lib = None
+
+
+def load(path=None):
+    """Load libss.so (raises if it was not built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise SSError("libss.so not built (%s); run __graft_entry__.build()" % p)
+    L = C.CDLL(p)
+    for name, (argt, rest) in SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.argtypes = argt
+        fn.restype = rest
+    if path is None:
+        _lib = L
+    return L
+
+
+def _check(rc):
+    if rc != SS_OK:
+        L = load()
+        msg = L.ss_status_string(rc).decode()
+        if rc == 3:
+            msg += " (cudaError %d)" % L.ss_last_cuda_error()
+        raise SSError("libss: " + msg)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+PARAM_FIELDS = ("temperature", "top_k", "top_p", "min_p", "repetition", "frequency", "presence",
+                "hist_offsets", "hist_ids", "bias_offsets", "bias_ids", "bias_vals", "bitmask",
+                "use_bitmask", "seed", "position")
+
+
+def make_params(p):
+    """ss_params from a dict of device tensors (missing / None = off)."""
+    sp = ss_params()
+    for name in PARAM_FIELDS:
+        setattr(sp, name, _ptr(p.get(name)))
+    sp.bitmask_stride = int(p.get("bitmask_stride", 0) or 0)
+    return sp
+
+
+def ss_version():
+    return load().ss_version().decode()
+
+
+def ss_cluster_size(vocab, dtype):
+    return int(load().ss_cluster_size(int(vocab), SS_DTYPE[dtype]))
+
+
+def ss_workspace_size(max_requests, max_draft):
+    return int(load().ss_workspace_size(int(max_requests), int(max_draft)))
+
+
+def ss_workspace_init(workspace, stream=None):
+    _check(load().ss_workspace_init(C.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(),
+                                    _stream_handle(stream)))
+
+
+def ss_process_sample(logits, params, out_token, out_status, *, vocab, dtype, row_stride=None, out_kept=None,
+                      debug_processed=None, stream=None):
+    """Sample one token per row of `logits` (device tensor, [rows, row_stride])."""
+    a = ss_sample_args()
+    a.num_rows = int(out_token.numel())
+    a.vocab = int(vocab)
+    a.row_stride = int(vocab if row_stride is None else row_stride)
+    a.dtype = SS_DTYPE[dtype]
+    a.logits = _ptr(logits)
+    a.params = make_params(params)
+    a.out_token = _ptr(out_token)
+    a.out_status = _ptr(out_status)
+    a.out_kept = _ptr(out_kept)
+    a.debug_processed = _ptr(debug_processed)
+    _check(load().ss_process_sample(C.byref(a), _stream_handle(stream)))
+
+
+def ss_spec_verify(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
+                   out_status, workspace, *, vocab, max_draft, dtype, row_stride=None, draft_stride=None,
+                   out_kept=None, debug_processed=None, stream=None):
+    """Verify the drafts of `out_num_accepted.numel()` requests."""
+    a = ss_verify_args()
+    a.num_requests = int(out_num_accepted.numel())
+    a.vocab = int(vocab)
+    a.max_draft = int(max_draft)
+    a.row_stride = int(vocab if row_stride is None else row_stride)
+    a.dtype = SS_DTYPE[dtype]
+    a.target_logits = _ptr(target_logits)
+    a.draft_offsets = _ptr(draft_offsets)
+    a.draft_tokens = _ptr(draft_tokens) if draft_tokens is not None and draft_tokens.numel() else None
+    a.draft_probs = _ptr(draft_probs) if draft_probs is not None and draft_probs.numel() else None
+    a.draft_stride = int(vocab if draft_stride is None else draft_stride)
+    a.params = make_params(params)
+    a.out_tokens = _ptr(out_tokens)
+    a.out_num_accepted = _ptr(out_num_accepted)
+    a.out_status = _ptr(out_status)
+    a.out_kept = _ptr(out_kept)
+    a.debug_processed = _ptr(debug_processed)
+    _check(load().ss_spec_verify(C.byref(a), C.c_void_p(workspace.data_ptr()),
+                                 workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+
+
+# ------------------------------------------------------------ workloads --
+
+_NP_TO_TORCH = None
+
+
+def _torch_dtype(np_dtype):
+    import torch
+    global _NP_TO_TORCH
+    if _NP_TO_TORCH is None:
+        _NP_TO_TORCH = {np.dtype(np.float32): torch.float32, np.dtype(np.int32): torch.int32,
+                        np.dtype(np.int64): torch.int64, np.dtype(np.uint8): torch.uint8,
+                        np.dtype(np.uint64): torch.int64, np.dtype(np.uint16): torch.int16}
+    return _NP_TO_TORCH[np.dtype(np_dtype)]
+
+
+def to_device(w, device="cuda", pin=False):
+    """Copy a workload dictionary's arrays to the device (seed bits and bf16
+    bits are reinterpreted, not converted).  With pin=True, returns pinned host
+    tensors instead (for end-to-end timing)."""
+    import torch
+    out = {}
+    for key, val in w.items():
+        if isinstance(val, np.ndarray):
+            arr = np.ascontiguousarray(val)
+            if arr.dtype == np.uint64:
+                arr = arr.view(np.int64)
+            elif arr.dtype == np.uint16:
+                arr = arr.view(np.int16)
+            t = torch.from_numpy(arr)
+            if pin:
+                t = t.pin_memory()
+            else:
+                t = t.to(device)
+            if np.dtype(val.dtype) == np.uint16:
+                t = t.view(torch.bfloat16)
+            out[key] = t
+        else:
+            out[key] = val
+    return out
+
+
+class Outputs(dict):
+    pass
+
+
+def alloc_outputs(dw, device="cuda", debug=False):
+    """Output tensors for a device workload."""
+    import torch
+    o = Outputs()
+    V = int(dw["vocab"])
+    if dw["kind"] == "sample":
+        n = int(dw["num_rows"])
+        o["token"] = torch.empty(n, dtype=torch.int32, device=device)
+        o["status"] = torch.empty(n, dtype=torch.int32, device=device)
+        o["kept"] = torch.empty(n, dtype=torch.int32, device=device)
+        rows = n
+    else:
+        R = int(dw["num_requests"])
+        rows = int(dw["draft_offsets"][-1].item()) + R
+        o["out_tokens"] = torch.empty((R, int(dw["max_draft"]) + 1), dtype=torch.int32, device=device)
+        o["num_accepted"] = torch.empty(R, dtype=torch.int32, device=device)
+        o["status"] = torch.empty(R, dtype=torch.int32, device=device)
+        o["kept"] = torch.empty(rows, dtype=torch.int32, device=device)
+        nbytes = ss_workspace_size(R, int(dw["max_draft"]))
+        o["workspace"] = torch.zeros((nbytes + 15) // 16 * 4, dtype=torch.int32, device=device)
+    if debug:
+        o["processed"] = torch.empty((rows, V), dtype=torch.float32, device=device)
+    return o
+
+
+def run(dw, o, stream=None, debug=False):
+    """One library call on a device workload `dw` into outputs `o`."""
+    params = {k: dw.get(k) for k in PARAM_FIELDS}
+    params["bitmask_stride"] = dw.get("bitmask_stride", 0)
+    dbg = o.get("processed") if debug else None
+    if dw["kind"] == "sample":
+        ss_process_sample(dw["logits"], params, o["token"], o["status"], vocab=dw["vocab"], dtype=dw["dtype"],
+                          row_stride=dw["row_stride"], out_kept=o["kept"], debug_processed=dbg, stream=stream)
+    else:
+        ss_spec_verify(dw["target_logits"], dw["draft_offsets"], dw["draft_tokens"], dw["draft_probs"], params,
+                       o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],
+                       max_draft=dw["max_draft"], dtype=dw["dtype"], row_stride=dw["row_stride"],
+                       draft_stride=dw["draft_stride"], out_kept=o["kept"], debug_processed=dbg, stream=stream)

@@ -6,11 +6,14 @@ from speculative_verification_gb300 import workloads as W
 
 def sample_workload(logits, dtype="f32", temperature=1.0, top_k=None, top_p=None, min_p=None,
                     repetition=None, frequency=None, presence=None, history=None, bias=None,
-                    mask_words=None, use_mask=None, seed=0, position=None, row_stride=None):
+                    mask_words=None, use_mask=None, seed=0, position=None, row_stride=None, num_rows=None):
     """logits: [rows, V] float array.  Scalars broadcast over rows; history is a
-    list of id lists; bias a list of (ids, vals); mask_words [rows, W] int32."""
+    list of id lists; bias a list of (ids, vals); mask_words [rows, W] int32.
+    With row_stride=0 every one of `num_rows` rows reads logits row 0."""
     z = np.atleast_2d(np.asarray(logits, np.float32))
     n, V = z.shape
+    if num_rows is not None:
+        n = int(num_rows)
     def col(v, dt):
         if v is None:
             return None

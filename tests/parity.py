@@ -1,0 +1,91 @@
+"""Element-by-element comparison of the CUDA path with the CPU oracle."""
+import numpy as np
+
+from oracle import oracle as O
+
+
+def _bits_equal(a, b):
+    a = np.asarray(a, np.float32)
+    b = np.asarray(b, np.float32)
+    both_nan = np.isnan(a) & np.isnan(b)
+    return np.all((a.view(np.uint32) == b.view(np.uint32)) | both_nan)
+
+
+def check_sample(w, gpu, rows=None):
+    """gpu: dict of numpy arrays token/status/kept[/processed].  Returns
+    (checked rows, sub-margin rows).  `rows` restricts the check (and the
+    oracle run) to a subset, for full-size workloads."""
+    if rows is not None:
+        w = subset_sample(w, rows)
+        gpu = {k: (v[rows] if isinstance(v, np.ndarray) else v) for k, v in gpu.items()}
+    ref = O.process_sample(w, want_processed="processed" in gpu, force_kept=gpu["kept"])
+    assert np.array_equal(gpu["status"], ref["status"]), (gpu["status"], ref["status"])
+    ok = ref["status"] == 0
+    if "processed" in gpu:
+        cmp = ref["status"] <= 2
+        for r in np.flatnonzero(cmp):
+            assert _bits_equal(gpu["processed"][r], ref["processed"][r]), ("processed", r)
+    lo, hi = ref["kept_lo"], ref["kept_hi"]
+    bad = ok & ((gpu["kept"] < lo) | (gpu["kept"] > hi))
+    assert not bad.any(), ("kept outside margin range", np.flatnonzero(bad), gpu["kept"][bad], lo[bad], hi[bad])
+    assert np.all(gpu["token"][~ok] == -1)
+    sub = ok & (ref["sub_margin"] != 0)
+    chk = ok & ~sub
+    mism = np.flatnonzero(chk & (gpu["token"] != ref["token"]))
+    assert mism.size == 0, ("token mismatch", mism, gpu["token"][mism], ref["token"][mism])
+    return int(chk.sum()), int(sub.sum())
+
+
+def subset_sample(w, rows):
+    rows = np.asarray(rows)
+    n = int(w["num_rows"])
+    out = dict(w)
+    out["num_rows"] = len(rows)
+    stride = int(w["row_stride"])
+    out["logits"] = w["logits"][rows] if stride else w["logits"]
+    for key in ("temperature", "top_k", "top_p", "min_p", "repetition", "frequency", "presence",
+                "use_bitmask", "seed", "position"):
+        if w.get(key) is not None:
+            out[key] = w[key][rows]
+    if w.get("bitmask") is not None:
+        out["bitmask"] = w["bitmask"][rows]
+    for off, vals in (("hist_offsets", ("hist_ids",)), ("bias_offsets", ("bias_ids", "bias_vals"))):
+        if w.get(off) is None:
+            continue
+        o = w[off]
+        new_off = np.zeros(len(rows) + 1, np.int32)
+        parts = {v: [] for v in vals}
+        for i, r in enumerate(rows):
+            a, b = int(o[r]), int(o[r + 1])
+            new_off[i + 1] = new_off[i] + (b - a)
+            for v in vals:
+                parts[v].append(w[v][a:b])
+        out[off] = new_off
+        for v in vals:
+            out[v] = np.concatenate(parts[v]) if parts[v] else w[v][:0]
+    assert n >= len(rows)
+    return out
+
+
+def check_verify(w, gpu):
+    """gpu: out_tokens/num_accepted/status/kept[/processed].  Returns
+    (checked requests, sub-margin requests)."""
+    ref = O.spec_verify(w, want_processed="processed" in gpu, force_kept=gpu["kept"])
+    assert np.array_equal(gpu["status"], ref["status"]), (gpu["status"], ref["status"])
+    ok = ref["status"] == 0
+    R = int(w["num_requests"])
+    d_off = w["draft_offsets"]
+    for i in np.flatnonzero(ok):
+        rows = np.arange(int(d_off[i]) + i, int(d_off[i + 1]) + i + 1)
+        k = gpu["kept"][rows]
+        assert np.all((k >= ref["kept_lo"][rows]) & (k <= ref["kept_hi"][rows])), ("kept", i, k, ref["kept_lo"][rows], ref["kept_hi"][rows])
+        if "processed" in gpu:
+            for r in rows:
+                assert _bits_equal(gpu["processed"][r], ref["processed"][r]), ("processed", i, r)
+    assert np.all(gpu["out_tokens"][~ok] == -1)
+    sub = ok & (ref["sub_margin"] != 0)
+    chk = ok & ~sub
+    for i in np.flatnonzero(chk):
+        assert gpu["num_accepted"][i] == ref["num_accepted"][i], ("accepted", i, gpu["num_accepted"][i], ref["num_accepted"][i])
+        assert np.array_equal(gpu["out_tokens"][i], ref["out_tokens"][i]), ("tokens", i, gpu["out_tokens"][i], ref["out_tokens"][i])
+    return int(chk.sum()), int(sub.sum())

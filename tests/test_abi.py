@@ -1,0 +1,76 @@
+"""The C ABI library builds, loads and exports every symbol include/ss.h
+declares (no compute calls: this runs without a GPU)."""
+import os
+import re
+
+import pytest
+
+from speculative_verification_gb300 import build as ss_build
+from speculative_verification_gb300 import ss
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "ss.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ss_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ss_build.build()
+    return ss.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert "ss_process_sample" in names and "ss_spec_verify" in names
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in ss.SIGNATURES, name
+
+
+def test_host_only_queries(lib):
+    assert ss.ss_version().startswith("ss ")
+    assert ss.ss_cluster_size(128256, "bf16") == 4
+    assert ss.ss_cluster_size(262144, "bf16") == 8
+    assert ss.ss_cluster_size(32000, "f32") == 2
+    assert ss.ss_cluster_size(10, "f32") == 1
+    assert ss.ss_cluster_size(0, "f32") == 0
+    assert ss.ss_cluster_size(10_000_000, "bf16") == 0
+    assert ss.ss_workspace_size(32, 4) >= 32 * 5 * 16 + 32 * 4
+    assert lib.ss_status_string(0) == b"ok"
+
+
+def test_host_side_argument_errors_launch_nothing(lib):
+    import ctypes as C
+    a = ss.ss_sample_args()
+    a.num_rows = 4
+    a.vocab = 0  # invalid
+    assert lib.ss_process_sample(C.byref(a), None) == 1
+    a.vocab = 100
+    a.dtype = 7  # invalid dtype
+    assert lib.ss_process_sample(C.byref(a), None) == 1
+    a.dtype = 1
+    a.logits = 16  # no output pointers
+    assert lib.ss_process_sample(C.byref(a), None) == 1
+    a.num_rows = 0  # empty batch: nothing to do
+    assert lib.ss_process_sample(C.byref(a), None) == 0
+    assert lib.ss_process_sample(None, None) == 1
+    v = ss.ss_verify_args()
+    v.num_requests = 2
+    v.vocab = 64
+    v.max_draft = 2
+    v.row_stride = 64
+    v.target_logits = 16
+    v.draft_offsets = 32
+    v.draft_tokens = 48
+    v.draft_probs = 64
+    v.draft_stride = 64
+    v.out_tokens, v.out_num_accepted, v.out_status = 80, 96, 112
+    v.params.temperature, v.params.seed, v.params.position = 128, 144, 160
+    assert lib.ss_spec_verify(C.byref(v), None, 0, None) == 4  # workspace missing
+    assert lib.ss_spec_verify(C.byref(v), C.c_void_p(256), 8, None) == 4  # too small
+    v.row_stride = 63  # stride < vocab
+    assert lib.ss_spec_verify(C.byref(v), C.c_void_p(256), 1 << 20, None) == 1

@@ -1,0 +1,214 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Token ids, statuses, accepted counts and processed logits must match exactly;
+the only latitude is what the 1e-5 decision margin allows: the kept-set size
+may be any size the oracle reaches under a 1e-5 relative perturbation (the
+oracle then re-draws from the GPU's kept set), and rows whose final draw /
+accept / residual comparison is itself within the margin are counted, not
+compared.
+"""
+import numpy as np
+import pytest
+
+from speculative_verification_gb300 import workloads as W
+from tests import parity
+from tests.helpers import sample_workload, verify_workload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def ss():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_verification_gb300 import build as ss_build
+    ss_build.build()
+    from speculative_verification_gb300 import ss as _ss
+    _ss.load()
+    return _ss
+
+
+def run_gpu(ss, w, debug=True):
+    dw = ss.to_device(w)
+    o = ss.alloc_outputs(dw, debug=debug)
+    ss.run(dw, o, debug=debug)
+    torch.cuda.synchronize()
+    res = {k: v.cpu().numpy() for k, v in o.items() if k != "workspace"}
+    return res
+
+
+def _report(name, checked, sub):
+    print("%s: %d checked exactly, %d within the 1e-5 draw margin" % (name, checked, sub))
+    assert checked > 0
+
+
+# ----------------------------------------------------------- workloads
+
+
+def test_tiny_sampling_full_size(ss):
+    w = W.make(1)
+    _report("tiny", *parity.check_sample(w, run_gpu(ss, w)))
+
+
+@pytest.mark.parametrize("rows,vocab", [(32, 5003), (12, 128256)])
+def test_heterogeneous_decode(ss, rows, vocab):
+    w = W.make(2, rows=rows, vocab=vocab)
+    _report("decode", *parity.check_sample(w, run_gpu(ss, w)))
+
+
+def test_heterogeneous_decode_full_size(ss):
+    w = W.make(2)  # 64 x 128256 bf16: the benchmarked launch
+    g = run_gpu(ss, w, debug=False)
+    _report("decode full", *parity.check_sample(w, g))
+
+
+def test_grammar_constrained(ss):
+    w = W.make(3, rows=24, vocab=20011)
+    _report("grammar", *parity.check_sample(w, run_gpu(ss, w)))
+
+
+def test_grammar_constrained_full_size(ss):
+    w = W.make(3)
+    _report("grammar full", *parity.check_sample(w, run_gpu(ss, w, debug=False)))
+
+
+def test_spec_verify_linear(ss):
+    w = W.make(4, requests=12, k=4, vocab=7001)
+    _report("verify", *parity.check_verify(w, run_gpu(ss, w)))
+
+
+def test_spec_verify_full_size(ss):
+    w = W.make(4)
+    _report("verify full", *parity.check_verify(w, run_gpu(ss, w, debug=False)))
+
+
+def test_mixed_stress_small(ss):
+    w = W.make(5, requests=32, vocab=9001, max_draft=7, plain_top_k_max=600)
+    _report("mixed", *parity.check_verify(w, run_gpu(ss, w)))
+
+
+def test_mixed_stress_full_vocab(ss):
+    w = W.make(5, requests=24)
+    _report("mixed full V", *parity.check_verify(w, run_gpu(ss, w, debug=False)))
+
+
+# ---------------------------------------------------------- edge cases
+
+
+@pytest.mark.parametrize("V", [1, 7, 33, 100, 1023])
+def test_small_and_ragged_vocab(ss, V):
+    rng = np.random.default_rng(V)
+    n = 16
+    z = (rng.integers(-8, 9, size=(n, V)) / 4.0).astype(np.float32)
+    w = sample_workload(z, dtype="bf16", temperature=rng.choice([0.0, 0.7, 1.0], size=n),
+                        top_k=rng.choice([0, 1, 3, V, V + 2], size=n), top_p=rng.choice([1.0, 0.5, 0.9], size=n),
+                        min_p=rng.choice([0.0, 0.1], size=n), seed=5)
+    _report("V=%d" % V, *parity.check_sample(w, run_gpu(ss, w)))
+
+
+def test_ties_everywhere(ss):
+    V = 4096
+    z = np.zeros((8, V), np.float32)
+    z[:, ::7] = 1.0
+    w = sample_workload(z, dtype="bf16", temperature=1.0, top_k=np.array([1, 5, 100, 585, 586, 600, 0, 4095]),
+                        top_p=np.array([1, 1, 1, 1, 0.5, 0.3, 0.2, 1.0]))
+    g = run_gpu(ss, w)
+    parity.check_sample(w, g)
+    assert g["kept"][:4].tolist() == [1, 5, 100, 585]
+
+
+def test_statuses(ss):
+    V = 300
+    z = np.random.default_rng(0).normal(size=(9, V)).astype(np.float32)
+    z[3, 7] = np.nan
+    z[4, 9] = np.inf
+    temp = np.array([1, -1, 1, 1, 1, 1, 1, 0, np.nan], np.float32)
+    top_p = np.array([1, 1, 0, 1, 1, 1, 1, 1, 1], np.float32)
+    mask = np.full((9, 10), 0xFFFFFFFF, np.uint32)
+    mask[5] = 0
+    hist = [[], [], [], [], [], [], [V], [1, 2], []]
+    bias = [([1, 1], [0.5, 0.5])] + [([], [])] * 6 + [([3], [1.0]), ([], [])]
+    w = sample_workload(z, temperature=temp, top_p=top_p, mask_words=mask, history=hist, bias=bias)
+    g = run_gpu(ss, w)
+    parity.check_sample(w, g)
+    assert g["status"].tolist() == [3, 4, 4, 2, 2, 1, 3, 0, 4]
+
+
+def test_broadcast_rows_and_long_history(ss):
+    rng = np.random.default_rng(1)
+    V = 50000
+    z = rng.normal(0, 2, size=(1, V)).astype(np.float32)
+    n = 40
+    hist = [rng.integers(0, V, size=int(rng.integers(0, 3000))).tolist() for _ in range(n)]
+    w = sample_workload(z, dtype="f32", temperature=rng.uniform(0.5, 1.5, size=n), top_k=rng.choice([0, 10, 200], size=n),
+                        top_p=rng.choice([1.0, 0.9], size=n), repetition=1.3, frequency=0.1, presence=0.2,
+                        history=hist, row_stride=0, num_rows=n, seed=np.arange(n),
+                        position=rng.integers(0, 1000, size=n))
+    _report("broadcast", *parity.check_sample(w, run_gpu(ss, w)))
+
+
+def test_patch_table_overflow_reports_limit(ss):
+    V = 32768  # one slice per row at bf16
+    z = np.zeros((2, V), np.float32)
+    hist = [list(range(0, 4000)), list(range(0, 500))]
+    w = sample_workload(z, dtype="bf16", temperature=1.0, repetition=1.1, history=hist)
+    g = run_gpu(ss, w)
+    assert g["status"].tolist() == [6, 0]
+
+
+def test_verify_without_drafts_equals_sampling(ss):
+    w = W.make(2, rows=16, vocab=6007)
+    dw = dict(w)
+    v = dict(kind="verify", num_requests=16, vocab=w["vocab"], max_draft=0, dtype=w["dtype"],
+             target_logits=w["logits"], row_stride=w["row_stride"], draft_offsets=np.zeros(17, np.int32),
+             draft_tokens=np.zeros(0, np.int32), draft_probs=np.zeros((0, w["vocab"]), np.float32),
+             draft_stride=w["vocab"])
+    for key in W.PARAM_KEYS:
+        if key in w:
+            v[key] = w[key]
+    gs = run_gpu(ss, dw)
+    gv = run_gpu(ss, v)
+    assert np.array_equal(gv["out_tokens"][:, 0], gs["token"])
+    assert np.array_equal(gv["status"], gs["status"])
+    assert np.all(gv["num_accepted"] == 0)
+
+
+def test_verify_greedy_and_bad_draft_count(ss):
+    rng = np.random.default_rng(4)
+    V, R, k = 600, 10, 3
+    z = rng.normal(0, 1, size=(R * (k + 1), V)).astype(np.float32)
+    arg = np.argmax(z, axis=1).reshape(R, k + 1)
+    drafts = arg[:, :k].copy()
+    drafts[::3, 1] = (drafts[::3, 1] + 1) % V
+    q = rng.dirichlet(np.ones(V), size=R * k).astype(np.float32)
+    w = verify_workload(z, np.full(R, k), drafts.reshape(-1), q, temperature=0.0, max_draft=k)
+    g = run_gpu(ss, w)
+    parity.check_verify(w, g)
+    assert g["num_accepted"].tolist() == [1 if i % 3 == 0 else 3 for i in range(R)]
+    # a draft count above max_draft is a parameter error of that request only
+    w2 = verify_workload(z[:8], [3, 3], drafts.reshape(-1)[:6], q[:6], temperature=1.0, max_draft=2)
+    g2 = run_gpu(ss, w2, debug=False)
+    assert g2["status"].tolist() == [4, 4]
+
+
+def test_deterministic_and_graph_capturable(ss):
+    w = W.make(2, rows=16, vocab=40000)
+    dw = ss.to_device(w)
+    o1 = ss.alloc_outputs(dw)
+    o2 = ss.alloc_outputs(dw)
+    ss.run(dw, o1)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        ss.run(dw, o2, stream=s)  # warm-up on the capture stream
+        torch.cuda.synchronize()
+        o2["token"].fill_(-7)
+        with torch.cuda.graph(graph, stream=s):
+            ss.run(dw, o2, stream=s)
+    graph.replay()
+    torch.cuda.synchronize()
+    for key in ("token", "status", "kept"):
+        assert torch.equal(o1[key], o2[key]), key
