@@ -81,7 +81,9 @@ typedef enum {
   SS_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size or stride, misaligned ptr */
   SS_ERR_UNSUPPORTED = 2,  /* vocabulary too large for one thread-block cluster */
   SS_ERR_CUDA = 3,         /* a CUDA runtime call failed; ss_last_cuda_error() */
-  SS_ERR_WORKSPACE = 4     /* workspace NULL or smaller than ss_workspace_size */
+  SS_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than ss_workspace_size */
+  SS_ERR_SCRATCH_LIMIT = 5 /* ss_spec_verify_noalloc: batch needs more than
+                              SS_NOALLOC_SCRATCH_BYTES of scratch            */
 } ss_status;
 
 typedef enum { SS_DTYPE_F32 = 0, SS_DTYPE_BF16 = 1 } ss_dtype;
@@ -182,6 +184,35 @@ ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream);
  * have been zeroed once (ss_workspace_init). */
 ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t workspace_bytes,
                          ss_stream_t stream);
+
+/* Size of the static device scratch behind ss_spec_verify_noalloc (1 MiB):
+ * enough for ss_workspace_size(R, max_draft), e.g. 7000 requests with 7
+ * drafts each. */
+#define SS_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* ss_spec_verify_noalloc: ss_spec_verify without a caller workspace and
+ * without allocating.  (The pages describe no such call; it exists for
+ * callers that cannot allocate device memory -- e.g. a serving engine that
+ * hands all GPU memory to its own pool at start-up, or a plugin whose host
+ * interface provides no allocator -- and so cannot pass a workspace.)
+ *
+ * The scratch is one file-scope device array of SS_NOALLOC_SCRATCH_BYTES in
+ * this library; every GPU that uses the library holds it until the process
+ * exits.  A batch whose ss_workspace_size(num_requests, max_draft) exceeds it
+ * is rejected with SS_ERR_SCRATCH_LIMIT and nothing is launched.  The call
+ * itself allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call clears the per-request counters with cudaMemsetAsync on
+ *     `stream`, then launches the verification kernel; the results are
+ *     identical to ss_spec_verify's.
+ *   - All calls on one device share the array: calls that overlap on the GPU
+ *     (different streams, or host threads not ordered by a stream) race and
+ *     produce undefined results.  Serialise them.
+ * Arguments, outputs and the other errors are those of ss_spec_verify. */
+ss_status ss_spec_verify_noalloc(const ss_verify_args* args, ss_stream_t stream);
 
 /* Cluster size (CTAs per vocabulary row) the kernels use for this vocabulary
  * and dtype, or 0 if unsupported. */

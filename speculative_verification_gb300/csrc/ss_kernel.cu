@@ -26,6 +26,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "ss.h"
 #include "ss_philox.cuh"
 #include "ss_ptx.cuh"
@@ -1247,6 +1249,55 @@ ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t wor
   return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ----------------------------------------------------- allocation-free --
+// Scratch for ss_spec_verify_noalloc: one file-scope device array, loaded with
+// the library and kept by every GPU that uses it until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SS_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64] = {};  // device address of g_noalloc_scratch, per device
+}  // namespace
+
+ss_status ss_spec_verify_noalloc(const ss_verify_args* args, ss_stream_t stream) {
+  if (!args) return SS_ERR_INVALID_ARG;
+  const size_t need = ss_workspace_size(args->num_requests, args->max_draft);
+  if (args->num_requests < 0 || args->max_draft < 0) return SS_ERR_INVALID_ARG;
+  if (need > SS_NOALLOC_SCRATCH_BYTES) return SS_ERR_SCRATCH_LIMIT;
+  if (args->num_requests == 0) return SS_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    ss::g_last_cuda_error = static_cast<int32_t>(e);
+    return SS_ERR_CUDA;
+  }
+  void* scratch = nullptr;
+  {
+    // First call on this device: look the array's device address up with the
+    // device current (host code only sees a stand-in for the symbol).
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+      e = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch);
+      if (e != cudaSuccess) {
+        g_noalloc_ptr[dev] = nullptr;
+        ss::g_last_cuda_error = static_cast<int32_t>(e);
+        return SS_ERR_CUDA;
+      }
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  // The per-request arrival counters must start at zero; the array keeps
+  // whatever the previous call left, so clear them on every call.
+  const size_t results = static_cast<size_t>(args->num_requests) * static_cast<size_t>(args->max_draft + 1) * 16u;
+  e = cudaMemsetAsync(static_cast<char*>(scratch) + results, 0, static_cast<size_t>(args->num_requests) * 4u,
+                      reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    ss::g_last_cuda_error = static_cast<int32_t>(e);
+    return SS_ERR_CUDA;
+  }
+  return ss_spec_verify(args, scratch, SS_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 int32_t ss_cluster_size(int32_t vocab, int32_t dtype) {
   if (vocab < 1 || (dtype != SS_DTYPE_F32 && dtype != SS_DTYPE_BF16)) return 0;
   return ss::choose_cluster(vocab, dtype == SS_DTYPE_BF16 ? 2 : 4);
@@ -1261,6 +1312,7 @@ const char* ss_status_string(ss_status status) {
     case SS_ERR_UNSUPPORTED: return "unsupported size";
     case SS_ERR_CUDA: return "CUDA runtime error";
     case SS_ERR_WORKSPACE: return "workspace missing or too small";
+    case SS_ERR_SCRATCH_LIMIT: return "batch exceeds the allocation-free entry point's static scratch";
   }
   return "unknown status";
 }

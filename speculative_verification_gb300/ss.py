@@ -14,6 +14,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libss.so")
 
 SS_OK = 0
+SS_ERR_SCRATCH_LIMIT = 5
 SS_DTYPE = {"f32": 0, "bf16": 1}
 ROW_STATUS = {0: "ok", 1: "empty_set", 2: "nonfinite", 3: "bad_index", 4: "bad_param", 5: "timeout", 6: "limit"}
 
@@ -86,6 +87,7 @@ SIGNATURES = {
     "ss_workspace_init": ([C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "ss_process_sample": ([C.POINTER(ss_sample_args), C.c_void_p], C.c_int),
     "ss_spec_verify": ([C.POINTER(ss_verify_args), C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
+    "ss_spec_verify_noalloc": ([C.POINTER(ss_verify_args), C.c_void_p], C.c_int),
     "ss_cluster_size": ([C.c_int32, C.c_int32], C.c_int32),
     "ss_last_cuda_error": ([], C.c_int32),
     "ss_status_string": ([C.c_int], C.c_char_p),
@@ -180,10 +182,8 @@ def ss_process_sample(logits, params, out_token, out_status, *, vocab, dtype, ro
     _check(load().ss_process_sample(C.byref(a), _stream_handle(stream)))
 
 
-def ss_spec_verify(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
-                   out_status, workspace, *, vocab, max_draft, dtype, row_stride=None, draft_stride=None,
-                   out_kept=None, debug_processed=None, stream=None):
-    """Verify the drafts of `out_num_accepted.numel()` requests."""
+def _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
+                 out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed):
     a = ss_verify_args()
     a.num_requests = int(out_num_accepted.numel())
     a.vocab = int(vocab)
@@ -201,8 +201,27 @@ def ss_spec_verify(target_logits, draft_offsets, draft_tokens, draft_probs, para
     a.out_status = _ptr(out_status)
     a.out_kept = _ptr(out_kept)
     a.debug_processed = _ptr(debug_processed)
+    return a
+
+
+def ss_spec_verify(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
+                   out_status, workspace, *, vocab, max_draft, dtype, row_stride=None, draft_stride=None,
+                   out_kept=None, debug_processed=None, stream=None):
+    """Verify the drafts of `out_num_accepted.numel()` requests."""
+    a = _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
+                     out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed)
     _check(load().ss_spec_verify(C.byref(a), C.c_void_p(workspace.data_ptr()),
                                  workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+
+
+def ss_spec_verify_noalloc(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens,
+                           out_num_accepted, out_status, *, vocab, max_draft, dtype, row_stride=None,
+                           draft_stride=None, out_kept=None, debug_processed=None, stream=None):
+    """ss_spec_verify with the library's static device scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    a = _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
+                     out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed)
+    _check(load().ss_spec_verify_noalloc(C.byref(a), _stream_handle(stream)))
 
 
 # ------------------------------------------------------------ workloads --
