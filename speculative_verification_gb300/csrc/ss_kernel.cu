@@ -9,18 +9,31 @@
 //   * penalised / biased tokens live in a per-CTA hash table ("patches") and
 //     are excluded from the raw slice; their processed values are computed
 //     from the global row and visited alongside the slice.
-//   * statistics are reduced warp -> CTA -> cluster (distributed shared
-//     memory reads after a cluster barrier); every CTA derives the same
-//     decisions from the same reduced values, so control flow stays uniform.
-//   * top-k / top-p cuts are exact radix selections over order-preserving
-//     32-bit keys of y (descending), with probability masses accumulated in
-//     40-bit fixed point so that sums do not depend on thread order; ties at a
-//     cut are resolved by a second selection over token indices.
+//   * stage 1, overlapped with the copies, stores for every 16-byte vector of
+//     the slice an upper bound of its largest processed logit (a tile max, as
+//     on the FlashSampling page: per-tile maxima, then a cross-tile
+//     reduction).  Every later pass skips whole vectors the bound rules out.
+//   * cuts (SonicSampler abstract: hierarchical two-stage top-k, top-p): a
+//     histogram of the tile maxima bounds the cut from below; tokens above the
+//     bound are bucketed by d = y_max - y into 64 buckets of a power-of-two
+//     width; the bucket holding a cut is refined into 64 sub-buckets (64x the
+//     scale, so levels nest exactly) until it holds at most kListCap tokens,
+//     which are gathered into every CTA, sorted by (y desc, index asc) and
+//     resolved exactly.  Counts are integers and probability masses 40-bit
+//     fixed point, so no result depends on the order in which threads add.
+//     Rows the buckets cannot resolve use an exact radix selection instead.
 //   * the draw is Gumbel-max over the kept set, per thread, then across the
-//     cluster (FlashSampling page: per-tile max, then a cross-tile reduction;
-//     the argmax decomposes over partitions).  Tokens whose logit plus the
-//     largest possible noise cannot beat the running best skip the RNG.
+//     cluster (the argmax decomposes over partitions).  Tokens whose logit
+//     plus the largest possible noise cannot beat the running best skip the
+//     RNG, whole vectors at a time.
+//   * CTAs exchange partial results by writing them into every CTA of the
+//     cluster (distributed shared memory) before a cluster barrier, so each
+//     exchange costs one barrier and every CTA derives identical decisions.
+//   * code size matters as much as instruction count: a row executes its
+//     passes once, so every pass is one out-of-line function that all call
+//     sites share, and the per-CTA state lives in shared memory (`g`).
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -36,14 +49,15 @@ namespace cg = cooperative_groups;
 
 namespace ss {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;  // 2 CTAs per SM with up to 128 registers per thread
 constexpr int kWarps = kThreads / 32;
 constexpr int kHashCap = SS_MAX_PATCHED;
 constexpr int kHashShift = 32 - 10;  // log2(kHashCap) = 10
 static_assert(kHashCap == 1024, "hash shift assumes 1024 slots");
+static_assert(kThreads >= 256, "histogram folding uses 4 threads per bucket");
 constexpr uint32_t kChunkBytes = 8192;
 constexpr int kMaxChunks = 20;
-constexpr uint32_t kTargetSliceBytes = 80u * 1024u;
+constexpr uint32_t kTargetSliceBytes = 66000u;
 constexpr uint32_t kMaxSliceBytes = kMaxChunks * kChunkBytes;
 constexpr int kMaxCluster = 8;
 constexpr uint32_t kWaitPolls = 1u << 22;
@@ -51,6 +65,15 @@ constexpr float kFixedScale = 1099511627776.0f;  // 2^40
 constexpr double kFixedInv = 1.0 / 1099511627776.0;
 constexpr int kBiasFlag = 1 << 30;
 constexpr int kNoCut = 0x7fffffff;
+constexpr int kBuckets = 64;
+constexpr int kCopies = 16;    // lane-private histogram copies
+constexpr int kListCap = 512;  // tokens gathered for an exact resolution
+constexpr int kMaxLevels = 3;  // bucket refinement depth
+constexpr int kRecs = kMaxLevels + 2;  // level 1, k-chain, scratch, tile level
+constexpr float kMassCutoff = 28.5f;  // exp(-28.5) * 2^40 < 1: zero in fixed point
+constexpr uint32_t kWorkBytes = 12288;
+constexpr int kPartSlots = 4;  // stage 1, draw, residual, normaliser
+constexpr int kRedBytes = 1024;
 
 enum TaskMode { kModeSample = 0, kModeVerify = 1 };
 
@@ -62,21 +85,76 @@ __device__ __forceinline__ uint32_t order_key(float y) {
   const uint32_t b = __float_as_uint(y);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+// Sort key: ascending order = (y descending, token index ascending).
+__device__ __forceinline__ unsigned long long sort_key(float y, int32_t t) {
+  return (static_cast<unsigned long long>(~order_key(y)) << 32) | static_cast<uint32_t>(t);
+}
+__device__ __forceinline__ uint32_t sort_key_order(unsigned long long e) { return ~static_cast<uint32_t>(e >> 32); }
+__device__ __forceinline__ int32_t sort_key_token(unsigned long long e) {
+  return static_cast<int32_t>(static_cast<uint32_t>(e));
+}
+
+// Largest of a and b, NaN if either is NaN.
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// trunc(exp(y - m) * 2^40) for y <= m, taken from the float's exponent and
+// significand with integer shifts: the float -> 64-bit integer conversion
+// instruction is several times slower than this on sm_103.
+__device__ __forceinline__ unsigned long long fixed_mass(float y, float m) {
+  const uint32_t b = __float_as_uint(fminf(__expf(y - m), 1.0f));
+  const int sh = static_cast<int>(b >> 23) - (127 + 23 - 40);
+  const unsigned long long sig = (b & 0x7fffffu) | 0x800000u;
+  if (sh >= 0) return sig << sh;
+  return sh > -24 ? (sig >> -sh) : 0ull;
+}
+
+// Absolute bucket index of y at a refinement scale (a power of two).
+// The floor is taken by adding 1.5 * 2^23 with round-down (the sum's unit in
+// the last place is 1) rather than by a rounding instruction: sm_103 issues
+// float rounding and float <-> integer conversions at a small fraction of the
+// add rate.  Values at or above 2^22 come back as 2^22, outside every bucket
+// range in use (absolute buckets stay below 64^3 + 64).
+__device__ __forceinline__ float bucket_of(float m, float y, float scale) {
+  const float x = fminf(__fmul_rn(__fsub_rn(m, y), scale), 4194304.0f);
+  return __fsub_rn(__fadd_rd(x, 12582912.0f), 12582912.0f);
+}
+
+// Integer value of an integral float in [0, 2^22], without a conversion
+// instruction.
+__device__ __forceinline__ int small_int(float b) { return __float_as_int(__fadd_rn(b, 12582912.0f)) - 0x4B400000; }
+
+// Smallest y a token of bucket `abs` at `scale` can have (rounded down).
+__device__ __forceinline__ float bucket_floor(float m, float abs, float scale) {
+  return m - (abs + 1.0f) / scale - fabsf(m) * 1e-6f - 1e-30f;
+}
+
+// Fixed-point mass target ceil(p * S): cum >= target  <=>  cum >= p * S.
+__device__ __forceinline__ unsigned long long mass_target(float p, unsigned long long S) {
+  return static_cast<unsigned long long>(ceil(static_cast<double>(p) * static_cast<double>(S)));
+}
 
 // ----------------------------------------------------------------- layout --
 
 struct Layout {
   int32_t slice_len;   // tokens per CTA, multiple of 32
   int32_t data_bytes;  // raw slice bytes (multiple of 16)
+  int32_t vmax_off;    // per-vector bound of the largest processed logit (bf16, rounded up)
   int32_t xm_off;      // exclusion bitmap, slice_len / 32 words
   int32_t hk_off;      // patch table: token ids
   int32_t hc_off;      // patch table: counts | kBiasFlag
   int32_t hv_off;      // patch table: bias value, then processed value
-  int32_t hist_off;    // 2 x 256 counts (u32) + 2 x 256 masses (u64)
-  int32_t merge_off;   // 256 counts + 256 masses, merged over the cluster
+  int32_t work_off;    // kWorkBytes: histograms / gathered lists / fallback buffers
+  int32_t rh_off;      // 2 x C x 64 pushed bucket masses (u64) and counts (u32)
+  int32_t rec_off;     // kRecs merged histograms
   int32_t red_off;     // per-warp reduction scratch
-  int32_t part_off;    // per-CTA partial results read by the other CTAs
-  int32_t ctl_off;     // task control block
+  int32_t part_off;    // kPartSlots x C pushed partials
   int32_t mbar_off;    // kMaxChunks mbarriers
   int32_t total;
 };
@@ -88,40 +166,33 @@ struct alignas(16) Part {
   int32_t count;
   int32_t status;
   unsigned long long mass;
-  float xw;       // exp(y_x - m) of the draft token if this CTA holds it, else -1
-  int32_t x_in;   // draft token in K (1) / not (0) / not here (-1)
-  float score;
-  int32_t pad;
+  float ymin;     // smallest allowed processed logit
+  float xy;       // processed logit of the draft token (its CTA only)
+  int32_t xhere;  // this CTA holds the draft token
+  float smax;     // online softmax: running max and
+  float ssum;     //   sum of exp(y - smax)
+  int32_t pad[3];
 };
-constexpr int kPartSlots = 6;
 
-// Result of one histogram pass (written by warp 0, read by all threads).
+// Merged histogram of one refinement level.
+struct alignas(16) LevelRec {
+  float scale;  // bucket(y) = floor((m - y) * scale) - base
+  float base;   // 64 * absolute index of the parent bucket (0 at level 1)
+  int32_t pad[2];
+  uint32_t cnt[kBuckets];
+  unsigned long long mass[kBuckets];
+};
+
+// Result of one histogram pass of the fallback selection.
 struct SelPass {
   uint32_t digit, cnt_before, cnt_bin, reached;
-  unsigned long long mass_before, mass_bin, total;
-  double target;
+  unsigned long long mass_before, mass_bin, total, target;
 };
 
-struct SelOut {
-  uint32_t key, cnt_gt, cnt_eq, reached;
-  unsigned long long mass_gt, mass_eq, total;
-};
-
-struct Ctl {
-  int32_t row, req, j, k, d0, drow, x;
-  int32_t bad_k;  // request's draft count outside [0, max_draft]
-  int32_t greedy, top_k, use_mask;
-  float temperature, inv_t, top_p, min_p, rep, freq, pres;
-  uint32_t seed_lo, seed_hi, pos;
-  int32_t h0, h1, b0, b1;
-  int32_t lo, n;  // slice start token, tokens in this slice
-  int32_t status;
-  // after stage 1
-  float m;
-  int32_t arg, count;
-  // selection result broadcast
-  SelPass sel;
-  double sel_target;
+struct Loc {  // where a count / mass target falls in a LevelRec
+  int32_t bucket, found;
+  uint32_t cnt_before, pad;
+  unsigned long long mass_before;
 };
 
 struct KArgs {
@@ -145,40 +216,60 @@ struct KArgs {
   Layout L;
 };
 
-struct Smem {
+// Per-CTA state in (static) shared memory, visible to every device function.
+struct Ctx {
+  // regions of the dynamic shared memory
   uint8_t* data;
+  __nv_bfloat16* vmax;
   uint32_t* xm;
   int32_t* hkey;
   int32_t* hcnt;
   float* hval;
-  uint32_t* hcnt_buf[2];
-  unsigned long long* hmass_buf[2];
-  uint32_t* mcnt;
-  unsigned long long* mmass;
+  uint8_t* work;
+  uint32_t* rh_cnt[2];  // [rank][bucket], by step parity
+  unsigned long long* rh_mass[2];
+  LevelRec* rec;
   uint8_t* red;
-  Part* part;
-  Ctl* ctl;
+  Part* part;  // [slot][rank]
   uint64_t* mbar;
+  int32_t ncta, rank;
+  // task
+  int32_t row, req, j, k, d0, drow, x;
+  int32_t bad_k;  // request's draft count outside [0, max_draft]
+  int32_t greedy, top_k, use_mask, want_s;
+  float temperature, inv_t, top_p, min_p, rep, freq, pres;
+  uint32_t seed_lo, seed_hi, pos;
+  int32_t h0, h1, b0, b1;
+  int32_t lo, n;  // slice start token, tokens in this slice
+  int32_t status;
+  // after stage 1
+  float m, ymin, s_all;
+  int32_t arg, count;
+  // broadcast slots
+  Part fold;
+  SelPass sel;
+  Loc loc;
+  int32_t pick;
+  uint32_t cursor[2];      // gather slot cursors (used in rank 0), by step parity
+  float kabs[kMaxLevels];  // absolute bucket of the top-k cut at each level
+  int32_t cut_on, cut_idx, cut_len;
+  uint32_t cut_key;
 };
 
-__device__ __forceinline__ Smem carve(uint8_t* base, const Layout& L) {
-  Smem s;
-  s.data = base;
-  s.xm = reinterpret_cast<uint32_t*>(base + L.xm_off);
-  s.hkey = reinterpret_cast<int32_t*>(base + L.hk_off);
-  s.hcnt = reinterpret_cast<int32_t*>(base + L.hc_off);
-  s.hval = reinterpret_cast<float*>(base + L.hv_off);
-  s.hcnt_buf[0] = reinterpret_cast<uint32_t*>(base + L.hist_off);
-  s.hcnt_buf[1] = s.hcnt_buf[0] + 256;
-  s.hmass_buf[0] = reinterpret_cast<unsigned long long*>(base + L.hist_off + 2048);
-  s.hmass_buf[1] = s.hmass_buf[0] + 256;
-  s.mcnt = reinterpret_cast<uint32_t*>(base + L.merge_off);
-  s.mmass = reinterpret_cast<unsigned long long*>(base + L.merge_off + 1024);
-  s.red = base + L.red_off;
-  s.part = reinterpret_cast<Part*>(base + L.part_off);
-  s.ctl = reinterpret_cast<Ctl*>(base + L.ctl_off);
-  s.mbar = reinterpret_cast<uint64_t*>(base + L.mbar_off);
-  return s;
+extern __shared__ __align__(128) uint8_t smem_raw[];
+__shared__ Ctx g;
+
+__device__ __forceinline__ float vec_bound(int v) {
+  return __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(g.vmax[v])) << 16);
+}
+
+// fp32 -> bf16 rounded toward +inf, by integer arithmetic on the bits
+// (NaN stays NaN, +inf and -inf stay put).
+__device__ __forceinline__ __nv_bfloat16 bf16_round_up(float x) {
+  const uint32_t b = __float_as_uint(x);
+  uint32_t h = (b & 0x80000000u) ? (b >> 16) : ((b + 0xffffu) >> 16);
+  if (x != x) h = 0x7fc0u;
+  return __ushort_as_bfloat16(static_cast<unsigned short>(h));
 }
 
 // ------------------------------------------------------------- dtype glue --
@@ -206,6 +297,9 @@ struct Vec<SS_DTYPE_F32> {
   }
   __device__ static __forceinline__ float load_global(const void* row, int64_t t) {
     return reinterpret_cast<const float*>(row)[t];
+  }
+  __device__ static __forceinline__ float load_smem(const uint8_t* data, int e) {
+    return reinterpret_cast<const float*>(data)[e];
   }
 };
 
@@ -239,184 +333,470 @@ struct Vec<SS_DTYPE_BF16> {
     const uint16_t h = reinterpret_cast<const uint16_t*>(row)[t];
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
   }
+  __device__ static __forceinline__ float load_smem(const uint8_t* data, int e) {
+    return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(data)[e]) << 16);
+  }
 };
 
 // --------------------------------------------------------- reductions --
 
-struct ArgMax {
-  float v;
-  int32_t i;
-};
+__device__ __forceinline__ bool beats(float v, int32_t i, float bv, int32_t bi) {
+  return v > bv || (v == bv && i < bi);
+}
 
-__device__ __forceinline__ void argmax_merge(ArgMax& a, float v, int32_t i) {
-  if (v > a.v || (v == a.v && i < a.i)) {
-    a.v = v;
-    a.i = i;
+// Merge of two online-softmax pairs (sum of exp(y - smax)).
+__device__ __forceinline__ void softmax_merge(float& m1, float& s1, float m2, float s2) {
+  if (m2 == neg_inf()) return;
+  if (m1 == neg_inf()) {
+    m1 = m2;
+    s1 = s2;
+    return;
+  }
+  const float M = fmaxf(m1, m2);
+  s1 = __fadd_rn(__fmul_rn(s1, __expf(m1 - M)), __fmul_rn(s2, __expf(m2 - M)));
+  m1 = M;
+}
+
+__device__ __forceinline__ void part_merge(Part& a, const Part& b) {
+  if (beats(b.best, b.arg, a.best, a.arg)) {
+    a.best = b.best;
+    a.arg = b.arg;
+  }
+  a.count += b.count;
+  a.status = max(a.status, b.status);
+  a.mass += b.mass;
+  a.ymin = fminf(a.ymin, b.ymin);
+  softmax_merge(a.smax, a.ssum, b.smax, b.ssum);
+  if (b.xhere) {
+    a.xy = b.xy;
+    a.xhere = 1;
   }
 }
 
-__device__ __forceinline__ ArgMax warp_argmax(ArgMax a) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float v = __shfl_xor_sync(0xffffffffu, a.v, off);
-    const int32_t i = __shfl_xor_sync(0xffffffffu, a.i, off);
-    argmax_merge(a, v, i);
-  }
-  return a;
+__device__ __forceinline__ Part part_shfl(const Part& p, int off) {
+  Part q;
+  q.best = __shfl_xor_sync(0xffffffffu, p.best, off);
+  q.arg = __shfl_xor_sync(0xffffffffu, p.arg, off);
+  q.count = __shfl_xor_sync(0xffffffffu, p.count, off);
+  q.status = __shfl_xor_sync(0xffffffffu, p.status, off);
+  q.mass = __shfl_xor_sync(0xffffffffu, p.mass, off);
+  q.ymin = __shfl_xor_sync(0xffffffffu, p.ymin, off);
+  q.xy = __shfl_xor_sync(0xffffffffu, p.xy, off);
+  q.xhere = __shfl_xor_sync(0xffffffffu, p.xhere, off);
+  q.smax = __shfl_xor_sync(0xffffffffu, p.smax, off);
+  q.ssum = __shfl_xor_sync(0xffffffffu, p.ssum, off);
+  return q;
 }
 
-template <typename T>
-__device__ __forceinline__ T warp_sum(T v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
+__device__ __forceinline__ Part empty_part() {
+  Part p{};
+  p.best = neg_inf();
+  p.arg = kNoCut;
+  p.ymin = pos_inf();
+  p.xy = neg_inf();
+  p.smax = neg_inf();
+  return p;
 }
 
-__device__ __forceinline__ int32_t warp_max_i(int32_t v) {
+// Reduces every thread's partial over the block and then over the cluster:
+// each CTA writes its block total into slot `slot` of every CTA, one cluster
+// barrier, then each CTA folds the C totals in rank order.  The result lands
+// in g.fold (identical in every CTA).  Called by all threads.
+__device__ __noinline__ void reduce_fold(int slot, float best, int32_t arg, int32_t count, int32_t status,
+                                         unsigned long long mass, float ymin, float smax, float ssum, float xy,
+                                         int32_t xhere) {
+  Part p;
+  p.best = best;
+  p.arg = arg;
+  p.count = count;
+  p.status = status;
+  p.mass = mass;
+  p.ymin = ymin;
+  p.xy = xy;
+  p.xhere = xhere;
+  p.smax = smax;
+  p.ssum = ssum;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
-  return v;
-}
-
-// Block reduction of (argmax, count, status max, mass sum); result valid in
-// every thread.  Uses the `red` scratch (kWarps * 32 bytes).
-struct BlockAcc {
-  ArgMax am;
-  int32_t count;
-  int32_t status;
-  unsigned long long mass;
-};
-
-__device__ BlockAcc block_reduce(const Smem& sm, BlockAcc a) {
-  a.am = warp_argmax(a.am);
-  a.count = warp_sum(a.count);
-  a.status = warp_max_i(a.status);
-  a.mass = warp_sum(a.mass);
-  struct alignas(8) W {
-    float v;
-    int32_t i, c, s;
-    unsigned long long m;
-  };
-  W* w = reinterpret_cast<W*>(sm.red);
+  for (int off = 16; off > 0; off >>= 1) part_merge(p, part_shfl(p, off));
+  Part* w = reinterpret_cast<Part*>(g.red);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   __syncthreads();
-  if (lane == 0) w[wid] = W{a.am.v, a.am.i, a.count, a.status, a.mass};
+  if (lane == 0) w[wid] = p;
   __syncthreads();
-  BlockAcc r;
-  r.am = ArgMax{neg_inf(), kNoCut};
-  r.count = 0;
-  r.status = 0;
-  r.mass = 0;
-  for (int k = 0; k < kWarps; ++k) {  // fixed order: deterministic
-    argmax_merge(r.am, w[k].v, w[k].i);
-    r.count += w[k].c;
-    r.status = max(r.status, w[k].s);
-    r.mass += w[k].m;
+  if (threadIdx.x == 0) {  // fixed order: deterministic
+    Part t = w[0];
+    for (int k = 1; k < kWarps; ++k) part_merge(t, w[k]);
+    w[kWarps] = t;
   }
-  return r;
-}
-
-// Exchange one Part per CTA through the cluster and fold them in rank order.
-__device__ Part cluster_fold(const Smem& sm, int slot, const Part& mine) {
+  __syncthreads();
   cg::cluster_group cl = cg::this_cluster();
-  if (threadIdx.x == 0) sm.part[slot] = mine;
+  const int n = g.ncta;
+  if (threadIdx.x < n) *cl.map_shared_rank(g.part + slot * n + g.rank, threadIdx.x) = w[kWarps];
   cl.sync();
-  Part r = mine;
-  r.best = neg_inf();
-  r.arg = kNoCut;
-  r.count = 0;
-  r.status = 0;
-  r.mass = 0;
-  r.xw = -1.0f;
-  r.x_in = -1;
-  r.score = neg_inf();
-  const int n = static_cast<int>(cl.num_blocks());
-  for (int c = 0; c < n; ++c) {
-    const Part* q = cl.map_shared_rank(sm.part + slot, c);
-    const Part p = *q;
-    if (p.best > r.best || (p.best == r.best && p.arg < r.arg)) {
-      r.best = p.best;
-      r.arg = p.arg;
-      r.score = p.score;
-    }
-    r.count += p.count;
-    r.status = max(r.status, p.status);
-    r.mass += p.mass;
-    if (p.x_in >= 0) {
-      r.x_in = p.x_in;
-      r.xw = p.xw;
-    }
+  if (threadIdx.x == 0) {
+    Part t = g.part[slot * n];
+    for (int c = 1; c < n; ++c) part_merge(t, g.part[slot * n + c]);
+    g.fold = t;
   }
-  return r;
+  __syncthreads();
+}
+static_assert((kWarps + 1) * sizeof(Part) <= kRedBytes, "reduction scratch too small");
+static_assert(kWarps * sizeof(unsigned long long) <= kRedBytes, "scan scratch too small");
+static_assert(kListCap % kThreads == 0, "list runs");
+
+// ------------------------------------------------- bucket refinement --
+
+// Folds the lane-private histogram copies in the work region, writes the
+// CTA's totals into every CTA (buffer of this step's parity), one cluster
+// barrier, and merges the C totals in rank order into `out`.
+__device__ __forceinline__ void push_merge(LevelRec* out, float scale, float base, int step) {
+  cg::cluster_group cl = cg::this_cluster();
+  const uint32_t* hc = reinterpret_cast<const uint32_t*>(g.work);
+  const unsigned long long* hm = reinterpret_cast<const unsigned long long*>(g.work + kBuckets * kCopies * 4);
+  const int tid = threadIdx.x;
+  const int par = step & 1;
+  __syncthreads();
+  if (tid < kBuckets * 4) {  // 4 threads per bucket
+    const int b = tid >> 2, q = tid & 3;
+    uint32_t cnt = 0;
+    unsigned long long mass = 0;
+#pragma unroll
+    for (int i = 0; i < kCopies / 4; ++i) {
+      cnt += hc[b * kCopies + q * (kCopies / 4) + i];
+      mass += hm[b * kCopies + q * (kCopies / 4) + i];
+    }
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
+    mass += __shfl_xor_sync(0xffffffffu, mass, 1);
+    mass += __shfl_xor_sync(0xffffffffu, mass, 2);
+    if (q == 0)
+      for (int r = 0; r < g.ncta; ++r) {
+        *cl.map_shared_rank(g.rh_cnt[par] + g.rank * kBuckets + b, r) = cnt;
+        *cl.map_shared_rank(g.rh_mass[par] + g.rank * kBuckets + b, r) = mass;
+      }
+  }
+  cl.sync();
+  if (tid < kBuckets) {
+    uint32_t cnt = 0;
+    unsigned long long mass = 0;
+    for (int r = 0; r < g.ncta; ++r) {
+      cnt += g.rh_cnt[par][r * kBuckets + tid];
+      mass += g.rh_mass[par][r * kBuckets + tid];
+    }
+    out->cnt[tid] = cnt;
+    out->mass[tid] = mass;
+  }
+  if (tid == 0) {
+    out->scale = scale;
+    out->base = base;
+  }
+  __syncthreads();
 }
 
-// -------------------------------------------------------------- visitor --
-
-// Calls f(t, y) for every allowed token of this CTA's slice (raw slice plus
-// patch table); y is the processed logit (z for greedy rows).
-template <int DT, typename F>
-__device__ __forceinline__ void visit(const Smem& sm, const Ctl& c, F&& f) {
+// Histogram into `out`.  Token level (tile = 0): the tokens whose bucket at
+// `scale` lies in [base, base + 64), skipping vectors whose bound is below
+// lo_y.  Tile level (tile = 1, base 0): one entry per 16-byte vector valued at
+// a lower bound of its largest processed logit, one per patched token; k
+// entries at or above a bucket imply k tokens there, and their masses bound
+// the tokens' mass from below.
+template <int DT>
+__device__ __noinline__ void hist_pass(int tile, float scale, float base, int need_mass, float lo_y, int step,
+                                       LevelRec* out) {
   using V = Vec<DT>;
-  const int nvec = (c.n + V::kPer - 1) / V::kPer;
-  const uint4* data = reinterpret_cast<const uint4*>(sm.data);
-  const bool greedy = c.greedy != 0;
-  const float inv_t = c.inv_t;
+  uint32_t* hc = reinterpret_cast<uint32_t*>(g.work);
+  unsigned long long* hm = reinterpret_cast<unsigned long long*>(g.work + kBuckets * kCopies * 4);
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kBuckets * kCopies; i += kThreads) {
+    hc[i] = 0;
+    hm[i] = 0;
+  }
+  __syncthreads();
+  const int copy = tid & (kCopies - 1);
+  const float m = g.m;
+  auto add = [&](float y) {
+    const float b = bucket_of(m, y, scale) - base;
+    if (b >= 0.0f && b < static_cast<float>(kBuckets)) {
+      const int bi = small_int(b);
+      atomicAdd(hc + bi * kCopies + copy, 1u);
+      if (need_mass) atomicAdd(hm + bi * kCopies + copy, fixed_mass(y, m));
+    }
+  };
+  const int nvec = (g.n + V::kPer - 1) / V::kPer;
+  const uint4* __restrict__ data = reinterpret_cast<const uint4*>(g.data);
+  const __nv_bfloat16* __restrict__ vmax = g.vmax;
+  const float inv_t = g.inv_t;
+  if (tile) {
+    // the stored bound is rounded up to bf16: one bf16 step below is <= the max
+    constexpr int kB = 8;  // independent loads first, then the atomics
+    for (int v0 = tid; v0 < nvec; v0 += kThreads * kB) {
+      float ub[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int v = v0 + u * kThreads;
+        ub[u] = (v < nvec) ? __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(vmax[v])) << 16) : neg_inf();
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u)
+        if (ub[u] != neg_inf()) add(fminf(ub[u] - fabsf(ub[u]) * 0.0078125f - 1e-30f, m));
+    }
+  } else {
+    for (int v = tid; v < nvec; v += kThreads) {
+      if (__uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(vmax[v])) << 16) < lo_y) continue;
+      float z[V::kPer];
+      V::unpack(data[v], z);
+#pragma unroll
+      for (int e = 0; e < V::kPer; ++e) {
+        const float y = __fmul_rn(z[e], inv_t);
+        if (y != neg_inf()) add(y);
+      }
+    }
+  }
+  for (int s = tid; s < kHashCap; s += kThreads) {
+    const float y = g.hval[s];
+    if (g.hkey[s] >= 0 && y != neg_inf() && (tile || y >= lo_y)) add(y);
+  }
+  push_merge(out, scale, base, step);
+}
+
+// Bucket of `r` where the running count (or mass) from the top first reaches
+// `target`; warp 0 computes, the result lands in g.loc.
+__device__ __noinline__ void locate(const LevelRec* r, int by_mass, unsigned long long target, uint32_t above_c,
+                                    unsigned long long above_m) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const uint32_t c0 = r->cnt[2 * lane], c1 = r->cnt[2 * lane + 1];
+    const unsigned long long m0 = r->mass[2 * lane], m1 = r->mass[2 * lane + 1];
+    uint32_t ic = c0 + c1;
+    unsigned long long im = m0 + m1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t oc = __shfl_up_sync(0xffffffffu, ic, off);
+      const unsigned long long om = __shfl_up_sync(0xffffffffu, im, off);
+      if (lane >= off) {
+        ic += oc;
+        im += om;
+      }
+    }
+    const uint32_t ec = ic - c0 - c1;
+    const unsigned long long em = im - m0 - m1;
+    const bool hit_all = by_mass ? (above_m + im >= target) : (static_cast<unsigned long long>(above_c + ic) >= target);
+    const bool hit_one =
+        by_mass ? (above_m + em + m0 >= target) : (static_cast<unsigned long long>(above_c + ec + c0) >= target);
+    const unsigned ball = __ballot_sync(0xffffffffu, hit_all);
+    if (lane == 0 && !ball) g.loc = Loc{0, 0, 0, 0, 0};
+    if (ball && lane == __ffs(ball) - 1) {
+      Loc l;
+      l.found = 1;
+      l.pad = 0;
+      if (hit_one) {
+        l.bucket = 2 * lane;
+        l.cnt_before = ec;
+        l.mass_before = em;
+      } else {
+        l.bucket = 2 * lane + 1;
+        l.cnt_before = ec + c0;
+        l.mass_before = em + m0;
+      }
+      g.loc = l;
+    }
+  }
+  __syncthreads();
+}
+
+// Gathers every token of bucket `abs` at `scale` into every CTA's list (the
+// buffer of this step's parity).
+template <int DT>
+__device__ __noinline__ void gather_pass(float scale, float abs, float lo_y, int step) {
+  using V = Vec<DT>;
+  cg::cluster_group cl = cg::this_cluster();
+  const int par = step & 1;
+  unsigned long long* list = reinterpret_cast<unsigned long long*>(g.work) + par * kListCap;
+  uint32_t* cursor = cl.map_shared_rank(&g.cursor[par], 0);
+  const float m = g.m;
+  const int lane = threadIdx.x & 31;
+  const int ncta = g.ncta;
+  auto put = [&](int32_t t, float y) {
+    if (bucket_of(m, y, scale) != abs) return;
+    const unsigned act = __activemask();
+    const int leader = __ffs(act) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(cursor, static_cast<uint32_t>(__popc(act)));
+    base = __shfl_sync(act, base, leader);
+    const uint32_t slot = base + static_cast<uint32_t>(__popc(act & ((1u << lane) - 1u)));
+    if (slot < static_cast<uint32_t>(kListCap)) {
+      const unsigned long long e = sort_key(y, t);
+      for (int r = 0; r < ncta; ++r) *cl.map_shared_rank(list + slot, r) = e;
+    }
+  };
+  const int nvec = (g.n + V::kPer - 1) / V::kPer;
+  const uint4* data = reinterpret_cast<const uint4*>(g.data);
+  const float inv_t = g.inv_t;
+  const int lo = g.lo;
   for (int v = threadIdx.x; v < nvec; v += kThreads) {
+    if (vec_bound(v) < lo_y) continue;
     float z[V::kPer];
     V::unpack(data[v], z);
 #pragma unroll
     for (int e = 0; e < V::kPer; ++e) {
-      const float y = greedy ? z[e] : __fmul_rn(z[e], inv_t);
-      if (y != neg_inf()) f(c.lo + v * V::kPer + e, y);
+      const float y = __fmul_rn(z[e], inv_t);
+      if (y != neg_inf()) put(lo + v * V::kPer + e, y);
     }
   }
   for (int s = threadIdx.x; s < kHashCap; s += kThreads) {
-    const int32_t t = sm.hkey[s];
-    if (t >= 0) {
-      const float y = sm.hval[s];
-      if (y != neg_inf()) f(t, y);
+    const int32_t t = g.hkey[s];
+    const float y = g.hval[s];
+    if (t >= 0 && y != neg_inf() && y >= lo_y) put(t, y);
+  }
+  cl.sync();
+  if (g.rank == 0 && threadIdx.x == 0) g.cursor[par] = 0;  // its next use is two steps away
+}
+
+// Sorts list[0..n) ascending in place (bitonic network in shared memory,
+// n <= kListCap) and writes the inclusive prefix sums of the fixed-point
+// masses to `pre`.
+__device__ __noinline__ void sort_and_scan(unsigned long long* list, int n, unsigned long long* pre) {
+  const int tid = threadIdx.x;
+  int np2 = 2;
+  while (np2 < n) np2 <<= 1;
+  for (int i = n + tid; i < np2; i += kThreads) list[i] = ~0ull;  // padding sorts last
+  __syncthreads();
+  const int pairs = np2 >> 1;
+  for (int k = 2; k <= np2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int q = tid; q < pairs; q += kThreads) {
+        const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1));  // lower index of the pair (j a power of two)
+        const unsigned long long a = list[i], b = list[i + j];
+        const bool asc = (i & k) == 0;
+        if ((a > b) == asc) {
+          list[i] = b;
+          list[i + j] = a;
+        }
+      }
+      __syncthreads();
     }
   }
+  // inclusive scan of masses in sorted order: each thread owns a run
+  constexpr int kPer = kListCap / kThreads;
+  const float m = g.m;
+  unsigned long long run[kPer];
+  unsigned long long tot = 0;
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const int i = tid * kPer + r;
+    run[r] = (i < n) ? fixed_mass(key_value(sort_key_order(list[i])), m) : 0ull;
+    tot += run[r];
+  }
+  const int lane = tid & 31, wid = tid >> 5;
+  unsigned long long x = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  unsigned long long* ws = reinterpret_cast<unsigned long long*>(g.red);
+  if (lane == 31) ws[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    unsigned long long y = (lane < kWarps) ? ws[lane] : 0ull;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned long long z = __shfl_up_sync(0xffffffffu, y, off);
+      if (lane >= off) y += z;
+    }
+    if (lane < kWarps) ws[lane] = y;
+  }
+  __syncthreads();
+  unsigned long long acc = x - tot + ((wid > 0) ? ws[wid - 1] : 0ull);  // exclusive prefix of this run
+#pragma unroll
+  for (int r = 0; r < kPer; ++r) {
+    const int i = tid * kPer + r;
+    acc += run[r];
+    if (i < n) pre[i] = acc;
+  }
+  __syncthreads();
 }
 
-__device__ __forceinline__ unsigned long long fixed_mass(float y, float m) {
-  return __float2ull_rz(__expf(y - m) * kFixedScale);
+// First position i in [0, limit] where above + pre[i] >= target (limit when
+// none), computed by all threads cooperatively.
+__device__ __noinline__ int first_reaching(const unsigned long long* pre, int limit, unsigned long long above,
+                                           unsigned long long target) {
+  const int tid = threadIdx.x;
+  if (tid == 0) g.pick = limit;
+  __syncthreads();
+  for (int i = tid; i <= limit; i += kThreads) {
+    const bool here = above + pre[i] >= target;
+    const bool before = i > 0 && above + pre[i - 1] >= target;
+    if (here && !before) g.pick = i;
+  }
+  __syncthreads();
+  const int p = g.pick;
+  __syncthreads();
+  return p;
 }
 
-// One exact radix selection (4 passes of 8-bit digits over a 32-bit key).
-// Elements are those `accept(t, y)` admits; key(t, y) orders them, larger
-// first.  by_mass: the selected element is where the running fixed-point mass
-// first reaches `target` (or target_frac * total mass when target_frac > 0);
-// otherwise where the running count reaches `target`.
-template <int DT, bool kMass, typename KeyF, typename AccF>
-__device__ SelOut radix_select(const Smem& sm, const Ctl& c, int& pass, bool by_mass, double target,
-                               double target_frac, KeyF keyf, AccF accept) {
+// --------------------------------------------------- fallback selection --
+
+// Buffers of the fallback selection inside the work region.
+__device__ __forceinline__ uint32_t* fb_cnt(int buf) { return reinterpret_cast<uint32_t*>(g.work) + 256 * buf; }
+__device__ __forceinline__ unsigned long long* fb_mass(int buf) {
+  return reinterpret_cast<unsigned long long*>(g.work + 2048) + 256 * buf;
+}
+__device__ __forceinline__ uint32_t* fb_mcnt() { return reinterpret_cast<uint32_t*>(g.work + 6144); }
+__device__ __forceinline__ unsigned long long* fb_mmass() { return reinterpret_cast<unsigned long long*>(g.work + 7168); }
+
+// One exact radix selection over the whole slice (4 passes of 8-bit digits
+// over a 32-bit key), for rows the bucket refinement cannot resolve; slow.
+// Key: order_key(y) (by_index = 0) or ~index (by_index = 1, the tokens of
+// key `eq_key` only).  Tokens after the cut (lim_key, lim_idx) are ignored
+// when `limited`.  by_mass: where the running fixed-point mass first reaches
+// the target (target = ceil(frac * total mass) when frac > 0); otherwise
+// where the running count reaches it.  Result in g.sel (digit = final key).
+template <int DT>
+__device__ __noinline__ uint32_t radix_select(int& pass, int by_index, uint32_t eq_key, int limited, uint32_t lim_key,
+                                              int32_t lim_idx, int by_mass, unsigned long long target, float frac,
+                                              uint32_t& cnt_gt, uint32_t& cnt_eq, unsigned long long& mass_gt,
+                                              unsigned long long& mass_eq, unsigned long long& total,
+                                              uint32_t& reached_out) {
+  using V = Vec<DT>;
   cg::cluster_group cl = cg::this_cluster();
-  const int ncta = static_cast<int>(cl.num_blocks());
-  uint32_t prefix = 0, pmask = 0, base_c = 0;
-  unsigned long long base_m = 0, total = 0;
-  SelOut out{};
-  out.reached = 1;
-  const float m = c.m;
+  const int ncta = g.ncta;
+  uint32_t prefix = 0, pmask = 0, base_c = 0, reached_all = 1;
+  unsigned long long base_m = 0;
+  const float m = g.m;
   for (int level = 0; level < 4; ++level) {
     const int shift = 24 - 8 * level;
     const int buf = pass & 1;
     ++pass;
-    uint32_t* hc = sm.hcnt_buf[buf];
-    unsigned long long* hm = sm.hmass_buf[buf];
+    uint32_t* hc = fb_cnt(buf);
+    unsigned long long* hm = fb_mass(buf);
     for (int b = threadIdx.x; b < 256; b += kThreads) {
       hc[b] = 0;
-      if (kMass) hm[b] = 0;
+      hm[b] = 0;
     }
     __syncthreads();
-    visit<DT>(sm, c, [&](int32_t t, float y) {
-      const uint32_t key = keyf(t, y);
+    auto add = [&](int32_t t, float y) {
+      const uint32_t ky = order_key(y);
+      if (limited && !(ky > lim_key || (ky == lim_key && t <= lim_idx))) return;
+      if (by_index && ky != eq_key) return;
+      const uint32_t key = by_index ? ~static_cast<uint32_t>(t) : ky;
       if ((key & pmask) != prefix) return;
-      if (!accept(t, y)) return;
       const uint32_t d = (key >> shift) & 255u;
       atomicAdd(hc + d, 1u);
-      if (kMass) atomicAdd(hm + d, fixed_mass(y, m));
-    });
+      if (by_mass) atomicAdd(hm + d, fixed_mass(y, m));
+    };
+    const int nvec = (g.n + V::kPer - 1) / V::kPer;
+    const uint4* data = reinterpret_cast<const uint4*>(g.data);
+    for (int v = threadIdx.x; v < nvec; v += kThreads) {
+      float z[V::kPer];
+      V::unpack(data[v], z);
+#pragma unroll
+      for (int e = 0; e < V::kPer; ++e) {
+        const float y = __fmul_rn(z[e], g.inv_t);
+        if (y != neg_inf()) add(g.lo + v * V::kPer + e, y);
+      }
+    }
+    for (int s = threadIdx.x; s < kHashCap; s += kThreads)
+      if (g.hkey[s] >= 0 && g.hval[s] != neg_inf()) add(g.hkey[s], g.hval[s]);
     __syncthreads();
     cl.sync();
     for (int b = threadIdx.x; b < 256; b += kThreads) {
@@ -424,10 +804,10 @@ __device__ SelOut radix_select(const Smem& sm, const Ctl& c, int& pass, bool by_
       unsigned long long mm = 0;
       for (int r = 0; r < ncta; ++r) {
         cc += *cl.map_shared_rank(hc + b, r);
-        if (kMass) mm += *cl.map_shared_rank(hm + b, r);
+        mm += *cl.map_shared_rank(hm + b, r);
       }
-      sm.mcnt[b] = cc;
-      sm.mmass[b] = mm;
+      fb_mcnt()[b] = cc;
+      fb_mmass()[b] = mm;
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -439,8 +819,8 @@ __device__ SelOut radix_select(const Smem& sm, const Ctl& c, int& pass, bool by_
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int b = 255 - 8 * lane - i;
-        c8[i] = sm.mcnt[b];
-        m8[i] = kMass ? sm.mmass[b] : 0ull;
+        c8[i] = fb_mcnt()[b];
+        m8[i] = fb_mmass()[b];
         cs += c8[i];
         ms += m8[i];
       }
@@ -456,14 +836,15 @@ __device__ SelOut radix_select(const Smem& sm, const Ctl& c, int& pass, bool by_
         }
       }
       const unsigned long long tot_m = __shfl_sync(0xffffffffu, im, 31);
-      double tgt = target;
+      unsigned long long tgt = target;
       if (level > 0)
-        tgt = sm.ctl->sel_target;
-      else if (target_frac > 0.0)
-        tgt = target_frac * static_cast<double>(tot_m);
-      const bool cross = by_mass ? (static_cast<double>(base_m + im) >= tgt)
-                                 : (static_cast<double>(base_c + ic) >= tgt);
-      const unsigned ball = __ballot_sync(0xffffffffu, cross);
+        tgt = g.sel.target;
+      else if (frac > 0.0f)
+        tgt = mass_target(frac, tot_m);
+      auto hit = [&](uint32_t cc, unsigned long long mm) {
+        return by_mass ? (base_m + mm >= tgt) : (static_cast<unsigned long long>(base_c + cc) >= tgt);
+      };
+      const unsigned ball = __ballot_sync(0xffffffffu, hit(ic, im));
       const unsigned nz = __ballot_sync(0xffffffffu, cs > 0);
       int L;
       uint32_t reached = 1;
@@ -477,81 +858,514 @@ __device__ SelOut radix_select(const Smem& sm, const Ctl& c, int& pass, bool by_
       if (lane == L) {
         uint32_t cc = ic - cs;
         unsigned long long mmv = im - ms;
+        int last = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (c8[i] > 0) last = i;
+        bool done = false;
         int pick = 7;
-        if (reached) {
-          for (int i = 0; i < 8; ++i) {
-            const bool hit = by_mass ? (static_cast<double>(base_m + mmv + m8[i]) >= tgt)
-                                     : (static_cast<double>(base_c + cc + c8[i]) >= tgt);
-            if (hit) {
-              pick = i;
-              break;
-            }
-            cc += c8[i];
-            mmv += m8[i];
+        uint32_t pc = 0, pcb = 0;
+        unsigned long long pm = 0, pmb = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const bool h = reached ? hit(cc + c8[i], mmv + m8[i]) : (i == last);
+          if (!done && h) {
+            done = true;
+            pick = i;
+            pc = cc;
+            pm = mmv;
+            pcb = c8[i];
+            pmb = m8[i];
           }
-        } else {
-          int last = 7;
-          for (int i = 7; i >= 0; --i)
-            if (c8[i] > 0) {
-              last = i;
-              break;
-            }
-          for (int i = 0; i < last; ++i) {
-            cc += c8[i];
-            mmv += m8[i];
-          }
-          pick = last;
+          cc += c8[i];
+          mmv += m8[i];
         }
         SelPass sp;
         sp.digit = static_cast<uint32_t>(255 - 8 * L - pick);
-        sp.cnt_before = cc;
-        sp.cnt_bin = c8[pick];
-        sp.mass_before = mmv;
-        sp.mass_bin = m8[pick];
+        sp.cnt_before = pc;
+        sp.cnt_bin = pcb;
+        sp.mass_before = pm;
+        sp.mass_bin = pmb;
         sp.reached = reached;
         sp.total = tot_m;
         sp.target = tgt;
-        sm.ctl->sel = sp;
-        sm.ctl->sel_target = tgt;
+        g.sel = sp;
       }
     }
     __syncthreads();
-    const SelPass sp = sm.ctl->sel;
+    const SelPass sp = g.sel;
     if (level == 0) total = sp.total;  // mass of every admitted element
     prefix |= sp.digit << shift;
     pmask |= 255u << shift;
     base_c += sp.cnt_before;
     base_m += sp.mass_before;
-    out.cnt_eq = sp.cnt_bin;
-    out.mass_eq = sp.mass_bin;
-    if (!sp.reached) out.reached = 0;
+    cnt_eq = sp.cnt_bin;
+    mass_eq = sp.mass_bin;
+    if (!sp.reached) reached_all = 0;
     __syncthreads();
   }
-  out.key = prefix;
-  out.cnt_gt = base_c;
-  out.mass_gt = base_m;
-  out.total = total;
-  return out;
+  cnt_gt = base_c;
+  mass_gt = base_m;
+  reached_out = reached_all;
+  return prefix;
 }
 
+// Exact top-k / top-p cut by radix selection over the slice; result in g.cut_*.
+template <int DT>
+__device__ __noinline__ void fallback_cuts(int k_on, int p_on) {
+  int pass = 0;
+  uint32_t cnt_gt, cnt_eq, reached;
+  unsigned long long mass_gt, mass_eq, total;
+  uint32_t k_key = 0;
+  int32_t k_idx = kNoCut;
+  int on = 0;
+  uint32_t cut_key = 0;
+  int32_t cut_idx = kNoCut;
+  if (k_on) {
+    const uint32_t key = radix_select<DT>(pass, 0, 0u, 0, 0u, 0, 0, static_cast<unsigned long long>(g.top_k), 0.0f,
+                                          cnt_gt, cnt_eq, mass_gt, mass_eq, total, reached);
+    const uint32_t ntie = static_cast<uint32_t>(g.top_k) - cnt_gt;
+    int32_t idx = kNoCut;
+    if (ntie < cnt_eq) {
+      uint32_t a, b, r2;
+      unsigned long long c2, d2, e2;
+      idx = static_cast<int32_t>(~radix_select<DT>(pass, 1, key, 0, 0u, 0, 0, ntie, 0.0f, a, b, c2, d2, e2, r2));
+    }
+    k_key = key;
+    k_idx = idx;
+    on = 1;
+    cut_key = key;
+    cut_idx = idx;
+  }
+  if (p_on) {
+    const uint32_t key = radix_select<DT>(pass, 0, 0u, k_on, k_key, k_idx, 1, 0ull, g.top_p, cnt_gt, cnt_eq, mass_gt,
+                                          mass_eq, total, reached);
+    const unsigned long long target = mass_target(g.top_p, total);
+    uint32_t ntie = cnt_eq;
+    if (reached && cnt_eq > 0) {
+      const unsigned long long w = mass_eq / cnt_eq;  // every tie has the same mass
+      if (w > 0 && target > mass_gt) {
+        const unsigned long long nt = (target - mass_gt + w - 1) / w;
+        if (nt < cnt_eq) ntie = static_cast<uint32_t>(nt > 0 ? nt : 1);
+      } else if (target <= mass_gt) {
+        ntie = 1;
+      }
+    }
+    int32_t idx = kNoCut;
+    if (ntie < cnt_eq) {
+      uint32_t a, b, r2;
+      unsigned long long c2, d2, e2;
+      idx = static_cast<int32_t>(~radix_select<DT>(pass, 1, key, k_on, k_key, k_idx, 0, ntie, 0.0f, a, b, c2, d2, e2, r2));
+    }
+    if (!on || key > cut_key || (key == cut_key && idx < cut_idx)) {
+      cut_key = key;
+      cut_idx = idx;
+    }
+    on = 1;
+  }
+  if (threadIdx.x == 0) {
+    g.cut_on = on;
+    g.cut_key = cut_key;
+    g.cut_idx = cut_idx;
+    g.cut_len = -1;
+  }
+  __syncthreads();
+}
+
+// The kept set K = the first `len` tokens of the (y desc, index asc) order,
+// ending at (key, idx).
+__device__ __forceinline__ void tighten(uint32_t key, int32_t idx, int32_t len) {
+  if (threadIdx.x == 0 && (!g.cut_on || key > g.cut_key || (key == g.cut_key && idx < g.cut_idx))) {
+    g.cut_key = key;
+    g.cut_idx = idx;
+    g.cut_len = len;
+    g.cut_on = 1;
+  }
+  __syncthreads();
+}
+
+// Refines bucket `abs` at `scale` (refinement level `level`) until it holds at
+// most kListCap tokens, following a count or mass target; false if it cannot
+// within kMaxLevels.  Updates the bucket description in place.
+template <int DT>
+__device__ __forceinline__ bool refine(int& step, int& level, float& scale, float& abs, uint32_t& above_c,
+                                    unsigned long long& above_m, uint32_t& n, int by_mass, unsigned long long target,
+                                    LevelRec* scratch) {
+  while (n > static_cast<uint32_t>(kListCap)) {
+    if (level >= kMaxLevels) return false;
+    const float sub = scale * static_cast<float>(kBuckets);
+    hist_pass<DT>(0, sub, abs * static_cast<float>(kBuckets), 1, bucket_floor(g.m, abs, scale), step++, scratch);
+    locate(scratch, by_mass, target, above_c, above_m);
+    const Loc l = g.loc;
+    if (!l.found) return false;
+    above_c += l.cnt_before;
+    above_m += l.mass_before;
+    n = scratch->cnt[l.bucket];
+    abs = abs * static_cast<float>(kBuckets) + static_cast<float>(l.bucket);
+    scale = sub;
+    ++level;
+  }
+  return true;
+}
+
+// Resolves the top-k and top-p cuts of a sampling row into g.cut_*.
+template <int DT>
+__device__ __noinline__ void resolve_cuts(int k_on, int p_on) {
+  const float m = g.m;
+  int step = 0;
+  bool fallback = false;
+  if (threadIdx.x == 0) {
+    g.cut_on = 0;
+    g.cut_key = 0;
+    g.cut_idx = kNoCut;
+    g.cut_len = -1;
+  }
+  // level 1: 64 buckets of a power-of-two width covering [ymin, m]
+  const float range = fminf(m - g.ymin, 64.0f);
+  float s1 = 1.0f;
+  while (s1 < 1048576.0f && s1 * 2.0f * range < 64.0f) s1 *= 2.0f;
+  // R[0] level 1, R[1..kMaxLevels-1] the k-chain, R[kRecs-2] scratch, R[kRecs-1] tile level
+  LevelRec* R = g.rec;
+  LevelRec* RS = R + (kRecs - 2);
+  LevelRec* RT = R + (kRecs - 1);
+
+  // Without top-k, top-p needs the row's normaliser: from stage 1, or (top_k
+  // asked for but inactive) from an exact pass.
+  unsigned long long S_all = 0;
+  if (p_on && !k_on) {
+    if (g.want_s) {
+      S_all = static_cast<unsigned long long>(static_cast<double>(g.s_all) * static_cast<double>(kFixedScale));
+    } else {
+      using V = Vec<DT>;
+      unsigned long long mine = 0;
+      const float lo_y = m - kMassCutoff - 1.0f - fabsf(m) * 1e-6f;
+      const int nvec = (g.n + V::kPer - 1) / V::kPer;
+      const uint4* data = reinterpret_cast<const uint4*>(g.data);
+      for (int v = threadIdx.x; v < nvec; v += kThreads) {
+        if (vec_bound(v) < lo_y) continue;
+        float z[V::kPer];
+        V::unpack(data[v], z);
+#pragma unroll
+        for (int e = 0; e < V::kPer; ++e) {
+          const float y = __fmul_rn(z[e], g.inv_t);
+          if (y != neg_inf()) mine += fixed_mass(y, m);
+        }
+      }
+      for (int s = threadIdx.x; s < kHashCap; s += kThreads)
+        if (g.hkey[s] >= 0 && g.hval[s] != neg_inf()) mine += fixed_mass(g.hval[s], m);
+      reduce_fold(3, neg_inf(), kNoCut, 0, 0, mine, pos_inf(), neg_inf(), 0.0f, neg_inf(), 0);
+      S_all = g.fold.mass;
+    }
+  }
+  const unsigned long long T_all = mass_target(g.top_p, S_all);
+
+  // Tile level (two-stage selection): the vector maxima bound the cut from
+  // below, so the token histogram only needs the vectors above that bound.
+  float lo1 = bucket_floor(m, 63.0f, s1);
+  hist_pass<DT>(1, s1, 0.0f, p_on && !k_on, 0.0f, step++, RT);
+  locate(RT, !k_on, k_on ? static_cast<unsigned long long>(g.top_k) : T_all, 0, 0);
+  if (g.loc.found) lo1 = fmaxf(lo1, bucket_floor(m, static_cast<float>(g.loc.bucket), s1));
+  hist_pass<DT>(0, s1, 0.0f, p_on, lo1, step++, R);
+
+  // ---- top-k: the k-th token of the order
+  unsigned long long S_k = 0;
+  int kchain_levels = 0;
+  unsigned long long* klist = nullptr;
+  unsigned long long* kpre = reinterpret_cast<unsigned long long*>(g.work) + 2 * kListCap;
+  int k_pos = -1;
+  if (k_on) {
+    const unsigned long long target = static_cast<unsigned long long>(g.top_k);
+    locate(R, 0, target, 0, 0);
+    const Loc l = g.loc;
+    if (!l.found) {
+      fallback = true;
+    } else {
+      int level = 1;
+      float scale = s1, abs = static_cast<float>(l.bucket);
+      uint32_t above_c = l.cnt_before, n_in = R[0].cnt[l.bucket];
+      unsigned long long above_m = l.mass_before;
+      if (threadIdx.x == 0) g.kabs[0] = abs;
+      while (n_in > static_cast<uint32_t>(kListCap)) {
+        if (level >= kMaxLevels) {
+          fallback = true;
+          break;
+        }
+        const float sub = scale * static_cast<float>(kBuckets);
+        hist_pass<DT>(0, sub, abs * static_cast<float>(kBuckets), p_on, bucket_floor(m, abs, scale), step++, R + level);
+        locate(R + level, 0, target, above_c, above_m);
+        const Loc ll = g.loc;
+        if (!ll.found) {
+          fallback = true;
+          break;
+        }
+        above_c += ll.cnt_before;
+        above_m += ll.mass_before;
+        n_in = R[level].cnt[ll.bucket];
+        abs = abs * static_cast<float>(kBuckets) + static_cast<float>(ll.bucket);
+        scale = sub;
+        if (threadIdx.x == 0) g.kabs[level] = abs;
+        ++level;
+      }
+      if (!fallback) {
+        kchain_levels = level;
+        const int par = step & 1;
+        gather_pass<DT>(scale, abs, bucket_floor(m, abs, scale), step++);
+        klist = reinterpret_cast<unsigned long long*>(g.work) + par * kListCap;
+        sort_and_scan(klist, static_cast<int>(n_in), kpre);
+        k_pos = g.top_k - static_cast<int>(above_c) - 1;
+        const unsigned long long e = klist[k_pos];
+        S_k = above_m + kpre[k_pos];
+        tighten(sort_key_order(e), sort_key_token(e), g.top_k);
+      }
+    }
+  }
+
+  // ---- top-p: where the mass of the (top-k) prefix reaches p
+  if (p_on && !fallback) {
+    const unsigned long long T = k_on ? mass_target(g.top_p, S_k) : T_all;
+    int level = 1;
+    const LevelRec* rec = R;
+    uint32_t above_c = 0;
+    unsigned long long above_m = 0;
+    float scale = s1, abs = 0.0f;
+    while (true) {
+      locate(rec, 1, T, above_c, above_m);
+      const Loc l = g.loc;
+      if (!l.found) {  // the target is not reached within the chain (rounding)
+        if (!k_on) fallback = true;
+        break;  // with top-k on, K stays the top-k prefix
+      }
+      abs = rec->base + static_cast<float>(l.bucket);
+      above_c += l.cnt_before;
+      above_m += l.mass_before;
+      if (k_on && level <= kchain_levels && abs == g.kabs[level - 1]) {
+        if (level < kchain_levels) {  // follow the k-chain one level down
+          rec = R + level;
+          scale *= static_cast<float>(kBuckets);
+          ++level;
+          continue;
+        }
+        // inside the gathered k bucket: exact, limited to the k-prefix
+        const int pos = first_reaching(kpre, k_pos, above_m, T);
+        const unsigned long long e = klist[pos];
+        tighten(sort_key_order(e), sort_key_token(e), static_cast<int32_t>(above_c) + pos + 1);
+        break;
+      }
+      // a bucket entirely above the k-cut (or no top-k): refine and gather it
+      uint32_t n_in = rec->cnt[l.bucket];
+      if (!refine<DT>(step, level, scale, abs, above_c, above_m, n_in, 1, T, RS)) {
+        fallback = true;
+        break;
+      }
+      const int par = step & 1;
+      gather_pass<DT>(scale, abs, bucket_floor(m, abs, scale), step++);
+      unsigned long long* plist = reinterpret_cast<unsigned long long*>(g.work) + par * kListCap;
+      sort_and_scan(plist, static_cast<int>(n_in), kpre);
+      const int pos = first_reaching(kpre, static_cast<int>(n_in) - 1, above_m, T);
+      const unsigned long long e = plist[pos];
+      tighten(sort_key_order(e), sort_key_token(e), static_cast<int32_t>(above_c) + pos + 1);
+      break;
+    }
+  }
+  __syncthreads();
+  if (fallback) fallback_cuts<DT>(k_on, p_on);
+}
+
+// Processed logit of token t if this CTA holds it (slice or patch table).
+template <int DT>
+__device__ __forceinline__ bool local_value(int32_t t, float& y) {
+  using V = Vec<DT>;
+  if (t < g.lo || t >= g.lo + g.n) return false;
+  uint32_t h = (static_cast<uint32_t>(t) * 2654435761u) >> kHashShift;
+  for (int probe = 0; probe < kHashCap; ++probe) {
+    const int32_t k = g.hkey[h];
+    if (k == t) {
+      y = g.hval[h];
+      return true;
+    }
+    if (k < 0) break;
+    h = (h + 1) & (kHashCap - 1);
+  }
+  const float z = V::load_smem(g.data, t - g.lo);  // -inf when excluded
+  y = g.greedy ? z : __fmul_rn(z, g.inv_t);
+  return true;
+}
+
+__device__ __forceinline__ bool in_kept(int32_t t, float y, float m, int mp_on, float min_p) {
+  if (g.cut_on) {
+    const uint32_t key = order_key(y);
+    if (!(key > g.cut_key || (key == g.cut_key && t <= g.cut_idx))) return false;
+  }
+  if (mp_on && !(__expf(y - m) >= min_p)) return false;
+  return true;
+}
+
+// The draw: Gumbel-max over K (stream 0).  Also counts |K| and, for a
+// verification position, its fixed-point mass; result in g.fold.
+template <int DT>
+__device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, int spec_pos, uint64_t seed) {
+  using V = Vec<DT>;
+  const float m = g.m, min_p = g.min_p, inv_t = g.inv_t;
+  const uint32_t rowid = static_cast<uint32_t>(g.req), pos = g.pos;
+  const int32_t arg = g.arg;
+  // the argmax token is always in K: its score seeds the running best
+  const float g0 = gumbel_from_numerator(uniform_numerator(philox_word(seed, rowid, pos, arg, 0)));
+  float bv = __fadd_rn(m, g0);
+  int32_t bi = arg;
+  int32_t kcount = 0;
+  unsigned long long kmass = 0;
+  auto element = [&](int32_t t, float y) {
+    if (!in_kept(t, y, m, mp_on, min_p)) return;
+    ++kcount;
+    if (spec_pos) kmass += fixed_mass(y, m);
+    const float slack = 1e-3f + fabsf(y) * 1e-6f;
+    if (y + kGumbelMax + slack < bv) return;
+    const uint32_t num = uniform_numerator(philox_word(seed, rowid, pos, static_cast<uint32_t>(t), 0));
+    if (y + gumbel_upper_bound(num) + slack < bv) return;
+    const float s = __fadd_rn(y, gumbel_from_numerator(num));
+    if (beats(s, t, bv, bi)) {
+      bv = s;
+      bi = t;
+    }
+  };
+  const int nvec = (g.n + V::kPer - 1) / V::kPer;
+  const uint4* data = reinterpret_cast<const uint4*>(g.data);
+  const int lo = g.lo;
+  const uint32_t key0 = static_cast<uint32_t>(seed), key1 = static_cast<uint32_t>(seed >> 32);
+  constexpr int kGroups = V::kPer / 4;  // Philox blocks per vector: 4 tokens share one block
+  for (int v = threadIdx.x; v < nvec; v += kThreads) {
+    const float ub = vec_bound(v);
+    if (ub < k_lo) continue;
+    // plain rows need no mass: a vector that cannot beat the best is skipped
+    if (prune_best && ub + kGumbelMax + 1e-3f + fabsf(ub) * 1e-6f < bv) continue;
+    float z[V::kPer];
+    V::unpack(data[v], z);
+    const int32_t t0 = lo + v * V::kPer;  // a multiple of 4
+    uint32_t cand = 0;  // members that may still beat the running best
+#pragma unroll
+    for (int e = 0; e < V::kPer; ++e) {
+      const float y = __fmul_rn(z[e], inv_t);
+      z[e] = y;
+      if (y == neg_inf() || !in_kept(t0 + e, y, m, mp_on, min_p)) continue;
+      ++kcount;
+      if (spec_pos) kmass += fixed_mass(y, m);
+      if (!(y + kGumbelMax + 1e-3f + fabsf(y) * 1e-6f < bv)) cand |= 1u << e;
+    }
+    if (!cand) continue;
+    uint32_t w[V::kPer];
+#pragma unroll
+    for (int q = 0; q < kGroups; ++q) {  // independent blocks: their rounds interleave
+      const Philox4 r = philox4x32_10(static_cast<uint32_t>(t0 >> 2) + q, pos, rowid, 0u, key0, key1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[q * 4 + i] = r.w[i];
+    }
+#pragma unroll
+    for (int e = 0; e < V::kPer; ++e) {
+      if (!((cand >> e) & 1u)) continue;
+      const float y = z[e];
+      const float slack = 1e-3f + fabsf(y) * 1e-6f;
+      const uint32_t num = uniform_numerator(w[e]);
+      if (y + gumbel_upper_bound(num) + slack < bv) continue;
+      const float s = __fadd_rn(y, gumbel_from_numerator(num));
+      if (beats(s, t0 + e, bv, bi)) {
+        bv = s;
+        bi = t0 + e;
+      }
+    }
+  }
+  for (int s = threadIdx.x; s < kHashCap; s += kThreads) {
+    const int32_t t = g.hkey[s];
+    const float y = g.hval[s];
+    if (t >= 0 && y != neg_inf() && y >= k_lo) element(t, y);
+  }
+  // the draft token's processed logit, from the CTA that holds it
+  float xy = neg_inf();
+  int32_t xhere = 0;
+  if (spec_pos && threadIdx.x == 0) xhere = local_value<DT>(g.x, xy) ? 1 : 0;
+  reduce_fold(1, bv, bi, kcount, 0, kmass, pos_inf(), neg_inf(), 0.0f, xy, xhere);
+}
+
+// Residual max(P - q, 0) at a rejected position: argmax of log r + g over K
+// (stream 2); result in g.fold (arg kNoCut when no token has P > q).
+template <int DT>
+__device__ __noinline__ void residual_pass(int mp_on, float memb_lo, float inv_s, float log_s, const float* qrow,
+                                           uint64_t seed) {
+  using V = Vec<DT>;
+  const float m = g.m, min_p = g.min_p, inv_t = g.inv_t;
+  const uint32_t rowid = static_cast<uint32_t>(g.req), pos = g.pos;
+  float bv = neg_inf();
+  int32_t bi = kNoCut;
+  auto relem = [&](int32_t t, float y) {
+    if (!in_kept(t, y, m, mp_on, min_p)) return;
+    // log r <= log P = y - m - log S
+    if (y - m - log_s + kGumbelMax + 1e-3f + fabsf(y) * 1e-6f < bv) return;
+    const float P = __fmul_rn(__expf(y - m), inv_s);
+    const float r = __fsub_rn(P, qrow[t]);
+    if (!(r > 0.0f)) return;
+    const uint32_t num = uniform_numerator(philox_word(seed, rowid, pos, static_cast<uint32_t>(t), 2));
+    const float s = __fadd_rn(logf(r), gumbel_from_numerator(num));
+    if (beats(s, t, bv, bi)) {
+      bv = s;
+      bi = t;
+    }
+  };
+  const int nvec = (g.n + V::kPer - 1) / V::kPer;
+  const uint4* data = reinterpret_cast<const uint4*>(g.data);
+  const int lo = g.lo;
+  for (int v = threadIdx.x; v < nvec; v += kThreads) {
+    const float ub = vec_bound(v);
+    if (ub < memb_lo) continue;
+    if (ub - m - log_s + kGumbelMax + 1e-3f + fabsf(ub) * 1e-6f < bv) continue;
+    float z[V::kPer];
+    V::unpack(data[v], z);
+#pragma unroll
+    for (int e = 0; e < V::kPer; ++e) {
+      const float y = __fmul_rn(z[e], inv_t);
+      if (y != neg_inf()) relem(lo + v * V::kPer + e, y);
+    }
+  }
+  for (int s = threadIdx.x; s < kHashCap; s += kThreads) {
+    const int32_t t = g.hkey[s];
+    const float y = g.hval[s];
+    if (t >= 0 && y != neg_inf()) relem(t, y);
+  }
+  reduce_fold(2, bv, bi, 0, 0, 0, pos_inf(), neg_inf(), 0.0f, neg_inf(), 0);
+}
 // ------------------------------------------------------------- kernel --
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   using V = Vec<DT>;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
   cg::cluster_group cl = cg::this_cluster();
   const int rank = static_cast<int>(cl.block_rank());
   const int ncta = static_cast<int>(cl.num_blocks());
   const int task = static_cast<int>(blockIdx.x) / ncta;
   const Layout& L = a.L;
-  Smem sm = carve(smem_raw, L);
-  Ctl& c = *sm.ctl;
+  Ctx& c = g;
   const int tid = threadIdx.x;
   const int V_ = a.vocab;
 
   // ---------------------------------------------------------------- setup
   if (tid == 0) {
+    uint8_t* base = smem_raw;
+    c.data = base;
+    c.vmax = reinterpret_cast<__nv_bfloat16*>(base + L.vmax_off);
+    c.xm = reinterpret_cast<uint32_t*>(base + L.xm_off);
+    c.hkey = reinterpret_cast<int32_t*>(base + L.hk_off);
+    c.hcnt = reinterpret_cast<int32_t*>(base + L.hc_off);
+    c.hval = reinterpret_cast<float*>(base + L.hv_off);
+    c.work = base + L.work_off;
+    const int per = ncta * kBuckets;
+    c.rh_mass[0] = reinterpret_cast<unsigned long long*>(base + L.rh_off);
+    c.rh_mass[1] = c.rh_mass[0] + per;
+    c.rh_cnt[0] = reinterpret_cast<uint32_t*>(base + L.rh_off + 2 * per * 8);
+    c.rh_cnt[1] = c.rh_cnt[0] + per;
+    c.rec = reinterpret_cast<LevelRec*>(base + L.rec_off);
+    c.red = base + L.red_off;
+    c.part = reinterpret_cast<Part*>(base + L.part_off);
+    c.mbar = reinterpret_cast<uint64_t*>(base + L.mbar_off);
+    c.ncta = ncta;
+    c.rank = rank;
     int32_t status = SS_ROW_OK;
     int32_t req = task, j = 0, k = 0, d0 = 0, row = task, x = -1, drow = -1;
     bool live = true;
@@ -612,15 +1426,17 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
       status = SS_ROW_BAD_PARAM;
     c.status = status;
     c.lo = rank * L.slice_len;
+    // A row with invalid parameters (including a bad draft count, which makes
+    // its row index meaningless) touches no logits: it only reports its status.
     c.n = (status == SS_ROW_BAD_PARAM) ? 0 : max(0, min(V_ - c.lo, L.slice_len));
+    c.cursor[0] = 0;
+    c.cursor[1] = 0;
+    c.want_s = (T > 0.0f && c.top_p < 1.0f && c.top_k <= 0) ? 1 : 0;
   }
   __syncthreads();
   if (c.row < 0) return;  // whole cluster: no such target position
 
-  // A row with invalid parameters (including a bad draft count, which makes
-  // its row index meaningless) touches no logits: it only reports its status.
-  const bool touch = (c.status != SS_ROW_BAD_PARAM);
-  const int lo = c.lo, n = touch ? c.n : 0;
+  const int lo = c.lo, n = c.n;
   const char* row_ptr = reinterpret_cast<const char*>(a.logits) + static_cast<int64_t>(c.row) * a.row_stride * V::kBytes;
   const uint32_t slice_bytes = static_cast<uint32_t>(n) * V::kBytes;
   // Bulk (TMA) copies need a 16-byte aligned source; a row whose byte stride
@@ -632,23 +1448,23 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
 
   // Issue the slice's bulk copies first so that HBM traffic starts at once.
   if (tid == 0) {
-    for (int ch = 0; ch < nchunks; ++ch) mbar_init(sm.mbar + ch, 1);
+    for (int ch = 0; ch < nchunks; ++ch) mbar_init(c.mbar + ch, 1);
     fence_barrier_init();
     const char* src = row_ptr + static_cast<int64_t>(lo) * V::kBytes;
     for (int ch = 0; ch < nchunks; ++ch) {
       const uint32_t off = static_cast<uint32_t>(ch) * kChunkBytes;
       const uint32_t bytes = min(kChunkBytes, bulk_bytes - off);
-      mbar_arrive_expect_tx(sm.mbar + ch, bytes);
-      bulk_load(sm.data + off, src + off, bytes, sm.mbar + ch);
+      mbar_arrive_expect_tx(c.mbar + ch, bytes);
+      bulk_load(c.data + off, src + off, bytes, c.mbar + ch);
     }
   }
   // The rest (a ragged tail < 16 bytes, or the whole slice when unaligned)
   // with plain loads.
   for (int e = static_cast<int>(bulk_bytes / V::kBytes) + tid; e < n; e += kThreads) {
     if (V::kBytes == 4)
-      reinterpret_cast<uint32_t*>(sm.data)[e] = reinterpret_cast<const uint32_t*>(row_ptr)[lo + e];
+      reinterpret_cast<uint32_t*>(c.data)[e] = reinterpret_cast<const uint32_t*>(row_ptr)[lo + e];
     else
-      reinterpret_cast<uint16_t*>(sm.data)[e] = reinterpret_cast<const uint16_t*>(row_ptr)[lo + e];
+      reinterpret_cast<uint16_t*>(c.data)[e] = reinterpret_cast<const uint16_t*>(row_ptr)[lo + e];
   }
 
   // Exclusion bitmap: grammar mask (inverted) and the tail beyond the slice.
@@ -662,12 +1478,12 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
         ex = ~static_cast<uint32_t>(a.p.bitmask[static_cast<int64_t>(c.req) * a.p.bitmask_stride + (lo >> 5) + w]);
       if (first + 32 > n) ex |= 0xffffffffu << (n - first);
     }
-    sm.xm[w] = ex;
+    c.xm[w] = ex;
   }
   for (int s = tid; s < kHashCap; s += kThreads) {
-    sm.hkey[s] = -1;
-    sm.hcnt[s] = 0;
-    sm.hval[s] = 0.0f;
+    c.hkey[s] = -1;
+    c.hcnt[s] = 0;
+    c.hval[s] = 0.0f;
   }
   __syncthreads();
 
@@ -676,7 +1492,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   auto insert = [&](int32_t t) -> int {
     uint32_t h = (static_cast<uint32_t>(t) * 2654435761u) >> kHashShift;
     for (int probe = 0; probe < kHashCap; ++probe) {
-      const int32_t prev = atomicCAS(sm.hkey + h, -1, t);
+      const int32_t prev = atomicCAS(c.hkey + h, -1, t);
       if (prev == -1 || prev == t) return static_cast<int>(h);
       h = (h + 1) & (kHashCap - 1);
     }
@@ -694,7 +1510,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
       if (s < 0)
         st_local = max(st_local, SS_ROW_LIMIT);
       else
-        atomicAdd(sm.hcnt + s, 1);
+        atomicAdd(c.hcnt + s, 1);
     }
     if (a.mode == kModeVerify) {
       for (int e = tid; e < c.k; e += kThreads) {  // every draft must be a token id
@@ -708,7 +1524,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
         if (s < 0)
           st_local = max(st_local, SS_ROW_LIMIT);
         else
-          atomicAdd(sm.hcnt + s, 1);
+          atomicAdd(c.hcnt + s, 1);
       }
     }
     for (int e = c.b0 + tid; e < c.b1; e += kThreads) {
@@ -725,118 +1541,176 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
         st_local = max(st_local, SS_ROW_LIMIT);
         continue;
       }
-      if (atomicOr(sm.hcnt + s, kBiasFlag) & kBiasFlag) st_local = max(st_local, SS_ROW_BAD_INDEX);  // duplicate
-      sm.hval[s] = b;
+      if (atomicOr(c.hcnt + s, kBiasFlag) & kBiasFlag) st_local = max(st_local, SS_ROW_BAD_INDEX);  // duplicate
+      c.hval[s] = b;
     }
   }
   __syncthreads();
   // Processed values of patched tokens (read straight from the global row).
   for (int s = tid; s < kHashCap; s += kThreads) {
-    const int32_t t = sm.hkey[s];
+    const int32_t t = c.hkey[s];
     if (t < 0) continue;
-    atomicOr(sm.xm + ((t - lo) >> 5), 1u << ((t - lo) & 31));
+    atomicOr(c.xm + ((t - lo) >> 5), 1u << ((t - lo) & 31));
     float z = V::load_global(row_ptr, t);
-    const int32_t hc = sm.hcnt[s];
+    const int32_t hc = c.hcnt[s];
     const int32_t cnt = hc & ~kBiasFlag;
     if (cnt > 0) {
       z = (z > 0.0f) ? __fdiv_rn(z, c.rep) : __fmul_rn(z, c.rep);
       z = __fsub_rn(z, __fmul_rn(c.freq, static_cast<float>(cnt)));
       z = __fsub_rn(z, c.pres);
     }
-    if (hc & kBiasFlag) z = __fadd_rn(z, sm.hval[s]);
+    if (hc & kBiasFlag) z = __fadd_rn(z, c.hval[s]);
     if (c.use_mask) {
       const uint32_t word = static_cast<uint32_t>(a.p.bitmask[static_cast<int64_t>(c.req) * a.p.bitmask_stride + (t >> 5)]);
       if (((word >> (t & 31)) & 1u) == 0u) z = neg_inf();
     }
-    sm.hval[s] = c.greedy ? z : __fmul_rn(z, c.inv_t);
+    c.hval[s] = c.greedy ? z : __fmul_rn(z, c.inv_t);
   }
 
   // --------------------------------------------------------------- stage 1
-  // Wait for each chunk, write -inf over excluded lanes, and accumulate the
-  // row max (lowest index on ties), the allowed count and non-finite flags.
-  BlockAcc acc;
-  acc.am = ArgMax{neg_inf(), kNoCut};
-  acc.count = 0;
-  acc.status = st_local;
-  acc.mass = 0;
+  // Wait for each chunk, write -inf over excluded lanes, store each vector's
+  // bound, and accumulate the row max (lowest index on ties), the smallest
+  // allowed value, the allowed count and non-finite flags.
+  float a_best = neg_inf(), a_ymin = pos_inf(), a_smax = neg_inf(), a_ssum = 0.0f;
+  int32_t a_arg = kNoCut, a_count = 0, a_status = st_local;
   bool timed_out = false;
   __syncthreads();  // exclusion bits of patched tokens are in place
   {
     const int nvec = (n + V::kPer - 1) / V::kPer;
     const int vec_per_chunk = static_cast<int>(kChunkBytes / 16);
-    uint4* data = reinterpret_cast<uint4*>(sm.data);
+    uint4* data = reinterpret_cast<uint4*>(c.data);
     float* dbg = (a.debug_processed && !c.bad_k) ? a.debug_processed + static_cast<int64_t>(c.row) * V_ : nullptr;
+    const bool greedy = c.greedy != 0;
+    const float inv_t = c.inv_t;
     int waited = -1;
-    for (int v = tid; v < nvec; v += kThreads) {
-      const int ch = min(v / vec_per_chunk, nchunks - 1);
+    float best_v = neg_inf();
+    int best_vec = -1;
+    const bool want_s = c.want_s != 0;
+    // Two vectors per iteration: both loads are issued before any arithmetic.
+    constexpr int kB = 2;
+    for (int v0 = tid; v0 < nvec; v0 += kB * kThreads) {
+      const int vlast = min(v0 + (kB - 1) * kThreads, nvec - 1);
+      const int ch = min(vlast / vec_per_chunk, nchunks - 1);
       if (nchunks > 0 && ch > waited) {
         for (int w = waited + 1; w <= ch; ++w)
-          if (!mbar_wait_bounded(sm.mbar + w, 0, kWaitPolls)) timed_out = true;
+          if (!mbar_wait_bounded(c.mbar + w, 0, kWaitPolls)) timed_out = true;
         waited = ch;
       }
-      const int e0 = v * V::kPer;
-      const uint32_t bits = (sm.xm[e0 >> 5] >> (e0 & 31)) & ((1u << V::kPer) - 1u);
-      uint4 raw = data[v];
-      if (bits) {
-        raw = V::exclude(raw, bits);
-        data[v] = raw;
-      }
-      float z[V::kPer];
-      V::unpack(raw, z);
+      uint4 raw[kB];
+      uint32_t bits[kB];
 #pragma unroll
-      for (int e = 0; e < V::kPer; ++e) {
-        const float y = c.greedy ? z[e] : __fmul_rn(z[e], c.inv_t);
-        const int32_t t = lo + e0 + e;
-        if (dbg && e0 + e < n) dbg[t] = y;
-        if (y == neg_inf()) continue;
-        acc.count += 1;
-        if (!(y < pos_inf())) acc.status = max(acc.status, SS_ROW_NONFINITE);
-        argmax_merge(acc.am, y, t);
+      for (int u = 0; u < kB; ++u) {
+        const int v = v0 + u * kThreads;
+        const int e0 = v * V::kPer;
+        if (v < nvec) {
+          raw[u] = data[v];
+          bits[u] = (c.xm[e0 >> 5] >> (e0 & 31)) & ((1u << V::kPer) - 1u);
+        } else {
+          raw[u] = V::exclude(make_uint4(0u, 0u, 0u, 0u), 0xffu);
+          bits[u] = 0;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int v = v0 + u * kThreads;
+        if (bits[u]) raw[u] = V::exclude(raw[u], bits[u]);
+        float z[V::kPer];
+        V::unpack(raw[u], z);
+        float vmax = neg_inf(), vmin = pos_inf();
+        int allowed = 0;
+#pragma unroll
+        for (int e = 0; e < V::kPer; ++e) {
+          const float y = greedy ? z[e] : __fmul_rn(z[e], inv_t);
+          vmax = max_nan(vmax, y);
+          const bool ok = (y != neg_inf());
+          allowed += ok ? 1 : 0;
+          vmin = fminf(vmin, ok ? y : pos_inf());
+        }
+        if (want_s && allowed) {  // online softmax normaliser of the row
+          float part = 0.0f;
+#pragma unroll
+          for (int e = 0; e < V::kPer; ++e) {
+            const float y = __fmul_rn(z[e], inv_t);
+            if (y != neg_inf()) part = __fadd_rn(part, __expf(y - vmax));
+          }
+          softmax_merge(a_smax, a_ssum, vmax, part);
+        }
+        a_count += allowed;
+        a_ymin = fminf(a_ymin, vmin);
+        if (vmax != vmax || vmax == pos_inf()) a_status = max(a_status, SS_ROW_NONFINITE);
+        if (vmax > best_v) {
+          best_v = vmax;
+          best_vec = v;
+        }
+        if (v < nvec) {
+          if (bits[u]) data[v] = raw[u];
+          c.vmax[v] = bf16_round_up(vmax);
+        }
       }
     }
     // chunks no thread of this CTA touched still need their completion
     if (tid == 0)
       for (int w = waited + 1; w < nchunks; ++w)
-        if (!mbar_wait_bounded(sm.mbar + w, 0, kWaitPolls)) timed_out = true;
-    if (timed_out) acc.status = max(acc.status, SS_ROW_TIMEOUT);
+        if (!mbar_wait_bounded(c.mbar + w, 0, kWaitPolls)) timed_out = true;
+    if (timed_out) a_status = max(a_status, SS_ROW_TIMEOUT);
+    if (best_vec >= 0) {  // lowest index of the maximum inside the best vector
+      float z[V::kPer];
+      V::unpack(data[best_vec], z);
+#pragma unroll
+      for (int e = V::kPer - 1; e >= 0; --e) {
+        const float y = greedy ? z[e] : __fmul_rn(z[e], inv_t);
+        if (y == best_v) {
+          a_best = best_v;
+          a_arg = lo + best_vec * V::kPer + e;
+        }
+      }
+    }
+    if (dbg) {
+      __syncthreads();
+      for (int v = tid; v < nvec; v += kThreads) {
+        float z[V::kPer];
+        V::unpack(data[v], z);
+#pragma unroll
+        for (int e = 0; e < V::kPer; ++e)
+          if (v * V::kPer + e < n) dbg[lo + v * V::kPer + e] = greedy ? z[e] : __fmul_rn(z[e], inv_t);
+      }
+    }
     __syncthreads();  // debug writes of the raw slice precede the patched ones
     for (int s = tid; s < kHashCap; s += kThreads) {
-      const int32_t t = sm.hkey[s];
+      const int32_t t = c.hkey[s];
       if (t < 0) continue;
-      const float y = sm.hval[s];
+      const float y = c.hval[s];
       if (dbg) dbg[t] = y;
       if (y == neg_inf()) continue;
-      acc.count += 1;
-      if (!(y < pos_inf())) acc.status = max(acc.status, SS_ROW_NONFINITE);
-      argmax_merge(acc.am, y, t);
+      a_count += 1;
+      a_ymin = fminf(a_ymin, y);
+      if (!(y < pos_inf())) a_status = max(a_status, SS_ROW_NONFINITE);
+      if (beats(y, t, a_best, a_arg)) {
+        a_best = y;
+        a_arg = t;
+      }
+      if (want_s) softmax_merge(a_smax, a_ssum, y, 1.0f);
     }
   }
-  BlockAcc blk = block_reduce(sm, acc);
-  Part mine{};
-  mine.best = blk.am.v;
-  mine.arg = blk.am.i;
-  mine.count = blk.count;
-  mine.status = max(blk.status, c.status);
-  mine.x_in = -1;
-  mine.xw = -1.0f;
-  mine.score = neg_inf();
-  Part all = cluster_fold(sm, 0, mine);
+  reduce_fold(0, a_best, a_arg, a_count, max(a_status, c.status), 0, a_ymin, a_smax, a_ssum, neg_inf(), 0);
+  const Part all = g.fold;
   int32_t status = all.status;
   if (status == SS_ROW_OK && all.count == 0) status = SS_ROW_EMPTY_SET;
   const float m = all.best;
   const int32_t argmax_tok = all.arg;
   if (tid == 0) {
     c.m = m;
+    c.ymin = all.ymin;
     c.arg = argmax_tok;
     c.count = all.count;
+    c.s_all = (all.smax == neg_inf()) ? 0.0f : __fmul_rn(all.ssum, __expf(all.smax - m));
   }
   __syncthreads();
 
   int32_t token = -1, kept = 0, accept = 0;
   if (status == SS_ROW_OK) {
     const bool spec_pos = (a.mode == kModeVerify) && (c.j < c.k);
-    const uint32_t seed_lo = c.seed_lo, seed_hi = c.seed_hi;
-    const uint64_t seed = (static_cast<uint64_t>(seed_hi) << 32) | seed_lo;
+    const uint64_t seed = (static_cast<uint64_t>(c.seed_hi) << 32) | c.seed_lo;
     const uint32_t rowid = static_cast<uint32_t>(c.req);
     if (c.greedy) {
       kept = 1;
@@ -850,168 +1724,51 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
       }
     } else {
       // ------------------------------------------------------ the cuts
-      int pass = 0;
       const bool k_on = c.top_k > 0 && c.top_k < c.count;
       const bool p_on = c.top_p < 1.0f;
       const bool mp_on = c.min_p > 0.0f;
-      bool has_cut = false;
-      uint32_t cut_key = 0;
-      int32_t cut_idx = kNoCut;
-      uint32_t k_key = 0;
-      int32_t k_idx = kNoCut;
-      auto ykey = [](int32_t, float y) { return order_key(y); };
-      auto all_ok = [](int32_t, float) { return true; };
-      if (k_on) {
-        SelOut s = radix_select<DT, true>(sm, c, pass, false, static_cast<double>(c.top_k), 0.0, ykey, all_ok);
-        const uint32_t ntie = static_cast<uint32_t>(c.top_k) - s.cnt_gt;
-        int32_t idx = kNoCut;
-        if (ntie < s.cnt_eq) {
-          const uint32_t kk = s.key;
-          SelOut ti = radix_select<DT, false>(
-              sm, c, pass, false, static_cast<double>(ntie), 0.0,
-              [](int32_t t, float) { return ~static_cast<uint32_t>(t); },
-              [kk](int32_t, float y) { return order_key(y) == kk; });
-          idx = static_cast<int32_t>(~ti.key);
-        }
-        k_key = s.key;
-        k_idx = idx;
-        has_cut = true;
-        cut_key = k_key;
-        cut_idx = k_idx;
+      if (k_on || p_on) {
+        resolve_cuts<DT>(k_on, p_on);
+      } else if (tid == 0) {
+        c.cut_on = 0;
+        c.cut_key = 0;
+        c.cut_idx = kNoCut;
+        c.cut_len = -1;
       }
-      if (p_on) {
-        const uint32_t kk = k_key;
-        const int32_t ki = k_idx;
-        auto in_topk = [k_on, kk, ki](int32_t t, float y) {
-          if (!k_on) return true;
-          const uint32_t key = order_key(y);
-          return key > kk || (key == kk && t <= ki);
-        };
-        SelOut s = radix_select<DT, true>(sm, c, pass, true, 0.0, static_cast<double>(c.top_p), ykey, in_topk);
-        const double target = static_cast<double>(c.top_p) * static_cast<double>(s.total);
-        uint32_t ntie = s.cnt_eq;
-        if (s.reached && s.cnt_eq > 0) {
-          const unsigned long long w = s.mass_eq / s.cnt_eq;
-          if (w > 0) {
-            const double need = target - static_cast<double>(s.mass_gt);
-            double nt = ceil(need / static_cast<double>(w));
-            if (nt < 1.0) nt = 1.0;
-            if (nt < static_cast<double>(s.cnt_eq)) ntie = static_cast<uint32_t>(nt);
-          }
-        }
-        int32_t idx = kNoCut;
-        if (ntie < s.cnt_eq) {
-          const uint32_t pk = s.key;
-          SelOut ti = radix_select<DT, false>(
-              sm, c, pass, false, static_cast<double>(ntie), 0.0,
-              [](int32_t t, float) { return ~static_cast<uint32_t>(t); },
-              [pk, in_topk](int32_t t, float y) { return order_key(y) == pk && in_topk(t, y); });
-          idx = static_cast<int32_t>(~ti.key);
-        }
-        if (!has_cut || s.key > cut_key || (s.key == cut_key && idx < cut_idx)) {
-          cut_key = s.key;
-          cut_idx = idx;
-        }
-        has_cut = true;
-      }
+      __syncthreads();
+      const bool cut_on = c.cut_on != 0;
+      const int32_t cut_len = c.cut_len;
 
       // ------------------------------------------------------ the draw
       const float min_p = c.min_p;
-      auto in_K = [=](int32_t t, float y) {
-        if (has_cut) {
-          const uint32_t key = order_key(y);
-          if (!(key > cut_key || (key == cut_key && t <= cut_idx))) return false;
-        }
-        if (mp_on && !(__expf(y - m) >= min_p)) return false;
-        return true;
-      };
-      // the argmax token is always in K: its score seeds the running best
-      const float g0 = gumbel_from_numerator(uniform_numerator(philox_word(seed, rowid, c.pos, argmax_tok, 0)));
-      ArgMax best{__fadd_rn(m, g0), argmax_tok};
-      int32_t kcount = 0;
-      unsigned long long kmass = 0;
-      int32_t x_in = -1;
-      float xw = -1.0f;
-      const int32_t x = c.x;
-      visit<DT>(sm, c, [&](int32_t t, float y) {
-        if (t == x) {
-          x_in = in_K(t, y) ? 1 : 0;
-          xw = __expf(y - m);
-        }
-        if (!in_K(t, y)) return;
-        ++kcount;
-        kmass += fixed_mass(y, m);
-        const float slack = 1e-3f + fabsf(y) * 1e-6f;
-        if (y + kGumbelMax + slack < best.v) return;
-        const uint32_t num = uniform_numerator(philox_word(seed, rowid, c.pos, static_cast<uint32_t>(t), 0));
-        if (y + gumbel_upper_bound(num) + slack < best.v) return;
-        const float s = __fadd_rn(y, gumbel_from_numerator(num));
-        argmax_merge(best, s, t);
-      });
-      BlockAcc d;
-      d.am = best;
-      d.count = kcount;
-      d.status = 0;
-      d.mass = kmass;
-      // fold x info through the partial: per-block pick any thread holding x
-      __shared__ float s_xw;
-      __shared__ int s_xin;
-      if (tid == 0) {
-        s_xw = -1.0f;
-        s_xin = -1;
-      }
-      __syncthreads();
-      if (x_in >= 0) {
-        s_xw = xw;
-        s_xin = x_in;
-      }
-      BlockAcc db = block_reduce(sm, d);
-      Part pd{};
-      pd.best = db.am.v;
-      pd.arg = db.am.i;
-      pd.count = db.count;
-      pd.status = 0;
-      pd.mass = db.mass;
-      pd.xw = s_xw;
-      pd.x_in = s_xin;
-      pd.score = db.am.v;
-      Part dall = cluster_fold(sm, 1, pd);
-      kept = dall.count;
+      // |K| is known unless min-p or the fallback selection decided it
+      const bool need_count = mp_on || (cut_on && cut_len < 0);
+      // lowest logit a member can have: vectors below it hold no member
+      float k_lo = cut_on ? key_value(c.cut_key) : neg_inf();
+      if (mp_on) k_lo = fmaxf(k_lo, m + logf(min_p) - 1e-3f * (1.0f + fabsf(m)));
+      const float memb_lo = k_lo;
+      // the mass S_K needed by a verification position ignores tokens whose
+      // fixed-point mass is zero
+      if (spec_pos && !need_count) k_lo = fmaxf(k_lo, m - kMassCutoff - 1.0f - fabsf(m) * 1e-6f);
+      draw_pass<DT>(mp_on, k_lo, !spec_pos && !need_count, spec_pos, seed);
+      const Part dall = g.fold;
+      kept = need_count ? dall.count : (cut_on ? cut_len : c.count);
       token = dall.arg;
       if (spec_pos) {
+        const float yx = dall.xhere ? dall.xy : neg_inf();
+        const bool x_in = (yx != neg_inf()) && in_kept(c.x, yx, m, mp_on, min_p);
         const float SK = static_cast<float>(static_cast<double>(dall.mass) * kFixedInv);
         const float inv_s = __fdiv_rn(1.0f, SK);
-        const float Px = (dall.x_in == 1) ? __fmul_rn(dall.xw, inv_s) : 0.0f;
-        const float q = a.draft_probs[static_cast<int64_t>(c.drow) * a.draft_stride + x];
+        const float Px = x_in ? __fmul_rn(__expf(yx - m), inv_s) : 0.0f;
+        const float q = a.draft_probs[static_cast<int64_t>(c.drow) * a.draft_stride + c.x];
         const float u = uniform_from_numerator(uniform_numerator(philox_word(seed, rowid, c.pos, 0, 1)));
         accept = (__fmul_rn(u, q) < Px) ? 1 : 0;
         if (accept) {
-          token = x;
+          token = c.x;
         } else {
-          // residual max(P - q, 0): argmax of log r + g over K (stream 2)
           const float* qrow = a.draft_probs + static_cast<int64_t>(c.drow) * a.draft_stride;
-          ArgMax rb{neg_inf(), kNoCut};
-          visit<DT>(sm, c, [&](int32_t t, float y) {
-            if (!in_K(t, y)) return;
-            const float P = __fmul_rn(__expf(y - m), inv_s);
-            const float r = __fsub_rn(P, qrow[t]);
-            if (!(r > 0.0f)) return;
-            const uint32_t num = uniform_numerator(philox_word(seed, rowid, c.pos, static_cast<uint32_t>(t), 2));
-            const float s = __fadd_rn(logf(r), gumbel_from_numerator(num));
-            argmax_merge(rb, s, t);
-          });
-          BlockAcc rbk;
-          rbk.am = rb;
-          rbk.count = 0;
-          rbk.status = 0;
-          rbk.mass = 0;
-          BlockAcc rr = block_reduce(sm, rbk);
-          Part pr{};
-          pr.best = rr.am.v;
-          pr.arg = rr.am.i;
-          pr.x_in = -1;
-          pr.xw = -1.0f;
-          Part rall = cluster_fold(sm, 2, pr);
+          residual_pass<DT>(mp_on, memb_lo, inv_s, logf(SK), qrow, seed);
+          const Part rall = g.fold;
           if (rall.arg != kNoCut && rall.best > neg_inf()) token = rall.arg;
           // else: no token with P > q (rounding): keep the stream-0 draw
         }
@@ -1069,7 +1826,8 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
       }
     }
   }
-  // No CTA may leave while another can still read its shared memory.
+  // The fallback selection reads other CTAs' shared memory; no CTA may leave
+  // while that can still happen.
   cl.sync();
 }
 
@@ -1098,15 +1856,17 @@ static Layout make_layout(int32_t vocab, int32_t es, int cs) {
     off += bytes;
     return at;
   };
+  const int64_t nvec = L.slice_len / (16 / es);
+  L.vmax_off = take(nvec * 2, 16);
   L.xm_off = take(L.slice_len / 32 * 4, 16);
   L.hk_off = take(kHashCap * 4, 16);
   L.hc_off = take(kHashCap * 4, 16);
   L.hv_off = take(kHashCap * 4, 16);
-  L.hist_off = take(2 * 256 * 4 + 2 * 256 * 8, 16);
-  L.merge_off = take(256 * 4 + 256 * 8, 16);
-  L.red_off = take(kWarps * 32, 16);
-  L.part_off = take(kPartSlots * sizeof(Part), 16);
-  L.ctl_off = take(sizeof(Ctl), 16);
+  L.work_off = take(kWorkBytes, 16);
+  L.rh_off = take(2 * static_cast<int64_t>(cs) * kBuckets * 12, 16);
+  L.rec_off = take(kRecs * sizeof(LevelRec), 16);
+  L.red_off = take(kRedBytes, 16);
+  L.part_off = take(kPartSlots * static_cast<int64_t>(cs) * sizeof(Part), 16);
   L.mbar_off = take(kMaxChunks * 8, 16);
   L.total = static_cast<int32_t>((off + 127) / 128 * 128);
   return L;

@@ -39,8 +39,12 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
 // Odd 24-bit numerator n of u = n * 2^-24 in [2^-24, 1 - 2^-24].
 __device__ __forceinline__ uint32_t uniform_numerator(uint32_t x) { return ((x >> 9) << 1) | 1u; }
 
+// u = n * 2^-24, built from the bits: 1 + (n >> 1) * 2^-23 minus 1 is
+// (n - 1) * 2^-24 exactly, and adding 2^-24 is exact too (n < 2^24).  This
+// avoids the integer -> float conversion instruction, which sm_103 issues at
+// a small fraction of the add rate.
 __device__ __forceinline__ float uniform_from_numerator(uint32_t n) {
-  return __uint2float_rn(n) * 5.9604644775390625e-08f;  // exact: n < 2^24
+  return __fadd_rn(__fsub_rn(__uint_as_float(0x3f800000u | (n >> 1)), 1.0f), 5.9604644775390625e-08f);
 }
 
 // Gumbel noise -log(-log u) with the accurate single-precision logf.
@@ -53,7 +57,8 @@ __device__ __forceinline__ float gumbel_from_numerator(uint32_t n) {
 // g <= -log(1 - u) = ln2 * (24 - log2(2^24 - n)) <= ln2 * (clz(2^24 - n) - 7).
 __device__ __forceinline__ float gumbel_upper_bound(uint32_t n) {
   const uint32_t m = (1u << 24) - n;  // in [1, 2^24 - 1]
-  return 0.69314718f * static_cast<float>(__clz(m) - 7);
+  // clz(m) - 7 is in [1, 24]: converted with the 2^23 bit-pattern trick
+  return 0.69314718f * __fsub_rn(__uint_as_float(0x4b000000u + static_cast<uint32_t>(__clz(m) - 7)), 8388608.0f);
 }
 
 // Largest Gumbel value any token can get: -log(-log(1 - 2^-24)) = 16.6355...
