@@ -54,6 +54,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kHashCap = SS_MAX_PATCHED;
 constexpr int kHashShift = 32 - 10;  // log2(kHashCap) = 10
 static_assert(kHashCap == 1024, "hash shift assumes 1024 slots");
+static_assert(kHashCap % kThreads == 0, "patch-table loops run the same trip count in every thread");
 static_assert(kThreads >= 256, "histogram folding uses 4 threads per bucket");
 constexpr uint32_t kChunkBytes = 8192;
 constexpr int kMaxChunks = 20;
@@ -62,6 +63,12 @@ constexpr uint32_t kMaxSliceBytes = kMaxChunks * kChunkBytes;
 constexpr int kMaxCluster = 8;
 constexpr uint32_t kWaitPolls = 1u << 22;
 constexpr float kFixedScale = 1099511627776.0f;  // 2^40
+// A token's fixed-point mass (<= 2^40) is histogrammed as two 32-bit halves,
+// mass >> 20 and mass & (2^20 - 1).  Each copy of a bucket counter receives
+// the tokens of 16 threads, at most 16 * (ceil(kMaxSliceTokens / 8 / 256) * 8
+// + 1024 / 256) = 3904 of them, so neither half can wrap.
+constexpr int kMassSplit = 20;
+constexpr int kMaxSliceTokens = 61440;
 constexpr double kFixedInv = 1.0 / 1099511627776.0;
 constexpr int kBiasFlag = 1 << 30;
 constexpr int kNoCut = 0x7fffffff;
@@ -71,7 +78,8 @@ constexpr int kListCap = 512;  // tokens gathered for an exact resolution
 constexpr int kMaxLevels = 3;  // bucket refinement depth
 constexpr int kRecs = kMaxLevels + 2;  // level 1, k-chain, scratch, tile level
 constexpr float kMassCutoff = 28.5f;  // exp(-28.5) * 2^40 < 1: zero in fixed point
-constexpr uint32_t kWorkBytes = 12288;
+constexpr int kHistRows = 65;  // 64 buckets and a spill row
+constexpr uint32_t kWorkBytes = 3 * kHistRows * kCopies * 4;  // histograms / gathered lists / fallback buffers
 constexpr int kPartSlots = 4;  // stage 1, draw, residual, normaliser
 constexpr int kRedBytes = 1024;
 
@@ -357,37 +365,6 @@ __device__ __forceinline__ void softmax_merge(float& m1, float& s1, float m2, fl
   m1 = M;
 }
 
-__device__ __forceinline__ void part_merge(Part& a, const Part& b) {
-  if (beats(b.best, b.arg, a.best, a.arg)) {
-    a.best = b.best;
-    a.arg = b.arg;
-  }
-  a.count += b.count;
-  a.status = max(a.status, b.status);
-  a.mass += b.mass;
-  a.ymin = fminf(a.ymin, b.ymin);
-  softmax_merge(a.smax, a.ssum, b.smax, b.ssum);
-  if (b.xhere) {
-    a.xy = b.xy;
-    a.xhere = 1;
-  }
-}
-
-__device__ __forceinline__ Part part_shfl(const Part& p, int off) {
-  Part q;
-  q.best = __shfl_xor_sync(0xffffffffu, p.best, off);
-  q.arg = __shfl_xor_sync(0xffffffffu, p.arg, off);
-  q.count = __shfl_xor_sync(0xffffffffu, p.count, off);
-  q.status = __shfl_xor_sync(0xffffffffu, p.status, off);
-  q.mass = __shfl_xor_sync(0xffffffffu, p.mass, off);
-  q.ymin = __shfl_xor_sync(0xffffffffu, p.ymin, off);
-  q.xy = __shfl_xor_sync(0xffffffffu, p.xy, off);
-  q.xhere = __shfl_xor_sync(0xffffffffu, p.xhere, off);
-  q.smax = __shfl_xor_sync(0xffffffffu, p.smax, off);
-  q.ssum = __shfl_xor_sync(0xffffffffu, p.ssum, off);
-  return q;
-}
-
 __device__ __forceinline__ Part empty_part() {
   Part p{};
   p.best = neg_inf();
@@ -398,10 +375,41 @@ __device__ __forceinline__ Part empty_part() {
   return p;
 }
 
+// Combines the partials of the 32 lanes; every lane ends with the total.
+// Integer fields use the warp reduction instructions (order-free); floats are
+// compared through their order-preserving keys (-0 folded into +0 so that it
+// ties with +0, as in a float comparison); the softmax sums are rescaled to the
+// common max and added in an xor butterfly, which gives every lane the same
+// bits.  Deterministic for a given assignment of partials to lanes.
+__device__ __forceinline__ void warp_part_reduce(Part& p) {
+  constexpr uint32_t kAll = 0xffffffffu;
+  const uint32_t kb = order_key(p.best + 0.0f);
+  const uint32_t kmax = __reduce_max_sync(kAll, kb);
+  p.arg = static_cast<int32_t>(__reduce_min_sync(kAll, kb == kmax ? static_cast<uint32_t>(p.arg) : 0xffffffffu));
+  p.best = key_value(kmax);
+  p.count = static_cast<int32_t>(__reduce_add_sync(kAll, static_cast<uint32_t>(p.count)));
+  p.status = static_cast<int32_t>(__reduce_max_sync(kAll, static_cast<uint32_t>(p.status)));
+  p.ymin = key_value(__reduce_min_sync(kAll, order_key(p.ymin + 0.0f)));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) p.mass += __shfl_xor_sync(kAll, p.mass, off);
+  const float M = key_value(__reduce_max_sync(kAll, order_key(p.smax + 0.0f)));
+  float sum = (p.smax == neg_inf()) ? 0.0f : __fmul_rn(p.ssum, __expf(p.smax - M));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(kAll, sum, off));
+  p.smax = M;
+  p.ssum = sum;
+  const uint32_t holders = __ballot_sync(kAll, p.xhere != 0);
+  if (holders) {
+    p.xy = __shfl_sync(kAll, p.xy, __ffs(holders) - 1);
+    p.xhere = 1;
+  }
+}
+
 // Reduces every thread's partial over the block and then over the cluster:
-// each CTA writes its block total into slot `slot` of every CTA, one cluster
-// barrier, then each CTA folds the C totals in rank order.  The result lands
-// in g.fold (identical in every CTA).  Called by all threads.
+// warp totals go to shared memory, warp 0 combines them, its lanes write the
+// CTA total into slot `slot` of every CTA, one cluster barrier, and warp 0
+// combines the C totals.  The result lands in g.fold (identical in every CTA).
+// Called by all threads.
 __device__ __noinline__ void reduce_fold(int slot, float best, int32_t arg, int32_t count, int32_t status,
                                          unsigned long long mass, float ymin, float smax, float ssum, float xy,
                                          int32_t xhere) {
@@ -416,27 +424,24 @@ __device__ __noinline__ void reduce_fold(int slot, float best, int32_t arg, int3
   p.xhere = xhere;
   p.smax = smax;
   p.ssum = ssum;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) part_merge(p, part_shfl(p, off));
+  warp_part_reduce(p);
   Part* w = reinterpret_cast<Part*>(g.red);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  __syncthreads();
+  __syncthreads();  // the previous user of g.red is done
   if (lane == 0) w[wid] = p;
-  __syncthreads();
-  if (threadIdx.x == 0) {  // fixed order: deterministic
-    Part t = w[0];
-    for (int k = 1; k < kWarps; ++k) part_merge(t, w[k]);
-    w[kWarps] = t;
-  }
   __syncthreads();
   cg::cluster_group cl = cg::this_cluster();
   const int n = g.ncta;
-  if (threadIdx.x < n) *cl.map_shared_rank(g.part + slot * n + g.rank, threadIdx.x) = w[kWarps];
+  if (wid == 0) {
+    Part t = (lane < kWarps) ? w[lane] : empty_part();
+    warp_part_reduce(t);
+    if (lane < n) *cl.map_shared_rank(g.part + slot * n + g.rank, lane) = t;
+  }
   cl.sync();
-  if (threadIdx.x == 0) {
-    Part t = g.part[slot * n];
-    for (int c = 1; c < n; ++c) part_merge(t, g.part[slot * n + c]);
-    g.fold = t;
+  if (wid == 0) {
+    Part t = (lane < n) ? g.part[slot * n + lane] : empty_part();
+    warp_part_reduce(t);
+    if (lane == 0) g.fold = t;
   }
   __syncthreads();
 }
@@ -452,28 +457,31 @@ static_assert(kListCap % kThreads == 0, "list runs");
 __device__ __forceinline__ void push_merge(LevelRec* out, float scale, float base, int step) {
   cg::cluster_group cl = cg::this_cluster();
   const uint32_t* hc = reinterpret_cast<const uint32_t*>(g.work);
-  const unsigned long long* hm = reinterpret_cast<const unsigned long long*>(g.work + kBuckets * kCopies * 4);
+  const uint32_t* hmh = hc + kHistRows * kCopies;
+  const uint32_t* hml = hmh + kHistRows * kCopies;
   const int tid = threadIdx.x;
   const int par = step & 1;
   __syncthreads();
-  if (tid < kBuckets * 4) {  // 4 threads per bucket
+  if (tid < kBuckets * 4) {  // 4 threads per bucket, each folds 4 copies
     const int b = tid >> 2, q = tid & 3;
     uint32_t cnt = 0;
     unsigned long long mass = 0;
 #pragma unroll
     for (int i = 0; i < kCopies / 4; ++i) {
-      cnt += hc[b * kCopies + q * (kCopies / 4) + i];
-      mass += hm[b * kCopies + q * (kCopies / 4) + i];
+      const int k = b * kCopies + q * (kCopies / 4) + i;
+      cnt += hc[k];
+      mass += (static_cast<unsigned long long>(hmh[k]) << kMassSplit) + hml[k];
     }
     cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
     cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
     mass += __shfl_xor_sync(0xffffffffu, mass, 1);
     mass += __shfl_xor_sync(0xffffffffu, mass, 2);
-    if (q == 0)
-      for (int r = 0; r < g.ncta; ++r) {
-        *cl.map_shared_rank(g.rh_cnt[par] + g.rank * kBuckets + b, r) = cnt;
-        *cl.map_shared_rank(g.rh_mass[par] + g.rank * kBuckets + b, r) = mass;
-      }
+    // the 4 threads of a bucket hold its total: each writes it into every
+    // fourth CTA of the cluster
+    for (int r = q; r < g.ncta; r += 4) {
+      *cl.map_shared_rank(g.rh_cnt[par] + g.rank * kBuckets + b, r) = cnt;
+      *cl.map_shared_rank(g.rh_mass[par] + g.rank * kBuckets + b, r) = mass;
+    }
   }
   cl.sync();
   if (tid < kBuckets) {
@@ -493,67 +501,96 @@ __device__ __forceinline__ void push_merge(LevelRec* out, float scale, float bas
   __syncthreads();
 }
 
-// Histogram into `out`.  Token level (tile = 0): the tokens whose bucket at
-// `scale` lies in [base, base + 64), skipping vectors whose bound is below
-// lo_y.  Tile level (tile = 1, base 0): one entry per 16-byte vector valued at
-// a lower bound of its largest processed logit, one per patched token; k
-// entries at or above a bucket imply k tokens there, and their masses bound
-// the tokens' mass from below.
+// Histogram entry of y: counter row of its bucket when that lies in
+// [base, base + 64), else the spill row kBuckets, so that every entry issues
+// the same instructions (a per-entry branch around the atomics costs far more
+// than the spilled atomics).  y = -inf lands in the spill row.
+__device__ __forceinline__ int hist_slot(float m, float y, float scale, float base, int copy) {
+  const float b = bucket_of(m, y, scale) - base;
+  const bool in = (b >= 0.0f) && (b < static_cast<float>(kBuckets));
+  return small_int(in ? b : static_cast<float>(kBuckets)) * kCopies + copy;
+}
+
+// Counts, and with kMass the fixed-point masses split into a high and a low
+// half (32-bit shared atomics; the 64-bit ones are several times slower).
+template <bool kMass>
+__device__ __forceinline__ void hist_add(uint32_t* hc, float m, float y, float scale, float base, int copy) {
+  const int k = hist_slot(m, y, scale, base, copy);
+  atomicAdd(hc + k, 1u);
+  if (kMass) {
+    const unsigned long long f = fixed_mass(y, m);  // 0 for y = -inf
+    atomicAdd(hc + kHistRows * kCopies + k, static_cast<uint32_t>(f >> kMassSplit));
+    atomicAdd(hc + 2 * kHistRows * kCopies + k, static_cast<uint32_t>(f) & ((1u << kMassSplit) - 1u));
+  }
+}
+
+// Token level: every token of the vectors whose bound reaches lo_y, and the
+// patched tokens at or above lo_y.
+template <int DT, bool kMass>
+__device__ __forceinline__ void hist_tokens(uint32_t* hc, float scale, float base, float lo_y, int copy) {
+  using V = Vec<DT>;
+  const int nvec = (g.n + V::kPer - 1) / V::kPer;
+  const uint4* __restrict__ data = reinterpret_cast<const uint4*>(g.data);
+  const float m = g.m, inv_t = g.inv_t;
+  for (int v = threadIdx.x; v < nvec; v += kThreads) {
+    if (vec_bound(v) < lo_y) continue;
+    float z[V::kPer];
+    V::unpack(data[v], z);
+#pragma unroll
+    for (int e = 0; e < V::kPer; ++e) hist_add<kMass>(hc, m, __fmul_rn(z[e], inv_t), scale, base, copy);
+  }
+  for (int s = threadIdx.x; s < kHashCap; s += kThreads) {
+    const float y = g.hval[s];
+    hist_add<kMass>(hc, m, (g.hkey[s] >= 0 && y >= lo_y) ? y : neg_inf(), scale, base, copy);
+  }
+}
+
+// Tile level (base 0): one entry per 16-byte vector valued at a lower bound
+// of its largest processed logit, one per patched token; k entries at or
+// above a bucket imply k tokens there, and their masses bound the tokens'
+// mass from below.
+template <bool kMass>
+__device__ __forceinline__ void hist_tiles(uint32_t* hc, float scale, int nvec, int copy) {
+  const float m = g.m;
+  constexpr int kB = 8;  // independent loads first, then the atomics
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * kB) {
+    float ub[kB];
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int v = v0 + u * kThreads;
+      ub[u] = (v < nvec) ? vec_bound(v) : neg_inf();
+    }
+    // the stored bound is rounded up to bf16: one bf16 step below is <= the max
+#pragma unroll
+    for (int u = 0; u < kB; ++u)
+      hist_add<kMass>(hc, m, fminf(ub[u] - fabsf(ub[u]) * 0.0078125f - 1e-30f, m), scale, 0.0f, copy);
+  }
+  for (int s = threadIdx.x; s < kHashCap; s += kThreads)
+    hist_add<kMass>(hc, m, g.hkey[s] >= 0 ? g.hval[s] : neg_inf(), scale, 0.0f, copy);
+}
+
+// Histogram into `out`: token level (tile = 0) of the buckets
+// [base, base + 64) at `scale`, skipping vectors whose bound is below lo_y, or
+// tile level (tile = 1).
 template <int DT>
 __device__ __noinline__ void hist_pass(int tile, float scale, float base, int need_mass, float lo_y, int step,
                                        LevelRec* out) {
   using V = Vec<DT>;
   uint32_t* hc = reinterpret_cast<uint32_t*>(g.work);
-  unsigned long long* hm = reinterpret_cast<unsigned long long*>(g.work + kBuckets * kCopies * 4);
   const int tid = threadIdx.x;
-  for (int i = tid; i < kBuckets * kCopies; i += kThreads) {
-    hc[i] = 0;
-    hm[i] = 0;
-  }
+  for (int i = tid; i < 3 * kHistRows * kCopies; i += kThreads) hc[i] = 0;
   __syncthreads();
   const int copy = tid & (kCopies - 1);
-  const float m = g.m;
-  auto add = [&](float y) {
-    const float b = bucket_of(m, y, scale) - base;
-    if (b >= 0.0f && b < static_cast<float>(kBuckets)) {
-      const int bi = small_int(b);
-      atomicAdd(hc + bi * kCopies + copy, 1u);
-      if (need_mass) atomicAdd(hm + bi * kCopies + copy, fixed_mass(y, m));
-    }
-  };
-  const int nvec = (g.n + V::kPer - 1) / V::kPer;
-  const uint4* __restrict__ data = reinterpret_cast<const uint4*>(g.data);
-  const __nv_bfloat16* __restrict__ vmax = g.vmax;
-  const float inv_t = g.inv_t;
   if (tile) {
-    // the stored bound is rounded up to bf16: one bf16 step below is <= the max
-    constexpr int kB = 8;  // independent loads first, then the atomics
-    for (int v0 = tid; v0 < nvec; v0 += kThreads * kB) {
-      float ub[kB];
-#pragma unroll
-      for (int u = 0; u < kB; ++u) {
-        const int v = v0 + u * kThreads;
-        ub[u] = (v < nvec) ? __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(vmax[v])) << 16) : neg_inf();
-      }
-#pragma unroll
-      for (int u = 0; u < kB; ++u)
-        if (ub[u] != neg_inf()) add(fminf(ub[u] - fabsf(ub[u]) * 0.0078125f - 1e-30f, m));
-    }
+    const int nvec = (g.n + V::kPer - 1) / V::kPer;
+    if (need_mass)
+      hist_tiles<true>(hc, scale, nvec, copy);
+    else
+      hist_tiles<false>(hc, scale, nvec, copy);
+  } else if (need_mass) {
+    hist_tokens<DT, true>(hc, scale, base, lo_y, copy);
   } else {
-    for (int v = tid; v < nvec; v += kThreads) {
-      if (__uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(vmax[v])) << 16) < lo_y) continue;
-      float z[V::kPer];
-      V::unpack(data[v], z);
-#pragma unroll
-      for (int e = 0; e < V::kPer; ++e) {
-        const float y = __fmul_rn(z[e], inv_t);
-        if (y != neg_inf()) add(y);
-      }
-    }
-  }
-  for (int s = tid; s < kHashCap; s += kThreads) {
-    const float y = g.hval[s];
-    if (g.hkey[s] >= 0 && y != neg_inf() && (tile || y >= lo_y)) add(y);
+    hist_tokens<DT, false>(hc, scale, base, lo_y, copy);
   }
   push_merge(out, scale, base, step);
 }
@@ -605,6 +642,42 @@ __device__ __noinline__ void locate(const LevelRec* r, int by_mass, unsigned lon
 
 // Gathers every token of bucket `abs` at `scale` into every CTA's list (the
 // buffer of this step's parity).
+// Appends the entries flagged in `hits` (bit e: token t0 + e, logit y[e]) of
+// every lane of the warp to the cluster's list: one slot reservation per warp
+// at the cursor in rank 0, then each lane writes its entries into every CTA.
+// Called by all 32 lanes.
+template <int N>
+__device__ __forceinline__ void warp_append(uint32_t hits, const float (&y)[N], int32_t t0, uint32_t* cursor,
+                                            unsigned long long* list) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int lane = threadIdx.x & 31;
+  const uint32_t nh = static_cast<uint32_t>(__popc(hits));
+  uint32_t incl = nh;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+  uint32_t base = 0;
+  if (lane == 0) base = atomicAdd(cursor, total);
+  uint32_t slot = __shfl_sync(0xffffffffu, base, 0) + incl - nh;
+  const int ncta = g.ncta;
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    if ((hits >> e) & 1u) {
+      if (slot < static_cast<uint32_t>(kListCap)) {
+        const unsigned long long k = sort_key(y[e], t0 + e);
+        for (int r = 0; r < ncta; ++r) *cl.map_shared_rank(list + slot, r) = k;
+      }
+      ++slot;
+    }
+  }
+}
+
+// Gathers the tokens of absolute bucket `abs` at `scale` (their logits are at
+// least lo_y) into every CTA's list of this step's parity; the count is known
+// from the histogram.
 template <int DT>
 __device__ __noinline__ void gather_pass(float scale, float abs, float lo_y, int step) {
   using V = Vec<DT>;
@@ -612,40 +685,32 @@ __device__ __noinline__ void gather_pass(float scale, float abs, float lo_y, int
   const int par = step & 1;
   unsigned long long* list = reinterpret_cast<unsigned long long*>(g.work) + par * kListCap;
   uint32_t* cursor = cl.map_shared_rank(&g.cursor[par], 0);
-  const float m = g.m;
-  const int lane = threadIdx.x & 31;
-  const int ncta = g.ncta;
-  auto put = [&](int32_t t, float y) {
-    if (bucket_of(m, y, scale) != abs) return;
-    const unsigned act = __activemask();
-    const int leader = __ffs(act) - 1;
-    uint32_t base = 0;
-    if (lane == leader) base = atomicAdd(cursor, static_cast<uint32_t>(__popc(act)));
-    base = __shfl_sync(act, base, leader);
-    const uint32_t slot = base + static_cast<uint32_t>(__popc(act & ((1u << lane) - 1u)));
-    if (slot < static_cast<uint32_t>(kListCap)) {
-      const unsigned long long e = sort_key(y, t);
-      for (int r = 0; r < ncta; ++r) *cl.map_shared_rank(list + slot, r) = e;
-    }
-  };
+  const float m = g.m, inv_t = g.inv_t;
   const int nvec = (g.n + V::kPer - 1) / V::kPer;
   const uint4* data = reinterpret_cast<const uint4*>(g.data);
-  const float inv_t = g.inv_t;
   const int lo = g.lo;
-  for (int v = threadIdx.x; v < nvec; v += kThreads) {
-    if (vec_bound(v) < lo_y) continue;
-    float z[V::kPer];
-    V::unpack(data[v], z);
+  // every thread runs the same number of iterations (warp-collective appends)
+  for (int vb = 0; vb < nvec; vb += kThreads) {
+    const int v = vb + static_cast<int>(threadIdx.x);
+    float y[V::kPer];
+    uint32_t hits = 0;
+    if (v < nvec && vec_bound(v) >= lo_y) {
+      float z[V::kPer];
+      V::unpack(data[v], z);
 #pragma unroll
-    for (int e = 0; e < V::kPer; ++e) {
-      const float y = __fmul_rn(z[e], inv_t);
-      if (y != neg_inf()) put(lo + v * V::kPer + e, y);
+      for (int e = 0; e < V::kPer; ++e) {
+        y[e] = __fmul_rn(z[e], inv_t);
+        hits |= static_cast<uint32_t>(bucket_of(m, y[e], scale) == abs) << e;  // -inf: never
+      }
     }
+    if (__any_sync(0xffffffffu, hits != 0)) warp_append<V::kPer>(hits, y, lo + v * V::kPer, cursor, list);
   }
-  for (int s = threadIdx.x; s < kHashCap; s += kThreads) {
+  for (int sb = 0; sb < kHashCap; sb += kThreads) {
+    const int s = sb + static_cast<int>(threadIdx.x);
     const int32_t t = g.hkey[s];
-    const float y = g.hval[s];
-    if (t >= 0 && y != neg_inf() && y >= lo_y) put(t, y);
+    float y[1] = {g.hval[s]};
+    const uint32_t hit = (t >= 0 && y[0] >= lo_y && bucket_of(m, y[0], scale) == abs) ? 1u : 0u;
+    if (__any_sync(0xffffffffu, hit != 0)) warp_append<1>(hit, y, t, cursor, list);
   }
   cl.sync();
   if (g.rank == 0 && threadIdx.x == 0) g.cursor[par] = 0;  // its next use is two steps away
@@ -1232,6 +1297,9 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
   const uint4* data = reinterpret_cast<const uint4*>(g.data);
   const int lo = g.lo;
   const uint32_t key0 = static_cast<uint32_t>(seed), key1 = static_cast<uint32_t>(seed >> 32);
+  const bool cut_on = g.cut_on != 0;
+  const uint32_t cut_key = g.cut_key;
+  const int32_t cut_idx = g.cut_idx;
   constexpr int kGroups = V::kPer / 4;  // Philox blocks per vector: 4 tokens share one block
   for (int v = threadIdx.x; v < nvec; v += kThreads) {
     const float ub = vec_bound(v);
@@ -1241,16 +1309,21 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
     float z[V::kPer];
     V::unpack(data[v], z);
     const int32_t t0 = lo + v * V::kPer;  // a multiple of 4
-    uint32_t cand = 0;  // members that may still beat the running best
+    // membership in K and candidacy, without a branch per token
+    uint32_t mem = 0, cand = 0;
 #pragma unroll
     for (int e = 0; e < V::kPer; ++e) {
       const float y = __fmul_rn(z[e], inv_t);
       z[e] = y;
-      if (y == neg_inf() || !in_kept(t0 + e, y, m, mp_on, min_p)) continue;
-      ++kcount;
-      if (spec_pos) kmass += fixed_mass(y, m);
-      if (!(y + kGumbelMax + 1e-3f + fabsf(y) * 1e-6f < bv)) cand |= 1u << e;
+      const uint32_t key = order_key(y);
+      bool in = (y != neg_inf());
+      if (cut_on) in = in && (key > cut_key || (key == cut_key && t0 + e <= cut_idx));
+      if (mp_on) in = in && (__expf(y - m) >= min_p);
+      mem |= static_cast<uint32_t>(in) << e;
+      cand |= static_cast<uint32_t>(in && !(y + kGumbelMax + 1e-3f + fabsf(y) * 1e-6f < bv)) << e;
+      if (spec_pos) kmass += in ? fixed_mass(y, m) : 0ull;
     }
+    kcount += __popc(mem);
     if (!cand) continue;
     uint32_t w[V::kPer];
 #pragma unroll
@@ -1259,16 +1332,22 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
 #pragma unroll
       for (int i = 0; i < 4; ++i) w[q * 4 + i] = r.w[i];
     }
+    // the cheap bound of each noise value, then the exact noise only where
+    // that bound still reaches the running best
+    uint32_t live = 0;
 #pragma unroll
     for (int e = 0; e < V::kPer; ++e) {
-      if (!((cand >> e) & 1u)) continue;
-      const float y = z[e];
-      const float slack = 1e-3f + fabsf(y) * 1e-6f;
-      const uint32_t num = uniform_numerator(w[e]);
-      if (y + gumbel_upper_bound(num) + slack < bv) continue;
-      const float s = __fadd_rn(y, gumbel_from_numerator(num));
-      if (beats(s, t0 + e, bv, bi)) {
-        bv = s;
+      w[e] = uniform_numerator(w[e]);
+      live |= static_cast<uint32_t>(!(z[e] + gumbel_upper_bound(w[e]) + 1e-3f + fabsf(z[e]) * 1e-6f < bv)) << e;
+    }
+    live &= cand;
+    if (!live) continue;
+#pragma unroll
+    for (int e = 0; e < V::kPer; ++e) {
+      if (!((live >> e) & 1u)) continue;
+      const float sc = __fadd_rn(z[e], gumbel_from_numerator(w[e]));
+      if (beats(sc, t0 + e, bv, bi)) {
+        bv = sc;
         bi = t0 + e;
       }
     }
@@ -1613,27 +1692,29 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
 #pragma unroll
       for (int u = 0; u < kB; ++u) {
         const int v = v0 + u * kThreads;
-        if (bits[u]) raw[u] = V::exclude(raw[u], bits[u]);
+        raw[u] = V::exclude(raw[u], bits[u]);  // selects: no branch per vector
         float z[V::kPer];
         V::unpack(raw[u], z);
         float vmax = neg_inf(), vmin = pos_inf();
         int allowed = 0;
 #pragma unroll
         for (int e = 0; e < V::kPer; ++e) {
-          const float y = greedy ? z[e] : __fmul_rn(z[e], inv_t);
-          vmax = max_nan(vmax, y);
-          const bool ok = (y != neg_inf());
+          z[e] = greedy ? z[e] : __fmul_rn(z[e], inv_t);
+          vmax = max_nan(vmax, z[e]);
+          const bool ok = (z[e] != neg_inf());
           allowed += ok ? 1 : 0;
-          vmin = fminf(vmin, ok ? y : pos_inf());
+          vmin = fminf(vmin, ok ? z[e] : pos_inf());
         }
-        if (want_s && allowed) {  // online softmax normaliser of the row
+        if (want_s) {  // online softmax normaliser of the row
+          if (vmax > a_smax) {  // a new running max (rare after the first vectors)
+            a_ssum = (a_smax == neg_inf()) ? 0.0f : __fmul_rn(a_ssum, __expf(a_smax - vmax));
+            a_smax = vmax;
+          }
+          const float ms = (a_smax == neg_inf()) ? 0.0f : a_smax;  // exp(-inf - ms) = 0
           float part = 0.0f;
 #pragma unroll
-          for (int e = 0; e < V::kPer; ++e) {
-            const float y = __fmul_rn(z[e], inv_t);
-            if (y != neg_inf()) part = __fadd_rn(part, __expf(y - vmax));
-          }
-          softmax_merge(a_smax, a_ssum, vmax, part);
+          for (int e = 0; e < V::kPer; ++e) part = __fadd_rn(part, __expf(z[e] - ms));
+          a_ssum = __fadd_rn(a_ssum, part);
         }
         a_count += allowed;
         a_ymin = fminf(a_ymin, vmin);
@@ -1643,7 +1724,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
           best_vec = v;
         }
         if (v < nvec) {
-          if (bits[u]) data[v] = raw[u];
+          data[v] = raw[u];
           c.vmax[v] = bf16_round_up(vmax);
         }
       }
@@ -1841,7 +1922,7 @@ static int choose_cluster(int32_t vocab, int32_t es) {
     if (slice * es <= kTargetSliceBytes) return cs;
   }
   const int64_t slice = ((static_cast<int64_t>(vocab) + kMaxCluster - 1) / kMaxCluster + 31) / 32 * 32;
-  if (slice * es <= kMaxSliceBytes) return kMaxCluster;
+  if (slice * es <= kMaxSliceBytes && slice <= kMaxSliceTokens) return kMaxCluster;
   return 0;
 }
 

@@ -39,6 +39,11 @@ def test_host_only_queries(lib):
     assert ss.ss_cluster_size(10, "f32") == 1
     assert ss.ss_cluster_size(0, "f32") == 0
     assert ss.ss_cluster_size(10_000_000, "bf16") == 0
+    # largest supported rows: 8 slices of at most 61,440 tokens / 160 KiB
+    assert ss.ss_cluster_size(491_520, "bf16") == 8
+    assert ss.ss_cluster_size(491_521, "bf16") == 0
+    assert ss.ss_cluster_size(327_680, "f32") == 8
+    assert ss.ss_cluster_size(327_681, "f32") == 0
     assert ss.ss_workspace_size(32, 4) >= 32 * 5 * 16 + 32 * 4
     assert lib.ss_status_string(0) == b"ok"
 
