@@ -49,7 +49,7 @@ namespace cg = cooperative_groups;
 
 namespace ss {
 
-constexpr int kThreads = 256;  // 2 CTAs per SM with up to 128 registers per thread
+constexpr int kThreads = 512;  // 2 CTAs per SM with up to 64 registers per thread
 constexpr int kWarps = kThreads / 32;
 constexpr int kHashCap = SS_MAX_PATCHED;
 constexpr int kHashShift = 32 - 10;  // log2(kHashCap) = 10
@@ -81,7 +81,7 @@ constexpr float kMassCutoff = 28.5f;  // exp(-28.5) * 2^40 < 1: zero in fixed po
 constexpr int kHistRows = 65;  // 64 buckets and a spill row
 constexpr uint32_t kWorkBytes = 3 * kHistRows * kCopies * 4;  // histograms / gathered lists / fallback buffers
 constexpr int kPartSlots = 4;  // stage 1, draw, residual, normaliser
-constexpr int kRedBytes = 1024;
+constexpr int kRedBytes = 2048;
 
 enum TaskMode { kModeSample = 0, kModeVerify = 1 };
 
