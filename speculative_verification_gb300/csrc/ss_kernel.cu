@@ -716,30 +716,43 @@ __device__ __noinline__ void gather_pass(float scale, float abs, float lo_y, int
   if (g.rank == 0 && threadIdx.x == 0) g.cursor[par] = 0;  // its next use is two steps away
 }
 
-// Sorts list[0..n) ascending in place (bitonic network in shared memory,
-// n <= kListCap) and writes the inclusive prefix sums of the fixed-point
-// masses to `pre`.
+// Sorts list[0..n) ascending in place (n <= kListCap) and writes the
+// inclusive prefix sums of the fixed-point masses to `pre`.
 __device__ __noinline__ void sort_and_scan(unsigned long long* list, int n, unsigned long long* pre) {
+  // Rank sort: the keys are distinct (a token is gathered once), so the
+  // position of an entry is the number of smaller keys.  One pass of
+  // broadcast reads and a single barrier, instead of the log^2 barriers of
+  // a sorting network.
   const int tid = threadIdx.x;
-  int np2 = 2;
-  while (np2 < n) np2 <<= 1;
-  for (int i = n + tid; i < np2; i += kThreads) list[i] = ~0ull;  // padding sorts last
-  __syncthreads();
-  const int pairs = np2 >> 1;
-  for (int k = 2; k <= np2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int q = tid; q < pairs; q += kThreads) {
-        const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1));  // lower index of the pair (j a power of two)
-        const unsigned long long a = list[i], b = list[i + j];
-        const bool asc = (i & k) == 0;
-        if ((a > b) == asc) {
-          list[i] = b;
-          list[i + j] = a;
-        }
-      }
-      __syncthreads();
+  constexpr int kMine = (kListCap + kThreads - 1) / kThreads;
+  unsigned long long key[kMine];
+  int rank[kMine];
+#pragma unroll
+  for (int r = 0; r < kMine; ++r) {
+    const int i = tid + r * kThreads;
+    key[r] = (i < n) ? list[i] : 0ull;
+    rank[r] = 0;
+  }
+  if (tid < n) {
+    int j = 0;
+    for (; j + 4 <= n; j += 4) {
+      const unsigned long long b0 = list[j], b1 = list[j + 1], b2 = list[j + 2], b3 = list[j + 3];
+#pragma unroll
+      for (int r = 0; r < kMine; ++r)
+        rank[r] += static_cast<int>(b0 < key[r]) + static_cast<int>(b1 < key[r]) + static_cast<int>(b2 < key[r]) +
+                   static_cast<int>(b3 < key[r]);
+    }
+    for (; j < n; ++j) {
+      const unsigned long long b = list[j];
+#pragma unroll
+      for (int r = 0; r < kMine; ++r) rank[r] += static_cast<int>(b < key[r]);
     }
   }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kMine; ++r)
+    if (tid + r * kThreads < n) list[rank[r]] = key[r];
+  __syncthreads();
   // inclusive scan of masses in sorted order: each thread owns a run
   constexpr int kPer = kListCap / kThreads;
   const float m = g.m;

@@ -17,8 +17,11 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
   for (int round = 0; round < 10; ++round) {
     // S-box of one round: two 32x32 -> 64-bit products; the high halves are
     // mixed with the other counter words and the round key.
-    const uint32_t a_hi = __umulhi(0xD2511F53u, c0), a_lo = 0xD2511F53u * c0;
-    const uint32_t b_hi = __umulhi(0xCD9E8D57u, c2), b_lo = 0xCD9E8D57u * c2;
+    // one 32 x 32 -> 64-bit multiply each (a single wide multiply-add)
+    const uint64_t a = static_cast<uint64_t>(0xD2511F53u) * c0;
+    const uint64_t b = static_cast<uint64_t>(0xCD9E8D57u) * c2;
+    const uint32_t a_hi = static_cast<uint32_t>(a >> 32), a_lo = static_cast<uint32_t>(a);
+    const uint32_t b_hi = static_cast<uint32_t>(b >> 32), b_lo = static_cast<uint32_t>(b);
     const uint32_t n0 = b_hi ^ c1 ^ k0;
     const uint32_t n2 = a_hi ^ c3 ^ k1;
     c0 = n0;
