@@ -112,26 +112,39 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return r;
 }
 
-// trunc(exp(y - m) * 2^40) for y <= m, taken from the float's exponent and
-// significand with integer shifts: the float -> 64-bit integer conversion
-// instruction is several times slower than this on sm_103.
-__device__ __forceinline__ unsigned long long fixed_mass(float y, float m) {
-  const uint32_t b = __float_as_uint(fminf(__expf(y - m), 1.0f));
-  const int sh = static_cast<int>(b >> 23) - (127 + 23 - 40);
-  const unsigned long long sig = (b & 0x7fffffu) | 0x800000u;
-  if (sh >= 0) return sig << sh;
-  return sh > -24 ? (sig >> -sh) : 0ull;
+// Floor of x for 0 <= x < 2^22, as an integer: adding 1.5 * 2^23 with
+// round-down leaves floor(x) in the low mantissa bits (the sum's unit in the
+// last place is 1).  sm_103 issues float rounding and float <-> integer
+// conversion instructions at a small fraction of the add rate, so the hot
+// loops use this instead.  For larger x (and +inf) the result is at least
+// 2^22, for x < 0 it is negative.
+__device__ __forceinline__ int floor_small(float x) { return __float_as_int(__fadd_rd(x, 12582912.0f)) - 0x4B400000; }
+
+// The fixed-point mass trunc(exp(y - m) * 2^40) of a token (y <= m) as a high
+// half trunc(e * 2^20) <= 2^20 and a low half < 2^20, e = exp(y - m): both
+// scalings by 2^20 and the subtraction of the high half are exact, so
+// hi * 2^20 + lo is exactly the truncated product.
+__device__ __forceinline__ void fixed_mass_parts(float y, float m, uint32_t& hi, uint32_t& lo) {
+  const float t = __fmul_rn(fminf(__expf(y - m), 1.0f), 1048576.0f);
+  const float th = __fadd_rd(t, 12582912.0f);
+  hi = __float_as_uint(th) - 0x4B400000u;
+  const float fr = __fmul_rn(__fsub_rn(t, __fsub_rn(th, 12582912.0f)), 1048576.0f);
+  lo = __float_as_uint(__fadd_rd(fr, 12582912.0f)) - 0x4B400000u;
 }
 
-// Absolute bucket index of y at a refinement scale (a power of two).
-// The floor is taken by adding 1.5 * 2^23 with round-down (the sum's unit in
-// the last place is 1) rather than by a rounding instruction: sm_103 issues
-// float rounding and float <-> integer conversions at a small fraction of the
-// add rate.  Values at or above 2^22 come back as 2^22, outside every bucket
-// range in use (absolute buckets stay below 64^3 + 64).
-__device__ __forceinline__ float bucket_of(float m, float y, float scale) {
-  const float x = fminf(__fmul_rn(__fsub_rn(m, y), scale), 4194304.0f);
-  return __fsub_rn(__fadd_rd(x, 12582912.0f), 12582912.0f);
+__device__ __forceinline__ unsigned long long fixed_mass(float y, float m) {
+  uint32_t hi, lo;
+  fixed_mass_parts(y, m, hi, lo);
+  return (static_cast<unsigned long long>(hi) << kMassSplit) + lo;
+}
+
+// Absolute bucket floor((m - y) * scale) of y at a refinement scale (a power
+// of two), given ms = m * scale (exact): the fused multiply-add rounds
+// m * scale - y * scale once, which equals the rounded m - y times scale.
+// y = -inf gives a huge index, outside every bucket range in use (absolute
+// buckets stay below 64^3 + 64).
+__device__ __forceinline__ int bucket_index(float y, float scale, float ms) {
+  return floor_small(__fmaf_rn(-y, scale, ms));
 }
 
 // Integer value of an integral float in [0, 2^22], without a conversion
@@ -505,22 +518,22 @@ __device__ __forceinline__ void push_merge(LevelRec* out, float scale, float bas
 // [base, base + 64), else the spill row kBuckets, so that every entry issues
 // the same instructions (a per-entry branch around the atomics costs far more
 // than the spilled atomics).  y = -inf lands in the spill row.
-__device__ __forceinline__ int hist_slot(float m, float y, float scale, float base, int copy) {
-  const float b = bucket_of(m, y, scale) - base;
-  const bool in = (b >= 0.0f) && (b < static_cast<float>(kBuckets));
-  return small_int(in ? b : static_cast<float>(kBuckets)) * kCopies + copy;
+__device__ __forceinline__ int hist_slot(float y, float scale, float ms, int base, int copy) {
+  const int b = bucket_index(y, scale, ms) - base;
+  return (static_cast<uint32_t>(b) < static_cast<uint32_t>(kBuckets) ? b : kBuckets) * kCopies + copy;
 }
 
 // Counts, and with kMass the fixed-point masses split into a high and a low
 // half (32-bit shared atomics; the 64-bit ones are several times slower).
 template <bool kMass>
-__device__ __forceinline__ void hist_add(uint32_t* hc, float m, float y, float scale, float base, int copy) {
-  const int k = hist_slot(m, y, scale, base, copy);
+__device__ __forceinline__ void hist_add(uint32_t* hc, float m, float y, float scale, float ms, int base, int copy) {
+  const int k = hist_slot(y, scale, ms, base, copy);
   atomicAdd(hc + k, 1u);
   if (kMass) {
-    const unsigned long long f = fixed_mass(y, m);  // 0 for y = -inf
-    atomicAdd(hc + kHistRows * kCopies + k, static_cast<uint32_t>(f >> kMassSplit));
-    atomicAdd(hc + 2 * kHistRows * kCopies + k, static_cast<uint32_t>(f) & ((1u << kMassSplit) - 1u));
+    uint32_t hi, lo;
+    fixed_mass_parts(y, m, hi, lo);  // 0 for y = -inf
+    atomicAdd(hc + kHistRows * kCopies + k, hi);
+    atomicAdd(hc + 2 * kHistRows * kCopies + k, lo);
   }
 }
 
@@ -531,17 +544,18 @@ __device__ __forceinline__ void hist_tokens(uint32_t* hc, float scale, float bas
   using V = Vec<DT>;
   const int nvec = (g.n + V::kPer - 1) / V::kPer;
   const uint4* __restrict__ data = reinterpret_cast<const uint4*>(g.data);
-  const float m = g.m, inv_t = g.inv_t;
+  const float m = g.m, inv_t = g.inv_t, ms = __fmul_rn(g.m, scale);
+  const int ib = small_int(base);
   for (int v = threadIdx.x; v < nvec; v += kThreads) {
     if (vec_bound(v) < lo_y) continue;
     float z[V::kPer];
     V::unpack(data[v], z);
 #pragma unroll
-    for (int e = 0; e < V::kPer; ++e) hist_add<kMass>(hc, m, __fmul_rn(z[e], inv_t), scale, base, copy);
+    for (int e = 0; e < V::kPer; ++e) hist_add<kMass>(hc, m, __fmul_rn(z[e], inv_t), scale, ms, ib, copy);
   }
   for (int s = threadIdx.x; s < kHashCap; s += kThreads) {
     const float y = g.hval[s];
-    hist_add<kMass>(hc, m, (g.hkey[s] >= 0 && y >= lo_y) ? y : neg_inf(), scale, base, copy);
+    hist_add<kMass>(hc, m, (g.hkey[s] >= 0 && y >= lo_y) ? y : neg_inf(), scale, ms, ib, copy);
   }
 }
 
@@ -551,7 +565,7 @@ __device__ __forceinline__ void hist_tokens(uint32_t* hc, float scale, float bas
 // mass from below.
 template <bool kMass>
 __device__ __forceinline__ void hist_tiles(uint32_t* hc, float scale, int nvec, int copy) {
-  const float m = g.m;
+  const float m = g.m, ms = __fmul_rn(g.m, scale);
   constexpr int kB = 8;  // independent loads first, then the atomics
   for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * kB) {
     float ub[kB];
@@ -563,10 +577,10 @@ __device__ __forceinline__ void hist_tiles(uint32_t* hc, float scale, int nvec, 
     // the stored bound is rounded up to bf16: one bf16 step below is <= the max
 #pragma unroll
     for (int u = 0; u < kB; ++u)
-      hist_add<kMass>(hc, m, fminf(ub[u] - fabsf(ub[u]) * 0.0078125f - 1e-30f, m), scale, 0.0f, copy);
+      hist_add<kMass>(hc, m, fminf(ub[u] - fabsf(ub[u]) * 0.0078125f - 1e-30f, m), scale, ms, 0, copy);
   }
   for (int s = threadIdx.x; s < kHashCap; s += kThreads)
-    hist_add<kMass>(hc, m, g.hkey[s] >= 0 ? g.hval[s] : neg_inf(), scale, 0.0f, copy);
+    hist_add<kMass>(hc, m, g.hkey[s] >= 0 ? g.hval[s] : neg_inf(), scale, ms, 0, copy);
 }
 
 // Histogram into `out`: token level (tile = 0) of the buckets
@@ -685,7 +699,8 @@ __device__ __noinline__ void gather_pass(float scale, float abs, float lo_y, int
   const int par = step & 1;
   unsigned long long* list = reinterpret_cast<unsigned long long*>(g.work) + par * kListCap;
   uint32_t* cursor = cl.map_shared_rank(&g.cursor[par], 0);
-  const float m = g.m, inv_t = g.inv_t;
+  const float inv_t = g.inv_t, ms = __fmul_rn(g.m, scale);
+  const int ia = small_int(abs);
   const int nvec = (g.n + V::kPer - 1) / V::kPer;
   const uint4* data = reinterpret_cast<const uint4*>(g.data);
   const int lo = g.lo;
@@ -700,7 +715,7 @@ __device__ __noinline__ void gather_pass(float scale, float abs, float lo_y, int
 #pragma unroll
       for (int e = 0; e < V::kPer; ++e) {
         y[e] = __fmul_rn(z[e], inv_t);
-        hits |= static_cast<uint32_t>(bucket_of(m, y[e], scale) == abs) << e;  // -inf: never
+        hits |= static_cast<uint32_t>(bucket_index(y[e], scale, ms) == ia) << e;  // -inf: never
       }
     }
     if (__any_sync(0xffffffffu, hits != 0)) warp_append<V::kPer>(hits, y, lo + v * V::kPer, cursor, list);
@@ -709,7 +724,7 @@ __device__ __noinline__ void gather_pass(float scale, float abs, float lo_y, int
     const int s = sb + static_cast<int>(threadIdx.x);
     const int32_t t = g.hkey[s];
     float y[1] = {g.hval[s]};
-    const uint32_t hit = (t >= 0 && y[0] >= lo_y && bucket_of(m, y[0], scale) == abs) ? 1u : 0u;
+    const uint32_t hit = (t >= 0 && y[0] >= lo_y && bucket_index(y[0], scale, ms) == ia) ? 1u : 0u;
     if (__any_sync(0xffffffffu, hit != 0)) warp_append<1>(hit, y, t, cursor, list);
   }
   cl.sync();
