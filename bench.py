@@ -40,6 +40,15 @@ L2_BYTES = 129 * 1024 * 1024
 KERNEL_NAME = "ss_row_kernel"
 
 
+def progress(msg):
+    """Phase markers on stderr (flushed), so that a stalled run shows where."""
+    if os.environ.get("SS_BENCH_PROGRESS"):
+        print("[bench %.1fs] %s" % (time.time() - _T0, msg), file=sys.stderr, flush=True)
+
+
+_T0 = time.time()
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_verification_gb300", "csrc")
@@ -185,6 +194,7 @@ def run_ours(args, rank, world, dist):
                     call(i)
         return g
 
+    progress("capturing graphs")
     g_main = capture(per_graph) if per_graph > 0 else None
     reps, rem = divmod(args.steps, per_graph) if per_graph > 0 else (0, 0)
     g_rem = capture(rem) if rem else None
@@ -198,6 +208,7 @@ def run_ours(args, rank, world, dist):
                 (g_rem if m == rem else capture(m)).replay()
 
     # warm-up (untimed)
+    progress("warm-up replay")
     replay_steps(max(args.warmup, 3))
     stream.synchronize()
 
@@ -227,10 +238,13 @@ def run_ours(args, rank, world, dist):
     value = rows_per_call * args.steps * world / (ms / 1e3)
 
     # end-to-end through the public API with host buffers (pinned)
+    progress("timed region done: %.3f ms" % ms)
     e2e = run_e2e(args, ss, ring_host, dev, stream, rows_per_call, dist)
+    progress("end-to-end done")
 
     # speculative-verify throughput (secondary metric), same protocol
     spec = run_spec(args, ss, rank, dev, stream) if args.spec_steps > 0 else None
+    progress("spec-verify done")
 
     peak, peak_kind = measured_peak()
     achieved = bytes_per_call / per_call_s / 1e9
@@ -458,7 +472,9 @@ def main():
     # the oracle runs before any CUDA work (no fork after the first GPU call)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        progress("cpu baseline")
         cpu = cpu_baseline_block(args.config, args.cpu_seconds)
+        progress("cpu baseline done")
 
     dist = None
     if world > 1:
