@@ -32,6 +32,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+from speculative_verification_gb300 import dp as DP  # noqa: E402
 from speculative_verification_gb300 import workloads as W  # noqa: E402
 
 METRIC = "sampled rows/s and logits HBM GB/s (% of peak) at V=128k B=64; spec-verify rows/s"
@@ -150,7 +151,7 @@ class ClockSampler:
 
 
 def workload_for(cfg, rank, idx):
-    return W.make(cfg, seed=cfg + 7919 * (rank * 1000 + idx))
+    return W.make(cfg, seed=DP.ring_seed(cfg, rank, idx))
 
 
 # --------------------------------------------------------------- our arm --
@@ -235,7 +236,7 @@ def run_ours(args, rank, world, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     per_call_s = ms / 1e3 / args.steps
-    value = rows_per_call * args.steps * world / (ms / 1e3)
+    value = DP.aggregate_rate(rows_per_call, args.steps, world, ms)
 
     # end-to-end through the public API with host buffers (pinned)
     progress("timed region done: %.3f ms" % ms)
@@ -334,7 +335,7 @@ def run_e2e(args, ss, ring_host, dev, stream, rows_per_call, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     world = dist.get_world_size() if dist else 1
-    return {"value": rows_per_call * n_steps * world / (ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+    return {"value": DP.aggregate_rate(rows_per_call, n_steps, world, ms), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": n_steps}
 
 

@@ -127,6 +127,10 @@ typedef struct {
   const uint8_t* use_bitmask;   /* NULL: every row uses its mask row             */
   const uint64_t* seed;         /* required: Philox key                          */
   const int64_t* position;      /* required: Philox counter word 1               */
+  const uint32_t* row_id;       /* Philox counter word 2; NULL: the row's (request's)
+                                   index in the call.  A stable id per request
+                                   keeps its draws independent of its slot in the
+                                   batch and of how a batch is split over GPUs. */
 } ss_params;
 
 /* ss_process_sample: one token per row.  Row r is logits + r * row_stride. */

@@ -38,6 +38,7 @@ class _Params(C.Structure):
         ("use_bitmask", C.c_void_p),
         ("seed", C.c_void_p),
         ("position", C.c_void_p),
+        ("row_id", C.c_void_p),
     ]
 
 
@@ -147,6 +148,7 @@ def _params(w, keep):
         "use_bitmask": np.uint8,
         "seed": np.uint64,
         "position": np.int64,
+        "row_id": np.uint32,
     }
     p = _Params()
     for name, dt in fields.items():

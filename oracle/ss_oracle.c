@@ -409,7 +409,9 @@ int or_process_sample(const or_sample_in* in, or_sample_out* out) {
     if (out->kept_hi) out->kept_hi[r] = (s.status == OR_ROW_OK) ? s.L_hi : 0;
     if (in->force_kept && in->force_kept[r] > 0) row_force_L(&s, in->force_kept[r]);
     if (s.status == OR_ROW_OK) {
-      tok = row_draw(&s, in->p.seed[r], r, (uint32_t)in->p.position[r], &flag);
+      /* Philox counter word 2: the caller's row id, else the row's index */
+      const int32_t rid = in->p.row_id ? (int32_t)in->p.row_id[r] : r;
+      tok = row_draw(&s, in->p.seed[r], rid, (uint32_t)in->p.position[r], &flag);
       flag |= s.flag_k;
     }
     out->token[r] = tok;
@@ -553,13 +555,15 @@ int or_spec_verify(const or_verify_in* in, or_verify_out* out) {
     if (status == OR_ROW_OK) {
       uint64_t seed = in->p.seed[i];
       uint32_t pos = (uint32_t)pos64;
+      /* Philox counter word 2: the caller's request id, else its index */
+      const int32_t rid = in->p.row_id ? (int32_t)in->p.row_id[i] : i;
       int32_t final_tok = -1;
       for (j = 0; j < k; ++j) {
         int32_t x = in->draft_tokens[d0 + j];
         const float* qrow = in->draft_probs + (size_t)(d0 + j) * (size_t)in->draft_stride;
         double P = row_prob(&rows[j], x);
         double q = (double)qrow[x];
-        double u = (double)or_uniform(seed, i, pos + (uint32_t)j, 0, OR_STREAM_ACCEPT);
+        double u = (double)or_uniform(seed, rid, pos + (uint32_t)j, 0, OR_STREAM_ACCEPT);
         double uq = u * q;
         flag |= rows[j].flag_k;
         if (fabs(uq - P) <= REL_MARGIN * fmax(P, uq) + ABS_FLOOR) flag = 1;
@@ -568,13 +572,13 @@ int or_spec_verify(const or_verify_in* in, or_verify_out* out) {
           ++n_acc;
           continue;
         }
-        final_tok = residual_draw(&rows[j], qrow, seed, i, pos + (uint32_t)j, &flag);
-        if (final_tok < 0) final_tok = row_draw(&rows[j], seed, i, pos + (uint32_t)j, &flag);
+        final_tok = residual_draw(&rows[j], qrow, seed, rid, pos + (uint32_t)j, &flag);
+        if (final_tok < 0) final_tok = row_draw(&rows[j], seed, rid, pos + (uint32_t)j, &flag);
         break;
       }
       if (j == k) { /* every draft accepted: the bonus token from row k */
         flag |= rows[k].flag_k;
-        final_tok = row_draw(&rows[k], seed, i, pos + (uint32_t)k, &flag);
+        final_tok = row_draw(&rows[k], seed, rid, pos + (uint32_t)k, &flag);
       }
       o[n_acc] = final_tok;
     } else {

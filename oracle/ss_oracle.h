@@ -67,6 +67,7 @@ typedef struct {
   const uint8_t* use_bitmask;    /* [n] or NULL (= every row uses the mask)    */
   const uint64_t* seed;          /* [n] required                               */
   const int64_t* position;       /* [n] required                               */
+  const uint32_t* row_id;        /* [n] or NULL (= the row's index): Philox counter word 2 */
 } or_params;
 
 typedef struct {

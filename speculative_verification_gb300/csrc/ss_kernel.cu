@@ -260,6 +260,7 @@ struct Ctx {
   int32_t greedy, top_k, use_mask, want_s;
   float temperature, inv_t, top_p, min_p, rep, freq, pres;
   uint32_t seed_lo, seed_hi, pos;
+  uint32_t rowid;  // Philox counter word 2
   int32_t h0, h1, b0, b1;
   int32_t lo, n;  // slice start token, tokens in this slice
   int32_t status;
@@ -1299,7 +1300,7 @@ template <int DT>
 __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, int spec_pos, uint64_t seed) {
   using V = Vec<DT>;
   const float m = g.m, min_p = g.min_p, inv_t = g.inv_t;
-  const uint32_t rowid = static_cast<uint32_t>(g.req), pos = g.pos;
+  const uint32_t rowid = g.rowid, pos = g.pos;
   const int32_t arg = g.arg;
   // the argmax token is always in K: its score seeds the running best
   const float g0 = gumbel_from_numerator(uniform_numerator(philox_word(seed, rowid, pos, arg, 0)));
@@ -1399,7 +1400,7 @@ __device__ __noinline__ void residual_pass(int mp_on, float memb_lo, float inv_s
                                            uint64_t seed) {
   using V = Vec<DT>;
   const float m = g.m, min_p = g.min_p, inv_t = g.inv_t;
-  const uint32_t rowid = static_cast<uint32_t>(g.req), pos = g.pos;
+  const uint32_t rowid = g.rowid, pos = g.pos;
   float bv = neg_inf();
   int32_t bi = kNoCut;
   auto relem = [&](int32_t t, float y) {
@@ -1500,6 +1501,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
     c.row = live ? row : -1;
     c.bad_k = bad_k;
     c.req = req;
+    c.rowid = a.p.row_id ? a.p.row_id[req] : static_cast<uint32_t>(req);
     c.j = j;
     c.k = k;
     c.d0 = d0;
@@ -1820,7 +1822,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   if (status == SS_ROW_OK) {
     const bool spec_pos = (a.mode == kModeVerify) && (c.j < c.k);
     const uint64_t seed = (static_cast<uint64_t>(c.seed_hi) << 32) | c.seed_lo;
-    const uint32_t rowid = static_cast<uint32_t>(c.req);
+    const uint32_t rowid = c.rowid;
     if (c.greedy) {
       kept = 1;
       token = argmax_tok;

@@ -42,6 +42,7 @@ class ss_params(C.Structure):
         ("use_bitmask", C.c_void_p),
         ("seed", C.c_void_p),
         ("position", C.c_void_p),
+        ("row_id", C.c_void_p),
     ]
 
 
@@ -136,7 +137,7 @@ def _stream_handle(stream):
 
 PARAM_FIELDS = ("temperature", "top_k", "top_p", "min_p", "repetition", "frequency", "presence",
                 "hist_offsets", "hist_ids", "bias_offsets", "bias_ids", "bias_vals", "bitmask",
-                "use_bitmask", "seed", "position")
+                "use_bitmask", "seed", "position", "row_id")
 
 
 def make_params(p):
@@ -250,6 +251,8 @@ def to_device(w, device="cuda", pin=False):
             arr = np.ascontiguousarray(val)
             if arr.dtype == np.uint64:
                 arr = arr.view(np.int64)
+            elif arr.dtype == np.uint32:
+                arr = arr.view(np.int32)
             elif arr.dtype == np.uint16:
                 arr = arr.view(np.int16)
             t = torch.from_numpy(arr)

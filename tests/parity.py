@@ -44,7 +44,7 @@ def subset_sample(w, rows):
     stride = int(w["row_stride"])
     out["logits"] = w["logits"][rows] if stride else w["logits"]
     for key in ("temperature", "top_k", "top_p", "min_p", "repetition", "frequency", "presence",
-                "use_bitmask", "seed", "position"):
+                "use_bitmask", "seed", "position", "row_id"):
         if w.get(key) is not None:
             out[key] = w[key][rows]
     if w.get("bitmask") is not None:

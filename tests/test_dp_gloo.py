@@ -1,0 +1,91 @@
+"""Row-sharded (data-parallel) host logic, on CPU with two gloo ranks.
+
+Each rank samples its own shard of one batch with the CPU oracle; the
+gathered tokens must equal those of the whole batch sampled at once (rows
+are independent, so the data path needs no collective), and the elapsed
+time reduction is the maximum over ranks, as the benchmark reports it.
+"""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+from oracle import oracle as O
+from speculative_verification_gb300 import dp as DP
+from speculative_verification_gb300 import workloads as W
+from tests.parity import subset_sample
+
+ROWS = 10
+
+
+def _batch():
+    return W.make(2, rows=ROWS)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = _batch()
+        start, stop = DP.shard_rows(w["num_rows"], rank, world)
+        shard = subset_sample(w, list(range(start, stop)))
+        shard["row_id"] = np.arange(start, stop, dtype=np.uint32)  # the rows' ids in the whole batch
+        ref = O.process_sample(shard)
+        tokens = [None] * world
+        dist.all_gather_object(tokens, (start, stop, ref["token"].tolist(), ref["status"].tolist()))
+        t = torch.tensor([10.0 * (rank + 1)])  # a stand-in elapsed time per rank
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        seeds = [None] * world
+        dist.all_gather_object(seeds, [DP.ring_seed(2, rank, i) for i in range(4)])
+        if rank == 0:
+            np.save(os.path.join(out_dir, "gathered.npy"), np.array(tokens, dtype=object), allow_pickle=True)
+            np.save(os.path.join(out_dir, "tmax.npy"), t.numpy())
+            np.save(os.path.join(out_dir, "seeds.npy"), np.array(seeds))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_shard_rows_partition():
+    for n in (0, 1, 7, 64, 65):
+        for world in (1, 2, 3, 8):
+            spans = [DP.shard_rows(n, r, world) for r in range(world)]
+            assert spans[0][0] == 0 and spans[-1][1] == n
+            assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+            sizes = [b - a for a, b in spans]
+            assert max(sizes) - min(sizes) <= 1
+    with pytest.raises(ValueError):
+        DP.shard_rows(8, 2, 2)
+
+
+def test_aggregate_rate():
+    assert DP.aggregate_rate(64, 100, 4, 1000.0) == pytest.approx(64 * 100 * 4)
+    with pytest.raises(ValueError):
+        DP.aggregate_rate(64, 1, 1, 0.0)
+
+
+def test_two_gloo_ranks_match_whole_batch(tmp_path):
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True,
+                       start_method="spawn")
+    gathered = np.load(tmp_path / "gathered.npy", allow_pickle=True)
+    whole = O.process_sample(_batch())
+    tok = np.full(ROWS, -2, np.int64)
+    st = np.full(ROWS, -2, np.int64)
+    for start, stop, t, s in gathered:
+        tok[start:stop] = t
+        st[start:stop] = s
+    assert np.array_equal(tok, whole["token"]) and np.array_equal(st, whole["status"])
+    assert float(np.load(tmp_path / "tmax.npy")[0]) == 20.0
+    seeds = np.load(tmp_path / "seeds.npy")
+    assert len(np.unique(seeds)) == seeds.size  # every rank samples its own batches

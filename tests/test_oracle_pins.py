@@ -22,6 +22,7 @@ from oracle import oracle as O
 from speculative_verification_gb300 import workloads as W
 from tests import brute
 from tests.helpers import sample_workload, verify_workload
+from tests.parity import subset_sample
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
@@ -358,3 +359,25 @@ def test_workload_generators_are_seeded():
         assert np.array_equal(a[key], b[key])
     m = W.make(3, rows=2, vocab=1000)
     assert m["bitmask"].shape == (2, 32)
+
+
+def test_row_id_is_philox_counter_word_2():
+    """The draw of a row depends on its own logits, parameters and row id
+    only: reordering a batch while carrying each row's id along leaves every
+    row's token unchanged, and an explicit id equal to the row's index is the
+    default.  The token is the Gumbel argmax with the id in counter word 2."""
+    w = W.make(2, rows=6, vocab=64)
+    base = O.process_sample(w)
+    ids = dict(w, row_id=np.arange(6, dtype=np.uint32))
+    assert np.array_equal(O.process_sample(ids)["token"], base["token"])
+    perm = np.array([4, 1, 5, 0, 3, 2])
+    moved = subset_sample(w, perm)
+    moved["row_id"] = perm.astype(np.uint32)
+    assert np.array_equal(O.process_sample(moved)["token"], base["token"][perm])
+    # brute force on an unfiltered row: argmax of y + g(seed, id, position, t)
+    z = np.random.default_rng(5).normal(0, 1, (1, 64)).astype(np.float32)
+    one = sample_workload(z, temperature=1.0, seed=77, position=[9])
+    for rid in (0, 3, 4000000000):
+        one["row_id"] = np.array([rid], np.uint32)
+        g = np.array([O.gumbel(77, int(np.int32(np.uint32(rid))), 9, t, 0) for t in range(64)])
+        assert O.process_sample(one)["token"][0] == int(np.argmax(z[0].astype(np.float64) + g))

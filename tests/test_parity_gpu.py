@@ -94,6 +94,17 @@ def test_mixed_stress_full_vocab(ss):
     _report("mixed full V", *parity.check_verify(w, run_gpu(ss, w, debug=False)))
 
 
+def test_row_ids(ss):
+    """Caller-given Philox row ids: parity with the oracle, and ids equal to
+    the rows' indices reproduce the default."""
+    w = W.make(2, rows=12, vocab=5003)
+    base = run_gpu(ss, w, debug=False)
+    same = run_gpu(ss, dict(w, row_id=np.arange(12, dtype=np.uint32)), debug=False)
+    assert np.array_equal(base["token"], same["token"])
+    wid = dict(w, row_id=np.random.default_rng(3).integers(0, 2**32, 12, dtype=np.uint64).astype(np.uint32))
+    _report("row ids", *parity.check_sample(wid, run_gpu(ss, wid)))
+
+
 # ---------------------------------------------------------- edge cases
 
 
