@@ -1158,7 +1158,14 @@ __device__ __noinline__ void resolve_cuts(int k_on, int p_on) {
   float lo1 = bucket_floor(m, 63.0f, s1);
   hist_pass<DT>(1, s1, 0.0f, p_on && !k_on, 0.0f, step++, RT);
   locate(RT, !k_on, k_on ? static_cast<unsigned long long>(g.top_k) : T_all, 0, 0);
-  if (g.loc.found) lo1 = fmaxf(lo1, bucket_floor(m, static_cast<float>(g.loc.bucket), s1));
+  if (g.loc.found) {
+    lo1 = fmaxf(lo1, bucket_floor(m, static_cast<float>(g.loc.bucket), s1));
+    // Every token at or above the cut lies in [lo1, m]: the token level only
+    // needs to cover that range, so its 64 buckets can be finer (fewer
+    // refinement passes).  (m - lo1) * s1 < 63 keeps lo1 inside bucket 62.
+    const float range1 = m - lo1;
+    while (s1 < 1048576.0f && s1 * 2.0f * range1 < 63.0f) s1 *= 2.0f;
+  }
   hist_pass<DT>(0, s1, 0.0f, p_on, lo1, step++, R);
 
   // ---- top-k: the k-th token of the order
@@ -1294,6 +1301,16 @@ __device__ __forceinline__ bool in_kept(int32_t t, float y, float m, int mp_on, 
   return true;
 }
 
+// Out-of-line copies of the Gumbel transform and of a single Philox word:
+// called from rarely taken branches of hot loops, where an inlined logf pair
+// or Philox block per unrolled lane would multiply the code the instruction
+// cache has to hold.
+__device__ __noinline__ float gumbel_noise(uint32_t num) { return gumbel_from_numerator(num); }
+__device__ __noinline__ uint32_t philox_numerator(uint64_t seed, uint32_t row, uint32_t pos, uint32_t token,
+                                                  uint32_t stream) {
+  return uniform_numerator(philox_word(seed, row, pos, token, stream));
+}
+
 // The draw: Gumbel-max over K (stream 0).  Also counts |K| and, for a
 // verification position, its fixed-point mass; result in g.fold.
 template <int DT>
@@ -1303,7 +1320,7 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
   const uint32_t rowid = g.rowid, pos = g.pos;
   const int32_t arg = g.arg;
   // the argmax token is always in K: its score seeds the running best
-  const float g0 = gumbel_from_numerator(uniform_numerator(philox_word(seed, rowid, pos, arg, 0)));
+  const float g0 = gumbel_noise(philox_numerator(seed, rowid, pos, arg, 0));
   float bv = __fadd_rn(m, g0);
   int32_t bi = arg;
   int32_t kcount = 0;
@@ -1314,9 +1331,9 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
     if (spec_pos) kmass += fixed_mass(y, m);
     const float slack = 1e-3f + fabsf(y) * 1e-6f;
     if (y + kGumbelMax + slack < bv) return;
-    const uint32_t num = uniform_numerator(philox_word(seed, rowid, pos, static_cast<uint32_t>(t), 0));
+    const uint32_t num = philox_numerator(seed, rowid, pos, static_cast<uint32_t>(t), 0);
     if (y + gumbel_upper_bound(num) + slack < bv) return;
-    const float s = __fadd_rn(y, gumbel_from_numerator(num));
+    const float s = __fadd_rn(y, gumbel_noise(num));
     if (beats(s, t, bv, bi)) {
       bv = s;
       bi = t;
@@ -1374,7 +1391,7 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
 #pragma unroll
     for (int e = 0; e < V::kPer; ++e) {
       if (!((live >> e) & 1u)) continue;
-      const float sc = __fadd_rn(z[e], gumbel_from_numerator(w[e]));
+      const float sc = __fadd_rn(z[e], gumbel_noise(w[e]));
       if (beats(sc, t0 + e, bv, bi)) {
         bv = sc;
         bi = t0 + e;
@@ -1410,8 +1427,8 @@ __device__ __noinline__ void residual_pass(int mp_on, float memb_lo, float inv_s
     const float P = __fmul_rn(__expf(y - m), inv_s);
     const float r = __fsub_rn(P, qrow[t]);
     if (!(r > 0.0f)) return;
-    const uint32_t num = uniform_numerator(philox_word(seed, rowid, pos, static_cast<uint32_t>(t), 2));
-    const float s = __fadd_rn(logf(r), gumbel_from_numerator(num));
+    const uint32_t num = philox_numerator(seed, rowid, pos, static_cast<uint32_t>(t), 2);
+    const float s = __fadd_rn(logf(r), gumbel_noise(num));
     if (beats(s, t, bv, bi)) {
       bv = s;
       bi = t;
