@@ -1611,6 +1611,34 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
     c.hcnt[s] = 0;
     c.hval[s] = 0.0f;
   }
+  // Raw logits of the patched tokens, by slot, until stage 1: the work region
+  // is not in use before the first histogram.
+  float* hraw = reinterpret_cast<float*>(c.work);
+  static_assert(kHashCap * sizeof(float) <= kWorkBytes, "raw patched logits fit the work region");
+
+  // The logit of a patched token, -inf when the grammar mask disallows it
+  // (the mask is applied after penalties and bias, which keep -inf at -inf).
+  auto raw_logit = [&](int32_t t) -> float {
+    float z = V::load_global(row_ptr, t);
+    if (c.use_mask) {
+      const uint32_t word = static_cast<uint32_t>(a.p.bitmask[static_cast<int64_t>(c.req) * a.p.bitmask_stride + (t >> 5)]);
+      if (((word >> (t & 31)) & 1u) == 0u) z = neg_inf();
+    }
+    return z;
+  };
+  // Prefetch, before the table is ready: this thread's first history entry,
+  // draft and bias entry, with their logits, so that the global round trips
+  // overlap the initialisation above.
+  const bool row_ok = (c.status == SS_ROW_OK);
+  const int eh = c.h0 + tid, eb = c.b0 + tid;
+  const int32_t th = (row_ok && eh < c.h1) ? a.p.hist_ids[eh] : -1;
+  const int32_t tb = (row_ok && eb < c.b1) ? a.p.bias_ids[eb] : -1;
+  const float bb = (row_ok && eb < c.b1) ? a.p.bias_vals[eb] : 0.0f;
+  const int32_t td = (row_ok && a.mode == kModeVerify && tid < c.k) ? a.draft_tokens[c.d0 + tid] : -1;
+  auto in_slice = [&](int32_t t) { return t >= lo && t < lo + n; };
+  const float zh = in_slice(th) ? raw_logit(th) : 0.0f;
+  const float zb = in_slice(tb) ? raw_logit(tb) : 0.0f;
+  const float zd = in_slice(td) ? raw_logit(td) : 0.0f;
   __syncthreads();
 
   // Patch table: history (+ drafts before this position) and bias entries.
@@ -1624,44 +1652,52 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
     }
     return -1;
   };
-  if (c.status == SS_ROW_OK) {
-    for (int e = c.h0 + tid; e < c.h1; e += kThreads) {
+  // one counted occurrence of t (its raw logit z): duplicates write the same z
+  auto count = [&](int32_t t, float z) {
+    if (t < 0 || t >= V_) {
+      st_local = max(st_local, SS_ROW_BAD_INDEX);
+      return;
+    }
+    if (!in_slice(t)) return;
+    const int s = insert(t);
+    if (s < 0) {
+      st_local = max(st_local, SS_ROW_LIMIT);
+      return;
+    }
+    atomicAdd(c.hcnt + s, 1);
+    hraw[s] = z;
+  };
+  if (row_ok) {
+    if (eh < c.h1) count(th, zh);
+    for (int e = eh + kThreads; e < c.h1; e += kThreads) {  // histories longer than the block
       const int32_t t = a.p.hist_ids[e];
-      if (t < 0 || t >= V_) {
-        st_local = max(st_local, SS_ROW_BAD_INDEX);
-        continue;
-      }
-      if (t < lo || t >= lo + n) continue;
-      const int s = insert(t);
-      if (s < 0)
-        st_local = max(st_local, SS_ROW_LIMIT);
-      else
-        atomicAdd(c.hcnt + s, 1);
+      count(t, in_slice(t) ? raw_logit(t) : 0.0f);
     }
     if (a.mode == kModeVerify) {
-      for (int e = tid; e < c.k; e += kThreads) {  // every draft must be a token id
-        const int32_t t = a.draft_tokens[c.d0 + e];
-        if (t < 0 || t >= V_) {
+      // every draft must be a token id; the history of position j holds the drafts before j
+      if (tid < c.k) {
+        if (td < 0 || td >= V_)
           st_local = max(st_local, SS_ROW_BAD_INDEX);
-          continue;
-        }
-        if (e >= c.j || t < lo || t >= lo + n) continue;  // history = drafts before j
-        const int s = insert(t);
-        if (s < 0)
-          st_local = max(st_local, SS_ROW_LIMIT);
-        else
-          atomicAdd(c.hcnt + s, 1);
+        else if (tid < c.j)
+          count(td, zd);
+      }
+      for (int e = tid + kThreads; e < c.k; e += kThreads) {
+        const int32_t t = a.draft_tokens[c.d0 + e];
+        if (t < 0 || t >= V_)
+          st_local = max(st_local, SS_ROW_BAD_INDEX);
+        else if (e < c.j)
+          count(t, in_slice(t) ? raw_logit(t) : 0.0f);
       }
     }
-    for (int e = c.b0 + tid; e < c.b1; e += kThreads) {
-      const int32_t t = a.p.bias_ids[e];
-      const float b = a.p.bias_vals[e];
+    for (int e = eb; e < c.b1; e += kThreads) {
+      const int32_t t = (e == eb) ? tb : a.p.bias_ids[e];
+      const float b = (e == eb) ? bb : a.p.bias_vals[e];
       if (!isfinite(b)) st_local = max(st_local, SS_ROW_BAD_PARAM);
       if (t < 0 || t >= V_) {
         st_local = max(st_local, SS_ROW_BAD_INDEX);
         continue;
       }
-      if (t < lo || t >= lo + n) continue;
+      if (!in_slice(t)) continue;
       const int s = insert(t);
       if (s < 0) {
         st_local = max(st_local, SS_ROW_LIMIT);
@@ -1669,15 +1705,16 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
       }
       if (atomicOr(c.hcnt + s, kBiasFlag) & kBiasFlag) st_local = max(st_local, SS_ROW_BAD_INDEX);  // duplicate
       c.hval[s] = b;
+      hraw[s] = (e == eb) ? zb : raw_logit(t);
     }
   }
   __syncthreads();
-  // Processed values of patched tokens (read straight from the global row).
+  // Processed values of patched tokens.
   for (int s = tid; s < kHashCap; s += kThreads) {
     const int32_t t = c.hkey[s];
     if (t < 0) continue;
     atomicOr(c.xm + ((t - lo) >> 5), 1u << ((t - lo) & 31));
-    float z = V::load_global(row_ptr, t);
+    float z = hraw[s];
     const int32_t hc = c.hcnt[s];
     const int32_t cnt = hc & ~kBiasFlag;
     if (cnt > 0) {
@@ -1686,10 +1723,6 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
       z = __fsub_rn(z, c.pres);
     }
     if (hc & kBiasFlag) z = __fadd_rn(z, c.hval[s]);
-    if (c.use_mask) {
-      const uint32_t word = static_cast<uint32_t>(a.p.bitmask[static_cast<int64_t>(c.req) * a.p.bitmask_stride + (t >> 5)]);
-      if (((word >> (t & 31)) & 1u) == 0u) z = neg_inf();
-    }
     c.hval[s] = c.greedy ? z : __fmul_rn(z, c.inv_t);
   }
 
