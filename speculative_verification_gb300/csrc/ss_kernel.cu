@@ -273,6 +273,8 @@ struct Ctx {
   Loc loc;
   int32_t pick;
   uint32_t cursor[2];      // gather slot cursors (used in rank 0), by step parity
+  uint32_t vcount;         // vectors found by for_vectors_above
+  int32_t vlist_cap;       // entries of its index list (the exclusion-bitmap region)
   float kabs[kMaxLevels];  // absolute bucket of the top-k cut at each level
   int32_t cut_on, cut_idx, cut_len;
   uint32_t cut_key;
@@ -515,6 +517,56 @@ __device__ __forceinline__ void push_merge(LevelRec* out, float scale, float bas
   __syncthreads();
 }
 
+// Visits the vectors whose bound reaches `lo` (v < nvec), densely: one scan
+// of the bounds records each thread's passing vectors in a bit mask (vector
+// tid + j * kThreads is bit j); when they fit, their indices are compacted
+// into the exclusion-bitmap region (free once stage 1 is done) so that every
+// lane of a warp has a vector, rather than the few whose vector passes while
+// the rest idle through the same instructions; when more pass, the slice is
+// walked with the masks.  Every thread calls f(v) the same number of times,
+// v = -1 for none, so f may use warp-collective operations.  Called by all
+// threads.
+template <int DT, typename F>
+__device__ __forceinline__ void for_vectors_above(float lo, F&& f) {
+  using V = Vec<DT>;
+  static_assert(kMaxSliceTokens / 4 <= 32 * kThreads, "one mask bit per vector and thread");
+  const int nvec = (g.n + V::kPer - 1) / V::kPer;
+  const int iters = (nvec + kThreads - 1) / kThreads;
+  uint16_t* list = reinterpret_cast<uint16_t*>(g.xm);
+  const uint32_t cap = static_cast<uint32_t>(g.vlist_cap);
+  const int lane = threadIdx.x & 31;
+  __syncthreads();  // the previous call's readers are done
+  if (threadIdx.x == 0) g.vcount = 0;
+  uint32_t bits = 0;
+  for (int j = 0; j < iters; ++j) {
+    const int v = j * kThreads + static_cast<int>(threadIdx.x);
+    if (v < nvec && vec_bound(v) >= lo) bits |= 1u << j;
+  }
+  const uint32_t mine = static_cast<uint32_t>(__popc(bits));
+  uint32_t incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  __syncthreads();  // vcount reset is visible
+  uint32_t at = 0;
+  if (lane == 31 && incl) at = atomicAdd(&g.vcount, incl);
+  at = __shfl_sync(0xffffffffu, at, 31) + incl - mine;
+  __syncthreads();
+  const uint32_t total = g.vcount;
+  if (total <= cap) {
+    for (uint32_t r = bits; r; r &= r - 1u) list[at++] = static_cast<uint16_t>((__ffs(r) - 1) * kThreads + threadIdx.x);
+    __syncthreads();
+    for (uint32_t b = 0; b < total; b += kThreads) {
+      const uint32_t i = b + threadIdx.x;
+      f(i < total ? static_cast<int>(list[i]) : -1);
+    }
+  } else {
+    for (int j = 0; j < iters; ++j) f(((bits >> j) & 1u) ? j * kThreads + static_cast<int>(threadIdx.x) : -1);
+  }
+}
+
 // Histogram entry of y: counter row of its bucket when that lies in
 // [base, base + 64), else the spill row kBuckets, so that every entry issues
 // the same instructions (a per-entry branch around the atomics costs far more
@@ -547,13 +599,13 @@ __device__ __forceinline__ void hist_tokens(uint32_t* hc, float scale, float bas
   const uint4* __restrict__ data = reinterpret_cast<const uint4*>(g.data);
   const float m = g.m, inv_t = g.inv_t, ms = __fmul_rn(g.m, scale);
   const int ib = small_int(base);
-  for (int v = threadIdx.x; v < nvec; v += kThreads) {
-    if (vec_bound(v) < lo_y) continue;
+  for_vectors_above<DT>(lo_y, [&](int v) {
+    if (v < 0) return;
     float z[V::kPer];
     V::unpack(data[v], z);
 #pragma unroll
     for (int e = 0; e < V::kPer; ++e) hist_add<kMass>(hc, m, __fmul_rn(z[e], inv_t), scale, ms, ib, copy);
-  }
+  });
   for (int s = threadIdx.x; s < kHashCap; s += kThreads) {
     const float y = g.hval[s];
     hist_add<kMass>(hc, m, (g.hkey[s] >= 0 && y >= lo_y) ? y : neg_inf(), scale, ms, ib, copy);
@@ -705,12 +757,11 @@ __device__ __noinline__ void gather_pass(float scale, float abs, float lo_y, int
   const int nvec = (g.n + V::kPer - 1) / V::kPer;
   const uint4* data = reinterpret_cast<const uint4*>(g.data);
   const int lo = g.lo;
-  // every thread runs the same number of iterations (warp-collective appends)
-  for (int vb = 0; vb < nvec; vb += kThreads) {
-    const int v = vb + static_cast<int>(threadIdx.x);
+  // every thread makes the same number of calls (warp-collective appends)
+  for_vectors_above<DT>(lo_y, [&](int v) {
     float y[V::kPer];
     uint32_t hits = 0;
-    if (v < nvec && vec_bound(v) >= lo_y) {
+    if (v >= 0) {
       float z[V::kPer];
       V::unpack(data[v], z);
 #pragma unroll
@@ -720,7 +771,7 @@ __device__ __noinline__ void gather_pass(float scale, float abs, float lo_y, int
       }
     }
     if (__any_sync(0xffffffffu, hits != 0)) warp_append<V::kPer>(hits, y, lo + v * V::kPer, cursor, list);
-  }
+  });
   for (int sb = 0; sb < kHashCap; sb += kThreads) {
     const int s = sb + static_cast<int>(threadIdx.x);
     const int32_t t = g.hkey[s];
@@ -1135,16 +1186,13 @@ __device__ __noinline__ void resolve_cuts(int k_on, int p_on) {
       const float lo_y = m - kMassCutoff - 1.0f - fabsf(m) * 1e-6f;
       const int nvec = (g.n + V::kPer - 1) / V::kPer;
       const uint4* data = reinterpret_cast<const uint4*>(g.data);
-      for (int v = threadIdx.x; v < nvec; v += kThreads) {
-        if (vec_bound(v) < lo_y) continue;
+      for_vectors_above<DT>(lo_y, [&](int v) {
+        if (v < 0) return;
         float z[V::kPer];
         V::unpack(data[v], z);
 #pragma unroll
-        for (int e = 0; e < V::kPer; ++e) {
-          const float y = __fmul_rn(z[e], g.inv_t);
-          if (y != neg_inf()) mine += fixed_mass(y, m);
-        }
-      }
+        for (int e = 0; e < V::kPer; ++e) mine += fixed_mass(__fmul_rn(z[e], g.inv_t), m);  // 0 for -inf
+      });
       for (int s = threadIdx.x; s < kHashCap; s += kThreads)
         if (g.hkey[s] >= 0 && g.hval[s] != neg_inf()) mine += fixed_mass(g.hval[s], m);
       reduce_fold(3, neg_inf(), kNoCut, 0, 0, mine, pos_inf(), neg_inf(), 0.0f, neg_inf(), 0);
@@ -1347,11 +1395,11 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
   const uint32_t cut_key = g.cut_key;
   const int32_t cut_idx = g.cut_idx;
   constexpr int kGroups = V::kPer / 4;  // Philox blocks per vector: 4 tokens share one block
-  for (int v = threadIdx.x; v < nvec; v += kThreads) {
+  for_vectors_above<DT>(k_lo, [&](int v) {
+    if (v < 0) return;
     const float ub = vec_bound(v);
-    if (ub < k_lo) continue;
     // plain rows need no mass: a vector that cannot beat the best is skipped
-    if (prune_best && ub + kGumbelMax + 1e-3f + fabsf(ub) * 1e-6f < bv) continue;
+    if (prune_best && ub + kGumbelMax + 1e-3f + fabsf(ub) * 1e-6f < bv) return;
     float z[V::kPer];
     V::unpack(data[v], z);
     const int32_t t0 = lo + v * V::kPer;  // a multiple of 4
@@ -1370,7 +1418,7 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
       if (spec_pos) kmass += in ? fixed_mass(y, m) : 0ull;
     }
     kcount += __popc(mem);
-    if (!cand) continue;
+    if (!cand) return;
     uint32_t w[V::kPer];
 #pragma unroll
     for (int q = 0; q < kGroups; ++q) {  // independent blocks: their rounds interleave
@@ -1378,26 +1426,58 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
 #pragma unroll
       for (int i = 0; i < 4; ++i) w[q * 4 + i] = r.w[i];
     }
-    // the cheap bound of each noise value, then the exact noise only where
-    // that bound still reaches the running best
+    // A candidate can still reach the running best only if its noise
+    // g >= bv - y - slack >= d, d taken at the largest candidate logit with a
+    // slack that covers every candidate (|y| <= |bv| + 20 for candidates).
+    // g increases with u, so that is u >= exp(-exp(-d)): one threshold on
+    // the 24-bit numerators per vector, lowered by a margin for the fast
+    // exponentials; the exact noise is computed only for the survivors.
+    float ymax = neg_inf();
+#pragma unroll
+    for (int e = 0; e < V::kPer; ++e) ymax = fmaxf(ymax, ((cand >> e) & 1u) ? z[e] : neg_inf());
+    const float d = bv - ymax - (1e-3f + (fabsf(bv) + 20.0f) * 1e-6f);
+    uint32_t thr = 0;
+    if (d > 0.0f) {
+      const float u_min = __expf(-__expf(-d));
+      thr = __float2uint_rd(fmaxf(u_min * 16777216.0f * (1.0f - 1e-5f) - 4.0f, 0.0f));
+    }
     uint32_t live = 0;
 #pragma unroll
     for (int e = 0; e < V::kPer; ++e) {
       w[e] = uniform_numerator(w[e]);
-      live |= static_cast<uint32_t>(!(z[e] + gumbel_upper_bound(w[e]) + 1e-3f + fabsf(z[e]) * 1e-6f < bv)) << e;
+      live |= static_cast<uint32_t>(w[e] >= thr) << e;
     }
     live &= cand;
-    if (!live) continue;
+    if (!live) return;
+    if (live & (live - 1u)) {
+      // several survivors: every lane's noise without branches, so that the
+      // independent logf chains overlap
+      float sc[V::kPer];
 #pragma unroll
-    for (int e = 0; e < V::kPer; ++e) {
-      if (!((live >> e) & 1u)) continue;
-      const float sc = __fadd_rn(z[e], gumbel_noise(w[e]));
+      for (int e = 0; e < V::kPer; ++e) sc[e] = __fadd_rn(z[e], gumbel_from_numerator(w[e]));
+#pragma unroll
+      for (int e = 0; e < V::kPer; ++e)
+        if (((live >> e) & 1u) && beats(sc[e], t0 + e, bv, bi)) {
+          bv = sc[e];
+          bi = t0 + e;
+        }
+    } else {
+      const int e = __ffs(live) - 1;
+      float ze = z[0];
+      uint32_t we = w[0];
+#pragma unroll
+      for (int q = 1; q < V::kPer; ++q)
+        if (q == e) {
+          ze = z[q];
+          we = w[q];
+        }
+      const float sc = __fadd_rn(ze, gumbel_noise(we));
       if (beats(sc, t0 + e, bv, bi)) {
         bv = sc;
         bi = t0 + e;
       }
     }
-  }
+  });
   for (int s = threadIdx.x; s < kHashCap; s += kThreads) {
     const int32_t t = g.hkey[s];
     const float y = g.hval[s];
@@ -1437,10 +1517,10 @@ __device__ __noinline__ void residual_pass(int mp_on, float memb_lo, float inv_s
   const int nvec = (g.n + V::kPer - 1) / V::kPer;
   const uint4* data = reinterpret_cast<const uint4*>(g.data);
   const int lo = g.lo;
-  for (int v = threadIdx.x; v < nvec; v += kThreads) {
+  for_vectors_above<DT>(memb_lo, [&](int v) {
+    if (v < 0) return;
     const float ub = vec_bound(v);
-    if (ub < memb_lo) continue;
-    if (ub - m - log_s + kGumbelMax + 1e-3f + fabsf(ub) * 1e-6f < bv) continue;
+    if (ub - m - log_s + kGumbelMax + 1e-3f + fabsf(ub) * 1e-6f < bv) return;
     float z[V::kPer];
     V::unpack(data[v], z);
 #pragma unroll
@@ -1448,7 +1528,7 @@ __device__ __noinline__ void residual_pass(int mp_on, float memb_lo, float inv_s
       const float y = __fmul_rn(z[e], inv_t);
       if (y != neg_inf()) relem(lo + v * V::kPer + e, y);
     }
-  }
+  });
   for (int s = threadIdx.x; s < kHashCap; s += kThreads) {
     const int32_t t = g.hkey[s];
     const float y = g.hval[s];
@@ -1476,6 +1556,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
     c.data = base;
     c.vmax = reinterpret_cast<__nv_bfloat16*>(base + L.vmax_off);
     c.xm = reinterpret_cast<uint32_t*>(base + L.xm_off);
+    c.vlist_cap = L.slice_len / 32 * 2;  // 16-bit entries in the bitmap's words
     c.hkey = reinterpret_cast<int32_t*>(base + L.hk_off);
     c.hcnt = reinterpret_cast<int32_t*>(base + L.hc_off);
     c.hval = reinterpret_cast<float*>(base + L.hv_off);
