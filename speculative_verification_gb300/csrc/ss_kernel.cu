@@ -88,9 +88,10 @@ enum TaskMode { kModeSample = 0, kModeVerify = 1 };
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 __device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
 
-// Order-preserving key: larger y -> larger key.
+// Order-preserving key: larger y -> larger key.  -0 is folded into +0 first
+// so that the two compare equal, as floats do (equal logits order by index).
 __device__ __forceinline__ uint32_t order_key(float y) {
-  const uint32_t b = __float_as_uint(y);
+  const uint32_t b = __float_as_uint(y + 0.0f);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 __device__ __forceinline__ float key_value(uint32_t k) {
@@ -1362,7 +1363,7 @@ __device__ __noinline__ uint32_t philox_numerator(uint64_t seed, uint32_t row, u
 // The draw: Gumbel-max over K (stream 0).  Also counts |K| and, for a
 // verification position, its fixed-point mass; result in g.fold.
 template <int DT>
-__device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, int spec_pos, uint64_t seed) {
+__device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, int spec_pos, int count_k, uint64_t seed) {
   using V = Vec<DT>;
   const float m = g.m, min_p = g.min_p, inv_t = g.inv_t;
   const uint32_t rowid = g.rowid, pos = g.pos;
@@ -1392,7 +1393,7 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
   const int lo = g.lo;
   const uint32_t key0 = static_cast<uint32_t>(seed), key1 = static_cast<uint32_t>(seed >> 32);
   const bool cut_on = g.cut_on != 0;
-  const uint32_t cut_key = g.cut_key;
+  const float yc = key_value(g.cut_key);  // the cut token's logit (when cut_on)
   const int32_t cut_idx = g.cut_idx;
   constexpr int kGroups = V::kPer / 4;  // Philox blocks per vector: 4 tokens share one block
   for_vectors_above<DT>(k_lo, [&](int v) {
@@ -1403,18 +1404,20 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
     float z[V::kPer];
     V::unpack(data[v], z);
     const int32_t t0 = lo + v * V::kPer;  // a multiple of 4
-    // membership in K and candidacy, without a branch per token
+    // membership in K and candidacy, without a branch per token: y > yc or
+    // (y == yc and t <= cut_idx) is the key order of the cut (finite yc, so
+    // -inf is never a member); a candidate needs y + G >= bv, tested with a
+    // slack that covers every candidate (|y| <= |bv| + 20 for candidates)
+    const float cand_lo = bv - kGumbelMax - (1e-3f + (fabsf(bv) + 20.0f) * 1e-6f);
     uint32_t mem = 0, cand = 0;
 #pragma unroll
     for (int e = 0; e < V::kPer; ++e) {
       const float y = __fmul_rn(z[e], inv_t);
       z[e] = y;
-      const uint32_t key = order_key(y);
-      bool in = (y != neg_inf());
-      if (cut_on) in = in && (key > cut_key || (key == cut_key && t0 + e <= cut_idx));
+      bool in = cut_on ? (y > yc || (y == yc && t0 + e <= cut_idx)) : (y != neg_inf());
       if (mp_on) in = in && (__expf(y - m) >= min_p);
-      mem |= static_cast<uint32_t>(in) << e;
-      cand |= static_cast<uint32_t>(in && !(y + kGumbelMax + 1e-3f + fabsf(y) * 1e-6f < bv)) << e;
+      if (count_k) mem |= static_cast<uint32_t>(in) << e;
+      cand |= static_cast<uint32_t>(in && y >= cand_lo) << e;
       if (spec_pos) kmass += in ? fixed_mass(y, m) : 0ull;
     }
     kcount += __popc(mem);
@@ -1992,7 +1995,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
       // the mass S_K needed by a verification position ignores tokens whose
       // fixed-point mass is zero
       if (spec_pos && !need_count) k_lo = fmaxf(k_lo, m - kMassCutoff - 1.0f - fabsf(m) * 1e-6f);
-      draw_pass<DT>(mp_on, k_lo, !spec_pos && !need_count, spec_pos, seed);
+      draw_pass<DT>(mp_on, k_lo, !spec_pos && !need_count, spec_pos, need_count, seed);
       const Part dall = g.fold;
       kept = need_count ? dall.count : (cut_on ? cut_len : c.count);
       token = dall.arg;
