@@ -538,10 +538,14 @@ __device__ __forceinline__ void for_vectors_above(float lo, F&& f) {
   const int lane = threadIdx.x & 31;
   __syncthreads();  // the previous call's readers are done
   if (threadIdx.x == 0) g.vcount = 0;
+  // the bounds as raw bf16 bits: with the pointer hoisted and the loop
+  // unrolled, the loads of several iterations are in flight together
+  const unsigned short* __restrict__ vb = reinterpret_cast<const unsigned short*>(g.vmax);
   uint32_t bits = 0;
+#pragma unroll 8
   for (int j = 0; j < iters; ++j) {
     const int v = j * kThreads + static_cast<int>(threadIdx.x);
-    if (v < nvec && vec_bound(v) >= lo) bits |= 1u << j;
+    if (v < nvec && __uint_as_float(static_cast<uint32_t>(vb[v]) << 16) >= lo) bits |= 1u << j;
   }
   const uint32_t mine = static_cast<uint32_t>(__popc(bits));
   uint32_t incl = mine;
@@ -1397,18 +1401,21 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
   const int32_t cut_idx = g.cut_idx;
   constexpr int kGroups = V::kPer / 4;  // Philox blocks per vector: 4 tokens share one block
   for_vectors_above<DT>(k_lo, [&](int v) {
+    // prune against the best score any lane of the warp has reached (a token
+    // below it cannot win); the lane's own best (bv, bi) is what it reports
+    const float pb = key_value(__reduce_max_sync(0xffffffffu, order_key(bv)));
     if (v < 0) return;
     const float ub = vec_bound(v);
     // plain rows need no mass: a vector that cannot beat the best is skipped
-    if (prune_best && ub + kGumbelMax + 1e-3f + fabsf(ub) * 1e-6f < bv) return;
+    if (prune_best && ub + kGumbelMax + 1e-3f + fabsf(ub) * 1e-6f < pb) return;
     float z[V::kPer];
     V::unpack(data[v], z);
     const int32_t t0 = lo + v * V::kPer;  // a multiple of 4
     // membership in K and candidacy, without a branch per token: y > yc or
     // (y == yc and t <= cut_idx) is the key order of the cut (finite yc, so
-    // -inf is never a member); a candidate needs y + G >= bv, tested with a
-    // slack that covers every candidate (|y| <= |bv| + 20 for candidates)
-    const float cand_lo = bv - kGumbelMax - (1e-3f + (fabsf(bv) + 20.0f) * 1e-6f);
+    // -inf is never a member); a candidate needs y + G >= pb, tested with a
+    // slack that covers every candidate (|y| <= |pb| + 20 for candidates)
+    const float cand_lo = pb - kGumbelMax - (1e-3f + (fabsf(pb) + 20.0f) * 1e-6f);
     uint32_t mem = 0, cand = 0;
 #pragma unroll
     for (int e = 0; e < V::kPer; ++e) {
@@ -1430,15 +1437,15 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
       for (int i = 0; i < 4; ++i) w[q * 4 + i] = r.w[i];
     }
     // A candidate can still reach the running best only if its noise
-    // g >= bv - y - slack >= d, d taken at the largest candidate logit with a
-    // slack that covers every candidate (|y| <= |bv| + 20 for candidates).
+    // g >= pb - y - slack >= d, d taken at the largest candidate logit with a
+    // slack that covers every candidate (|y| <= |pb| + 20 for candidates).
     // g increases with u, so that is u >= exp(-exp(-d)): one threshold on
     // the 24-bit numerators per vector, lowered by a margin for the fast
     // exponentials; the exact noise is computed only for the survivors.
     float ymax = neg_inf();
 #pragma unroll
     for (int e = 0; e < V::kPer; ++e) ymax = fmaxf(ymax, ((cand >> e) & 1u) ? z[e] : neg_inf());
-    const float d = bv - ymax - (1e-3f + (fabsf(bv) + 20.0f) * 1e-6f);
+    const float d = pb - ymax - (1e-3f + (fabsf(pb) + 20.0f) * 1e-6f);
     uint32_t thr = 0;
     if (d > 0.0f) {
       const float u_min = __expf(-__expf(-d));
