@@ -99,8 +99,10 @@ enum {
                             frequency / presence / bias value non-finite, negative list
                             length, position outside [0, 2^32 - 1 - k], k > max_draft */
   SS_ROW_TIMEOUT = 5,    /* a bounded wait for an asynchronous copy gave up         */
-  SS_ROW_LIMIT = 6       /* more distinct penalised/biased tokens in one vocabulary
+  SS_ROW_LIMIT = 6,      /* more distinct penalised/biased tokens in one vocabulary
                             slice than the slice's table holds (SS_MAX_PATCHED)     */
+  SS_ROW_UNSUPPORTED = 7 /* vocabulary-sharded path only: top-p or min-p without
+                            top-k, or top_k above the records' list capacity      */
 };
 
 /* Distinct penalised or biased tokens one vocabulary slice can hold. */
@@ -217,6 +219,40 @@ ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t wor
  *     produce undefined results.  Serialise them.
  * Arguments, outputs and the other errors are those of ss_spec_verify. */
 ss_status ss_spec_verify_noalloc(const ss_verify_args* args, ss_stream_t stream);
+
+/* ---------------------------------------------------- vocabulary shards --
+ * Sampling when each GPU holds only a slice of the vocabulary of every row
+ * (a tensor-parallel LM head).  The draw is a Gumbel-max with noise keyed by
+ * the global token id, and the maximum of per-partition maxima is the maximum
+ * (FlashSampling news page: per-tile maxima, then a cross-tile reduction), so
+ * a plain row needs one (score, token) pair per shard; a top-k row needs each
+ * shard's top-k (two-stage top-k, SonicSampler abstract), after which the
+ * merge applies top-p and min-p to the merged top-k exactly as the unsharded
+ * call does.  The result is identical to ss_process_sample on the whole rows.
+ * Rows with top-p or min-p but without top-k would need the whole
+ * distribution and report SS_ROW_UNSUPPORTED.
+ *
+ * ss_sample_shard: args->vocab is the whole vocabulary V; args->logits holds
+ * tokens [vocab_offset, vocab_offset + shard_len) of every row (row r at
+ * logits + r * row_stride elements, row_stride >= shard_len or 0);
+ * vocab_offset is a multiple of 32; history, bias and mask ids are global
+ * (each shard applies the ones it holds).  out_token / out_status / out_kept
+ * and debug_processed are not used (debug_processed must be NULL).  Writes
+ * one record of ss_shard_record_bytes(list_cap) bytes per row to `records`
+ * (device, 8-byte aligned, caller-owned); list_cap in [1, SS_SHARD_MAX_LIST]
+ * bounds the top_k the rows may use.
+ *
+ * ss_merge_shards: the records of num_shards (1..8) shards that together
+ * cover [0, V) exactly once, in any order (`records` is a host array of
+ * device pointers); args supplies num_rows, the same params and the outputs
+ * (out_token, out_status, out_kept as for ss_process_sample); logits is not
+ * read.  Both calls are asynchronous on `stream`. */
+#define SS_SHARD_MAX_LIST 1024
+size_t ss_shard_record_bytes(int32_t list_cap);
+ss_status ss_sample_shard(const ss_sample_args* args, int32_t vocab_offset, int32_t shard_len, int32_t list_cap,
+                          void* records, ss_stream_t stream);
+ss_status ss_merge_shards(const ss_sample_args* args, int32_t num_shards, void* const* records, int32_t list_cap,
+                          ss_stream_t stream);
 
 /* Cluster size (CTAs per vocabulary row) the kernels use for this vocabulary
  * and dtype, or 0 if unsupported.  A row is split over at most 8 CTAs of at

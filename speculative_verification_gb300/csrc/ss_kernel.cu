@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <algorithm>
 #include <string.h>
 
 #include <mutex>
@@ -235,8 +236,27 @@ struct KArgs {
   float* debug_processed;
   int4* ws_results;
   int32_t* ws_counters;
+  // vocabulary shard: tokens [shard_off, shard_off + shard_len) of the rows;
+  // the whole vocabulary (0, vocab) outside the sharded entry point
+  int32_t shard_off, shard_len;
+  uint8_t* shard_rec;  // sharded entry point: per-row records, else NULL
+  int32_t shard_cap;   // list entries per record
   Layout L;
 };
+
+// Head of a row's shard record (followed by shard_cap (y, token) entries).
+struct ShardHead {
+  int32_t status;  // the shard's row status (EMPTY_SET: no allowed token here)
+  int32_t kind;    // 0 greedy (m, arg), 1 draw (best, best_token), 2 list
+  int32_t count;   // allowed tokens in the shard
+  int32_t n;       // list entries written
+  float m;         // largest processed logit (greedy: logit)
+  int32_t arg;     // its lowest token id
+  float best;      // draw: largest y + g of the shard
+  int32_t best_token;
+};
+static_assert(sizeof(ShardHead) == 32, "shard record head is 32 bytes");
+constexpr int kShardGreedy = 0, kShardDraw = 1, kShardList = 2;
 
 // Per-CTA state in (static) shared memory, visible to every device function.
 struct Ctx {
@@ -1500,6 +1520,39 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
   reduce_fold(1, bv, bi, kcount, 0, kmass, pos_inf(), neg_inf(), 0.0f, xy, xhere);
 }
 
+// Sharded top-k row: appends the shard's members of K (the k-cut's prefix,
+// or every allowed token when there is no cut) to the row's record as
+// (y, token id) pairs; `cursor` counts them (set to 0 at set-up).
+template <int DT>
+__device__ __noinline__ void emit_members(float2* list, int32_t* cursor, int cap) {
+  using V = Vec<DT>;
+  const bool cut_on = g.cut_on != 0;
+  const float yc = key_value(g.cut_key);
+  const int32_t cut_idx = g.cut_idx;
+  const float inv_t = g.inv_t;
+  const int lo = g.lo;
+  const uint4* data = reinterpret_cast<const uint4*>(g.data);
+  auto put = [&](int32_t t, float y) {
+    const bool in = cut_on ? (y > yc || (y == yc && t <= cut_idx)) : (y != neg_inf());
+    if (in) {
+      const int i = atomicAdd(cursor, 1);
+      if (i < cap) list[i] = make_float2(y, __int_as_float(t));
+    }
+  };
+  for_vectors_above<DT>(cut_on ? yc : neg_inf(), [&](int v) {
+    if (v < 0) return;
+    float z[V::kPer];
+    V::unpack(data[v], z);
+#pragma unroll
+    for (int e = 0; e < V::kPer; ++e) put(lo + v * V::kPer + e, __fmul_rn(z[e], inv_t));
+  });
+  for (int s = threadIdx.x; s < kHashCap; s += kThreads) {
+    const int32_t t = g.hkey[s];
+    if (t >= 0) put(t, g.hval[s]);
+  }
+  __syncthreads();
+}
+
 // Residual max(P - q, 0) at a rejected position: argmax of log r + g over K
 // (stream 2); result in g.fold (arg kNoCut when no token has P > q).
 template <int DT>
@@ -1641,11 +1694,23 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
         !(c.rep > 0.0f) || isinf(c.rep) || !isfinite(c.freq) || !isfinite(c.pres) || c.h1 < c.h0 ||
         c.b1 < c.b0 || pos < 0 || pos + k > 0xffffffffll)
       status = SS_ROW_BAD_PARAM;
+    if (a.shard_rec && status == SS_ROW_OK) {
+      // a shard can list at most shard_cap candidates, and top-p / min-p
+      // without top-k need the whole distribution: not decidable by shards
+      if (c.top_k > a.shard_cap || (c.top_k == 0 && !c.greedy && (c.top_p < 1.0f || c.min_p > 0.0f)))
+        status = SS_ROW_UNSUPPORTED;
+      c.top_p = 1.0f;  // applied by the merge, over the merged top-k list
+      c.min_p = 0.0f;
+    }
     c.status = status;
-    c.lo = rank * L.slice_len;
+    c.lo = a.shard_off + rank * L.slice_len;
     // A row with invalid parameters (including a bad draft count, which makes
     // its row index meaningless) touches no logits: it only reports its status.
-    c.n = (status == SS_ROW_BAD_PARAM) ? 0 : max(0, min(V_ - c.lo, L.slice_len));
+    c.n = (status == SS_ROW_BAD_PARAM || status == SS_ROW_UNSUPPORTED)
+              ? 0
+              : max(0, min(a.shard_off + a.shard_len - c.lo, L.slice_len));
+    if (a.shard_rec && rank == 0)
+      reinterpret_cast<ShardHead*>(a.shard_rec + static_cast<int64_t>(task) * (32 + 8 * a.shard_cap))->n = 0;
     c.cursor[0] = 0;
     c.cursor[1] = 0;
     c.want_s = (T > 0.0f && c.top_p < 1.0f && c.top_k <= 0) ? 1 : 0;
@@ -1654,7 +1719,10 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   if (c.row < 0) return;  // whole cluster: no such target position
 
   const int lo = c.lo, n = c.n;
-  const char* row_ptr = reinterpret_cast<const char*>(a.logits) + static_cast<int64_t>(c.row) * a.row_stride * V::kBytes;
+  // addressed by token id: element t of the row is row_ptr[t] (a shard's
+  // buffer starts at token shard_off)
+  const char* row_ptr = reinterpret_cast<const char*>(a.logits) +
+                        (static_cast<int64_t>(c.row) * a.row_stride - a.shard_off) * V::kBytes;
   const uint32_t slice_bytes = static_cast<uint32_t>(n) * V::kBytes;
   // Bulk (TMA) copies need a 16-byte aligned source; a row whose byte stride
   // is not a multiple of 16 (an odd vocabulary size) is staged with plain,
@@ -2002,10 +2070,24 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
       // the mass S_K needed by a verification position ignores tokens whose
       // fixed-point mass is zero
       if (spec_pos && !need_count) k_lo = fmaxf(k_lo, m - kMassCutoff - 1.0f - fabsf(m) * 1e-6f);
+      if (a.shard_rec && c.top_k > 0) {
+        // sharded top-k row: the shard's top-k (all its allowed tokens when
+        // it has no more than k) go to the record; the merge selects and draws
+        emit_members<DT>(reinterpret_cast<float2*>(a.shard_rec + static_cast<int64_t>(task) * (32 + 8 * a.shard_cap) + 32),
+                         &reinterpret_cast<ShardHead*>(a.shard_rec + static_cast<int64_t>(task) * (32 + 8 * a.shard_cap))->n,
+                         a.shard_cap);
+        kept = cut_on ? cut_len : c.count;
+        token = -1;
+      } else {
       draw_pass<DT>(mp_on, k_lo, !spec_pos && !need_count, spec_pos, need_count, seed);
       const Part dall = g.fold;
       kept = need_count ? dall.count : (cut_on ? cut_len : c.count);
       token = dall.arg;
+      if (a.shard_rec && rank == 0 && tid == 0) {
+        ShardHead* h = reinterpret_cast<ShardHead*>(a.shard_rec + static_cast<int64_t>(task) * (32 + 8 * a.shard_cap));
+        h->best = dall.best;
+        h->best_token = dall.arg;
+      }
       if (spec_pos) {
         const float yx = dall.xhere ? dall.xy : neg_inf();
         const bool x_in = (yx != neg_inf()) && in_kept(c.x, yx, m, mp_on, min_p);
@@ -2025,6 +2107,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
           // else: no token with P > q (rounding): keep the stream-0 draw
         }
       }
+      }
     }
   }
 
@@ -2035,8 +2118,19 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
       kept = 0;
       accept = 0;
     }
-    if (a.out_kept && !c.bad_k) a.out_kept[c.row] = kept;
-    if (a.mode == kModeSample) {
+    if (a.shard_rec) {
+      ShardHead* h = reinterpret_cast<ShardHead*>(a.shard_rec + static_cast<int64_t>(task) * (32 + 8 * a.shard_cap));
+      h->status = status;
+      h->kind = c.greedy ? kShardGreedy : (c.top_k > 0 ? kShardList : kShardDraw);
+      h->count = (status == SS_ROW_OK) ? c.count : 0;
+      h->m = m;
+      h->arg = argmax_tok;
+    } else if (a.out_kept && !c.bad_k) {
+      a.out_kept[c.row] = kept;
+    }
+    if (a.shard_rec) {
+      // the record is the output
+    } else if (a.mode == kModeSample) {
       a.out_token[c.row] = token;
       a.out_status[c.row] = status;
     } else {
@@ -2081,6 +2175,197 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   // The fallback selection reads other CTAs' shared memory; no CTA may leave
   // while that can still happen.
   cl.sync();
+}
+
+// ------------------------------------------------ vocabulary shards --
+
+constexpr int kMaxShards = 8;
+
+struct MergeArgs {
+  int32_t num_rows, num_shards, cap;
+  const uint8_t* rec[kMaxShards];
+  ss_params p;
+  int32_t* out_token;
+  int32_t* out_status;
+  int32_t* out_kept;
+};
+
+// Inclusive block-wide scan of one 64-bit value per thread.
+__device__ __forceinline__ unsigned long long block_scan_u64(unsigned long long x, unsigned long long* ws) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) ws[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    unsigned long long y = (lane < kWarps) ? ws[lane] : 0ull;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned long long z = __shfl_up_sync(0xffffffffu, y, off);
+      if (lane >= off) y += z;
+    }
+    if (lane < kWarps) ws[lane] = y;
+  }
+  __syncthreads();
+  return x + ((wid > 0) ? ws[wid - 1] : 0ull);
+}
+
+// Merge of the shards' records of one row (one CTA per row).  Greedy rows:
+// the largest logit over the shards (lowest id on ties); draw rows: the
+// largest y + g (Gumbel-max decomposes over any partition of the
+// vocabulary); top-k rows: the top-k of the union of the shards' top-k lists
+// (two-stage top-k), then top-p over its renormalised fixed-point masses and
+// min-p, exactly as the unsharded kernel takes them, then the draw over the
+// kept prefix with the same counter-based noise.
+__global__ void __launch_bounds__(kThreads) ss_merge_kernel(const MergeArgs a) {
+  extern __shared__ __align__(16) unsigned long long mkeys[];
+  __shared__ unsigned long long ws[kWarps];
+  __shared__ int32_t s_status, s_kind, s_token, s_kept, s_total, s_lim;
+  __shared__ unsigned long long s_sum;
+  __shared__ int32_t s_n[kMaxShards];
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const int64_t rec_bytes = 32 + 8 * static_cast<int64_t>(a.cap);
+  if (tid == 0) {
+    int32_t st = SS_ROW_OK, kind = kShardDraw, token = -1, kept = 0, total = 0;
+    bool any = false;
+    float bv = neg_inf();
+    int32_t bi = kNoCut;
+    for (int s = 0; s < a.num_shards; ++s) {
+      const ShardHead* h = reinterpret_cast<const ShardHead*>(a.rec[s] + r * rec_bytes);
+      kind = h->kind;
+      s_n[s] = 0;
+      if (h->status == SS_ROW_EMPTY_SET) continue;
+      if (h->status != SS_ROW_OK) {
+        st = max(st, h->status);
+        continue;
+      }
+      any = true;
+      kept += h->count;
+      const float v = (kind == kShardGreedy) ? h->m : h->best;
+      const int32_t t = (kind == kShardGreedy) ? h->arg : h->best_token;
+      if (kind != kShardList && beats(v, t, bv, bi)) {
+        bv = v;
+        bi = t;
+      }
+      s_n[s] = min(h->n, a.cap);
+      total += s_n[s];
+    }
+    if (st == SS_ROW_OK && !any) st = SS_ROW_EMPTY_SET;
+    if (kind == kShardGreedy) kept = 1;
+    token = bi;
+    s_status = st;
+    s_kind = kind;
+    s_token = token;
+    s_kept = kept;
+    s_total = total;
+  }
+  __syncthreads();
+  if (s_status == SS_ROW_OK && s_kind == kShardList) {
+    // the union of the lists as sort keys (y descending, id ascending)
+    const int total = s_total;
+    int np2 = 1;
+    while (np2 < total) np2 <<= 1;
+    int at = 0;
+    for (int s = 0; s < a.num_shards; ++s) {
+      const float2* list = reinterpret_cast<const float2*>(a.rec[s] + r * rec_bytes + 32);
+      for (int i = tid; i < s_n[s]; i += kThreads) {
+        const float2 e = list[i];
+        mkeys[at + i] = sort_key(e.x, __float_as_int(e.y));
+      }
+      at += s_n[s];
+    }
+    for (int i = total + tid; i < np2; i += kThreads) mkeys[i] = ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= np2; k <<= 1)
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int q = tid; q < (np2 >> 1); q += kThreads) {
+          const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1));
+          const unsigned long long x = mkeys[i], y = mkeys[i + j];
+          if ((x > y) == ((i & k) == 0)) {
+            mkeys[i] = y;
+            mkeys[i + j] = x;
+          }
+        }
+        __syncthreads();
+      }
+    const int32_t top_k = a.p.top_k ? a.p.top_k[r] : 0;
+    const float top_p = a.p.top_p ? a.p.top_p[r] : 1.0f;
+    const float min_p = a.p.min_p ? a.p.min_p[r] : 0.0f;
+    const int kk = min(top_k, total);  // the exact top-k (all when k >= allowed)
+    const float m = key_value(sort_key_order(mkeys[0]));
+    if (tid == 0) s_lim = kk;
+    __syncthreads();
+    if (top_p < 1.0f) {
+      // S = the top-k's fixed-point mass; the cut is the first prefix whose
+      // mass reaches ceil(p * S)
+      unsigned long long part = 0;
+      for (int i = tid; i < kk; i += kThreads) part += fixed_mass(key_value(sort_key_order(mkeys[i])), m);
+      unsigned long long incl = block_scan_u64(part, ws);
+      if (tid == kThreads - 1) s_sum = incl;
+      __syncthreads();
+      const unsigned long long T = mass_target(top_p, s_sum);
+      unsigned long long before = 0;
+      for (int base = 0; base < kk; base += kThreads) {
+        const int i = base + tid;
+        const unsigned long long f = (i < kk) ? fixed_mass(key_value(sort_key_order(mkeys[i])), m) : 0ull;
+        incl = block_scan_u64(f, ws) + before;
+        if (i < kk && incl >= T && incl - f < T) s_lim = i + 1;  // the one crossing entry
+        if (tid == kThreads - 1) s_sum = incl;
+        __syncthreads();
+        before = s_sum;
+        __syncthreads();
+        if (s_lim < kk || before >= T) break;
+      }
+    }
+    if (min_p > 0.0f) {
+      for (int i = tid; i < kk; i += kThreads)
+        if (!(__expf(key_value(sort_key_order(mkeys[i])) - m) >= min_p)) atomicMin(&s_lim, i);
+      __syncthreads();
+    }
+    const int L = s_lim;
+    // the draw over the kept prefix
+    const uint64_t seed = a.p.seed[r];
+    const uint32_t rowid = a.p.row_id ? a.p.row_id[r] : static_cast<uint32_t>(r);
+    const uint32_t pos = static_cast<uint32_t>(a.p.position[r]);
+    float bv = neg_inf();
+    int32_t bi = kNoCut;
+    for (int i = tid; i < L; i += kThreads) {
+      const unsigned long long e = mkeys[i];
+      const int32_t t = sort_key_token(e);
+      const float sc = __fadd_rn(key_value(sort_key_order(e)), gumbel_noise(philox_numerator(seed, rowid, pos, t, 0)));
+      if (beats(sc, t, bv, bi)) {
+        bv = sc;
+        bi = t;
+      }
+    }
+    Part pp = empty_part();
+    pp.best = bv;
+    pp.arg = bi;
+    warp_part_reduce(pp);
+    Part* wp = reinterpret_cast<Part*>(mkeys);  // the keys are no longer needed
+    __syncthreads();
+    if ((tid & 31) == 0) wp[tid >> 5] = pp;
+    __syncthreads();
+    if (tid < 32) {
+      Part t = (tid < kWarps) ? wp[tid] : empty_part();
+      warp_part_reduce(t);
+      if (tid == 0) {
+        s_token = t.arg;
+        s_kept = L;
+      }
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const bool ok = (s_status == SS_ROW_OK);
+    a.out_token[r] = ok ? s_token : -1;
+    a.out_status[r] = s_status;
+    if (a.out_kept) a.out_kept[r] = ok ? s_kept : 0;
+  }
 }
 
 // ------------------------------------------------------------------ host --
@@ -2155,10 +2440,14 @@ static ss_status check_params(const ss_params& p) {
 
 static ss_status run(const KArgs& ka, int32_t dtype, cudaStream_t stream) {
   const int es = (dtype == SS_DTYPE_BF16) ? 2 : 4;
-  const int cs = choose_cluster(ka.vocab, es);
-  if (cs == 0) return SS_ERR_UNSUPPORTED;
   KArgs k = ka;
-  k.L = make_layout(ka.vocab, es, cs);
+  if (!k.shard_rec) {  // the whole vocabulary
+    k.shard_off = 0;
+    k.shard_len = k.vocab;
+  }
+  const int cs = choose_cluster(k.shard_len, es);
+  if (cs == 0) return SS_ERR_UNSUPPORTED;
+  k.L = make_layout(k.shard_len, es, cs);
   const cudaError_t e = (dtype == SS_DTYPE_BF16) ? launch<SS_DTYPE_BF16>(k, cs, stream)
                                                  : launch<SS_DTYPE_F32>(k, cs, stream);
   if (e != cudaSuccess) {
@@ -2215,6 +2504,82 @@ ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream) {
   k.out_kept = A.out_kept;
   k.debug_processed = A.debug_processed;
   return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t ss_shard_record_bytes(int32_t list_cap) {
+  if (list_cap < 1 || list_cap > SS_SHARD_MAX_LIST) return 0;
+  return 32 + 8 * static_cast<size_t>(list_cap);
+}
+
+ss_status ss_sample_shard(const ss_sample_args* args, int32_t vocab_offset, int32_t shard_len, int32_t list_cap,
+                          void* records, ss_stream_t stream) {
+  using namespace ss;
+  if (!args) return SS_ERR_INVALID_ARG;
+  const ss_sample_args& A = *args;
+  if (A.num_rows < 0 || A.vocab < 1) return SS_ERR_INVALID_ARG;
+  if (A.dtype != SS_DTYPE_F32 && A.dtype != SS_DTYPE_BF16) return SS_ERR_INVALID_ARG;
+  if (vocab_offset < 0 || (vocab_offset & 31) != 0 || shard_len < 1 ||
+      static_cast<int64_t>(vocab_offset) + shard_len > A.vocab)
+    return SS_ERR_INVALID_ARG;
+  if (ss_shard_record_bytes(list_cap) == 0 || !records || (reinterpret_cast<uintptr_t>(records) & 7u) != 0)
+    return SS_ERR_INVALID_ARG;
+  if (A.debug_processed) return SS_ERR_INVALID_ARG;
+  if (A.num_rows == 0) return SS_OK;
+  const int es = (A.dtype == SS_DTYPE_BF16) ? 2 : 4;
+  if (!A.logits || (reinterpret_cast<uintptr_t>(A.logits) % es) != 0) return SS_ERR_INVALID_ARG;
+  if (A.row_stride != 0 && A.row_stride < shard_len) return SS_ERR_INVALID_ARG;
+  if (check_params(A.params) != SS_OK) return SS_ERR_INVALID_ARG;
+  if (A.params.bitmask && A.params.bitmask_stride < (static_cast<int64_t>(A.vocab) + 31) / 32) return SS_ERR_INVALID_ARG;
+  KArgs k{};
+  k.mode = kModeSample;
+  k.num_tasks = A.num_rows;
+  k.vocab = A.vocab;
+  k.dtype = A.dtype;
+  k.row_stride = A.row_stride;
+  k.logits = A.logits;
+  k.p = A.params;
+  k.shard_off = vocab_offset;
+  k.shard_len = shard_len;
+  k.shard_rec = static_cast<uint8_t*>(records);
+  k.shard_cap = list_cap;
+  return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ss_status ss_merge_shards(const ss_sample_args* args, int32_t num_shards, void* const* records, int32_t list_cap,
+                          ss_stream_t stream) {
+  using namespace ss;
+  if (!args || !records) return SS_ERR_INVALID_ARG;
+  const ss_sample_args& A = *args;
+  if (A.num_rows < 0 || A.vocab < 1 || num_shards < 1 || num_shards > kMaxShards) return SS_ERR_INVALID_ARG;
+  if (ss_shard_record_bytes(list_cap) == 0) return SS_ERR_INVALID_ARG;
+  if (A.num_rows == 0) return SS_OK;
+  if (!A.out_token || !A.out_status || check_params(A.params) != SS_OK) return SS_ERR_INVALID_ARG;
+  MergeArgs m{};
+  m.num_rows = A.num_rows;
+  m.num_shards = num_shards;
+  m.cap = list_cap;
+  for (int s = 0; s < num_shards; ++s) {
+    if (!records[s] || (reinterpret_cast<uintptr_t>(records[s]) & 7u) != 0) return SS_ERR_INVALID_ARG;
+    m.rec[s] = static_cast<const uint8_t*>(records[s]);
+  }
+  m.p = A.params;
+  m.out_token = A.out_token;
+  m.out_status = A.out_status;
+  m.out_kept = A.out_kept;
+  // the merged keys, reused for the warp partials of the final argmax
+  const size_t smem = std::max(static_cast<size_t>(num_shards) * list_cap * sizeof(unsigned long long),
+                               static_cast<size_t>(kWarps) * sizeof(Part));
+  const void* fn = reinterpret_cast<const void*>(&ss_merge_kernel);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess) {
+    ss_merge_kernel<<<A.num_rows, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(m);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    g_last_cuda_error = static_cast<int32_t>(e);
+    return SS_ERR_CUDA;
+  }
+  return SS_OK;
 }
 
 ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t workspace_bytes, ss_stream_t stream) {

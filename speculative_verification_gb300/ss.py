@@ -93,6 +93,9 @@ SIGNATURES = {
     "ss_last_cuda_error": ([], C.c_int32),
     "ss_status_string": ([C.c_int], C.c_char_p),
     "ss_version": ([], C.c_char_p),
+    "ss_shard_record_bytes": ([C.c_int32], C.c_size_t),
+    "ss_sample_shard": ([C.POINTER(ss_sample_args), C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p], C.c_int),
+    "ss_merge_shards": ([C.POINTER(ss_sample_args), C.c_int32, C.POINTER(C.c_void_p), C.c_int32, C.c_void_p], C.c_int),
 }
 
 _lib = None
@@ -181,6 +184,38 @@ def ss_process_sample(logits, params, out_token, out_status, *, vocab, dtype, ro
     a.out_kept = _ptr(out_kept)
     a.debug_processed = _ptr(debug_processed)
     _check(load().ss_process_sample(C.byref(a), _stream_handle(stream)))
+
+
+def ss_shard_record_bytes(list_cap):
+    return int(load().ss_shard_record_bytes(int(list_cap)))
+
+
+def ss_sample_shard(logits, params, records, *, vocab, vocab_offset, shard_len, list_cap, num_rows, dtype,
+                    row_stride=None, stream=None):
+    """Records of one vocabulary shard: `logits` holds tokens
+    [vocab_offset, vocab_offset + shard_len) of every row."""
+    a = ss_sample_args()
+    a.num_rows = int(num_rows)
+    a.vocab = int(vocab)
+    a.row_stride = int(shard_len if row_stride is None else row_stride)
+    a.dtype = SS_DTYPE[dtype]
+    a.logits = _ptr(logits)
+    a.params = make_params(params)
+    _check(load().ss_sample_shard(C.byref(a), int(vocab_offset), int(shard_len), int(list_cap), _ptr(records),
+                                  _stream_handle(stream)))
+
+
+def ss_merge_shards(records, params, out_token, out_status, *, vocab, list_cap, out_kept=None, stream=None):
+    """Merge of the records of the shards that cover the vocabulary."""
+    a = ss_sample_args()
+    a.num_rows = int(out_token.numel())
+    a.vocab = int(vocab)
+    a.params = make_params(params)
+    a.out_token = _ptr(out_token)
+    a.out_status = _ptr(out_status)
+    a.out_kept = _ptr(out_kept)
+    ptrs = (C.c_void_p * len(records))(*[r.data_ptr() for r in records])
+    _check(load().ss_merge_shards(C.byref(a), len(records), ptrs, int(list_cap), _stream_handle(stream)))
 
 
 def _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,

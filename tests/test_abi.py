@@ -79,3 +79,33 @@ def test_host_side_argument_errors_launch_nothing(lib):
     assert lib.ss_spec_verify(C.byref(v), C.c_void_p(256), 8, None) == 4  # too small
     v.row_stride = 63  # stride < vocab
     assert lib.ss_spec_verify(C.byref(v), C.c_void_p(256), 1 << 20, None) == 1
+
+
+def test_shard_entry_points_reject_bad_arguments(lib):
+    import ctypes as C
+    assert ss.ss_shard_record_bytes(1) == 40
+    assert ss.ss_shard_record_bytes(1024) == 32 + 8 * 1024
+    assert ss.ss_shard_record_bytes(0) == 0 and ss.ss_shard_record_bytes(1025) == 0
+    a = ss.ss_sample_args()
+    a.num_rows, a.vocab, a.dtype, a.row_stride, a.logits = 2, 1000, 1, 1000, 16
+    a.params.temperature, a.params.seed, a.params.position = 128, 144, 160
+    rec = C.c_void_p(4096)
+    f = lib.ss_sample_shard
+    assert f(C.byref(a), 16, 100, 8, rec, None) == 1    # offset not a multiple of 32
+    assert f(C.byref(a), 960, 100, 8, rec, None) == 1   # shard past the vocabulary
+    assert f(C.byref(a), 0, 0, 8, rec, None) == 1       # empty shard
+    assert f(C.byref(a), 0, 100, 0, rec, None) == 1     # list capacity out of range
+    assert f(C.byref(a), 0, 100, 8, C.c_void_p(4100), None) == 1  # records not 8-byte aligned
+    assert f(C.byref(a), 0, 100, 8, None, None) == 1
+    a.debug_processed = 512
+    assert f(C.byref(a), 0, 100, 8, rec, None) == 1     # no debug output on a shard
+    a.debug_processed = None
+    a.num_rows = 0
+    assert f(C.byref(a), 0, 100, 8, rec, None) == 0     # nothing to do
+    a.num_rows = 2
+    ptrs = (C.c_void_p * 9)(*([4096] * 9))
+    m = lib.ss_merge_shards
+    assert m(C.byref(a), 0, ptrs, 8, None) == 1         # no shards
+    assert m(C.byref(a), 9, ptrs, 8, None) == 1         # more than 8 shards
+    assert m(C.byref(a), 2, ptrs, 8, None) == 1         # no outputs
+    assert m(None, 2, ptrs, 8, None) == 1
