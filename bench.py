@@ -246,6 +246,8 @@ def run_ours(args, rank, world, dist):
     # speculative-verify throughput (secondary metric), same protocol
     spec = run_spec(args, ss, rank, dev, stream) if args.spec_steps > 0 else None
     progress("spec-verify done")
+    sharded = run_sharded(args, ss, rank, dev, stream) if args.shard_steps > 0 else None
+    progress("sharded done")
 
     peak, peak_kind = measured_peak()
     achieved = bytes_per_call / per_call_s / 1e9
@@ -290,6 +292,8 @@ def run_ours(args, rank, world, dist):
     }
     if spec is not None:
         res["spec_verify"] = spec
+    if sharded is not None:
+        res["vocab_sharded"] = sharded
     return res
 
 
@@ -377,6 +381,59 @@ def run_spec(args, ss, rank, dev, stream):
             "logits_GBps": W.algorithmic_bytes(ring_host[0]) * calls / (ms / 1e3) / 1e9}
 
 
+def run_sharded(args, ss, rank, dev, stream, parts=4):
+    """The vocabulary-sharded path on one GPU: `parts` shard launches and
+    one merge per call, on the headline workload with a top-k of 200 given
+    to its top-p / min-p rows (the sharded path needs one)."""
+    import torch
+    ring_host = [W.shardable(workload_for(2, rank, i)) for i in range(max(2, args.ring // 2))]
+    ring = [ss.to_device(w, dev) for w in ring_host]
+    n = int(ring_host[0]["num_rows"])
+    V = int(ring_host[0]["vocab"])
+    cap = 1024
+    bounds = W.even_shards(V, parts)
+    recs = [torch.empty(n * ss.ss_shard_record_bytes(cap), dtype=torch.uint8, device=dev) for _ in bounds]
+    tok = torch.empty(n, dtype=torch.int32, device=dev)
+    st = torch.empty(n, dtype=torch.int32, device=dev)
+    kept = torch.empty(n, dtype=torch.int32, device=dev)
+
+    def call(dw):
+        params = {k: dw.get(k) for k in ss.PARAM_FIELDS}
+        params["bitmask_stride"] = dw.get("bitmask_stride", 0)
+        for (off, length), rec in zip(bounds, recs):
+            ss.ss_sample_shard(dw["logits"][:, off:], params, rec, vocab=V, vocab_offset=off, shard_len=length,
+                               list_cap=cap, num_rows=n, dtype=dw["dtype"], row_stride=int(dw["row_stride"]),
+                               stream=stream)
+        ss.ss_merge_shards(recs, params, tok, st, vocab=V, list_cap=cap, out_kept=kept, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for dw in ring:
+            call(dw)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for dw in ring:
+                call(dw)
+    reps = max(1, args.shard_steps // len(ring))
+    for _ in range(3):
+        g.replay()
+    stream.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    calls = reps * len(ring)
+    return {"workload": W.CONFIG_NAMES[2] + ", top-p / min-p rows with top-k 200", "shards": len(bounds),
+            "rows_per_s": n * calls / (ms / 1e3), "ms_per_call": ms / calls, "calls": calls,
+            "launches_per_call": len(bounds) + 1}
+
+
 # -------------------------------------------------------- oracle timing --
 
 
@@ -457,6 +514,7 @@ def main():
     ap.add_argument("--ring", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--spec-steps", type=int, default=4000)
+    ap.add_argument("--shard-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

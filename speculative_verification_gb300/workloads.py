@@ -279,3 +279,25 @@ def algorithmic_bytes(w):
     if w["kind"] == "verify":
         total += 8 * int(w["draft_tokens"].size)
     return int(total)
+
+
+def shardable(w, k=200):
+    """The same workload with a top-k of `k` on every sampling row that uses
+    top-p or min-p without one (what the vocabulary-sharded path needs)."""
+    w = dict(w)
+    n = int(w["num_rows"])
+    tk = np.array(w["top_k"], np.int32) if w.get("top_k") is not None else np.zeros(n, np.int32)
+    tp = w["top_p"] if w.get("top_p") is not None else np.ones(n, np.float32)
+    mp = w["min_p"] if w.get("min_p") is not None else np.zeros(n, np.float32)
+    need = (tk <= 0) & ((tp < 1) | (mp > 0)) & (w["temperature"] > 0)
+    tk[need] = k
+    w["top_k"] = tk
+    return w
+
+
+def even_shards(vocab, parts):
+    """[(offset, length)] of `parts` shards covering [0, vocab), offsets
+    multiples of 32 (the last shard takes the remainder)."""
+    size = -(-int(vocab) // int(parts))
+    size = -(-size // 32) * 32
+    return [(o, min(size, int(vocab) - o)) for o in range(0, int(vocab), size)]

@@ -29,18 +29,6 @@ def ss():
     return _ss
 
 
-def _shardable(w, k=200):
-    """Top-p / min-p rows also get a top-k (what the sharded path needs)."""
-    w = dict(w)
-    tk = w["top_k"].copy() if w.get("top_k") is not None else np.zeros(w["num_rows"], np.int32)
-    tp = w["top_p"] if w.get("top_p") is not None else np.ones(w["num_rows"], np.float32)
-    mp = w["min_p"] if w.get("min_p") is not None else np.zeros(w["num_rows"], np.float32)
-    need = (tk <= 0) & ((tp < 1) | (mp > 0)) & (w["temperature"] > 0)
-    tk[need] = k
-    w["top_k"] = tk
-    return w
-
-
 def _whole(ss, w):
     dw = ss.to_device(w)
     o = ss.alloc_outputs(dw)
@@ -71,24 +59,18 @@ def _sharded(ss, dw, bounds, order=None):
     return {"token": tok.cpu().numpy(), "status": st.cpu().numpy(), "kept": kept.cpu().numpy()}
 
 
-def _even(V, P):
-    size = -(-V // P)
-    size = -(-size // 32) * 32
-    return [(o, min(size, V - o)) for o in range(0, V, size)]
-
-
 @pytest.mark.parametrize("P", [1, 2, 4, 8])
 def test_sharded_equals_whole_decode(ss, P):
-    w = _shardable(W.make(2, rows=16))
+    w = W.shardable(W.make(2, rows=16))
     dw, whole = _whole(ss, w)
-    got = _sharded(ss, dw, _even(int(w["vocab"]), P))
+    got = _sharded(ss, dw, W.even_shards(int(w["vocab"]), P))
     for k in ("token", "status", "kept"):
         assert np.array_equal(got[k], whole[k]), (k, got[k], whole[k])
     parity.check_sample(w, got)
 
 
 def test_sharded_uneven_shards_any_order_with_mask(ss):
-    w = _shardable(W.make(3, rows=12, vocab=20011), k=64)  # grammar mask, ragged vocabulary
+    w = W.shardable(W.make(3, rows=12, vocab=20011), k=64)  # grammar mask, ragged vocabulary
     dw, whole = _whole(ss, w)
     bounds = [(0, 4000), (4000, 96), (4096, 9600), (13696, 6315)]
     got = _sharded(ss, dw, bounds, order=[2, 0, 3, 1])
@@ -104,7 +86,7 @@ def test_sharded_unsupported_rows(ss):
     w["top_p"] = np.array([0.9, 1.0, 1.0, 0.9, 1.0, 1.0, 1.0, 1.0], np.float32)
     w["min_p"] = np.array([0.0, 0.05, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0], np.float32)
     dw, whole = _whole(ss, w)
-    got = _sharded(ss, dw, _even(5003, 3))
+    got = _sharded(ss, dw, W.even_shards(5003, 3))
     # top-p or min-p without top-k, and top_k above the list capacity
     assert list(got["status"][[0, 1, 4]]) == [7, 7, 7]
     ok = np.array([2, 3, 5, 6, 7])
