@@ -375,7 +375,37 @@ def run_spec(args, ss, rank, dev, stream):
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
     calls = reps * len(ring)
+    # the step after verification (tokens placed for the next step on the
+    # device), timed on its own
+    R, width = out["out_tokens"].shape
+    cap = 4096
+    tokens = torch.zeros((R, cap), dtype=torch.int32, device=dev)
+    seq = torch.zeros(R, dtype=torch.int32, device=dev)
+    pos = torch.zeros(R, dtype=torch.int64, device=dev)
+    nxt = torch.empty(R, dtype=torch.int32, device=dev)
+    cst = torch.empty(R, dtype=torch.int32, device=dev)
+    gc = torch.cuda.CUDAGraph()
+    n_commit = 256
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(gc, stream=stream):
+            for _ in range(n_commit):
+                ss.ss_commit_accepted(out["out_tokens"], out["num_accepted"], out["status"], tokens, seq, pos, nxt,
+                                      cst, stream=stream)
+    with torch.cuda.stream(stream):
+        seq.zero_()
+        gc.replay()
+        seq.zero_()
+    stream.synchronize()
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    with torch.cuda.stream(stream):
+        gc.replay()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    commit_us = c0.elapsed_time(c1) * 1e3 / n_commit
     return {"workload": W.CONFIG_NAMES[4], "target_rows_per_s": rows * calls / (ms / 1e3),
+            "commit_accepted_us_per_call": commit_us,
             "requests_per_s": int(ring_host[0]["num_requests"]) * calls / (ms / 1e3),
             "ms_per_call": ms / calls, "calls": calls,
             "logits_GBps": W.algorithmic_bytes(ring_host[0]) * calls / (ms / 1e3) / 1e9}

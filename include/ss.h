@@ -220,6 +220,27 @@ ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t wor
  * Arguments, outputs and the other errors are those of ss_spec_verify. */
 ss_status ss_spec_verify_noalloc(const ss_verify_args* args, ss_stream_t stream);
 
+/* After a verification call, the next step's inputs without a device-to-host
+ * copy (Accelerating Sonar through speculation, "MTP schedule for a single
+ * token": once the target's inputs are shifted in, a kernel places the next
+ * target tokens into their slots, avoiding the GPU-to-CPU synchronisation on
+ * the accepted lengths).  For each request i whose status[i] is SS_ROW_OK,
+ * its num_accepted[i] + 1 emitted tokens out_tokens[i * (max_draft + 1) +
+ * 0 .. num_accepted[i]] (the accepted drafts and the residual or bonus token)
+ * are appended to tokens[i * capacity + seq_len[i] ...]; seq_len[i] and
+ * position[i] advance by that count and next_token[i] becomes the last of
+ * them; commit_status[i] = SS_ROW_OK.  A request whose tokens would not fit
+ * in `capacity` (or whose num_accepted lies outside [0, max_draft], or whose
+ * seq_len is negative) is left unchanged with commit_status SS_ROW_LIMIT; one whose
+ * status is not SS_ROW_OK is left unchanged with that status copied.  All
+ * pointers are device pointers; tokens is [num_requests, capacity] int32,
+ * seq_len int32, position int64, next_token and commit_status int32.
+ * Asynchronous on `stream`; graph-capturable. */
+ss_status ss_commit_accepted(int32_t num_requests, int32_t max_draft, const int32_t* out_tokens,
+                             const int32_t* num_accepted, const int32_t* status, int32_t* tokens, int32_t capacity,
+                             int32_t* seq_len, int64_t* position, int32_t* next_token, int32_t* commit_status,
+                             ss_stream_t stream);
+
 /* ---------------------------------------------------- vocabulary shards --
  * Sampling when each GPU holds only a slice of the vocabulary of every row
  * (a tensor-parallel LM head).  The draw is a Gumbel-max with noise keyed by

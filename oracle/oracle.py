@@ -115,6 +115,8 @@ def lib():
         L.or_row_probs.restype = C.c_int32
         L.or_residual_probs.argtypes = [C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]
         L.or_residual_probs.restype = C.c_int32
+        L.or_commit_accepted.argtypes = [C.c_int32, C.c_int32] + [C.c_void_p] * 4 + [C.c_int32] + [C.c_void_p] * 4
+        L.or_commit_accepted.restype = None
         _lib = L
     return _lib
 
@@ -287,3 +289,21 @@ def residual_probs(P, q):
     out = np.zeros(P.size, np.float64)
     empty = lib().or_residual_probs(P.size, P.ctypes.data, q.ctypes.data, out.ctypes.data)
     return int(empty), out
+
+
+def commit_accepted(out_tokens, num_accepted, status, tokens, seq_len, position):
+    """The step after verification on copies of the state arrays; returns
+    (tokens, seq_len, position, next_token, commit_status)."""
+    out_tokens = np.ascontiguousarray(out_tokens, np.int32)
+    R, width = out_tokens.shape
+    tokens = np.array(tokens, np.int32, copy=True)
+    seq_len = np.array(seq_len, np.int32, copy=True)
+    position = np.array(position, np.int64, copy=True)
+    next_token = np.full(R, -1, np.int32)
+    cst = np.zeros(R, np.int32)
+    na = np.ascontiguousarray(num_accepted, np.int32)
+    st = np.ascontiguousarray(status, np.int32)
+    lib().or_commit_accepted(R, width - 1, out_tokens.ctypes.data, na.ctypes.data, st.ctypes.data, tokens.ctypes.data,
+                             tokens.shape[1], seq_len.ctypes.data, position.ctypes.data, next_token.ctypes.data,
+                             cst.ctypes.data)
+    return tokens, seq_len, position, next_token, cst

@@ -593,3 +593,29 @@ int or_spec_verify(const or_verify_in* in, or_verify_out* out) {
   }
   return 0;
 }
+
+/* Step after verification: append the emitted tokens of each accepted
+ * request to its token buffer and advance its length and position. */
+void or_commit_accepted(int32_t num_requests, int32_t max_draft, const int32_t* out_tokens,
+                        const int32_t* num_accepted, const int32_t* status, int32_t* tokens, int32_t capacity,
+                        int32_t* seq_len, int64_t* position, int32_t* next_token, int32_t* commit_status) {
+  int32_t i, j;
+  for (i = 0; i < num_requests; ++i) {
+    const int32_t* emitted = out_tokens + (size_t)i * (size_t)(max_draft + 1);
+    int32_t count;
+    if (status[i] != 0) {
+      commit_status[i] = status[i];
+      continue;
+    }
+    count = num_accepted[i] + 1;
+    if (count < 1 || count > max_draft + 1 || seq_len[i] < 0 || (int64_t)seq_len[i] + count > capacity) {
+      commit_status[i] = 6;
+      continue;
+    }
+    for (j = 0; j < count; ++j) tokens[(size_t)i * (size_t)capacity + (size_t)(seq_len[i] + j)] = emitted[j];
+    seq_len[i] += count;
+    position[i] += count;
+    next_token[i] = emitted[count - 1];
+    commit_status[i] = 0;
+  }
+}

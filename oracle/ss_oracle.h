@@ -133,6 +133,21 @@ int or_process_sample(const or_sample_in* in, or_sample_out* out);
 /* Batched speculative verification.  Returns 0. */
 int or_spec_verify(const or_verify_in* in, or_verify_out* out);
 
+/* The step after verification, on the host-visible definition: for request
+ * i whose status is 0, its num_accepted[i] + 1 emitted tokens
+ * out_tokens[i * (max_draft + 1) + 0 .. num_accepted[i]] are appended to
+ * tokens[i * capacity + seq_len[i] ...], seq_len[i] and position[i] advance
+ * by their count and next_token[i] becomes the last of them; commit_status[i]
+ * is 0.  A request whose tokens would not fit (or whose num_accepted lies
+ * outside [0, max_draft], or whose seq_len is negative) is left unchanged
+ * with commit_status 6 (limit); one whose status is not 0 is left unchanged
+ * with that status copied.  (Accelerating Sonar through speculation, "MTP
+ * schedule for a single token": the next target tokens are placed into their
+ * slots on the GPU, with no GPU-to-CPU synchronisation.) */
+void or_commit_accepted(int32_t num_requests, int32_t max_draft, const int32_t* out_tokens,
+                        const int32_t* num_accepted, const int32_t* status, int32_t* tokens, int32_t capacity,
+                        int32_t* seq_len, int64_t* position, int32_t* next_token, int32_t* commit_status);
+
 /* The filtered, renormalised distribution of one sampling row (fp64, zero
  * outside the kept set K; one-hot for greedy rows).  `extra_hist` are tokens
  * appended to the row's history (the drafts preceding a target position).

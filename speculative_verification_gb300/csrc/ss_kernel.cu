@@ -2177,6 +2177,40 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   cl.sync();
 }
 
+// ------------------------------------------------ accepted-token commit --
+
+// One thread per request: append the emitted tokens, advance the length and
+// the position, set the next input token (see ss_commit_accepted).
+__global__ void ss_commit_kernel(int32_t num_requests, int32_t width, const int32_t* __restrict__ out_tokens,
+                                 const int32_t* __restrict__ num_accepted, const int32_t* __restrict__ status,
+                                 int32_t* __restrict__ tokens, int32_t capacity, int32_t* __restrict__ seq_len,
+                                 int64_t* __restrict__ position, int32_t* __restrict__ next_token,
+                                 int32_t* __restrict__ commit_status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= num_requests) return;
+  if (status[i] != SS_ROW_OK) {
+    commit_status[i] = status[i];
+    return;
+  }
+  const int32_t count = num_accepted[i] + 1;
+  const int32_t len = seq_len[i];
+  if (count < 1 || count > width || len < 0 || static_cast<int64_t>(len) + count > capacity) {
+    commit_status[i] = SS_ROW_LIMIT;
+    return;
+  }
+  const int32_t* emitted = out_tokens + static_cast<int64_t>(i) * width;
+  int32_t* dst = tokens + static_cast<int64_t>(i) * capacity + len;
+  int32_t last = -1;
+  for (int j = 0; j < count; ++j) {
+    last = emitted[j];
+    dst[j] = last;
+  }
+  seq_len[i] = len + count;
+  position[i] += count;
+  next_token[i] = last;
+  commit_status[i] = SS_ROW_OK;
+}
+
 // ------------------------------------------------ vocabulary shards --
 
 constexpr int kMaxShards = 8;
@@ -2504,6 +2538,27 @@ ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream) {
   k.out_kept = A.out_kept;
   k.debug_processed = A.debug_processed;
   return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ss_status ss_commit_accepted(int32_t num_requests, int32_t max_draft, const int32_t* out_tokens,
+                             const int32_t* num_accepted, const int32_t* status, int32_t* tokens, int32_t capacity,
+                             int32_t* seq_len, int64_t* position, int32_t* next_token, int32_t* commit_status,
+                             ss_stream_t stream) {
+  using namespace ss;
+  if (num_requests < 0 || max_draft < 0 || capacity < 1) return SS_ERR_INVALID_ARG;
+  if (num_requests == 0) return SS_OK;
+  if (!out_tokens || !num_accepted || !status || !tokens || !seq_len || !position || !next_token || !commit_status)
+    return SS_ERR_INVALID_ARG;
+  const int threads = 256;
+  ss_commit_kernel<<<(num_requests + threads - 1) / threads, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      num_requests, max_draft + 1, out_tokens, num_accepted, status, tokens, capacity, seq_len, position, next_token,
+      commit_status);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    g_last_cuda_error = static_cast<int32_t>(e);
+    return SS_ERR_CUDA;
+  }
+  return SS_OK;
 }
 
 size_t ss_shard_record_bytes(int32_t list_cap) {

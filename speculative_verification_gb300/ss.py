@@ -94,6 +94,7 @@ SIGNATURES = {
     "ss_status_string": ([C.c_int], C.c_char_p),
     "ss_version": ([], C.c_char_p),
     "ss_shard_record_bytes": ([C.c_int32], C.c_size_t),
+    "ss_commit_accepted": ([C.c_int32, C.c_int32] + [C.c_void_p] * 4 + [C.c_int32] + [C.c_void_p] * 5, C.c_int),
     "ss_sample_shard": ([C.POINTER(ss_sample_args), C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p], C.c_int),
     "ss_merge_shards": ([C.POINTER(ss_sample_args), C.c_int32, C.POINTER(C.c_void_p), C.c_int32, C.c_void_p], C.c_int),
 }
@@ -184,6 +185,16 @@ def ss_process_sample(logits, params, out_token, out_status, *, vocab, dtype, ro
     a.out_kept = _ptr(out_kept)
     a.debug_processed = _ptr(debug_processed)
     _check(load().ss_process_sample(C.byref(a), _stream_handle(stream)))
+
+
+def ss_commit_accepted(out_tokens, num_accepted, status, tokens, seq_len, position, next_token, commit_status,
+                       stream=None):
+    """Append each accepted request's emitted tokens to its row of `tokens`
+    ([R, capacity] int32) and advance seq_len / position, on the device."""
+    R, width = out_tokens.shape
+    _check(load().ss_commit_accepted(int(R), int(width) - 1, _ptr(out_tokens), _ptr(num_accepted), _ptr(status),
+                                     _ptr(tokens), int(tokens.shape[1]), _ptr(seq_len), _ptr(position),
+                                     _ptr(next_token), _ptr(commit_status), _stream_handle(stream)))
 
 
 def ss_shard_record_bytes(list_cap):

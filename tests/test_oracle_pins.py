@@ -381,3 +381,22 @@ def test_row_id_is_philox_counter_word_2():
         one["row_id"] = np.array([rid], np.uint32)
         g = np.array([O.gumbel(77, int(np.int32(np.uint32(rid))), 9, t, 0) for t in range(64)])
         assert O.process_sample(one)["token"][0] == int(np.argmax(z[0].astype(np.float64) + g))
+
+
+def test_commit_accepted_hand_example():
+    """The step after verification, on a hand-worked example: request 0
+    accepted 2 drafts (emits 5, 6, 7 after 1 held token), request 1 none
+    (emits 8 at slot 5), request 2 failed (status 3: unchanged), request 3
+    would overflow its buffer, request 4 reports an impossible count."""
+    out = np.array([[5, 6, 7], [8, -1, -1], [1, 2, 3], [4, 4, 4], [9, 9, 9]], np.int32)
+    tokens = np.full((5, 6), -9, np.int32)
+    t, n, p, nxt, st = O.commit_accepted(out, [2, 0, 2, 2, 3], [0, 0, 3, 0, 0], tokens, [1, 5, 0, 4, 0],
+                                         [10, 20, 30, 40, 50])
+    expect = np.full((5, 6), -9, np.int32)
+    expect[0, 1:4] = [5, 6, 7]
+    expect[1, 5] = 8
+    assert np.array_equal(t, expect)
+    assert list(n) == [4, 6, 0, 4, 0]
+    assert list(p) == [13, 21, 30, 40, 50]
+    assert list(nxt) == [7, 8, -1, -1, -1]
+    assert list(st) == [0, 0, 3, 6, 6]

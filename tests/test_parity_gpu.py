@@ -105,6 +105,55 @@ def test_row_ids(ss):
     _report("row ids", *parity.check_sample(wid, run_gpu(ss, wid)))
 
 
+def test_commit_accepted_random(ss):
+    """The device-side commit step equals the oracle's on random states."""
+    from oracle import oracle as O
+    rng = np.random.default_rng(11)
+    R, k, cap = 300, 7, 40
+    out = rng.integers(0, 1000, (R, k + 1)).astype(np.int32)
+    na = rng.integers(-1, k + 2, R).astype(np.int32)  # includes impossible counts
+    st = np.where(rng.random(R) < 0.1, 3, 0).astype(np.int32)
+    tokens = rng.integers(0, 1000, (R, cap)).astype(np.int32)
+    seq = rng.integers(0, cap + 1, R).astype(np.int32)
+    pos = rng.integers(0, 10**6, R).astype(np.int64)
+    ref = O.commit_accepted(out, na, st, tokens, seq, pos)
+    d = {k_: torch.from_numpy(v).cuda() for k_, v in dict(out=out, na=na, st=st, tokens=tokens, seq=seq, pos=pos).items()}
+    nxt = torch.full((R,), -1, dtype=torch.int32, device="cuda")
+    cst = torch.empty(R, dtype=torch.int32, device="cuda")
+    ss.ss_commit_accepted(d["out"], d["na"], d["st"], d["tokens"], d["seq"], d["pos"], nxt, cst)
+    torch.cuda.synchronize()
+    got = (d["tokens"].cpu().numpy(), d["seq"].cpu().numpy(), d["pos"].cpu().numpy(), nxt.cpu().numpy(),
+           cst.cpu().numpy())
+    for a, b in zip(got, ref):
+        assert np.array_equal(a, b)
+
+
+def test_verify_then_commit_on_device(ss):
+    """Verification followed by the commit step with no host copy in
+    between: the appended tokens are the verified outputs."""
+    w = W.make(4, requests=12, k=4, vocab=7001)
+    g = run_gpu(ss, w, debug=False)
+    R, width = g["out_tokens"].shape
+    from oracle import oracle as O
+    tokens = np.zeros((R, 16), np.int32)
+    seq = np.full(R, 3, np.int32)
+    pos = np.asarray(w["position"], np.int64).copy()
+    ref = O.commit_accepted(g["out_tokens"], g["num_accepted"], g["status"], tokens, seq, pos)
+    dw = ss.to_device(w)
+    o = ss.alloc_outputs(dw)
+    ss.run(dw, o)
+    dt = torch.from_numpy(tokens).cuda()
+    ds = torch.from_numpy(seq).cuda()
+    dp = torch.from_numpy(pos).cuda()
+    nxt = torch.empty(R, dtype=torch.int32, device="cuda")
+    cst = torch.empty(R, dtype=torch.int32, device="cuda")
+    ss.ss_commit_accepted(o["out_tokens"], o["num_accepted"], o["status"], dt, ds, dp, nxt, cst)
+    torch.cuda.synchronize()
+    for a, b in zip((dt.cpu().numpy(), ds.cpu().numpy(), dp.cpu().numpy(), nxt.cpu().numpy(), cst.cpu().numpy()), ref):
+        assert np.array_equal(a, b)
+    assert (ds.cpu().numpy() == 3 + g["num_accepted"] + 1).all()
+
+
 # ---------------------------------------------------------- edge cases
 
 
