@@ -275,6 +275,42 @@ ss_status ss_sample_shard(const ss_sample_args* args, int32_t vocab_offset, int3
 ss_status ss_merge_shards(const ss_sample_args* args, int32_t num_shards, void* const* records, int32_t list_cap,
                           ss_stream_t stream);
 
+/* ------------------------------------------------ fused LM head + draw --
+ * The LM-head matrix multiply fused with the draw (FlashSampling news page:
+ * the sample is taken inside the matrix multiply that produces the logits,
+ * per-tile maxima of logit + Gumbel noise reduced across tiles, so the [B, V]
+ * logits are never written).  logits[r, t] = sum_k hidden[r, k] * weight[t, k]
+ * with bf16 inputs and fp32 accumulation on the tensor cores; then exactly
+ * the sampling kernel's draw without filters: y = logit * fp32(1/T),
+ * token = argmax over t of y + g(seed, row id, position, t) (stream 0),
+ * temperature 0 = the lowest id of the largest logit.  Penalties, bias,
+ * masks and the top-k / top-p / min-p filters need the materialised row:
+ * use ss_process_sample for them.
+ *   batch in [1, 128]; hidden a multiple of 64; hidden_states [batch, hidden]
+ *   and weight [vocab, hidden] bf16, row-major, 16-byte aligned.
+ *   scratch: device memory of ss_fused_scratch_bytes(batch) bytes, 8-byte
+ *   aligned, cleared by the call (calls sharing it must not overlap).
+ *   out_status: SS_ROW_OK, SS_ROW_BAD_PARAM (temperature < 0 or non-finite,
+ *   position outside [0, 2^32 - 1]), SS_ROW_NONFINITE (a NaN / inf logit),
+ *   SS_ROW_TIMEOUT (a bounded wait inside the kernel gave up).
+ *   debug_logits: [batch, vocab] fp32 logits for tests, or NULL (slow). */
+typedef struct {
+  int32_t batch, hidden, vocab;
+  const void* hidden_states;
+  const void* weight;
+  const float* temperature;     /* [batch] */
+  const uint64_t* seed;         /* [batch] */
+  const int64_t* position;      /* [batch] */
+  const uint32_t* row_id;       /* [batch] or NULL: the row's index */
+  void* scratch;
+  size_t scratch_bytes;
+  int32_t* out_token;           /* [batch] */
+  int32_t* out_status;          /* [batch] */
+  float* debug_logits;
+} ss_fused_args;
+size_t ss_fused_scratch_bytes(int32_t batch);
+ss_status ss_fused_lmhead_sample(const ss_fused_args* args, ss_stream_t stream);
+
 /* Cluster size (CTAs per vocabulary row) the kernels use for this vocabulary
  * and dtype, or 0 if unsupported.  A row is split over at most 8 CTAs of at
  * most 61,440 tokens and 160 KiB each, so the largest vocabulary is 491,520

@@ -307,3 +307,25 @@ def commit_accepted(out_tokens, num_accepted, status, tokens, seq_len, position)
                              tokens.shape[1], seq_len.ctypes.data, position.ctypes.data, next_token.ctypes.data,
                              cst.ctypes.data)
     return tokens, seq_len, position, next_token, cst
+
+
+def lmhead_logits(hidden_bits, weight_bits):
+    """logits = hidden @ weight.T of bf16 inputs, summed in fp64 and rounded
+    to fp32 (a library matrix multiply as one step of the definition)."""
+    h = (np.asarray(hidden_bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    w = (np.asarray(weight_bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return (h @ w.T).astype(np.float32)
+
+
+def lmhead_sample(w):
+    """The draw of the fused LM head: the sampling definition (temperature
+    only) on the fp32 logits; returns process_sample's dict plus the logits."""
+    z = lmhead_logits(w["hidden_states"], w["weight"])
+    B, V = z.shape
+    s = dict(kind="sample", num_rows=B, vocab=V, dtype="f32", logits=z, row_stride=V,
+             temperature=w["temperature"], seed=w["seed"], position=w["position"])
+    if w.get("row_id") is not None:
+        s["row_id"] = w["row_id"]
+    out = process_sample(s)
+    out["logits"] = z
+    return out

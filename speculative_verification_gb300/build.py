@@ -1,6 +1,6 @@
 """Compile libss.so (the sm_103a CUDA kernels + C ABI) in-tree with nvcc.
 
-One translation unit, one -gencode (sm_103a), no cmake; the output goes to
+Two translation units, one -gencode (sm_103a), no cmake; the output goes to
 speculative_verification_gb300/_build/libss.so.
 """
 import os
@@ -12,8 +12,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libss.so")
-SOURCES = ["ss_kernel.cu"]
-DEPS = ["ss_kernel.cu", "ss_philox.cuh", "ss_ptx.cuh"]
+SOURCES = ["ss_kernel.cu", "ss_fused.cu"]
+DEPS = ["ss_kernel.cu", "ss_fused.cu", "ss_philox.cuh", "ss_ptx.cuh"]
 
 NVCC_FLAGS = [
     "-std=c++17", "-O3", "-lineinfo",

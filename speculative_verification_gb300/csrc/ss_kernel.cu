@@ -2405,6 +2405,7 @@ __global__ void __launch_bounds__(kThreads) ss_merge_kernel(const MergeArgs a) {
 // ------------------------------------------------------------------ host --
 
 static thread_local int32_t g_last_cuda_error = 0;
+void set_last_cuda_error(int32_t e) { g_last_cuda_error = e; }
 
 static int choose_cluster(int32_t vocab, int32_t es) {
   for (int cs = 1; cs <= kMaxCluster; cs <<= 1) {

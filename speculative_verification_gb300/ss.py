@@ -46,6 +46,25 @@ class ss_params(C.Structure):
     ]
 
 
+class ss_fused_args(C.Structure):
+    _fields_ = [
+        ("batch", C.c_int32),
+        ("hidden", C.c_int32),
+        ("vocab", C.c_int32),
+        ("hidden_states", C.c_void_p),
+        ("weight", C.c_void_p),
+        ("temperature", C.c_void_p),
+        ("seed", C.c_void_p),
+        ("position", C.c_void_p),
+        ("row_id", C.c_void_p),
+        ("scratch", C.c_void_p),
+        ("scratch_bytes", C.c_size_t),
+        ("out_token", C.c_void_p),
+        ("out_status", C.c_void_p),
+        ("debug_logits", C.c_void_p),
+    ]
+
+
 class ss_sample_args(C.Structure):
     _fields_ = [
         ("num_rows", C.c_int32),
@@ -94,6 +113,8 @@ SIGNATURES = {
     "ss_status_string": ([C.c_int], C.c_char_p),
     "ss_version": ([], C.c_char_p),
     "ss_shard_record_bytes": ([C.c_int32], C.c_size_t),
+    "ss_fused_scratch_bytes": ([C.c_int32], C.c_size_t),
+    "ss_fused_lmhead_sample": ([C.POINTER(ss_fused_args), C.c_void_p], C.c_int),
     "ss_commit_accepted": ([C.c_int32, C.c_int32] + [C.c_void_p] * 4 + [C.c_int32] + [C.c_void_p] * 5, C.c_int),
     "ss_sample_shard": ([C.POINTER(ss_sample_args), C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p], C.c_int),
     "ss_merge_shards": ([C.POINTER(ss_sample_args), C.c_int32, C.POINTER(C.c_void_p), C.c_int32, C.c_void_p], C.c_int),
@@ -195,6 +216,26 @@ def ss_commit_accepted(out_tokens, num_accepted, status, tokens, seq_len, positi
     _check(load().ss_commit_accepted(int(R), int(width) - 1, _ptr(out_tokens), _ptr(num_accepted), _ptr(status),
                                      _ptr(tokens), int(tokens.shape[1]), _ptr(seq_len), _ptr(position),
                                      _ptr(next_token), _ptr(commit_status), _stream_handle(stream)))
+
+
+def ss_fused_scratch_bytes(batch):
+    return int(load().ss_fused_scratch_bytes(int(batch)))
+
+
+def ss_fused_lmhead_sample(hidden_states, weight, temperature, seed, position, scratch, out_token, out_status, *,
+                           row_id=None, debug_logits=None, stream=None):
+    """Sample one token per row of hidden_states @ weight.T (bf16 device
+    tensors [B, d] and [V, d]) without materialising the logits."""
+    a = ss_fused_args()
+    a.batch, a.hidden = int(hidden_states.shape[0]), int(hidden_states.shape[1])
+    a.vocab = int(weight.shape[0])
+    a.hidden_states, a.weight = _ptr(hidden_states), _ptr(weight)
+    a.temperature, a.seed, a.position, a.row_id = _ptr(temperature), _ptr(seed), _ptr(position), _ptr(row_id)
+    a.scratch = _ptr(scratch)
+    a.scratch_bytes = int(scratch.numel() * scratch.element_size())
+    a.out_token, a.out_status = _ptr(out_token), _ptr(out_status)
+    a.debug_logits = _ptr(debug_logits)
+    _check(load().ss_fused_lmhead_sample(C.byref(a), _stream_handle(stream)))
 
 
 def ss_shard_record_bytes(list_cap):

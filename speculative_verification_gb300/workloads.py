@@ -301,3 +301,19 @@ def even_shards(vocab, parts):
     size = -(-int(vocab) // int(parts))
     size = -(-size // 32) * 32
     return [(o, min(size, int(vocab) - o)) for o in range(0, int(vocab), size)]
+
+
+def lmhead(batch=64, hidden=4096, vocab=128256, seed=6):
+    """Synthetic LM-head inputs: hidden states N(0, 1) and weights
+    N(0, 3 / sqrt(hidden)) as bf16 bits (logits about N(0, 3), as in the
+    decode workload), 25% greedy rows, else T ~ U[0.5, 1.5], seeds and
+    positions as in the decode workload."""
+    rng = np.random.default_rng(seed)
+    h = to_bf16_bits(rng.standard_normal((batch, hidden), dtype=np.float32))
+    w = to_bf16_bits((rng.standard_normal((vocab, hidden), dtype=np.float32) * np.float32(3.0 / np.sqrt(hidden))))
+    temp = rng.uniform(0.5, 1.5, batch).astype(np.float32)
+    temp[rng.random(batch) < 0.25] = 0.0
+    return dict(kind="lmhead", name="lmhead B=%d d=%d V=%d bf16" % (batch, hidden, vocab), batch=batch, hidden=hidden,
+                vocab=vocab, hidden_states=h, weight=w, temperature=temp,
+                seed=(1000 + np.arange(batch)).astype(np.uint64),
+                position=rng.integers(0, 4096, batch).astype(np.int64))
