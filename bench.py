@@ -71,10 +71,10 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(workload_key):
+def recorded_traffic(workload_key, name="ss_row_kernel_traffic.md"):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken
     on the current kernel source; otherwise None."""
-    path = os.path.join(ROOT, "profiles", "ss_row_kernel_traffic.md")
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     want = kernel_source_hash()
@@ -248,6 +248,8 @@ def run_ours(args, rank, world, dist):
     progress("spec-verify done")
     sharded = run_sharded(args, ss, rank, dev, stream) if args.shard_steps > 0 else None
     progress("sharded done")
+    fused = run_fused(args, ss, dev, stream, measured_peak()[0]) if args.fused_steps > 0 else None
+    progress("fused done")
 
     peak, peak_kind = measured_peak()
     achieved = bytes_per_call / per_call_s / 1e9
@@ -294,6 +296,8 @@ def run_ours(args, rank, world, dist):
         res["spec_verify"] = spec
     if sharded is not None:
         res["vocab_sharded"] = sharded
+    if fused is not None:
+        res["fused_lmhead"] = fused
     return res
 
 
@@ -464,6 +468,61 @@ def run_sharded(args, ss, rank, dev, stream, parts=4):
             "launches_per_call": len(bounds) + 1}
 
 
+def run_fused(args, ss, dev, stream, peak):
+    """The LM head fused with the draw (B=64, d=4096, V=128256 bf16): the
+    weight matrix (1.05 GB, larger than L2) is streamed from HBM every call;
+    roofline = weight + hidden-state bytes per call over the call's time."""
+    import torch
+    B, d, V = 64, 4096, 128256
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(6)
+    h = torch.randn(B, d, device=dev, generator=gen).to(torch.bfloat16)
+    wt = (torch.randn(V, d, device=dev, generator=gen) * (3.0 / d ** 0.5)).to(torch.bfloat16)
+    temp = torch.rand(B, device=dev, generator=gen) + 0.5
+    seed = torch.arange(B, device=dev, dtype=torch.int64) + 1000
+    pos = torch.zeros(B, device=dev, dtype=torch.int64)
+    scratch = torch.empty(ss.ss_fused_scratch_bytes(B), dtype=torch.uint8, device=dev)
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    st = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def call():
+        ss.ss_fused_lmhead_sample(h, wt, temp, seed, pos, scratch, tok, st, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    stream.synchronize()
+    per_graph = 20
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(per_graph):
+                call()
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    reps = max(1, args.fused_steps // per_graph)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    calls = reps * per_graph
+    ms = t0.elapsed_time(t1) / calls
+    alg = V * d * 2 + B * d * 2
+    ach = alg / (ms / 1e3) / 1e9
+    return {"workload": "fused LM head + draw B=%d d=%d V=%d bf16" % (B, d, V), "kernel": "ss_fused_kernel",
+            "rows_per_s": B / (ms / 1e3), "us_per_call": ms * 1e3, "calls": calls,
+            "tflops": 2.0 * B * d * V / (ms / 1e3) / 1e12, "launches_per_call": 3,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                         "algorithmic_bytes_per_launch": alg,
+                         "traffic": recorded_traffic("fused LM head + draw B=%d d=%d V=%d bf16" % (B, d, V),
+                                                     "ss_fused_kernel_traffic.md")}}
+
+
 # -------------------------------------------------------- oracle timing --
 
 
@@ -545,6 +604,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--spec-steps", type=int, default=4000)
     ap.add_argument("--shard-steps", type=int, default=2000)
+    ap.add_argument("--fused-steps", type=int, default=400)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
