@@ -10,13 +10,15 @@
 // temperature 0 = greedy (lowest id of the largest logit).
 //
 // sm_103a design: one persistent CTA per SM walks vocabulary tiles of 128
-// tokens.  Warp 0 streams 64-wide K slices of the hidden states ([B, d],
-// padded to 128 rows by the copy's zero fill) and of the tile's weight rows
-// with 2-D tensor copies (128-byte swizzle) into a 6-stage shared-memory
+// tokens.  Warp 0 streams 64-wide K slices of the hidden states ([B, d]:
+// 64 rows when B <= 64, the rest of the 128-row tile kept zero) and of the
+// tile's weight rows
+// with 2-D tensor copies (128-byte swizzle) into a 7-stage shared-memory
 // ring; warp 1 issues tcgen05.mma (M = 128 rows, N = 128 tokens, K = 16,
 // bf16 in, fp32 accumulate) into one of two tensor-memory accumulators;
-// warps 4-7 (one per 32-lane quarter of tensor memory) read the finished
-// accumulator with tcgen05.ld, add the noise and keep each row's best, while
+// warps 4-11 (two per 32-lane quarter of tensor memory, each on half of the
+// columns) read the finished accumulator with tcgen05.ld, add the noise and
+// keep each row's best, while
 // the next tile accumulates into the other buffer.  Rows end with one 64-bit
 // atomic maximum per CTA on (order key of the score, inverted token id).
 #include <cuda.h>
@@ -40,11 +42,12 @@ constexpr int kBM = 128;                     // batch rows per MMA (rows past th
 constexpr int kBN = 128;                     // vocabulary tokens per tile
 constexpr int kBK = 64;                      // K per stage: one 128-byte swizzle span of bf16
 constexpr int kUK = 16;                      // K of one tcgen05.mma for 16-bit inputs
-constexpr int kStages = 6;
+constexpr int kStages = 7;
 constexpr int kTileA = kBM * kBK * 2;        // 16 KiB
 constexpr int kTileB = kBN * kBK * 2;        // 16 KiB
 constexpr int kStageBytes = kTileA + kTileB;
-constexpr int kThreadsF = 256;
+constexpr int kEpiWarps = 8;                 // two per tensor-memory lane quarter, each half of the columns
+constexpr int kThreadsF = 128 + 32 * kEpiWarps;
 constexpr int kTmemCols = 2 * kBN;           // two fp32 accumulators of 128 columns
 constexpr uint32_t kPolls = 1u << 24;        // bounded waits
 constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + 1024;  // + alignment slack
@@ -59,6 +62,7 @@ struct FArgs {
   int32_t* flags;            // [batch] bit 0: non-finite logit seen, bit 1: bad parameters
   int32_t* error;            // [1] a bounded wait gave up
   float* debug_logits;       // [batch, vocab] or NULL
+  int32_t a_rows;            // rows of hidden states each copy brings (64 when batch <= 64, else 128)
 };
 
 __device__ __forceinline__ float f_neg_inf() { return __int_as_float(0xff800000); }
@@ -158,9 +162,18 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull + i, 1);
-      mbar_init(tempty + i, 128);
+      mbar_init(tempty + i, 32 * kEpiWarps);
     }
     fence_barrier_init();
+  }
+  if (a.a_rows < kBM) {
+    // the copies fill rows [0, a_rows) of each stage's A tile; the rest stays
+    // zero for the whole launch (the MMA reads 128 rows)
+    for (int s = 0; s < kStages; ++s) {
+      uint4* z = reinterpret_cast<uint4*>(ring + s * kStageBytes + a.a_rows * kBK * 2);
+      for (int i = threadIdx.x; i < (kBM - a.a_rows) * kBK * 2 / 16; i += kThreadsF) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
   }
   if (warp == 1) {  // the whole warp allocates the accumulators
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_slot)),
@@ -183,7 +196,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           ok = wait_bounded(empty + stage, phase ^ 1u, a.error);
           if (!ok) break;
           uint8_t* sa = ring + stage * kStageBytes;
-          mbar_arrive_expect_tx(full + stage, kStageBytes);
+          mbar_arrive_expect_tx(full + stage, static_cast<uint32_t>(a.a_rows * kBK * 2 + kTileB));
           tma_2d(sa, &tm_h, k * kBK, 0, full + stage);
           tma_2d(sa + kTileA, &tm_w, k * kBK, tile * kBN, full + stage);
           if (++stage == kStages) {
@@ -223,8 +236,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         }
       }
     }
-  } else if (warp >= 4) {  // epilogue: one batch row per thread
-    const int q = warp - 4;  // tensor-memory lane quarter
+  } else if (warp >= 4) {  // epilogue: one batch row per thread, half of each tile's columns
+    const int q = warp & 3;                       // tensor-memory lane quarter (warp % 4)
+    const int half = (warp - 4) >> 2;             // which 64 columns of the tile
+    constexpr int kHalfCols = kBN / 2;
     const int r = q * 32 + lane;
     const bool live = r < a.batch;
     float inv_t = 1.0f;
@@ -250,7 +265,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       ok = wait_bounded(tfull + acc, acc_phase, a.error);
       if (!ok) break;
       tc_fence_after();
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = half * (kHalfCols / 32); c < (half + 1) * (kHalfCols / 32); ++c) {
         uint32_t v[32];
         __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-row work
         tmem_ld32(tmem + static_cast<uint32_t>(acc * kBN + c * 32) + (static_cast<uint32_t>(q * 32) << 16), v);
@@ -390,7 +405,9 @@ ss_status ss_fused_lmhead_sample(const ss_fused_args* args, ss_stream_t stream) 
   if (A.scratch_bytes < ss_fused_scratch_bytes(A.batch)) return SS_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   CUtensorMap mh, mw;
-  if (!make_map(&mh, A.hidden_states, A.batch, A.hidden, kBM) || !make_map(&mw, A.weight, A.vocab, A.hidden, kBN))
+  const int a_rows = (A.batch <= 64) ? 64 : kBM;
+  if (!make_map(&mh, A.hidden_states, A.batch, A.hidden, static_cast<uint32_t>(a_rows)) ||
+      !make_map(&mw, A.weight, A.vocab, A.hidden, kBN))
     return SS_ERR_UNSUPPORTED;
   uint8_t* sc = static_cast<uint8_t*>(A.scratch);
   unsigned long long* best = reinterpret_cast<unsigned long long*>(sc);
@@ -417,6 +434,7 @@ ss_status ss_fused_lmhead_sample(const ss_fused_args* args, ss_stream_t stream) 
     f.flags = flags;
     f.error = error;
     f.debug_logits = A.debug_logits;
+    f.a_rows = a_rows;
     ss_fused_check<<<(A.batch + 127) / 128, 128, 0, s>>>(A.batch, A.temperature, A.position, flags);
     ss_fused_kernel<<<tiles < sms ? tiles : sms, kThreadsF, kSmemBytes, s>>>(mh, mw, f);
     ss_fused_finish<<<(A.batch + 127) / 128, 128, 0, s>>>(A.batch, best, flags, error, A.out_token, A.out_status);
