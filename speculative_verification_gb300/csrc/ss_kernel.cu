@@ -241,8 +241,82 @@ struct KArgs {
   int32_t shard_off, shard_len;
   uint8_t* shard_rec;  // sharded entry point: per-row records, else NULL
   int32_t shard_cap;   // list entries per record
+  // 0: every row; 1 / 2: only the light / heavy rows (see row_is_heavy),
+  // the others are left to a concurrent launch of the other class
+  int32_t row_class;
   Layout L;
 };
+
+// Rows with a top-p cut and no top-k need the probability mass of the whole
+// row (the online softmax sum, then a histogram descent over the flat part of
+// the distribution) and draw over a kept set of thousands of tokens: several
+// times the work of any other row.  The sampling call gives them twice the
+// CTAs of the others (a second, concurrent launch) so that the launch does not
+// wait on them.  A pure function of the row's parameters: every row is handled
+// by exactly one of the two launches.
+__device__ __forceinline__ bool row_is_heavy(float T, int32_t top_k, float top_p) {
+  return T > 0.0f && top_k <= 0 && top_p < 1.0f;
+}
+
+// Relative cost of a light row, 3 (most) to 0: a large top-k keeps and sorts
+// up to a thousand tokens, a row without top-k draws over most of the
+// vocabulary, a small top-k over a few tokens, and a greedy row only needs
+// the maximum.
+constexpr int32_t kLightTopK = 128;
+__device__ __forceinline__ int light_cost(float T, int32_t top_k) {
+  if (T == 0.0f) return 0;
+  if (top_k > kLightTopK) return 3;
+  return top_k <= 0 ? 2 : 1;
+}
+
+// In a launch that serves one class of rows, cluster i takes the i-th row of
+// the class, costliest first and in row order within a cost level, so that the
+// longest rows start in the first wave and the clusters left over (past the
+// class's rows, they return at once) come last.  Every thread of the CTA
+// calls it; every CTA of the cluster gets the same answer.  Returns the task,
+// or -1.  sm: 21 ints of shared memory.
+__device__ int class_task(const KArgs& a, int i, int32_t* sm) {
+  const ss_params& p = a.p;
+  const int n = a.num_tasks;
+  auto level = [&](int r) -> int {
+    const float T = p.temperature[r];
+    const int32_t tk = p.top_k ? p.top_k[r] : 0;
+    const bool heavy = row_is_heavy(T, tk, p.top_p ? p.top_p[r] : 1.0f);
+    if (1 + static_cast<int>(heavy) != a.row_class) return -1;
+    return heavy ? 0 : light_cost(T, tk);
+  };
+  if (threadIdx.x < 4) sm[threadIdx.x] = 0;
+  if (threadIdx.x == 0) sm[20] = -1;
+  __syncthreads();
+  for (int r = threadIdx.x; r < n; r += kThreads) {
+    const int l = level(r);
+    if (l >= 0) atomicAdd(&sm[l], 1);
+  }
+  __syncthreads();
+  int lv = 3, t = i;
+  while (lv >= 0 && t >= sm[lv]) t -= sm[lv--];
+  if (lv < 0) return -1;
+  // the t-th row of level lv, in row order
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int base = 0;
+  for (int r0 = 0; r0 < n; r0 += kThreads) {
+    const int r = r0 + static_cast<int>(threadIdx.x);
+    const bool f = r < n && level(r) == lv;
+    const unsigned b = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) sm[4 + warp] = __popc(b);
+    __syncthreads();
+    int before = base + __popc(b & ((1u << lane) - 1u)), total = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) before += sm[4 + w];
+      total += sm[4 + w];
+    }
+    if (f && before == t) sm[20] = r;
+    __syncthreads();
+    base += total;
+    if (base > t) break;  // the same for every thread
+  }
+  return sm[20];
+}
 
 // Head of a row's shard record (followed by shard_cap (y, token) entries).
 struct ShardHead {
@@ -1607,8 +1681,12 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   cg::cluster_group cl = cg::this_cluster();
   const int rank = static_cast<int>(cl.block_rank());
   const int ncta = static_cast<int>(cl.num_blocks());
-  const int task = static_cast<int>(blockIdx.x) / ncta;
   const Layout& L = a.L;
+  int task = static_cast<int>(blockIdx.x) / ncta;
+  if (a.row_class != 0) {
+    task = class_task(a, task, reinterpret_cast<int32_t*>(smem_raw + L.red_off));
+    if (task < 0) return;  // the whole cluster: no row of this class left
+  }
   Ctx& c = g;
   const int tid = threadIdx.x;
   const int V_ = a.vocab;
@@ -2449,6 +2527,11 @@ static cudaError_t launch(const KArgs& ka, int cs, cudaStream_t stream) {
   const void* fn = reinterpret_cast<const void*>(&ss_row_kernel<DT>);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ka.L.total);
   if (e != cudaSuccess) return e;
+  // The largest shared-memory carve-out for every launch, whatever its
+  // cluster size: an SM switches carve-outs only when idle, so launches that
+  // asked for different ones could not share SMs.
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(ka.num_tasks) * cs, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -2473,14 +2556,14 @@ static ss_status check_params(const ss_params& p) {
   return SS_OK;
 }
 
-static ss_status run(const KArgs& ka, int32_t dtype, cudaStream_t stream) {
+static ss_status run(const KArgs& ka, int32_t dtype, cudaStream_t stream, int cs_override = 0) {
   const int es = (dtype == SS_DTYPE_BF16) ? 2 : 4;
   KArgs k = ka;
   if (!k.shard_rec) {  // the whole vocabulary
     k.shard_off = 0;
     k.shard_len = k.vocab;
   }
-  const int cs = choose_cluster(k.shard_len, es);
+  const int cs = cs_override ? cs_override : choose_cluster(k.shard_len, es);
   if (cs == 0) return SS_ERR_UNSUPPORTED;
   k.L = make_layout(k.shard_len, es, cs);
   const cudaError_t e = (dtype == SS_DTYPE_BF16) ? launch<SS_DTYPE_BF16>(k, cs, stream)
@@ -2490,6 +2573,61 @@ static ss_status run(const KArgs& ka, int32_t dtype, cudaStream_t stream) {
     return SS_ERR_CUDA;
   }
   return SS_OK;
+}
+
+// A second stream and fork / join events per host thread and device, for the
+// concurrent heavy-row launch.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static SideStream* side_stream(cudaStream_t main) {
+  static thread_local SideStream side[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideStream& s = side[dev];
+  if (!s.stream) {
+    // created outside stream capture only
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(main, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
+    if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) {
+      s.stream = nullptr;
+      return nullptr;
+    }
+  }
+  return &s;
+}
+
+// Sampling launch: when the rows are many and the cluster can double, the
+// heavy rows run on a second stream with twice the CTAs per row while the
+// light rows run on the caller's stream; the caller's stream waits for both.
+static ss_status run_sample(const KArgs& ka, int32_t dtype, cudaStream_t stream) {
+  const int es = (dtype == SS_DTYPE_BF16) ? 2 : 4;
+  const int cs = choose_cluster(ka.vocab, es);
+  SideStream* side = nullptr;
+  if (ka.num_tasks >= 16 && cs >= 2 && 2 * cs <= kMaxCluster && !ka.debug_processed) side = side_stream(stream);
+  if (!side) return run(ka, dtype, stream);
+  KArgs heavy = ka, light = ka;
+  heavy.row_class = 2;
+  light.row_class = 1;
+  cudaError_t e = cudaEventRecord(side->fork, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = static_cast<int32_t>(e);
+    return SS_ERR_CUDA;
+  }
+  const ss_status sh = run(heavy, dtype, side->stream, 2 * cs);
+  const ss_status sl = run(light, dtype, stream, cs);
+  e = cudaEventRecord(side->join, side->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side->join, 0);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = static_cast<int32_t>(e);
+    return SS_ERR_CUDA;
+  }
+  return sh != SS_OK ? sh : sl;
 }
 
 }  // namespace ss
@@ -2538,7 +2676,7 @@ ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream) {
   k.out_status = A.out_status;
   k.out_kept = A.out_kept;
   k.debug_processed = A.debug_processed;
-  return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
+  return run_sample(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 ss_status ss_commit_accepted(int32_t num_requests, int32_t max_draft, const int32_t* out_tokens,
