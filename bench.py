@@ -50,10 +50,18 @@ def progress(msg):
 _T0 = time.time()
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "ss_row_kernel": "ss_kernel.cu",
+    "ss_fused_kernel": "ss_fused.cu",
+}
+
+
+def kernel_source_hash(kernel="ss_row_kernel"):
+    """Hash of the sources one kernel is compiled from: its translation unit,
+    the shared device headers and the C header."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_verification_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in (KERNEL_SOURCES[kernel], "ss_philox.cuh", "ss_ptx.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     with open(os.path.join(ROOT, "include", "ss.h"), "rb") as f:
@@ -71,13 +79,14 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(workload_key, name="ss_row_kernel_traffic.md"):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the current kernel source; otherwise None."""
-    path = os.path.join(ROOT, "profiles", name)
+def recorded_traffic(workload_key, kernel="ss_row_kernel"):
+    """Per-launch DRAM bytes from the committed ncu summary
+    (profiles/<kernel>_traffic.md), if it was taken on the current source of
+    that kernel; otherwise None."""
+    path = os.path.join(ROOT, "profiles", kernel + "_traffic.md")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     cur = {}
     for line in open(path):
         line = line.strip().strip("`")
@@ -520,7 +529,8 @@ def run_fused(args, ss, dev, stream, peak):
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
                          "algorithmic_bytes_per_launch": alg,
                          "traffic": recorded_traffic("fused LM head + draw B=%d d=%d V=%d bf16" % (B, d, V),
-                                                     "ss_fused_kernel_traffic.md")}}
+                                                     "ss_fused_kernel"),
+                         "kernel_sha256": kernel_source_hash("ss_fused_kernel")}}
 
 
 # -------------------------------------------------------- oracle timing --

@@ -241,8 +241,9 @@ struct KArgs {
   int32_t shard_off, shard_len;
   uint8_t* shard_rec;  // sharded entry point: per-row records, else NULL
   int32_t shard_cap;   // list entries per record
-  // 0: every row; 1 / 2: only the light / heavy rows (see row_is_heavy),
-  // the others are left to a concurrent launch of the other class
+  // 0: every task in launch order; 1 / 2: only the light / heavy rows (see
+  // row_is_heavy), the others are left to a concurrent launch of the other
+  // class; 3: every task, costliest first (see ordered_task)
   int32_t row_class;
   Layout L;
 };
@@ -269,53 +270,71 @@ __device__ __forceinline__ int light_cost(float T, int32_t top_k) {
   return top_k <= 0 ? 2 : 1;
 }
 
-// In a launch that serves one class of rows, cluster i takes the i-th row of
-// the class, costliest first and in row order within a cost level, so that the
-// longest rows start in the first wave and the clusters left over (past the
-// class's rows, they return at once) come last.  Every thread of the CTA
-// calls it; every CTA of the cluster gets the same answer.  Returns the task,
-// or -1.  sm: 21 ints of shared memory.
-__device__ int class_task(const KArgs& a, int i, int32_t* sm) {
+constexpr int kCostLevels = 5;
+
+// Ordered launches.  With row_class 1 or 2 a sampling launch serves one class
+// of rows (light or heavy, see row_is_heavy); with 3 a launch serves every
+// task, costliest first.  Cluster i takes the i-th task of its launch in that
+// order (cost level descending, task index ascending within a level), so the
+// longest tasks start in the first wave and the clusters left over (past the
+// launch's tasks, they return at once) come last.  A verification position
+// past its request's drafts has no work and is left out; one of a request with
+// a bad draft count only reports the status (cheapest level).  Every thread of
+// the CTA calls it; every CTA of the cluster gets the same answer.  Returns the
+// task, or -1.  sm: 2 + kCostLevels + kWarps ints of shared memory.
+__device__ int ordered_task(const KArgs& a, int i, int32_t* sm) {
   const ss_params& p = a.p;
   const int n = a.num_tasks;
-  auto level = [&](int r) -> int {
-    const float T = p.temperature[r];
-    const int32_t tk = p.top_k ? p.top_k[r] : 0;
-    const bool heavy = row_is_heavy(T, tk, p.top_p ? p.top_p[r] : 1.0f);
+  auto level = [&](int task) -> int {
+    int req = task;
+    if (a.mode == kModeVerify) {
+      const int width = a.max_draft + 1;
+      req = task / width;
+      const int j = task % width;
+      const int32_t k = a.draft_offsets[req + 1] - a.draft_offsets[req];
+      if (k < 0 || k > a.max_draft) return j == 0 ? 0 : -1;
+      if (j > k) return -1;
+    }
+    const float T = p.temperature[req];
+    const int32_t tk = p.top_k ? p.top_k[req] : 0;
+    const bool heavy = row_is_heavy(T, tk, p.top_p ? p.top_p[req] : 1.0f);
+    if (a.row_class == 3) return heavy ? 4 : light_cost(T, tk);
     if (1 + static_cast<int>(heavy) != a.row_class) return -1;
     return heavy ? 0 : light_cost(T, tk);
   };
-  if (threadIdx.x < 4) sm[threadIdx.x] = 0;
-  if (threadIdx.x == 0) sm[20] = -1;
+  int32_t* cnt = sm + 2;
+  int32_t* wsum = cnt + kCostLevels;
+  if (threadIdx.x < kCostLevels) cnt[threadIdx.x] = 0;
+  if (threadIdx.x == 0) sm[0] = -1;
   __syncthreads();
   for (int r = threadIdx.x; r < n; r += kThreads) {
     const int l = level(r);
-    if (l >= 0) atomicAdd(&sm[l], 1);
+    if (l >= 0) atomicAdd(&cnt[l], 1);
   }
   __syncthreads();
-  int lv = 3, t = i;
-  while (lv >= 0 && t >= sm[lv]) t -= sm[lv--];
+  int lv = kCostLevels - 1, t = i;
+  while (lv >= 0 && t >= cnt[lv]) t -= cnt[lv--];
   if (lv < 0) return -1;
-  // the t-th row of level lv, in row order
+  // the t-th task of level lv, in task order
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int base = 0;
   for (int r0 = 0; r0 < n; r0 += kThreads) {
     const int r = r0 + static_cast<int>(threadIdx.x);
     const bool f = r < n && level(r) == lv;
     const unsigned b = __ballot_sync(0xffffffffu, f);
-    if (lane == 0) sm[4 + warp] = __popc(b);
+    if (lane == 0) wsum[warp] = __popc(b);
     __syncthreads();
     int before = base + __popc(b & ((1u << lane) - 1u)), total = 0;
     for (int w = 0; w < kWarps; ++w) {
-      if (w < warp) before += sm[4 + w];
-      total += sm[4 + w];
+      if (w < warp) before += wsum[w];
+      total += wsum[w];
     }
-    if (f && before == t) sm[20] = r;
+    if (f && before == t) sm[0] = r;
     __syncthreads();
     base += total;
     if (base > t) break;  // the same for every thread
   }
-  return sm[20];
+  return sm[0];
 }
 
 // Head of a row's shard record (followed by shard_cap (y, token) entries).
@@ -1684,8 +1703,8 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   const Layout& L = a.L;
   int task = static_cast<int>(blockIdx.x) / ncta;
   if (a.row_class != 0) {
-    task = class_task(a, task, reinterpret_cast<int32_t*>(smem_raw + L.red_off));
-    if (task < 0) return;  // the whole cluster: no row of this class left
+    task = ordered_task(a, task, reinterpret_cast<int32_t*>(smem_raw + L.red_off));
+    if (task < 0) return;  // the whole cluster: no task left for it
   }
   Ctx& c = g;
   const int tid = threadIdx.x;
@@ -2817,6 +2836,8 @@ ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t wor
   k.ws_results = reinterpret_cast<int4*>(workspace);
   k.ws_counters = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
                                              static_cast<size_t>(tasks) * sizeof(int4));
+  // many positions run in several waves: start the costliest first
+  if (tasks >= 16) k.row_class = 3;
   return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
