@@ -96,6 +96,33 @@ class _VerifyOut(C.Structure):
     ]
 
 
+class _TreeIn(C.Structure):
+    _fields_ = [
+        ("num_requests", C.c_int32),
+        ("vocab", C.c_int32),
+        ("max_nodes", C.c_int32),
+        ("row_stride", C.c_int64),
+        ("dtype", C.c_int32),
+        ("target_logits", C.c_void_p),
+        ("node_offsets", C.c_void_p),
+        ("parents", C.c_void_p),
+        ("node_tokens", C.c_void_p),
+        ("draft_probs", C.c_void_p),
+        ("draft_stride", C.c_int64),
+        ("p", _Params),
+    ]
+
+
+class _TreeOut(C.Structure):
+    _fields_ = [
+        ("out_tokens", C.c_void_p),
+        ("out_path", C.c_void_p),
+        ("num_accepted", C.c_void_p),
+        ("status", C.c_void_p),
+        ("sub_margin", C.c_void_p),
+    ]
+
+
 def lib():
     global _lib
     if _lib is None:
@@ -117,6 +144,8 @@ def lib():
         L.or_residual_probs.restype = C.c_int32
         L.or_commit_accepted.argtypes = [C.c_int32, C.c_int32] + [C.c_void_p] * 4 + [C.c_int32] + [C.c_void_p] * 4
         L.or_commit_accepted.restype = None
+        L.or_tree_verify.argtypes = [C.POINTER(_TreeIn), C.POINTER(_TreeOut)]
+        L.or_tree_verify.restype = C.c_int
         _lib = L
     return _lib
 
@@ -270,6 +299,48 @@ def spec_verify(w, want_processed=False, force_kept=None):
     o.kept_lo = _ptr(res["kept_lo"])
     o.kept_hi = _ptr(res["kept_hi"])
     lib().or_spec_verify(C.byref(v), C.byref(o))
+    return res
+
+
+def tree_verify(w):
+    """Run the oracle on a tree-verification workload (kind 'tree'); returns a
+    dict of numpy arrays: out_tokens and out_path [R, max_nodes],
+    num_accepted, status, sub_margin [R]."""
+    keep = []
+    tl = np.ascontiguousarray(w["target_logits"])
+    nof = _c(w["node_offsets"], np.int32)
+    par = _c(w["parents"], np.int32)
+    ntk = _c(w["node_tokens"], np.int32)
+    dpr = _c(w["draft_probs"], np.float32)
+    keep += [tl, nof, par, ntk, dpr]
+    v = _TreeIn()
+    v.num_requests = int(w["num_requests"])
+    v.vocab = int(w["vocab"])
+    v.max_nodes = int(w["max_nodes"])
+    v.row_stride = int(w["row_stride"])
+    v.dtype = OR_DTYPE[w["dtype"]]
+    v.target_logits = tl.ctypes.data
+    v.node_offsets = nof.ctypes.data
+    v.parents = par.ctypes.data if par.size else None
+    v.node_tokens = ntk.ctypes.data if ntk.size else None
+    v.draft_probs = dpr.ctypes.data if dpr.size else None
+    v.draft_stride = int(w["draft_stride"])
+    v.p = _params(w, keep)
+    R, width = v.num_requests, v.max_nodes
+    res = {
+        "out_tokens": np.full((R, width), -1, np.int32),
+        "out_path": np.full((R, width), -1, np.int32),
+        "num_accepted": np.zeros(R, np.int32),
+        "status": np.zeros(R, np.int32),
+        "sub_margin": np.zeros(R, np.uint8),
+    }
+    o = _TreeOut()
+    o.out_tokens = _ptr(res["out_tokens"])
+    o.out_path = _ptr(res["out_path"])
+    o.num_accepted = _ptr(res["num_accepted"])
+    o.status = _ptr(res["status"])
+    o.sub_margin = _ptr(res["sub_margin"])
+    lib().or_tree_verify(C.byref(v), C.byref(o))
     return res
 
 

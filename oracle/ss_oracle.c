@@ -619,3 +619,189 @@ void or_commit_accepted(int32_t num_requests, int32_t max_draft, const int32_t* 
     commit_status[i] = 0;
   }
 }
+
+/* ------------------------------------------------- tree verification -- */
+
+/* Gumbel-max over t in K of log r_t + g_t (stream 2), r_t = p_t - q_t > 0,
+ * for a dense residual base p (fp64).  `scale` bounds how much the rounding
+ * of p may have grown through the normalisations before it (the product of
+ * 1/Z); the sub-margin test perturbs r_t by REL_MARGIN * scale * (p_t + q_t)
+ * and the noise by REL_MARGIN.  Returns -1 when no r_t > 0. */
+static int32_t residual_draw_dense(const row_state* s, const double* p, const float* qrow, double scale,
+                                   uint64_t seed, int32_t row, uint32_t pos, int* flag) {
+  int32_t i, best = -1;
+  double sb = -INFINITY, lo_best = -INFINITY;
+  double* hi = (double*)malloc(sizeof(double) * (size_t)(s->L > 0 ? s->L : 1));
+  int32_t* tok = (int32_t*)malloc(sizeof(int32_t) * (size_t)(s->L > 0 ? s->L : 1));
+  int any_contender = 0;
+  for (i = 0; i < s->L; ++i) {
+    int32_t t = s->order[i];
+    double q = (double)qrow[t];
+    double r = p[t] - q;
+    double d = REL_MARGIN * scale * (p[t] + fabs(q));
+    double g = or_gumbel(seed, row, pos, t, OR_STREAM_RESIDUAL);
+    double geps = REL_MARGIN * fmax(1.0, fabs(g));
+    tok[i] = t;
+    hi[i] = (r + d > 0.0) ? log(r + d) + g + geps : -INFINITY;
+    if (r + d > 0.0) any_contender = 1;
+    if (r > 0.0) {
+      double sc = log(r) + g;
+      if (best < 0 || sc > sb || (sc == sb && t < best)) {
+        best = t;
+        sb = sc;
+        lo_best = (r - d > 0.0) ? log(r - d) + g - geps : -INFINITY;
+      }
+    }
+  }
+  if (best < 0) {
+    if (any_contender) *flag = 1;
+  } else {
+    for (i = 0; i < s->L; ++i)
+      if (tok[i] != best && hi[i] >= lo_best) *flag = 1;
+    if (lo_best == -INFINITY) *flag = 1;
+  }
+  free(hi);
+  free(tok);
+  return best;
+}
+
+/* Depth of local node u (edges to the root); -1 when a parent on the way is
+ * not a smaller index.  path (optional) receives the tokens of the nodes on
+ * the way, u first, the root's child last. */
+static int32_t tree_depth(const int32_t* par, const int32_t* tok, int32_t u, int32_t* path) {
+  int32_t d = 0;
+  while (u > 0) {
+    int32_t pu = par[u];
+    if (pu < 0 || pu >= u) return -1;
+    if (path) path[d] = tok[u];
+    ++d;
+    u = pu;
+  }
+  return d;
+}
+
+int or_tree_verify(const or_tree_in* in, or_tree_out* out) {
+  int32_t i, V = in->vocab, width = in->max_nodes;
+  size_t es = (in->dtype == OR_DTYPE_BF16) ? 2 : 4;
+  for (i = 0; i < in->num_requests; ++i) {
+    int32_t g0 = in->node_offsets[i], nn = in->node_offsets[i + 1] - g0;
+    const int32_t* par = in->parents + g0;
+    const int32_t* tok = in->node_tokens + g0;
+    int32_t* o = out->out_tokens + (size_t)i * (size_t)width;
+    int32_t* op = out->out_path ? out->out_path + (size_t)i * (size_t)width : NULL;
+    int32_t j, u, status = OR_ROW_OK, n_acc = 0, bad_tree = 0, bad_tok = 0;
+    int64_t pos64 = in->p.position[i];
+    int flag = 0;
+    row_state* rows;
+    int32_t* depth;
+    for (j = 0; j < width; ++j) {
+      o[j] = -1;
+      if (op) op[j] = -1;
+    }
+    out->num_accepted[i] = 0;
+    if (out->sub_margin) out->sub_margin[i] = 0;
+    if (nn < 1 || nn > width || nn > 64) {
+      out->status[i] = OR_ROW_BAD_PARAM;
+      continue;
+    }
+    for (u = 1; u < nn; ++u) {
+      if (par[u] < 0 || par[u] >= u) bad_tree = 1;
+      if (tok[u] < 0 || tok[u] >= V) bad_tok = 1;
+    }
+    if (bad_tree) {
+      out->status[i] = OR_ROW_BAD_PARAM;
+      continue;
+    }
+    rows = (row_state*)calloc((size_t)nn, sizeof(row_state));
+    depth = (int32_t*)calloc((size_t)nn, sizeof(int32_t));
+    for (u = 0; u < nn; ++u) {
+      row_in ri;
+      int32_t path[64];
+      const char* zrow = (const char*)in->target_logits + (size_t)(g0 + u) * (size_t)in->row_stride * es;
+      depth[u] = tree_depth(par, tok, u, path);
+      fill_row_in(&ri, &in->p, i, V, in->dtype, zrow);
+      if (pos64 + (nn - 1) > (int64_t)0xFFFFFFFFLL) ri.bad_param = 1;
+      ri.hist2 = path;
+      ri.hist2_len = depth[u];
+      row_prepare(&ri, &rows[u]);
+      if (rows[u].status < OR_ROW_BAD_INDEX && bad_tok) rows[u].status = OR_ROW_BAD_INDEX;
+      if (rows[u].status > status) status = rows[u].status;
+    }
+    if (status == OR_ROW_OK) {
+      uint64_t seed = in->p.seed[i];
+      const int32_t rid = in->p.row_id ? (int32_t)in->p.row_id[i] : i;
+      double* p = (double*)malloc(sizeof(double) * (size_t)V);
+      u = 0;
+      for (;;) {
+        const row_state* s = &rows[u];
+        const float* qrow = in->draft_probs + (size_t)(g0 + u) * (size_t)in->draft_stride;
+        uint32_t pos = (uint32_t)pos64 + (uint32_t)depth[u];
+        int32_t kids[64], m = 0, c, next = -1, final_tok = -1, t;
+        double scale = 1.0;
+        for (c = u + 1; c < nn; ++c)
+          if (par[c] == u) kids[m++] = c;
+        flag |= s->flag_k;
+        if (m == 0) { /* a leaf: the bonus token */
+          final_tok = row_draw(s, seed, rid, pos, &flag);
+        } else if (s->greedy) {
+          for (c = 0; c < m; ++c)
+            if (tok[kids[c]] == s->order[0]) {
+              next = kids[c];
+              break;
+            }
+          if (next < 0) final_tok = s->order[0];
+        } else {
+          for (t = 0; t < V; ++t) p[t] = 0.0;
+          for (t = 0; t < s->L; ++t) p[s->order[t]] = s->w[t] / s->SK;
+          for (c = 0; c < m; ++c) {
+            int32_t x = tok[kids[c]];
+            double q = (double)qrow[x];
+            double uq = (double)or_uniform(seed, rid, pos, c, OR_STREAM_ACCEPT) * q;
+            double Z = 0.0;
+            if (fabs(uq - p[x]) <= REL_MARGIN * (1 + c) * scale * (p[x] + q) + ABS_FLOOR) flag = 1;
+            if (uq < p[x]) {
+              next = kids[c];
+              break;
+            }
+            if (c == m - 1) {
+              final_tok = residual_draw_dense(s, p, qrow, (1 + c) * scale, seed, rid, pos, &flag);
+              if (final_tok < 0) final_tok = row_draw(s, seed, rid, pos, &flag);
+              break;
+            }
+            for (t = 0; t < V; ++t) {
+              double r = p[t] - (double)qrow[t];
+              p[t] = (r > 0.0) ? r : 0.0;
+              Z += p[t];
+            }
+            if (Z < 1e-6) flag = 1; /* rounding decides whether anything is left */
+            if (!(Z > 0.0)) {
+              final_tok = row_draw(s, seed, rid, pos, &flag);
+              break;
+            }
+            for (t = 0; t < V; ++t) p[t] /= Z;
+            scale /= Z;
+          }
+        }
+        if (next >= 0) {
+          o[n_acc] = tok[next];
+          if (op) op[n_acc] = next;
+          ++n_acc;
+          u = next;
+          continue;
+        }
+        o[n_acc] = final_tok;
+        break;
+      }
+      free(p);
+    } else {
+      flag = 0;
+    }
+    out->num_accepted[i] = n_acc;
+    out->status[i] = status;
+    if (out->sub_margin) out->sub_margin[i] = (uint8_t)(flag != 0);
+    for (u = 0; u < nn; ++u) row_free(&rows[u]);
+    free(rows);
+    free(depth);
+  }
+  return 0;
+}

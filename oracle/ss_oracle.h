@@ -159,6 +159,57 @@ int32_t or_row_probs(const or_sample_in* in, int32_t row, const int32_t* extra_h
  * positive, 1 if P <= q everywhere (the residual is empty). */
 int32_t or_residual_probs(int32_t vocab, const double* P, const float* q, double* out);
 
+/* ------------------------------------------------- tree verification --
+ * Drafts arranged as a tree ("Accelerating Sonar through speculation",
+ * section "EAGLE": several draft sequences explored as a tree, the longest
+ * acceptable one kept, plus one token from the target).  The post gives no
+ * acceptance rule for trees; the reading used here is recursive rejection
+ * over each node's children: the children of node u are independent draws
+ * from the draft distribution q_u at u; they are tried in index order, child
+ * c_i is accepted with probability min(1, p_i(x)/q_u(x)) where p_0 = P_u and
+ * p_{i+1} = max(p_i - q_u, 0) / Z_{i+1}, Z_{i+1} its sum; on acceptance the
+ * walk continues at the child; when every child is rejected the emitted token
+ * is drawn from max(p_{m-1} - q_u, 0); at a leaf it is drawn from P_u (the
+ * bonus token).  A chain is exactly the linear rule of or_spec_verify.
+ *
+ * Request i owns nodes node_offsets[i] .. node_offsets[i+1]-1; local node 0
+ * is the root (the state after the request's accepted prefix).  Node u's
+ * target row is target_logits row node_offsets[i] + u; its history is the
+ * request's history plus the tokens on the path from the root's child to u;
+ * its Philox position is position[i] + depth(u).  Child c_i's uniform is
+ * word i of stream OR_STREAM_ACCEPT at u's position; the residual at u uses
+ * OR_STREAM_RESIDUAL and the bonus OR_STREAM_DRAW.  A greedy request (T = 0)
+ * accepts the first child whose token is the argmax and otherwise emits the
+ * argmax.  When a residual sums to zero before the last child, the walk ends
+ * with the draw from P_u. */
+typedef struct {
+  int32_t num_requests, vocab, max_nodes;
+  int64_t row_stride;
+  int32_t dtype;
+  const void* target_logits;     /* [sum n, row_stride]                          */
+  const int32_t* node_offsets;   /* [R+1]                                        */
+  const int32_t* parents;        /* [sum n] local index of the parent; the root's
+                                    entry is not read; parent < child required  */
+  const int32_t* node_tokens;    /* [sum n] draft token of each node (root: unused) */
+  const float* draft_probs;      /* [sum n, draft_stride] q at each node         */
+  int64_t draft_stride;
+  or_params p;                   /* per request                                  */
+} or_tree_in;
+
+typedef struct {
+  int32_t* out_tokens;           /* [R, max_nodes], -1 padded                    */
+  int32_t* out_path;             /* [R, max_nodes] accepted local nodes, or NULL */
+  int32_t* num_accepted;         /* [R]                                          */
+  int32_t* status;               /* [R]                                          */
+  uint8_t* sub_margin;           /* [R] or NULL                                  */
+} or_tree_out;
+
+/* Tree verification.  Status per request: node count outside [1, max_nodes]
+ * or a parent not in [0, child) -> bad parameter; a node token outside
+ * [0, V) -> bad index; otherwise the largest row status of its nodes.
+ * Returns 0. */
+int or_tree_verify(const or_tree_in* in, or_tree_out* out);
+
 #ifdef __cplusplus
 }
 #endif

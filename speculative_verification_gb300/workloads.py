@@ -245,6 +245,66 @@ def config5(seed=5, requests=256, vocab=262144, max_draft=7, plain_top_k_max=409
     return _verify_dict(CONFIG_NAMES[5], vocab, max_draft, ks, z, q, drafts, params)
 
 
+def random_tree(rng, n, window=4):
+    """Parent of every node of an n-node draft tree (the root's entry is -1):
+    node v hangs under one of the `window` nodes before it, so the shapes range
+    from chains to bushy levels."""
+    par = np.full(n, -1, np.int32)
+    for v in range(1, n):
+        par[v] = rng.integers(max(0, v - window), v)
+    return par
+
+
+def chain_tree(n):
+    par = np.arange(-1, n - 1, dtype=np.int32)
+    return par
+
+
+def tree(seed=6, requests=16, vocab=32000, max_nodes=16, dtype="bf16", shapes=None, greedy_frac=0.25):
+    """Tree-draft verification: request i has 1..max_nodes nodes (node 0 the
+    root); every node has a target row and a draft distribution q (a noisy copy
+    of its target row); the children of a node are independent draws from its
+    q.  `shapes` (optional) gives each request's parent array instead of a
+    random tree.  Mixed sampling parameters as in the decode workload;
+    penalties and bias on half of the requests."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    pars, toks, zs, qs = [], [], [], []
+    for i in range(requests):
+        if shapes is not None:
+            par = np.asarray(shapes[i], np.int32)
+        else:
+            par = random_tree(rng, int(rng.integers(1, max_nodes + 1)))
+        n = par.size
+        z = _spiky_rows(rng, n, vocab, 3.0, 1, 5, 6.0, 12.0)
+        zb = bf16_bits_to_f32(to_bf16_bits(z)) if dtype == "bf16" else z
+        q = _draft_probs(rng, zb)
+        tok = np.zeros(n, np.int32)
+        for v in range(1, n):
+            pv = q[par[v]].astype(np.float64)
+            tok[v] = rng.choice(vocab, p=pv / pv.sum())
+        pars.append(par)
+        toks.append(tok)
+        zs.append(z)
+        qs.append(q)
+    ns = np.array([p_.size for p_ in pars], np.int32)
+    off = np.zeros(requests + 1, np.int32)
+    off[1:] = np.cumsum(ns)
+    z = np.concatenate(zs, axis=0)
+    temp, top_k, top_p, min_p = _cfg2_params(rng, requests, greedy_frac=greedy_frac)
+    enabled = {"pen": rng.random(requests) < 0.5, "bias": rng.random(requests) < 0.5}
+    params = dict(temperature=temp, top_k=top_k, top_p=top_p, min_p=min_p,
+                  seed=(2000 + np.arange(requests)).astype(np.uint64),
+                  position=rng.integers(0, 4096, size=requests).astype(np.int64))
+    params.update(_penalty_lists(rng, requests, vocab, enabled))
+    w = dict(kind="tree", name="tree verify R=%d max_nodes=%d V=%d %s" % (requests, max_nodes, vocab, dtype),
+             num_requests=requests, vocab=vocab, max_nodes=max_nodes, dtype=dtype,
+             target_logits=to_bf16_bits(z) if dtype == "bf16" else z.astype(np.float32), row_stride=vocab,
+             node_offsets=off, parents=np.concatenate(pars), node_tokens=np.concatenate(toks),
+             draft_probs=np.concatenate(qs, axis=0), draft_stride=vocab)
+    w.update(params)
+    return w
+
+
 def make(cfg, **overrides):
     """Workload `cfg` (1..5) with optional size overrides (rows/requests/vocab)."""
     return {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}[cfg](**overrides)

@@ -84,3 +84,38 @@ def verify_workload(target_logits, ks, drafts, draft_probs, dtype="f32", tempera
         w["hist_ids"] = (np.concatenate([np.asarray(h, np.int32) for h in history])
                          if hoff[-1] else np.zeros(0, np.int32))
     return w
+
+
+def tree_workload(target_logits, node_offsets, parents, node_tokens, draft_probs, max_nodes=None, dtype="f32",
+                  temperature=1.0, top_k=None, top_p=None, min_p=None, seed=0, position=0, history=None,
+                  repetition=None, frequency=None, presence=None):
+    """target_logits / draft_probs: [sum n, V] (one row per node); node_offsets [R+1];
+    parents / node_tokens: [sum n], local indices (root -1)."""
+    z = np.atleast_2d(np.asarray(target_logits, np.float32))
+    V = z.shape[1]
+    off = np.asarray(node_offsets, np.int32)
+    R = off.size - 1
+    ns = np.diff(off)
+
+    def col(v, dt):
+        if v is None:
+            return None
+        a = np.asarray(v, dt)
+        return np.full(R, a, dt) if a.ndim == 0 else a
+    w = dict(kind="tree", num_requests=R, vocab=V, max_nodes=int(ns.max() if max_nodes is None else max_nodes),
+             dtype=dtype, target_logits=(W.to_bf16_bits(z) if dtype == "bf16" else z), row_stride=V,
+             node_offsets=off, parents=np.asarray(parents, np.int32).reshape(-1),
+             node_tokens=np.asarray(node_tokens, np.int32).reshape(-1),
+             draft_probs=np.asarray(draft_probs, np.float32).reshape(-1, V), draft_stride=V,
+             temperature=col(temperature, np.float32), top_k=col(top_k, np.int32),
+             top_p=col(top_p, np.float32), min_p=col(min_p, np.float32),
+             repetition=col(repetition, np.float32), frequency=col(frequency, np.float32),
+             presence=col(presence, np.float32),
+             seed=col(seed, np.uint64), position=col(position, np.int64))
+    if history is not None:
+        hoff = np.zeros(R + 1, np.int32)
+        hoff[1:] = np.cumsum([len(h) for h in history])
+        w["hist_offsets"] = hoff
+        w["hist_ids"] = (np.concatenate([np.asarray(h, np.int32) for h in history])
+                         if hoff[-1] else np.zeros(0, np.int32))
+    return w
