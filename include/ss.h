@@ -220,6 +220,66 @@ ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t wor
  * Arguments, outputs and the other errors are those of ss_spec_verify. */
 ss_status ss_spec_verify_noalloc(const ss_verify_args* args, ss_stream_t stream);
 
+/* ---------------------------------------------------- tree verification --
+ * Drafts arranged as a tree ("Accelerating Sonar through speculation",
+ * section "EAGLE": a draft model explores several sequences as a tree, the
+ * longest acceptable one is kept and the target adds one more token).  The
+ * post gives no acceptance rule for trees; this call implements recursive
+ * rejection over each node's children, which reduces to the linear rule of
+ * ss_spec_verify on a chain:
+ *   - request i owns nodes node_offsets[i] .. node_offsets[i+1] - 1, n_i of
+ *     them (1 <= n_i <= max_nodes); local node 0 is the root, the state after
+ *     the request's accepted prefix; every other node u carries the draft
+ *     token node_tokens[node_offsets[i] + u] and hangs under local node
+ *     parents[node_offsets[i] + u], which must be smaller than u (the root's
+ *     parent entry is not read);
+ *   - node u's target row (target_logits row node_offsets[i] + u) is the
+ *     target's next-token distribution after the tokens on the path from the
+ *     root to u; its history is the request's history plus those tokens, its
+ *     Philox position is position[i] + depth(u);
+ *   - the children of u are taken to be independent draws from the draft
+ *     distribution q_u (draft_probs row node_offsets[i] + u; leaves' rows are
+ *     not read).  They are tried in index order: child c (the c-th child of
+ *     u) is accepted with probability min(1, p_c(x)/q_u(x)), p_0 = P_u,
+ *     p_{c+1} = max(p_c - q_u, 0) / Z (Z its sum), by u * q_u(x) < p_c(x) with
+ *     u the Philox uniform of word c, stream 1, at u's position.  On
+ *     acceptance the walk continues at the child.  When every child is
+ *     rejected, the emitted token is the Gumbel-max draw (stream 2) from
+ *     max(p_{m-1} - q_u, 0); when a residual sums to zero before the last
+ *     child, it is the stream-0 draw from P_u.  At a leaf it is the stream-0
+ *     draw from P_u (the bonus token).  A greedy request (temperature 0)
+ *     accepts the first child carrying the argmax and otherwise emits it.
+ * Outputs: out_tokens[i, 0 .. num_accepted[i]] the accepted drafts then the
+ * final token, -1 after; out_path (or NULL) the accepted nodes' local
+ * indices, -1 after; out_status the worst row status of the request (a node
+ * count outside [1, max_nodes] or a parent not smaller than its child gives
+ * SS_ROW_BAD_PARAM, a node token outside [0, V) SS_ROW_BAD_INDEX).
+ * The workspace is that of ss_spec_verify for (num_requests, max_nodes - 1),
+ * zeroed once; one kernel launch, asynchronous on `stream`. */
+#define SS_TREE_MAX_NODES 64
+typedef struct {
+  int32_t num_requests;
+  int32_t vocab;
+  int32_t max_nodes;            /* in [1, SS_TREE_MAX_NODES], >= every n_i        */
+  int64_t row_stride;           /* elements between target rows (>= V)            */
+  int32_t dtype;
+  const void* target_logits;    /* [sum n_i, row_stride]                           */
+  const int32_t* node_offsets;  /* [R+1], non-decreasing, node_offsets[0] = 0     */
+  const int32_t* parents;       /* [sum n_i] local parent index                   */
+  const int32_t* node_tokens;   /* [sum n_i] draft token of each node             */
+  const float* draft_probs;     /* [sum n_i, draft_stride] q at each node         */
+  int64_t draft_stride;         /* elements, >= V                                 */
+  ss_params params;             /* indexed by request                             */
+  int32_t* out_tokens;          /* [R, max_nodes]                                 */
+  int32_t* out_path;            /* [R, max_nodes], or NULL                        */
+  int32_t* out_num_accepted;    /* [R]                                            */
+  int32_t* out_status;          /* [R]                                            */
+  int32_t* out_kept;            /* [sum n_i] |K| per node row, or NULL            */
+  float* debug_processed;       /* [sum n_i, V], or NULL                          */
+} ss_tree_args;
+
+ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t workspace_bytes, ss_stream_t stream);
+
 /* After a verification call, the next step's inputs without a device-to-host
  * copy (Accelerating Sonar through speculation, "MTP schedule for a single
  * token": once the target's inputs are shifted in, a kernel places the next

@@ -84,7 +84,12 @@ constexpr uint32_t kWorkBytes = 3 * kHistRows * kCopies * 4;  // histograms / ga
 constexpr int kPartSlots = 4;  // stage 1, draw, residual, normaliser
 constexpr int kRedBytes = 2048;
 
-enum TaskMode { kModeSample = 0, kModeVerify = 1 };
+enum TaskMode { kModeSample = 0, kModeVerify = 1, kModeTree = 2 };
+// Tree verification: nodes per request, and where the setup keeps the tree
+// (parents, tokens, the node's path) in the work region, past the raw logits
+// of the patched tokens.
+constexpr int kTreeMaxNodes = SS_TREE_MAX_NODES;
+constexpr uint32_t kTreeOff = 8192;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 __device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
@@ -239,6 +244,8 @@ struct KArgs {
   // vocabulary shard: tokens [shard_off, shard_off + shard_len) of the rows;
   // the whole vocabulary (0, vocab) outside the sharded entry point
   int32_t shard_off, shard_len;
+  const int32_t* tree_parents;  // tree verification: local parent of every node
+  int32_t* out_path;            // tree verification: accepted nodes [R, max_nodes], or NULL
   uint8_t* shard_rec;  // sharded entry point: per-row records, else NULL
   int32_t shard_cap;   // list entries per record
   // 0: every task in launch order; 1 / 2: only the light / heavy rows (see
@@ -287,11 +294,12 @@ __device__ int ordered_task(const KArgs& a, int i, int32_t* sm) {
   const int n = a.num_tasks;
   auto level = [&](int task) -> int {
     int req = task;
-    if (a.mode == kModeVerify) {
+    if (a.mode != kModeSample) {
       const int width = a.max_draft + 1;
       req = task / width;
       const int j = task % width;
-      const int32_t k = a.draft_offsets[req + 1] - a.draft_offsets[req];
+      // drafts of a linear request, non-root nodes of a tree
+      const int32_t k = a.draft_offsets[req + 1] - a.draft_offsets[req] - (a.mode == kModeTree ? 1 : 0);
       if (k < 0 || k > a.max_draft) return j == 0 ? 0 : -1;
       if (j > k) return -1;
     }
@@ -392,6 +400,11 @@ struct Ctx {
   float kabs[kMaxLevels];  // absolute bucket of the top-k cut at each level
   int32_t cut_on, cut_idx, cut_len;
   uint32_t cut_key;
+  // tree verification: the node's depth, the request's node count, the
+  // node's children (local index, token) in index order
+  int32_t depth, nn, nkids;
+  int32_t kid_node[kTreeMaxNodes];
+  int32_t kid_tok[kTreeMaxNodes];
 };
 
 extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -1650,7 +1663,7 @@ __device__ __noinline__ void emit_members(float2* list, int32_t* cursor, int cap
 // (stream 2); result in g.fold (arg kNoCut when no token has P > q).
 template <int DT>
 __device__ __noinline__ void residual_pass(int mp_on, float memb_lo, float inv_s, float log_s, const float* qrow,
-                                           uint64_t seed) {
+                                           uint64_t seed, const float* invz, int nz, int slot) {
   using V = Vec<DT>;
   const float m = g.m, min_p = g.min_p, inv_t = g.inv_t;
   const uint32_t rowid = g.rowid, pos = g.pos;
@@ -1658,10 +1671,12 @@ __device__ __noinline__ void residual_pass(int mp_on, float memb_lo, float inv_s
   int32_t bi = kNoCut;
   auto relem = [&](int32_t t, float y) {
     if (!in_kept(t, y, m, mp_on, min_p)) return;
-    // log r <= log P = y - m - log S
+    // log r <= log p_nz <= log P + sum log(1/Z) = y - m - log_s (log_s net of the 1/Z factors)
     if (y - m - log_s + kGumbelMax + 1e-3f + fabsf(y) * 1e-6f < bv) return;
-    const float P = __fmul_rn(__expf(y - m), inv_s);
-    const float r = __fsub_rn(P, qrow[t]);
+    const float qt = qrow[t];
+    float P = __fmul_rn(__expf(y - m), inv_s);
+    for (int z = 0; z < nz; ++z) P = __fmul_rn(fmaxf(__fsub_rn(P, qt), 0.0f), invz[z]);
+    const float r = __fsub_rn(P, qt);
     if (!(r > 0.0f)) return;
     const uint32_t num = philox_numerator(seed, rowid, pos, static_cast<uint32_t>(t), 2);
     const float s = __fadd_rn(logf(r), gumbel_noise(num));
@@ -1690,7 +1705,105 @@ __device__ __noinline__ void residual_pass(int mp_on, float memb_lo, float inv_s
     const float y = g.hval[s];
     if (t >= 0 && y != neg_inf()) relem(t, y);
   }
-  reduce_fold(2, bv, bi, 0, 0, 0, pos_inf(), neg_inf(), 0.0f, neg_inf(), 0);
+  reduce_fold(slot, bv, bi, 0, 0, 0, pos_inf(), neg_inf(), 0.0f, neg_inf(), 0);
+}
+
+// Fixed-point sum (2^-40 units) over the kept set of max(p_nz - q, 0), the
+// normaliser of the residual after a rejection at a tree node; p_0 = P and
+// p_{i+1} = max(p_i - q, 0) / Z_{i+1} (invz holds the 1/Z_i).  The result is
+// in g.fold.mass.
+template <int DT>
+__device__ __noinline__ void tree_mass_pass(int mp_on, float memb_lo, float inv_s, const float* qrow,
+                                            const float* invz, int nz, int slot) {
+  using V = Vec<DT>;
+  const float m = g.m, min_p = g.min_p, inv_t = g.inv_t;
+  unsigned long long mass = 0;
+  auto melem = [&](int32_t t, float y) {
+    if (!in_kept(t, y, m, mp_on, min_p)) return;
+    const float qt = qrow[t];
+    float P = __fmul_rn(__expf(y - m), inv_s);
+    for (int z = 0; z < nz; ++z) P = __fmul_rn(fmaxf(__fsub_rn(P, qt), 0.0f), invz[z]);
+    const float r = __fsub_rn(P, qt);
+    if (r > 0.0f) mass += static_cast<unsigned long long>(__fmul_rn(fminf(r, 1.0f), 1099511627776.0f));
+  };
+  const int lo = g.lo;
+  const uint4* data = reinterpret_cast<const uint4*>(g.data);
+  for_vectors_above<DT>(memb_lo, [&](int v) {
+    if (v < 0) return;
+    float z[V::kPer];
+    V::unpack(data[v], z);
+#pragma unroll
+    for (int e = 0; e < V::kPer; ++e) {
+      const float y = __fmul_rn(z[e], inv_t);
+      if (y != neg_inf()) melem(lo + v * V::kPer + e, y);
+    }
+  });
+  for (int s = threadIdx.x; s < kHashCap; s += kThreads) {
+    const int32_t t = g.hkey[s];
+    const float y = g.hval[s];
+    if (t >= 0 && y != neg_inf()) melem(t, y);
+  }
+  reduce_fold(slot, neg_inf(), kNoCut, 0, 0, mass, pos_inf(), neg_inf(), 0.0f, neg_inf(), 0);
+}
+
+// A tree node's children (recursive rejection; "Accelerating Sonar through
+// speculation", section "EAGLE", names tree drafts, the rule is a reading):
+// child i, drawn from q at this node, is accepted with probability
+// min(1, p_i(x)/q(x)), p_0 = P, p_{i+1} = max(p_i - q, 0) / Z_{i+1}; the uniform
+// is word i of stream 1 at this node's position.  On the first acceptance
+// acc_node is the child's local index; when every child is rejected, token is
+// the Gumbel-max draw from max(p_{m-1} - q, 0) (stream 2); when a residual
+// sums to zero before the last child, token stays the stream-0 draw from P.
+// Every CTA of the cluster takes the same decisions (cluster-wide sums).
+template <int DT>
+__device__ __noinline__ void tree_children(int mp_on, float memb_lo, float SK, const float* qrow, uint64_t seed,
+                                           int32_t& acc_node, int32_t& token) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int m = g.nkids;
+  // the processed logit of every child token, from the CTA whose slice holds
+  // it, to every CTA (one writer per entry; the work region is free now)
+  float* kid_y = reinterpret_cast<float*>(g.work);
+  float* invz = kid_y + kTreeMaxNodes;
+  if (threadIdx.x < m) {
+    float y;
+    if (local_value<DT>(g.kid_tok[threadIdx.x], y))
+      for (int r = 0; r < g.ncta; ++r) *cl.map_shared_rank(kid_y + threadIdx.x, r) = y;
+  }
+  cl.sync();
+  const float inv_s = __fdiv_rn(1.0f, SK);
+  float log_s = logf(SK);  // net of the 1/Z factors applied so far
+  int nz = 0;
+  for (int i = 0; i < m; ++i) {
+    const int32_t x = g.kid_tok[i];
+    const float y = kid_y[i];
+    const bool x_in = (y != neg_inf()) && in_kept(x, y, g.m, mp_on, g.min_p);
+    const float qx = qrow[x];
+    float px = x_in ? __fmul_rn(__expf(y - g.m), inv_s) : 0.0f;
+    for (int z = 0; z < nz; ++z) px = __fmul_rn(fmaxf(__fsub_rn(px, qx), 0.0f), invz[z]);
+    const float u = uniform_from_numerator(uniform_numerator(philox_word(seed, g.rowid, g.pos, i, 1)));
+    if (__fmul_rn(u, qx) < px) {
+      acc_node = g.kid_node[i];
+      token = x;
+      return;
+    }
+    // consecutive reductions alternate between two part slots
+    const int slot = 2 + (nz & 1);
+    if (i == m - 1) {
+      residual_pass<DT>(mp_on, memb_lo, inv_s, log_s, qrow, seed, invz, nz, slot);
+      const Part rall = g.fold;
+      if (rall.arg != kNoCut && rall.best > neg_inf()) token = rall.arg;
+      return;
+    }
+    tree_mass_pass<DT>(mp_on, memb_lo, inv_s, qrow, invz, nz, slot);
+    const unsigned long long zm = g.fold.mass;
+    if (zm == 0) return;  // nothing left (rounding): the stream-0 draw
+    const float Z = static_cast<float>(static_cast<double>(zm) * kFixedInv);
+    __syncthreads();  // every thread has read g.fold and invz
+    if (threadIdx.x == 0) invz[nz] = __fdiv_rn(1.0f, Z);
+    __syncthreads();
+    ++nz;
+    log_s += logf(Z);
+  }
 }
 // ------------------------------------------------------------- kernel --
 
@@ -1755,6 +1868,28 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
         drow = d0 + j;
         x = a.draft_tokens[drow];
       }
+    } else if (a.mode == kModeTree) {
+      // node j of request req; k = its non-root node count (the position
+      // range check below covers the deepest possible node)
+      const int width = a.max_draft + 1;
+      req = task / width;
+      j = task % width;
+      d0 = a.draft_offsets[req];
+      const int32_t nn = a.draft_offsets[req + 1] - d0;
+      k = nn - 1;
+      if (nn < 1 || nn > width) {
+        status = SS_ROW_BAD_PARAM;
+        live = (j == 0);
+        k = 0;
+        bad_k = 1;
+      } else if (j >= nn) {
+        live = false;
+      }
+      row = d0 + j;
+      drow = d0 + j;
+      c.nn = bad_k ? 1 : nn;
+      c.depth = 0;
+      c.nkids = 0;
     }
     c.row = live ? row : -1;
     c.bad_k = bad_k;
@@ -1815,6 +1950,43 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   __syncthreads();
   if (c.row < 0) return;  // whole cluster: no such target position
 
+  if (a.mode == kModeTree && !c.bad_k) {
+    // The request's tree, into shared memory: parents, tokens; then the
+    // node's depth (its Philox position), its path (its history additions)
+    // and its children.  Every node of the request checks every parent, so
+    // all of them agree on a malformed tree.
+    int32_t* tpar = reinterpret_cast<int32_t*>(c.work + kTreeOff);
+    int32_t* ttok = tpar + kTreeMaxNodes;
+    int32_t* tpath = ttok + kTreeMaxNodes;
+    const int nn = c.nn;
+    if (tid < nn) {
+      tpar[tid] = a.tree_parents[c.d0 + tid];
+      ttok[tid] = a.draft_tokens[c.d0 + tid];
+    }
+    __syncthreads();
+    if (tid == 0) {
+      bool ok = true;
+      for (int v = 1; v < nn; ++v) ok = ok && tpar[v] >= 0 && tpar[v] < v;
+      int dep = 0, m = 0;
+      if (ok) {
+        for (int v = c.j; v > 0; v = tpar[v]) tpath[dep++] = ttok[v];
+        for (int v = c.j + 1; v < nn; ++v)
+          if (tpar[v] == c.j) {
+            c.kid_node[m] = v;
+            c.kid_tok[m] = ttok[v];
+            ++m;
+          }
+      } else if (c.status == SS_ROW_OK) {
+        c.status = SS_ROW_BAD_PARAM;  // touches no logits
+        c.n = 0;
+      }
+      c.depth = dep;
+      c.nkids = m;
+      c.pos = static_cast<uint32_t>(a.p.position[c.req]) + static_cast<uint32_t>(dep);
+    }
+    __syncthreads();
+  }
+
   const int lo = c.lo, n = c.n;
   // addressed by token id: element t of the row is row_ptr[t] (a shard's
   // buffer starts at token shard_off)
@@ -1870,7 +2042,9 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   // Raw logits of the patched tokens, by slot, until stage 1: the work region
   // is not in use before the first histogram.
   float* hraw = reinterpret_cast<float*>(c.work);
-  static_assert(kHashCap * sizeof(float) <= kWorkBytes, "raw patched logits fit the work region");
+  static_assert(kHashCap * sizeof(float) <= kTreeOff, "raw patched logits stay below the tree");
+  static_assert(kTreeOff + 3 * kTreeMaxNodes * sizeof(int32_t) <= kWorkBytes, "the tree fits the work region");
+  static_assert(2 * kTreeMaxNodes * sizeof(float) <= kTreeOff, "child logits and 1/Z fit below the tree");
 
   // The logit of a patched token, -inf when the grammar mask disallows it
   // (the mask is applied after penalties and bias, which keep -inf at -inf).
@@ -1944,6 +2118,16 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
         else if (e < c.j)
           count(t, in_slice(t) ? raw_logit(t) : 0.0f);
       }
+    }
+    if (a.mode == kModeTree) {
+      // the tokens on the node's path; every node token must be a token id
+      const int32_t* ttok = reinterpret_cast<const int32_t*>(c.work + kTreeOff) + kTreeMaxNodes;
+      const int32_t* tpath = ttok + kTreeMaxNodes;
+      if (tid < c.depth) {
+        const int32_t t = tpath[tid];
+        count(t, in_slice(t) ? raw_logit(t) : 0.0f);
+      }
+      if (tid >= 1 && tid < c.nn && (ttok[tid] < 0 || ttok[tid] >= V_)) st_local = max(st_local, SS_ROW_BAD_INDEX);
     }
     for (int e = eb; e < c.b1; e += kThreads) {
       const int32_t t = (e == eb) ? tb : a.p.bias_ids[e];
@@ -2124,15 +2308,23 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   }
   __syncthreads();
 
-  int32_t token = -1, kept = 0, accept = 0;
+  int32_t token = -1, kept = 0, accept = 0, acc_node = -1;
   if (status == SS_ROW_OK) {
-    const bool spec_pos = (a.mode == kModeVerify) && (c.j < c.k);
+    // a position that tests drafts: a linear one before the last, a tree node with children
+    const bool spec_pos = (a.mode == kModeVerify) ? (c.j < c.k) : (a.mode == kModeTree && c.nkids > 0);
     const uint64_t seed = (static_cast<uint64_t>(c.seed_hi) << 32) | c.seed_lo;
     const uint32_t rowid = c.rowid;
     if (c.greedy) {
       kept = 1;
       token = argmax_tok;
-      if (spec_pos) {
+      if (spec_pos && a.mode == kModeTree) {
+        // greedy: the first child carrying the argmax is accepted
+        for (int i = 0; i < c.nkids; ++i)
+          if (c.kid_tok[i] == argmax_tok) {
+            acc_node = c.kid_node[i];
+            break;
+          }
+      } else if (spec_pos) {
         const float q = a.draft_probs[static_cast<int64_t>(c.drow) * a.draft_stride + c.x];
         const float u = uniform_from_numerator(uniform_numerator(philox_word(seed, rowid, c.pos, 0, 1)));
         const float P = (c.x == argmax_tok) ? 1.0f : 0.0f;
@@ -2185,7 +2377,11 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
         h->best = dall.best;
         h->best_token = dall.arg;
       }
-      if (spec_pos) {
+      if (spec_pos && a.mode == kModeTree) {
+        const float SK = static_cast<float>(static_cast<double>(dall.mass) * kFixedInv);
+        tree_children<DT>(mp_on, memb_lo, SK, a.draft_probs + static_cast<int64_t>(c.drow) * a.draft_stride, seed,
+                          acc_node, token);
+      } else if (spec_pos) {
         const float yx = dall.xhere ? dall.xy : neg_inf();
         const bool x_in = (yx != neg_inf()) && in_kept(c.x, yx, m, mp_on, min_p);
         const float SK = static_cast<float>(static_cast<double>(dall.mass) * kFixedInv);
@@ -2198,7 +2394,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
           token = c.x;
         } else {
           const float* qrow = a.draft_probs + static_cast<int64_t>(c.drow) * a.draft_stride;
-          residual_pass<DT>(mp_on, memb_lo, inv_s, logf(SK), qrow, seed);
+          residual_pass<DT>(mp_on, memb_lo, inv_s, logf(SK), qrow, seed, nullptr, 0, 2);
           const Part rall = g.fold;
           if (rall.arg != kNoCut && rall.best > neg_inf()) token = rall.arg;
           // else: no token with P > q (rounding): keep the stream-0 draw
@@ -2230,6 +2426,49 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
     } else if (a.mode == kModeSample) {
       a.out_token[c.row] = token;
       a.out_status[c.row] = status;
+    } else if (a.mode == kModeTree) {
+      const int width = a.max_draft + 1;
+      const int i = c.req;
+      int32_t* out = a.out_token + static_cast<int64_t>(i) * width;
+      int32_t* path = a.out_path ? a.out_path + static_cast<int64_t>(i) * width : nullptr;
+      if (c.bad_k) {
+        // invalid node count: only node 0 exists and reports it
+        for (int w = 0; w < width; ++w) {
+          out[w] = -1;
+          if (path) path[w] = -1;
+        }
+        a.out_num_accepted[i] = 0;
+        a.out_status[i] = status;
+      } else {
+        int4* res = a.ws_results + static_cast<int64_t>(i) * width;
+        res[c.j] = make_int4(status, acc_node, token, kept);
+        __threadfence();
+        const int prev = atomicAdd(a.ws_counters + i, 1);
+        if (prev == c.nn - 1) {  // last node of this request to finish: walk the tree
+          __threadfence();
+          int32_t st = SS_ROW_OK;
+          for (int w = 0; w < c.nn; ++w) st = max(st, __ldcg(&res[w].x));
+          int nacc = 0;
+          for (int w = 0; w < width; ++w) {
+            out[w] = -1;
+            if (path) path[w] = -1;
+          }
+          if (st == SS_ROW_OK) {
+            int u = 0;
+            for (int step = 0; step < c.nn; ++step) {  // accepted children have larger indices
+              const int4 r = __ldcg(res + u);
+              out[nacc] = r.z;
+              if (r.y <= u || r.y >= c.nn) break;
+              if (path) path[nacc] = r.y;
+              ++nacc;
+              u = r.y;
+            }
+          }
+          a.out_num_accepted[i] = nacc;
+          a.out_status[i] = st;
+          a.ws_counters[i] = 0;  // ready for the next call
+        }
+      }
     } else {
       const int width = a.max_draft + 1;
       const int i = c.req;
@@ -2837,6 +3076,55 @@ ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t wor
   k.ws_counters = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
                                              static_cast<size_t>(tasks) * sizeof(int4));
   // many positions run in several waves: start the costliest first
+  if (tasks >= 16) k.row_class = 3;
+  return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t workspace_bytes, ss_stream_t stream) {
+  using namespace ss;
+  if (!args) return SS_ERR_INVALID_ARG;
+  const ss_tree_args& A = *args;
+  if (A.num_requests < 0 || A.vocab < 1 || A.max_nodes < 1 || A.max_nodes > SS_TREE_MAX_NODES)
+    return SS_ERR_INVALID_ARG;
+  if (A.dtype != SS_DTYPE_F32 && A.dtype != SS_DTYPE_BF16) return SS_ERR_INVALID_ARG;
+  if (A.num_requests == 0) return SS_OK;
+  const int es = (A.dtype == SS_DTYPE_BF16) ? 2 : 4;
+  if (!A.target_logits || (reinterpret_cast<uintptr_t>(A.target_logits) % es) != 0 || !A.node_offsets ||
+      !A.parents || !A.node_tokens)
+    return SS_ERR_INVALID_ARG;
+  if (A.max_nodes > 1 && !A.draft_probs) return SS_ERR_INVALID_ARG;
+  if (A.row_stride < A.vocab) return SS_ERR_INVALID_ARG;
+  if (A.max_nodes > 1 && A.draft_stride < A.vocab) return SS_ERR_INVALID_ARG;
+  if (!A.out_tokens || !A.out_num_accepted || !A.out_status) return SS_ERR_INVALID_ARG;
+  if (check_params(A.params) != SS_OK) return SS_ERR_INVALID_ARG;
+  if (A.params.bitmask && A.params.bitmask_stride < (static_cast<int64_t>(A.vocab) + 31) / 32) return SS_ERR_INVALID_ARG;
+  const int64_t tasks = static_cast<int64_t>(A.num_requests) * A.max_nodes;
+  if (tasks > 0x7fffffff / kMaxCluster) return SS_ERR_UNSUPPORTED;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < ss_workspace_size(A.num_requests, A.max_nodes - 1))
+    return SS_ERR_WORKSPACE;
+  KArgs k{};
+  k.mode = kModeTree;
+  k.num_tasks = static_cast<int32_t>(tasks);
+  k.vocab = A.vocab;
+  k.max_draft = A.max_nodes - 1;
+  k.dtype = A.dtype;
+  k.row_stride = A.row_stride;
+  k.logits = A.target_logits;
+  k.draft_offsets = A.node_offsets;
+  k.draft_tokens = A.node_tokens;
+  k.tree_parents = A.parents;
+  k.draft_probs = A.draft_probs;
+  k.draft_stride = A.draft_stride;
+  k.p = A.params;
+  k.out_token = A.out_tokens;
+  k.out_path = A.out_path;
+  k.out_num_accepted = A.out_num_accepted;
+  k.out_status = A.out_status;
+  k.out_kept = A.out_kept;
+  k.debug_processed = A.debug_processed;
+  k.ws_results = reinterpret_cast<int4*>(workspace);
+  k.ws_counters = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
+                                             static_cast<size_t>(tasks) * sizeof(int4));
   if (tasks >= 16) k.row_class = 3;
   return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -101,6 +101,29 @@ class ss_verify_args(C.Structure):
     ]
 
 
+class ss_tree_args(C.Structure):
+    _fields_ = [
+        ("num_requests", C.c_int32),
+        ("vocab", C.c_int32),
+        ("max_nodes", C.c_int32),
+        ("row_stride", C.c_int64),
+        ("dtype", C.c_int32),
+        ("target_logits", C.c_void_p),
+        ("node_offsets", C.c_void_p),
+        ("parents", C.c_void_p),
+        ("node_tokens", C.c_void_p),
+        ("draft_probs", C.c_void_p),
+        ("draft_stride", C.c_int64),
+        ("params", ss_params),
+        ("out_tokens", C.c_void_p),
+        ("out_path", C.c_void_p),
+        ("out_num_accepted", C.c_void_p),
+        ("out_status", C.c_void_p),
+        ("out_kept", C.c_void_p),
+        ("debug_processed", C.c_void_p),
+    ]
+
+
 # Every symbol include/ss.h declares, with its ctypes signature.
 SIGNATURES = {
     "ss_workspace_size": ([C.c_int32, C.c_int32], C.c_size_t),
@@ -108,6 +131,7 @@ SIGNATURES = {
     "ss_process_sample": ([C.POINTER(ss_sample_args), C.c_void_p], C.c_int),
     "ss_spec_verify": ([C.POINTER(ss_verify_args), C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "ss_spec_verify_noalloc": ([C.POINTER(ss_verify_args), C.c_void_p], C.c_int),
+    "ss_tree_verify": ([C.POINTER(ss_tree_args), C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "ss_cluster_size": ([C.c_int32, C.c_int32], C.c_int32),
     "ss_last_cuda_error": ([], C.c_int32),
     "ss_status_string": ([C.c_int], C.c_char_p),
@@ -312,6 +336,33 @@ def ss_spec_verify_noalloc(target_logits, draft_offsets, draft_tokens, draft_pro
     _check(load().ss_spec_verify_noalloc(C.byref(a), _stream_handle(stream)))
 
 
+def ss_tree_verify(target_logits, node_offsets, parents, node_tokens, draft_probs, params, out_tokens,
+                   out_num_accepted, out_status, workspace, *, vocab, max_nodes, dtype, row_stride=None,
+                   draft_stride=None, out_path=None, out_kept=None, debug_processed=None, stream=None):
+    """Verify the draft trees of `out_num_accepted.numel()` requests."""
+    a = ss_tree_args()
+    a.num_requests = int(out_num_accepted.numel())
+    a.vocab = int(vocab)
+    a.max_nodes = int(max_nodes)
+    a.row_stride = int(vocab if row_stride is None else row_stride)
+    a.dtype = SS_DTYPE[dtype]
+    a.target_logits = _ptr(target_logits)
+    a.node_offsets = _ptr(node_offsets)
+    a.parents = _ptr(parents)
+    a.node_tokens = _ptr(node_tokens)
+    a.draft_probs = _ptr(draft_probs) if draft_probs is not None and draft_probs.numel() else None
+    a.draft_stride = int(vocab if draft_stride is None else draft_stride)
+    a.params = make_params(params)
+    a.out_tokens = _ptr(out_tokens)
+    a.out_path = _ptr(out_path)
+    a.out_num_accepted = _ptr(out_num_accepted)
+    a.out_status = _ptr(out_status)
+    a.out_kept = _ptr(out_kept)
+    a.debug_processed = _ptr(debug_processed)
+    _check(load().ss_tree_verify(C.byref(a), C.c_void_p(workspace.data_ptr()),
+                                 workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+
+
 # ------------------------------------------------------------ workloads --
 
 _NP_TO_TORCH = None
@@ -370,6 +421,17 @@ def alloc_outputs(dw, device="cuda", debug=False):
         o["status"] = torch.empty(n, dtype=torch.int32, device=device)
         o["kept"] = torch.empty(n, dtype=torch.int32, device=device)
         rows = n
+    elif dw["kind"] == "tree":
+        R = int(dw["num_requests"])
+        rows = int(dw["node_offsets"][-1].item())
+        width = int(dw["max_nodes"])
+        o["out_tokens"] = torch.empty((R, width), dtype=torch.int32, device=device)
+        o["out_path"] = torch.empty((R, width), dtype=torch.int32, device=device)
+        o["num_accepted"] = torch.empty(R, dtype=torch.int32, device=device)
+        o["status"] = torch.empty(R, dtype=torch.int32, device=device)
+        o["kept"] = torch.empty(rows, dtype=torch.int32, device=device)
+        nbytes = ss_workspace_size(R, width - 1)
+        o["workspace"] = torch.zeros((nbytes + 15) // 16 * 4, dtype=torch.int32, device=device)
     else:
         R = int(dw["num_requests"])
         rows = int(dw["draft_offsets"][-1].item()) + R
@@ -392,6 +454,12 @@ def run(dw, o, stream=None, debug=False):
     if dw["kind"] == "sample":
         ss_process_sample(dw["logits"], params, o["token"], o["status"], vocab=dw["vocab"], dtype=dw["dtype"],
                           row_stride=dw["row_stride"], out_kept=o["kept"], debug_processed=dbg, stream=stream)
+    elif dw["kind"] == "tree":
+        ss_tree_verify(dw["target_logits"], dw["node_offsets"], dw["parents"], dw["node_tokens"], dw["draft_probs"],
+                       params, o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],
+                       max_nodes=dw["max_nodes"], dtype=dw["dtype"], row_stride=dw["row_stride"],
+                       draft_stride=dw["draft_stride"], out_path=o["out_path"], out_kept=o["kept"],
+                       debug_processed=dbg, stream=stream)
     else:
         ss_spec_verify(dw["target_logits"], dw["draft_offsets"], dw["draft_tokens"], dw["draft_probs"], params,
                        o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],

@@ -260,7 +260,8 @@ def chain_tree(n):
     return par
 
 
-def tree(seed=6, requests=16, vocab=32000, max_nodes=16, dtype="bf16", shapes=None, greedy_frac=0.25):
+def tree(seed=6, requests=16, vocab=32000, max_nodes=16, dtype="bf16", shapes=None, greedy_frac=0.25,
+         draft_noise=0.5):
     """Tree-draft verification: request i has 1..max_nodes nodes (node 0 the
     root); every node has a target row and a draft distribution q (a noisy copy
     of its target row); the children of a node are independent draws from its
@@ -277,7 +278,7 @@ def tree(seed=6, requests=16, vocab=32000, max_nodes=16, dtype="bf16", shapes=No
         n = par.size
         z = _spiky_rows(rng, n, vocab, 3.0, 1, 5, 6.0, 12.0)
         zb = bf16_bits_to_f32(to_bf16_bits(z)) if dtype == "bf16" else z
-        q = _draft_probs(rng, zb)
+        q = _draft_probs(rng, zb, noise=draft_noise)
         tok = np.zeros(n, np.int32)
         for v in range(1, n):
             pv = q[par[v]].astype(np.float64)

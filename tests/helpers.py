@@ -119,3 +119,26 @@ def tree_workload(target_logits, node_offsets, parents, node_tokens, draft_probs
         w["hist_ids"] = (np.concatenate([np.asarray(h, np.int32) for h in history])
                          if hoff[-1] else np.zeros(0, np.int32))
     return w
+
+
+def chain_from_linear(w):
+    """The tree form of a linear verification workload: request i's nodes are
+    its k_i + 1 target rows in order, node j + 1 the child of node j."""
+    R, V = int(w["num_requests"]), int(w["vocab"])
+    dof = np.asarray(w["draft_offsets"])
+    ks = np.diff(dof)
+    ns = ks + 1
+    off = np.zeros(R + 1, np.int32)
+    off[1:] = np.cumsum(ns)
+    par, tok, q = [], [], []
+    for i in range(R):
+        k = int(ks[i])
+        par.append(np.arange(-1, k, dtype=np.int32))
+        tok.append(np.concatenate([[0], w["draft_tokens"][dof[i]:dof[i + 1]]]).astype(np.int32))
+        q.append(np.concatenate([w["draft_probs"][dof[i]:dof[i + 1]], np.zeros((1, V), np.float32)]))
+    t = dict(w)
+    t.update(kind="tree", max_nodes=int(w["max_draft"]) + 1, node_offsets=off, parents=np.concatenate(par),
+             node_tokens=np.concatenate(tok), draft_probs=np.concatenate(q))
+    for key in ("draft_offsets", "draft_tokens", "max_draft"):
+        t.pop(key)
+    return t

@@ -89,3 +89,33 @@ def check_verify(w, gpu):
         assert gpu["num_accepted"][i] == ref["num_accepted"][i], ("accepted", i, gpu["num_accepted"][i], ref["num_accepted"][i])
         assert np.array_equal(gpu["out_tokens"][i], ref["out_tokens"][i]), ("tokens", i, gpu["out_tokens"][i], ref["out_tokens"][i])
     return int(chk.sum()), int(sub.sum())
+
+
+def check_tree(w, gpu):
+    """gpu: out_tokens/out_path/num_accepted/status.  Returns (checked
+    requests, sub-margin requests); a sub-margin request must still be a
+    valid walk: accepted nodes form a downward path from the root, the
+    emitted drafts are their tokens and the final token is a token id."""
+    ref = O.tree_verify(w)
+    assert np.array_equal(gpu["status"], ref["status"]), (gpu["status"], ref["status"])
+    ok = ref["status"] == 0
+    assert np.all(gpu["out_tokens"][~ok] == -1)
+    assert np.all(gpu["num_accepted"][~ok] == 0)
+    sub = ok & (ref["sub_margin"] != 0)
+    chk = ok & ~sub
+    for i in np.flatnonzero(chk):
+        assert gpu["num_accepted"][i] == ref["num_accepted"][i], ("accepted", i, gpu["num_accepted"][i], ref["num_accepted"][i])
+        assert np.array_equal(gpu["out_tokens"][i], ref["out_tokens"][i]), ("tokens", i, gpu["out_tokens"][i], ref["out_tokens"][i])
+        assert np.array_equal(gpu["out_path"][i], ref["out_path"][i]), ("path", i, gpu["out_path"][i], ref["out_path"][i])
+    off, par, tok = w["node_offsets"], w["parents"], w["node_tokens"]
+    for i in np.flatnonzero(sub):
+        n = int(gpu["num_accepted"][i])
+        u = 0
+        for s in range(n):
+            v = int(gpu["out_path"][i, s])
+            assert 0 < v < off[i + 1] - off[i] and par[off[i] + v] == u, ("sub-margin walk", i)
+            assert gpu["out_tokens"][i, s] == tok[off[i] + v]
+            u = v
+        assert 0 <= gpu["out_tokens"][i, n] < int(w["vocab"])
+        assert np.all(gpu["out_tokens"][i, n + 1:] == -1)
+    return int(chk.sum()), int(sub.sum())

@@ -15,30 +15,7 @@ section "EAGLE", which names tree drafts without an acceptance rule).
 import numpy as np
 
 from oracle import oracle as O
-from tests.helpers import sample_workload, tree_workload, verify_workload
-
-
-def _chain_from_linear(w):
-    """The tree form of a linear verification workload: request i's nodes are
-    its k_i + 1 target rows in order, node j + 1 the child of node j."""
-    R, V = int(w["num_requests"]), int(w["vocab"])
-    dof = np.asarray(w["draft_offsets"])
-    ks = np.diff(dof)
-    ns = ks + 1
-    off = np.zeros(R + 1, np.int32)
-    off[1:] = np.cumsum(ns)
-    par, tok, q = [], [], []
-    for i in range(R):
-        k = int(ks[i])
-        par.append(np.arange(-1, k, dtype=np.int32))
-        tok.append(np.concatenate([[0], w["draft_tokens"][dof[i]:dof[i + 1]]]).astype(np.int32))
-        q.append(np.concatenate([w["draft_probs"][dof[i]:dof[i + 1]], np.zeros((1, V), np.float32)]))
-    t = dict(w)
-    t.update(kind="tree", max_nodes=int(w["max_draft"]) + 1, node_offsets=off, parents=np.concatenate(par),
-             node_tokens=np.concatenate(tok), draft_probs=np.concatenate(q))
-    for key in ("draft_offsets", "draft_tokens", "max_draft"):
-        t.pop(key)
-    return t
+from tests.helpers import chain_from_linear, sample_workload, tree_workload, verify_workload
 
 
 def test_chain_tree_is_the_linear_rule():
@@ -58,7 +35,7 @@ def test_chain_tree_is_the_linear_rule():
                         min_p=rng.choice([0.0, 0.05], R), repetition=1.3, frequency=0.2, presence=0.1,
                         seed=np.arange(R) + 5, position=rng.integers(0, 1000, R), history=hist)
     lin = O.spec_verify(w)
-    tr = O.tree_verify(_chain_from_linear(w))
+    tr = O.tree_verify(chain_from_linear(w))
     assert np.array_equal(lin["status"], tr["status"])
     assert np.array_equal(lin["num_accepted"], tr["num_accepted"])
     assert np.array_equal(lin["out_tokens"], tr["out_tokens"])
