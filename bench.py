@@ -180,6 +180,11 @@ def run_ours(args, rank, world, dist):
     cfg = args.config
     ring_host = [workload_for(cfg, rank, i) for i in range(args.ring)]
     bytes_per_call = W.algorithmic_bytes(ring_host[0])
+    # kernel launches per sampling call: with 16 rows or more and a cluster
+    # that can double, the heavy rows (top-p without top-k) get a concurrent
+    # launch of their own with twice the CTAs per row
+    cs = ss.ss_cluster_size(int(ring_host[0]["vocab"]), ring_host[0]["dtype"])
+    per_call = 2 if (ring_host[0]["kind"] == "sample" and int(ring_host[0]["num_rows"]) >= 16 and 2 <= cs <= 4) else 1
     rows_per_call = int(ring_host[0]["num_rows"]) if ring_host[0]["kind"] == "sample" else int(
         ring_host[0]["draft_offsets"][-1]) + int(ring_host[0]["num_requests"])
     ring = [ss.to_device(w, dev) for w in ring_host]
@@ -255,6 +260,8 @@ def run_ours(args, rank, world, dist):
     # speculative-verify throughput (secondary metric), same protocol
     spec = run_spec(args, ss, rank, dev, stream) if args.spec_steps > 0 else None
     progress("spec-verify done")
+    tree = run_tree(args, ss, rank, dev, stream) if args.tree_steps > 0 else None
+    progress("tree-verify done")
     sharded = run_sharded(args, ss, rank, dev, stream) if args.shard_steps > 0 else None
     progress("sharded done")
     fused = run_fused(args, ss, dev, stream, measured_peak()[0]) if args.fused_steps > 0 else None
@@ -283,7 +290,8 @@ def run_ours(args, rank, world, dist):
             "l2": "ring of %d input sets, %.0f MB > 2x L2" % (args.ring, args.ring * bytes_per_call / 1e6),
             "launch": "CUDA graph of %d calls, replayed" % per_graph,
             "parallelism": "dp%d replicas" % world,
-            "cluster_ctas_per_row": ss.ss_cluster_size(int(ring_host[0]["vocab"]), ring_host[0]["dtype"]),
+            "cluster_ctas_per_row": cs,
+            "heavy_row_ctas": 2 * cs if per_call == 2 else cs,
         },
         "roofline": {
             "bound": "hbm",
@@ -298,11 +306,13 @@ def run_ours(args, rank, world, dist):
             "kernel_sha256": kernel_source_hash(),
         },
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * per_call,
         "clocks": clocks.summary(),
     }
     if spec is not None:
         res["spec_verify"] = spec
+    if tree is not None:
+        res["tree_verify"] = tree
     if sharded is not None:
         res["vocab_sharded"] = sharded
     if fused is not None:
@@ -422,6 +432,49 @@ def run_spec(args, ss, rank, dev, stream):
             "requests_per_s": int(ring_host[0]["num_requests"]) * calls / (ms / 1e3),
             "ms_per_call": ms / calls, "calls": calls,
             "logits_GBps": W.algorithmic_bytes(ring_host[0]) * calls / (ms / 1e3) / 1e9}
+
+
+TREE_WORKLOAD = "tree verify R=32 trees of 1-16 nodes V=128256 bf16"
+
+
+def run_tree(args, ss, rank, dev, stream):
+    """Tree-draft verification: 32 requests, random draft trees of 1 to 16
+    nodes (each node under one of the 4 nodes before it), V = 128256 bf16,
+    drafts drawn from a noisy copy of each node's target row."""
+    import torch
+    ring_host = [W.tree(seed=9000 + 97 * rank + i, requests=32, vocab=128256, max_nodes=16) for i in range(3)]
+    ring = [ss.to_device(w, dev) for w in ring_host]
+    out = ss.alloc_outputs(ring[0], dev)
+    rows = sum(int(w["node_offsets"][-1]) for w in ring_host)
+    with torch.cuda.stream(stream):
+        ss.ss_workspace_init(out["workspace"], stream=stream)
+        for dw in ring:
+            ss.run(dw, out, stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for dw in ring:
+                ss.run(dw, out, stream=stream)
+    reps = max(1, args.tree_steps // len(ring))
+    for _ in range(3):
+        g.replay()
+    stream.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    calls = reps * len(ring)
+    alg = sum(W.algorithmic_bytes(w) for w in ring_host)
+    return {"workload": TREE_WORKLOAD, "node_rows_per_s": rows * reps / (ms / 1e3),
+            "requests_per_s": 32 * calls / (ms / 1e3), "ms_per_call": ms / calls, "calls": calls,
+            "mean_nodes_per_request": rows / (32.0 * len(ring)),
+            "logits_GBps": alg * reps / (ms / 1e3) / 1e9}
 
 
 def run_sharded(args, ss, rank, dev, stream, parts=4):
@@ -613,6 +666,7 @@ def main():
     ap.add_argument("--ring", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--spec-steps", type=int, default=4000)
+    ap.add_argument("--tree-steps", type=int, default=1500)
     ap.add_argument("--shard-steps", type=int, default=2000)
     ap.add_argument("--fused-steps", type=int, default=400)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -318,7 +318,8 @@ def algorithmic_bytes(w):
     8*len(bias) + 40 B of parameters + 4 B output.  Verification request:
     (k+1)*V*s target logits + 8k for the draft tokens and q_j(x_j) + the same
     per-request terms; the q gathers of a rejected position depend on the
-    outcome and are not counted.
+    outcome and are not counted.  Tree request: n*V*s target logits (one row
+    per node) + 8n for node tokens and parents + the per-request terms.
     """
     s = 2 if w["dtype"] == "bf16" else 4
     V = int(w["vocab"])
@@ -326,6 +327,9 @@ def algorithmic_bytes(w):
     if w["kind"] == "sample":
         n = int(w["num_rows"])
         rows = n
+    elif w["kind"] == "tree":
+        n = int(w["num_requests"])
+        rows = int(w["node_offsets"][-1])
     else:
         n = int(w["num_requests"])
         rows = int(w["draft_offsets"][-1]) + n
@@ -339,6 +343,8 @@ def algorithmic_bytes(w):
         total += 8 * int(w["bias_ids"].size)
     if w["kind"] == "verify":
         total += 8 * int(w["draft_tokens"].size)
+    if w["kind"] == "tree":
+        total += 8 * int(w["node_tokens"].size)  # token and parent of every node
     return int(total)
 
 
