@@ -278,6 +278,9 @@ __device__ __forceinline__ int light_cost(float T, int32_t top_k) {
 }
 
 constexpr int kCostLevels = 5;
+constexpr int kLevelCacheOff = 32;  // ints: past the counters and warp sums
+constexpr int kLevelCache = kRedBytes - kLevelCacheOff * 4;
+static_assert(2 + kCostLevels + kWarps <= kLevelCacheOff, "ordering scratch overlaps its level cache");
 
 // Ordered launches.  With row_class 1 or 2 a sampling launch serves one class
 // of rows (light or heavy, see row_is_heavy); with 3 a launch serves every
@@ -288,7 +291,7 @@ constexpr int kCostLevels = 5;
 // past its request's drafts has no work and is left out; one of a request with
 // a bad draft count only reports the status (cheapest level).  Every thread of
 // the CTA calls it; every CTA of the cluster gets the same answer.  Returns the
-// task, or -1.  sm: 2 + kCostLevels + kWarps ints of shared memory.
+// task, or -1.  sm: kRedBytes of shared memory.
 __device__ int ordered_task(const KArgs& a, int i, int32_t* sm) {
   const ss_params& p = a.p;
   const int n = a.num_tasks;
@@ -312,11 +315,14 @@ __device__ int ordered_task(const KArgs& a, int i, int32_t* sm) {
   };
   int32_t* cnt = sm + 2;
   int32_t* wsum = cnt + kCostLevels;
+  // the first pass keeps each task's level (+1) for the second, up to kLevelCache tasks
+  uint8_t* lev = reinterpret_cast<uint8_t*>(sm + kLevelCacheOff);
   if (threadIdx.x < kCostLevels) cnt[threadIdx.x] = 0;
   if (threadIdx.x == 0) sm[0] = -1;
   __syncthreads();
   for (int r = threadIdx.x; r < n; r += kThreads) {
     const int l = level(r);
+    if (r < kLevelCache) lev[r] = static_cast<uint8_t>(l + 1);
     if (l >= 0) atomicAdd(&cnt[l], 1);
   }
   __syncthreads();
@@ -328,7 +334,7 @@ __device__ int ordered_task(const KArgs& a, int i, int32_t* sm) {
   int base = 0;
   for (int r0 = 0; r0 < n; r0 += kThreads) {
     const int r = r0 + static_cast<int>(threadIdx.x);
-    const bool f = r < n && level(r) == lv;
+    const bool f = r < n && (r < kLevelCache ? static_cast<int>(lev[r]) - 1 : level(r)) == lv;
     const unsigned b = __ballot_sync(0xffffffffu, f);
     if (lane == 0) wsum[warp] = __popc(b);
     __syncthreads();
@@ -1894,37 +1900,51 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
     c.row = live ? row : -1;
     c.bad_k = bad_k;
     c.req = req;
-    c.rowid = a.p.row_id ? a.p.row_id[req] : static_cast<uint32_t>(req);
+    // Every per-request parameter in one batch of independent read-only
+    // loads (global, so none can alias the shared-memory stores below).
+    const ss_params& p = a.p;
+    const uint32_t rid = p.row_id ? __ldg(p.row_id + req) : static_cast<uint32_t>(req);
+    const float T = __ldg(p.temperature + req);
+    const int32_t top_k = p.top_k ? __ldg(p.top_k + req) : 0;
+    const float top_p = p.top_p ? __ldg(p.top_p + req) : 1.0f;
+    const float min_p = p.min_p ? __ldg(p.min_p + req) : 0.0f;
+    const float rep = p.repetition ? __ldg(p.repetition + req) : 1.0f;
+    const float freq = p.frequency ? __ldg(p.frequency + req) : 0.0f;
+    const float pres = p.presence ? __ldg(p.presence + req) : 0.0f;
+    const int32_t h0 = p.hist_offsets ? __ldg(p.hist_offsets + req) : 0;
+    const int32_t h1 = p.hist_offsets ? __ldg(p.hist_offsets + req + 1) : 0;
+    const int32_t b0 = p.bias_offsets ? __ldg(p.bias_offsets + req) : 0;
+    const int32_t b1 = p.bias_offsets ? __ldg(p.bias_offsets + req + 1) : 0;
+    const bool use_mask = (p.bitmask != nullptr) && (p.use_bitmask == nullptr || __ldg(p.use_bitmask + req) != 0);
+    const uint64_t seed = __ldg(reinterpret_cast<const unsigned long long*>(p.seed) + req);
+    const int64_t pos = __ldg(reinterpret_cast<const long long*>(p.position) + req);
+    c.rowid = rid;
     c.j = j;
     c.k = k;
     c.d0 = d0;
     c.drow = drow;
     c.x = x;
-    const ss_params& p = a.p;
-    const float T = p.temperature[req];
     c.temperature = T;
     c.greedy = (T == 0.0f);
     c.inv_t = __fdiv_rn(1.0f, T);
-    c.top_k = p.top_k ? p.top_k[req] : 0;
-    c.top_p = p.top_p ? p.top_p[req] : 1.0f;
-    c.min_p = p.min_p ? p.min_p[req] : 0.0f;
-    c.rep = p.repetition ? p.repetition[req] : 1.0f;
-    c.freq = p.frequency ? p.frequency[req] : 0.0f;
-    c.pres = p.presence ? p.presence[req] : 0.0f;
-    c.h0 = p.hist_offsets ? p.hist_offsets[req] : 0;
-    c.h1 = p.hist_offsets ? p.hist_offsets[req + 1] : 0;
-    c.b0 = p.bias_offsets ? p.bias_offsets[req] : 0;
-    c.b1 = p.bias_offsets ? p.bias_offsets[req + 1] : 0;
-    c.use_mask = (p.bitmask != nullptr) && (p.use_bitmask == nullptr || p.use_bitmask[req] != 0);
-    const uint64_t seed = p.seed[req];
+    c.top_k = top_k;
+    c.top_p = top_p;
+    c.min_p = min_p;
+    c.rep = rep;
+    c.freq = freq;
+    c.pres = pres;
+    c.h0 = h0;
+    c.h1 = h1;
+    c.b0 = b0;
+    c.b1 = b1;
+    c.use_mask = use_mask;
     c.seed_lo = static_cast<uint32_t>(seed);
     c.seed_hi = static_cast<uint32_t>(seed >> 32);
-    const int64_t pos = p.position[req];
     c.pos = static_cast<uint32_t>(pos) + static_cast<uint32_t>(j);
     // parameter validation (identical in every CTA of the cluster)
-    if (!(T >= 0.0f) || isinf(T) || c.top_k < 0 || !(c.top_p > 0.0f) || !(c.min_p >= 0.0f && c.min_p <= 1.0f) ||
-        !(c.rep > 0.0f) || isinf(c.rep) || !isfinite(c.freq) || !isfinite(c.pres) || c.h1 < c.h0 ||
-        c.b1 < c.b0 || pos < 0 || pos + k > 0xffffffffll)
+    if (!(T >= 0.0f) || isinf(T) || top_k < 0 || !(top_p > 0.0f) || !(min_p >= 0.0f && min_p <= 1.0f) ||
+        !(rep > 0.0f) || isinf(rep) || !isfinite(freq) || !isfinite(pres) || h1 < h0 || b1 < b0 || pos < 0 ||
+        pos + k > 0xffffffffll)
       status = SS_ROW_BAD_PARAM;
     if (a.shard_rec && status == SS_ROW_OK) {
       // a shard can list at most shard_cap candidates, and top-p / min-p

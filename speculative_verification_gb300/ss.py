@@ -406,6 +406,62 @@ def to_device(w, device="cuda", pin=False):
     return out
 
 
+def _host_array(val):
+    """A workload array as the bytes the device sees (the same
+    reinterpretations as to_device) and the torch dtype of its view."""
+    import torch
+    arr = np.ascontiguousarray(val)
+    if arr.dtype == np.uint64:
+        arr = arr.view(np.int64)
+    elif arr.dtype == np.uint32:
+        arr = arr.view(np.int32)
+    bf16 = arr.dtype == np.uint16
+    if bf16:
+        arr = arr.view(np.int16)
+    return arr, (torch.bfloat16 if bf16 else _torch_dtype(arr.dtype))
+
+
+def pack_layout(w, align=256):
+    """Byte layout of a workload's arrays in one contiguous buffer:
+    {key: (offset, nbytes, shape, torch dtype)} and the total size."""
+    lay, off = {}, 0
+    for key, val in w.items():
+        if isinstance(val, np.ndarray):
+            arr, dt = _host_array(val)
+            lay[key] = (off, arr.nbytes, arr.shape, dt)
+            off += (arr.nbytes + align - 1) // align * align
+    return lay, max(off, align)
+
+
+def pack_pinned(w, lay, total):
+    """The workload's arrays in one pinned host buffer laid out by `lay`, so
+    that one copy moves a whole input set to the device."""
+    import torch
+    buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    view = buf.numpy()
+    for key, (off, nbytes, _, _) in lay.items():
+        arr, _ = _host_array(w[key])
+        view[off:off + nbytes] = arr.reshape(-1).view(np.uint8)
+    return buf
+
+
+def views(buf, lay, w):
+    """A workload dictionary whose arrays are views into `buf` (a device
+    buffer filled by one copy of a pack_pinned buffer); scalars from `w`."""
+    import torch
+    out = {}
+    for key, val in w.items():
+        if key in lay:
+            off, nbytes, shape, dt = lay[key]
+            itemsize = torch.empty(0, dtype=dt).element_size()
+            out[key] = buf[off:off + nbytes].view(dt).view(shape) if nbytes else torch.empty(
+                shape, dtype=dt, device=buf.device)
+            assert out[key].numel() * itemsize == nbytes
+        else:
+            out[key] = val
+    return out
+
+
 class Outputs(dict):
     pass
 
