@@ -184,7 +184,7 @@ def run_ours(args, rank, world, dist):
     # that can double, the heavy rows (top-p without top-k) get a concurrent
     # launch of their own with twice the CTAs per row
     cs = ss.ss_cluster_size(int(ring_host[0]["vocab"]), ring_host[0]["dtype"])
-    per_call = 2 if (ring_host[0]["kind"] == "sample" and int(ring_host[0]["num_rows"]) >= 16 and 2 <= cs <= 4) else 1
+    per_call = 2 if (ring_host[0]["kind"] == "sample" and 16 <= int(ring_host[0]["num_rows"]) <= 4096 and 2 <= cs <= 4) else 1
     rows_per_call = int(ring_host[0]["num_rows"]) if ring_host[0]["kind"] == "sample" else int(
         ring_host[0]["draft_offsets"][-1]) + int(ring_host[0]["num_requests"])
     ring = [ss.to_device(w, dev) for w in ring_host]

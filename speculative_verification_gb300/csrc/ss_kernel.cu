@@ -278,6 +278,9 @@ __device__ __forceinline__ int light_cost(float T, int32_t top_k) {
 }
 
 constexpr int kCostLevels = 5;
+// Every CTA of an ordered launch reads the parameters of all its tasks: the
+// launches order at most this many (beyond, the launch order is kept).
+constexpr int kMaxOrderedTasks = 4096;
 constexpr int kLevelCacheOff = 32;  // ints: past the counters and warp sums
 constexpr int kLevelCache = kRedBytes - kLevelCacheOff * 4;
 static_assert(2 + kCostLevels + kWarps <= kLevelCacheOff, "ordering scratch overlaps its level cache");
@@ -2886,7 +2889,9 @@ static ss_status run_sample(const KArgs& ka, int32_t dtype, cudaStream_t stream)
   const int es = (dtype == SS_DTYPE_BF16) ? 2 : 4;
   const int cs = choose_cluster(ka.vocab, es);
   SideStream* side = nullptr;
-  if (ka.num_tasks >= 16 && cs >= 2 && 2 * cs <= kMaxCluster && !ka.debug_processed) side = side_stream(stream);
+  if (ka.num_tasks >= 16 && ka.num_tasks <= kMaxOrderedTasks && cs >= 2 && 2 * cs <= kMaxCluster &&
+      !ka.debug_processed)
+    side = side_stream(stream);
   if (!side) return run(ka, dtype, stream);
   KArgs heavy = ka, light = ka;
   heavy.row_class = 2;
@@ -3096,7 +3101,7 @@ ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t wor
   k.ws_counters = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
                                              static_cast<size_t>(tasks) * sizeof(int4));
   // many positions run in several waves: start the costliest first
-  if (tasks >= 16) k.row_class = 3;
+  if (tasks >= 16 && tasks <= kMaxOrderedTasks) k.row_class = 3;
   return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -3145,7 +3150,7 @@ ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t works
   k.ws_results = reinterpret_cast<int4*>(workspace);
   k.ws_counters = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
                                              static_cast<size_t>(tasks) * sizeof(int4));
-  if (tasks >= 16) k.row_class = 3;
+  if (tasks >= 16 && tasks <= kMaxOrderedTasks) k.row_class = 3;
   return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 

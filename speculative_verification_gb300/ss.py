@@ -190,10 +190,18 @@ PARAM_FIELDS = ("temperature", "top_k", "top_p", "min_p", "repetition", "frequen
 
 
 def make_params(p):
-    """ss_params from a dict of device tensors (missing / None = off)."""
+    """ss_params from a dict of device tensors (missing / None = off).  A
+    history or bias list with no entries at all is passed as off (an empty
+    tensor has no data pointer, and the library wants offsets and ids
+    together)."""
     sp = ss_params()
+    empty = set()
+    for off, ids in (("hist_offsets", ("hist_ids",)), ("bias_offsets", ("bias_ids", "bias_vals"))):
+        t = p.get(ids[0])
+        if t is not None and t.numel() == 0:
+            empty.update((off,) + ids)
     for name in PARAM_FIELDS:
-        setattr(sp, name, _ptr(p.get(name)))
+        setattr(sp, name, None if name in empty else _ptr(p.get(name)))
     sp.bitmask_stride = int(p.get("bitmask_stride", 0) or 0)
     return sp
 

@@ -109,3 +109,24 @@ def test_shard_entry_points_reject_bad_arguments(lib):
     assert m(C.byref(a), 9, ptrs, 8, None) == 1         # more than 8 shards
     assert m(C.byref(a), 2, ptrs, 8, None) == 1         # no outputs
     assert m(None, 2, ptrs, 8, None) == 1
+
+
+def test_empty_history_and_bias_lists_are_passed_as_off():
+    torch = pytest.importorskip("torch")
+    p = {"temperature": torch.ones(3), "hist_offsets": torch.zeros(4, dtype=torch.int32),
+         "hist_ids": torch.zeros(0, dtype=torch.int32), "bias_offsets": torch.tensor([0, 1, 1, 2], dtype=torch.int32),
+         "bias_ids": torch.tensor([5, 7], dtype=torch.int32), "bias_vals": torch.tensor([1.0, -1.0])}
+    sp = ss.make_params(p)
+    assert sp.hist_offsets is None and sp.hist_ids is None
+    assert sp.bias_offsets and sp.bias_ids and sp.bias_vals and sp.temperature
+
+
+def test_tree_entry_point_rejects_bad_arguments(lib):
+    a = ss.ss_tree_args()
+    assert lib.ss_tree_verify(None, None, 0, None) == 1
+    a.num_requests, a.vocab, a.max_nodes, a.dtype = 1, 100, 65, 1  # more nodes than the limit
+    assert lib.ss_tree_verify(ss.C.byref(a), None, 0, None) == 1
+    a.max_nodes = 0
+    assert lib.ss_tree_verify(ss.C.byref(a), None, 0, None) == 1
+    a.max_nodes, a.num_requests = 4, 0  # nothing to do
+    assert lib.ss_tree_verify(ss.C.byref(a), None, 0, None) == 0

@@ -272,3 +272,16 @@ def test_deterministic_and_graph_capturable(ss):
     torch.cuda.synchronize()
     for key in ("token", "status", "kept"):
         assert torch.equal(o1[key], o2[key]), key
+
+
+def test_split_launch_matches_single_launches(ss):
+    # 64 rows: the heavy rows (top-p without top-k) run on a concurrent launch
+    # with twice the CTAs per row; the same rows 8 at a time run as one launch
+    # each with the default cluster.  The results must not depend on that.
+    w = W.make(2, rows=64, vocab=128256)
+    w["row_id"] = np.arange(64, dtype=np.uint32)
+    big = run_gpu(ss, w, debug=False)
+    for s0 in range(0, 64, 8):
+        part = run_gpu(ss, parity.subset_sample(w, list(range(s0, s0 + 8))), debug=False)
+        for key in ("token", "status", "kept"):
+            assert np.array_equal(part[key], big[key][s0:s0 + 8]), (key, s0)
