@@ -235,9 +235,12 @@ def run_ours(args, rank, world, dist):
             dist.barrier()
         torch.cuda.synchronize()
         start.record(stream)
+        marks = []  # an event after every replay: best and median per replay
         with torch.cuda.stream(stream):
             for _ in range(reps):
                 g_main.replay()
+                marks.append(torch.cuda.Event(enable_timing=True))
+                marks[-1].record(stream)
             if g_rem is not None:
                 g_rem.replay()
         stop.record(stream)
@@ -251,6 +254,22 @@ def run_ours(args, rank, world, dist):
         ms = float(t.item())
     per_call_s = ms / 1e3 / args.steps
     value = DP.aggregate_rate(rows_per_call, args.steps, world, ms)
+    per_replay = [a.elapsed_time(b) * 1e3 / per_graph for a, b in zip([start] + marks[:-1], marks)]
+    # single calls without a graph, synchronised one by one (launch latency included)
+    single = []
+    for i in range(50):
+        a_ev = torch.cuda.Event(enable_timing=True)
+        b_ev = torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        with torch.cuda.stream(stream):
+            call(i)
+        b_ev.record(stream)
+        stream.synchronize()
+        single.append(a_ev.elapsed_time(b_ev) * 1e3)
+    call_us = {"mean": ms * 1e3 / args.steps,
+               "best_replay": min(per_replay) if per_replay else None,
+               "median_replay": statistics.median(per_replay) if per_replay else None,
+               "single_call_no_graph_median": statistics.median(single)}
 
     # end-to-end through the public API with host buffers (pinned)
     progress("timed region done: %.3f ms" % ms)
@@ -299,6 +318,7 @@ def run_ours(args, rank, world, dist):
             "peak": peak,
             "unit": "GB/s",
             "frac": achieved / peak,
+            "frac_of_nominal_7900": achieved / 7900.0,
             "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured" else "fallback",
             "algorithmic_bytes_per_launch": bytes_per_call,
             "traffic": recorded_traffic(W.CONFIG_NAMES[cfg]),
@@ -306,6 +326,7 @@ def run_ours(args, rank, world, dist):
             "kernel_sha256": kernel_source_hash(),
         },
         "e2e": e2e,
+        "us_per_call": call_us,
         "gpu_launches": args.steps * per_call,
         "clocks": clocks.summary(),
     }
@@ -652,6 +673,35 @@ def cpu_baseline_block(cfg, seconds):
             "sample": "%d rows of the %s workload (8-row batches) in %.1f s, one thread" % (rows, W.CONFIG_NAMES[cfg], el)}
 
 
+def cpu_parallel_block(cfg, seconds):
+    """The same oracle on every host core at once: one thread per core, each
+    sampling its own 8-row batches (rows are independent; the C oracle runs
+    without the interpreter lock)."""
+    import threading
+    from oracle import oracle as O
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    samples = [W.make(cfg, seed=cfg + 424242 + i, rows=8) for i in range(cores)]
+    O.process_sample(samples[0])  # build / load the oracle before the clock starts
+    counts = [0] * cores
+    t0 = time.perf_counter()
+
+    def work(i):
+        while time.perf_counter() - t0 < seconds:
+            O.process_sample(samples[i])
+            counts[i] += int(samples[i]["num_rows"])
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(cores)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    el = time.perf_counter() - t0
+    rows = sum(counts)
+    return {"value": rows / el, "unit": "rows/s", "cores": cores, "kind": "oracle, row-parallel",
+            "sample": "%d rows of the %s workload (8-row batches) in %.1f s, %d threads" % (
+                rows, W.CONFIG_NAMES[cfg], el, cores)}
+
+
 def run_reference(args):
     """The oracle as the reference arm: each step samples one 8-row batch of
     the same workload; at most as many steps as fit in ~90 s are timed."""
@@ -721,10 +771,11 @@ def main():
         return 0
 
     # the oracle runs before any CUDA work (no fork after the first GPU call)
-    cpu = None
+    cpu = cpu_par = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         progress("cpu baseline")
         cpu = cpu_baseline_block(args.config, args.cpu_seconds)
+        cpu_par = cpu_parallel_block(args.config, max(2.0, args.cpu_seconds / 2))
         progress("cpu baseline done")
 
     dist = None
@@ -737,6 +788,7 @@ def main():
     res = run_ours(args, rank, world, dist)
     if cpu is not None:
         res["cpu_baseline"] = cpu
+        res["cpu_baseline_all_cores"] = cpu_par
     if rank == 0:
         print(json.dumps(res))
     if dist:
