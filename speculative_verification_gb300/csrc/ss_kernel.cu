@@ -1501,14 +1501,14 @@ __device__ __noinline__ uint32_t philox_numerator(uint64_t seed, uint32_t row, u
 
 // The draw: Gumbel-max over K (stream 0).  Also counts |K| and, for a
 // verification position, its fixed-point mass; result in g.fold.
-template <int DT>
+template <int DT, bool kDraw>
 __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, int spec_pos, int count_k, uint64_t seed) {
   using V = Vec<DT>;
   const float m = g.m, min_p = g.min_p, inv_t = g.inv_t;
   const uint32_t rowid = g.rowid, pos = g.pos;
   const int32_t arg = g.arg;
   // the argmax token is always in K: its score seeds the running best
-  const float g0 = gumbel_noise(philox_numerator(seed, rowid, pos, arg, 0));
+  const float g0 = kDraw ? gumbel_noise(philox_numerator(seed, rowid, pos, arg, 0)) : 0.0f;
   float bv = __fadd_rn(m, g0);
   int32_t bi = arg;
   int32_t kcount = 0;
@@ -1517,6 +1517,7 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
     if (!in_kept(t, y, m, mp_on, min_p)) return;
     ++kcount;
     if (spec_pos) kmass += fixed_mass(y, m);
+    if (!kDraw) return;
     const float slack = 1e-3f + fabsf(y) * 1e-6f;
     if (y + kGumbelMax + slack < bv) return;
     const uint32_t num = philox_numerator(seed, rowid, pos, static_cast<uint32_t>(t), 0);
@@ -1538,7 +1539,7 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
   for_vectors_above<DT>(k_lo, [&](int v) {
     // prune against the best score any lane of the warp has reached (a token
     // below it cannot win); the lane's own best (bv, bi) is what it reports
-    const float pb = key_value(__reduce_max_sync(0xffffffffu, order_key(bv)));
+    const float pb = kDraw ? key_value(__reduce_max_sync(0xffffffffu, order_key(bv))) : 0.0f;
     if (v < 0) return;
     const float ub = vec_bound(v);
     // plain rows need no mass: a vector that cannot beat the best is skipped
@@ -1563,63 +1564,65 @@ __device__ __noinline__ void draw_pass(int mp_on, float k_lo, int prune_best, in
       if (spec_pos) kmass += in ? fixed_mass(y, m) : 0ull;
     }
     kcount += __popc(mem);
-    if (!cand) return;
-    uint32_t w[V::kPer];
+    if constexpr (kDraw) {
+      if (!cand) return;
+      uint32_t w[V::kPer];
 #pragma unroll
-    for (int q = 0; q < kGroups; ++q) {  // independent blocks: their rounds interleave
-      const Philox4 r = philox4x32_10(static_cast<uint32_t>(t0 >> 2) + q, pos, rowid, 0u, key0, key1);
+      for (int q = 0; q < kGroups; ++q) {  // independent blocks: their rounds interleave
+        const Philox4 r = philox4x32_10(static_cast<uint32_t>(t0 >> 2) + q, pos, rowid, 0u, key0, key1);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) w[q * 4 + i] = r.w[i];
-    }
-    // A candidate can still reach the running best only if its noise
-    // g >= pb - y - slack >= d, d taken at the largest candidate logit with a
-    // slack that covers every candidate (|y| <= |pb| + 20 for candidates).
-    // g increases with u, so that is u >= exp(-exp(-d)): one threshold on
-    // the 24-bit numerators per vector, lowered by a margin for the fast
-    // exponentials; the exact noise is computed only for the survivors.
-    float ymax = neg_inf();
+        for (int i = 0; i < 4; ++i) w[q * 4 + i] = r.w[i];
+      }
+      // A candidate can still reach the running best only if its noise
+      // g >= pb - y - slack >= d, d taken at the largest candidate logit with a
+      // slack that covers every candidate (|y| <= |pb| + 20 for candidates).
+      // g increases with u, so that is u >= exp(-exp(-d)): one threshold on
+      // the 24-bit numerators per vector, lowered by a margin for the fast
+      // exponentials; the exact noise is computed only for the survivors.
+      float ymax = neg_inf();
 #pragma unroll
-    for (int e = 0; e < V::kPer; ++e) ymax = fmaxf(ymax, ((cand >> e) & 1u) ? z[e] : neg_inf());
-    const float d = pb - ymax - (1e-3f + (fabsf(pb) + 20.0f) * 1e-6f);
-    uint32_t thr = 0;
-    if (d > 0.0f) {
-      const float u_min = __expf(-__expf(-d));
-      thr = __float2uint_rd(fmaxf(u_min * 16777216.0f * (1.0f - 1e-5f) - 4.0f, 0.0f));
-    }
-    uint32_t live = 0;
+      for (int e = 0; e < V::kPer; ++e) ymax = fmaxf(ymax, ((cand >> e) & 1u) ? z[e] : neg_inf());
+      const float d = pb - ymax - (1e-3f + (fabsf(pb) + 20.0f) * 1e-6f);
+      uint32_t thr = 0;
+      if (d > 0.0f) {
+        const float u_min = __expf(-__expf(-d));
+        thr = __float2uint_rd(fmaxf(u_min * 16777216.0f * (1.0f - 1e-5f) - 4.0f, 0.0f));
+      }
+      uint32_t live = 0;
 #pragma unroll
-    for (int e = 0; e < V::kPer; ++e) {
-      w[e] = uniform_numerator(w[e]);
-      live |= static_cast<uint32_t>(w[e] >= thr) << e;
-    }
-    live &= cand;
-    if (!live) return;
-    if (live & (live - 1u)) {
-      // several survivors: every lane's noise without branches, so that the
-      // independent logf chains overlap
-      float sc[V::kPer];
+      for (int e = 0; e < V::kPer; ++e) {
+        w[e] = uniform_numerator(w[e]);
+        live |= static_cast<uint32_t>(w[e] >= thr) << e;
+      }
+      live &= cand;
+      if (!live) return;
+      if (live & (live - 1u)) {
+        // several survivors: every lane's noise without branches, so that the
+        // independent logf chains overlap
+        float sc[V::kPer];
 #pragma unroll
-      for (int e = 0; e < V::kPer; ++e) sc[e] = __fadd_rn(z[e], gumbel_from_numerator(w[e]));
+        for (int e = 0; e < V::kPer; ++e) sc[e] = __fadd_rn(z[e], gumbel_from_numerator(w[e]));
 #pragma unroll
-      for (int e = 0; e < V::kPer; ++e)
-        if (((live >> e) & 1u) && beats(sc[e], t0 + e, bv, bi)) {
-          bv = sc[e];
+        for (int e = 0; e < V::kPer; ++e)
+          if (((live >> e) & 1u) && beats(sc[e], t0 + e, bv, bi)) {
+            bv = sc[e];
+            bi = t0 + e;
+          }
+      } else {
+        const int e = __ffs(live) - 1;
+        float ze = z[0];
+        uint32_t we = w[0];
+#pragma unroll
+        for (int q = 1; q < V::kPer; ++q)
+          if (q == e) {
+            ze = z[q];
+            we = w[q];
+          }
+        const float sc = __fadd_rn(ze, gumbel_noise(we));
+        if (beats(sc, t0 + e, bv, bi)) {
+          bv = sc;
           bi = t0 + e;
         }
-    } else {
-      const int e = __ffs(live) - 1;
-      float ze = z[0];
-      uint32_t we = w[0];
-#pragma unroll
-      for (int q = 1; q < V::kPer; ++q)
-        if (q == e) {
-          ze = z[q];
-          we = w[q];
-        }
-      const float sc = __fadd_rn(ze, gumbel_noise(we));
-      if (beats(sc, t0 + e, bv, bi)) {
-        bv = sc;
-        bi = t0 + e;
       }
     }
   });
@@ -1761,11 +1764,12 @@ __device__ __noinline__ void tree_mass_pass(int mp_on, float memb_lo, float inv_
 // min(1, p_i(x)/q(x)), p_0 = P, p_{i+1} = max(p_i - q, 0) / Z_{i+1}; the uniform
 // is word i of stream 1 at this node's position.  On the first acceptance
 // acc_node is the child's local index; when every child is rejected, token is
-// the Gumbel-max draw from max(p_{m-1} - q, 0) (stream 2); when a residual
-// sums to zero before the last child, token stays the stream-0 draw from P.
-// Every CTA of the cluster takes the same decisions (cluster-wide sums).
+// the Gumbel-max draw from max(p_{m-1} - q, 0) (stream 2).  Returns true when
+// the token must be the stream-0 draw from P instead (a residual that sums to
+// zero, by rounding): the caller draws it.  Every CTA of the cluster takes the
+// same decisions (cluster-wide sums).
 template <int DT>
-__device__ __noinline__ void tree_children(int mp_on, float memb_lo, float SK, const float* qrow, uint64_t seed,
+__device__ __noinline__ bool tree_children(int mp_on, float memb_lo, float SK, const float* qrow, uint64_t seed,
                                            int32_t& acc_node, int32_t& token) {
   cg::cluster_group cl = cg::this_cluster();
   const int m = g.nkids;
@@ -1793,19 +1797,20 @@ __device__ __noinline__ void tree_children(int mp_on, float memb_lo, float SK, c
     if (__fmul_rn(u, qx) < px) {
       acc_node = g.kid_node[i];
       token = x;
-      return;
+      return false;
     }
     // consecutive reductions alternate between two part slots
     const int slot = 2 + (nz & 1);
     if (i == m - 1) {
       residual_pass<DT>(mp_on, memb_lo, inv_s, log_s, qrow, seed, invz, nz, slot);
       const Part rall = g.fold;
-      if (rall.arg != kNoCut && rall.best > neg_inf()) token = rall.arg;
-      return;
+      if (rall.arg == kNoCut || !(rall.best > neg_inf())) return true;
+      token = rall.arg;
+      return false;
     }
     tree_mass_pass<DT>(mp_on, memb_lo, inv_s, qrow, invz, nz, slot);
     const unsigned long long zm = g.fold.mass;
-    if (zm == 0) return;  // nothing left (rounding): the stream-0 draw
+    if (zm == 0) return true;  // nothing left (rounding): the stream-0 draw
     const float Z = static_cast<float>(static_cast<double>(zm) * kFixedInv);
     __syncthreads();  // every thread has read g.fold and invz
     if (threadIdx.x == 0) invz[nz] = __fdiv_rn(1.0f, Z);
@@ -1813,7 +1818,47 @@ __device__ __noinline__ void tree_children(int mp_on, float memb_lo, float SK, c
     ++nz;
     log_s += logf(Z);
   }
+  return false;
 }
+// A position that tests drafts, after the pass that summed the mass of K
+// (mass, in 2^-40 units) and fetched the draft token's processed logit yx:
+// a linear position accepts its draft with u * q(x) < P(x) (stream 1, word 0)
+// and otherwise draws from the residual max(P - q, 0) (stream 2); a tree node
+// tests its children (tree_children).  When the residual is empty (rounding)
+// the token is the stream-0 draw from P, drawn here.  Out of line so that the
+// sampling path's register allocation does not carry it.
+template <int DT>
+__device__ __noinline__ void spec_position(int tree, int mp_on, float memb_lo, unsigned long long mass, float yx,
+                                           const float* qrow, uint64_t seed, int32_t& accept, int32_t& acc_node,
+                                           int32_t& token) {
+  const float SK = static_cast<float>(static_cast<double>(mass) * kFixedInv);
+  bool fallback = false;
+  if (tree) {
+    fallback = tree_children<DT>(mp_on, memb_lo, SK, qrow, seed, acc_node, token);
+  } else {
+    const bool x_in = (yx != neg_inf()) && in_kept(g.x, yx, g.m, mp_on, g.min_p);
+    const float inv_s = __fdiv_rn(1.0f, SK);
+    const float Px = x_in ? __fmul_rn(__expf(yx - g.m), inv_s) : 0.0f;
+    const float q = qrow[g.x];
+    const float u = uniform_from_numerator(uniform_numerator(philox_word(seed, g.rowid, g.pos, 0, 1)));
+    accept = (__fmul_rn(u, q) < Px) ? 1 : 0;
+    if (accept) {
+      token = g.x;
+    } else {
+      residual_pass<DT>(mp_on, memb_lo, inv_s, logf(SK), qrow, seed, nullptr, 0, 2);
+      const Part rall = g.fold;
+      if (rall.arg != kNoCut && rall.best > neg_inf())
+        token = rall.arg;
+      else
+        fallback = true;
+    }
+  }
+  if (fallback) {
+    draw_pass<DT, true>(mp_on, memb_lo, 1, 0, 0, seed);
+    token = g.fold.arg;
+  }
+}
+
 // ------------------------------------------------------------- kernel --
 
 template <int DT>
@@ -2391,7 +2436,12 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
         kept = cut_on ? cut_len : c.count;
         token = -1;
       } else {
-      draw_pass<DT>(mp_on, k_lo, !spec_pos && !need_count, spec_pos, need_count, seed);
+      // a position that tests a draft needs the mass of K, not the stream-0
+      // draw: that is only the fallback of an empty residual (drawn then)
+      if (spec_pos)
+        draw_pass<DT, false>(mp_on, k_lo, 0, 1, need_count, seed);
+      else
+        draw_pass<DT, true>(mp_on, k_lo, !need_count, 0, need_count, seed);
       const Part dall = g.fold;
       kept = need_count ? dall.count : (cut_on ? cut_len : c.count);
       token = dall.arg;
@@ -2400,29 +2450,10 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
         h->best = dall.best;
         h->best_token = dall.arg;
       }
-      if (spec_pos && a.mode == kModeTree) {
-        const float SK = static_cast<float>(static_cast<double>(dall.mass) * kFixedInv);
-        tree_children<DT>(mp_on, memb_lo, SK, a.draft_probs + static_cast<int64_t>(c.drow) * a.draft_stride, seed,
-                          acc_node, token);
-      } else if (spec_pos) {
-        const float yx = dall.xhere ? dall.xy : neg_inf();
-        const bool x_in = (yx != neg_inf()) && in_kept(c.x, yx, m, mp_on, min_p);
-        const float SK = static_cast<float>(static_cast<double>(dall.mass) * kFixedInv);
-        const float inv_s = __fdiv_rn(1.0f, SK);
-        const float Px = x_in ? __fmul_rn(__expf(yx - m), inv_s) : 0.0f;
-        const float q = a.draft_probs[static_cast<int64_t>(c.drow) * a.draft_stride + c.x];
-        const float u = uniform_from_numerator(uniform_numerator(philox_word(seed, rowid, c.pos, 0, 1)));
-        accept = (__fmul_rn(u, q) < Px) ? 1 : 0;
-        if (accept) {
-          token = c.x;
-        } else {
-          const float* qrow = a.draft_probs + static_cast<int64_t>(c.drow) * a.draft_stride;
-          residual_pass<DT>(mp_on, memb_lo, inv_s, logf(SK), qrow, seed, nullptr, 0, 2);
-          const Part rall = g.fold;
-          if (rall.arg != kNoCut && rall.best > neg_inf()) token = rall.arg;
-          // else: no token with P > q (rounding): keep the stream-0 draw
-        }
-      }
+      if (spec_pos)
+        spec_position<DT>(a.mode == kModeTree, mp_on, memb_lo, dall.mass, dall.xhere ? dall.xy : neg_inf(),
+                          a.draft_probs + static_cast<int64_t>(c.drow) * a.draft_stride, seed, accept, acc_node,
+                          token);
       }
     }
   }
