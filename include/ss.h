@@ -183,7 +183,14 @@ size_t ss_workspace_size(int32_t max_requests, int32_t max_draft);
  * once per buffer.  Calls sharing one workspace must not overlap in time. */
 ss_status ss_workspace_init(void* workspace, size_t workspace_bytes, ss_stream_t stream);
 
-/* Batched sampling; one kernel launch. */
+/* Batched sampling.  With 16 to 4096 rows and a vocabulary whose cluster
+ * can double (ss_cluster_size <= 4), the rows with a top-p cut and no top-k
+ * run on a second launch with twice the CTAs per row, on a library-owned
+ * stream (one per host thread and device, created by the first such call)
+ * forked from and joined back into `stream` with events; otherwise one
+ * launch.  Either way the call is asynchronous on `stream`, capturable in a
+ * CUDA graph, and its results do not depend on the split.  A capture that
+ * starts before the thread's first such call records the single launch. */
 ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream);
 
 /* Batched speculative verification; one kernel launch.  The workspace must
