@@ -2888,7 +2888,8 @@ static ss_status run(const KArgs& ka, int32_t dtype, cudaStream_t stream, int cs
 }
 
 // A second stream and fork / join events per host thread and device, for the
-// concurrent heavy-row launch.
+// concurrent heavy-row launch.  Created by the thread's first split call on
+// the device, outside stream capture; they live as long as the thread.
 struct SideStream {
   cudaStream_t stream = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
@@ -2900,15 +2901,27 @@ static SideStream* side_stream(cudaStream_t main) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   SideStream& s = side[dev];
   if (!s.stream) {
-    // created outside stream capture only
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(main, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
-    if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) {
-      s.stream = nullptr;
+    // relaxed capture mode for this thread while creating them, so that a
+    // graph another thread may be capturing is not disturbed
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) return nullptr;
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    const bool ok = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess &&
+                    cudaEventCreateWithFlags(&f, cudaEventDisableTiming) == cudaSuccess &&
+                    cudaEventCreateWithFlags(&j, cudaEventDisableTiming) == cudaSuccess;
+    cudaThreadExchangeStreamCaptureMode(&mode);  // restore the thread's mode
+    if (!ok) {
+      if (j) cudaEventDestroy(j);
+      if (f) cudaEventDestroy(f);
+      if (st) cudaStreamDestroy(st);
       return nullptr;
     }
+    s.stream = st;
+    s.fork = f;
+    s.join = j;
   }
   return &s;
 }
