@@ -380,8 +380,10 @@ ss_status ss_fused_lmhead_sample(const ss_fused_args* args, ss_stream_t stream);
 
 /* Cluster size (CTAs per vocabulary row) the kernels use for this vocabulary
  * and dtype, or 0 if unsupported.  A row is split over at most 8 CTAs of at
- * most 61,440 tokens and 160 KiB each, so the largest vocabulary is 491,520
- * for bf16 and 327,680 for f32; larger ones return SS_ERR_UNSUPPORTED. */
+ * most 61,440 tokens and 160 KiB each, whose slice and working tables must
+ * fit one CTA's 227 KiB of shared memory, so the largest vocabulary is
+ * 491,520 for bf16 and 321,536 for f32; larger ones return
+ * SS_ERR_UNSUPPORTED. */
 int32_t ss_cluster_size(int32_t vocab, int32_t dtype);
 
 /* The cudaError_t of the last SS_ERR_CUDA on this thread. */

@@ -2797,16 +2797,6 @@ __global__ void __launch_bounds__(kThreads) ss_merge_kernel(const MergeArgs a) {
 static thread_local int32_t g_last_cuda_error = 0;
 void set_last_cuda_error(int32_t e) { g_last_cuda_error = e; }
 
-static int choose_cluster(int32_t vocab, int32_t es) {
-  for (int cs = 1; cs <= kMaxCluster; cs <<= 1) {
-    const int64_t slice = ((static_cast<int64_t>(vocab) + cs - 1) / cs + 31) / 32 * 32;
-    if (slice * es <= kTargetSliceBytes) return cs;
-  }
-  const int64_t slice = ((static_cast<int64_t>(vocab) + kMaxCluster - 1) / kMaxCluster + 31) / 32 * 32;
-  if (slice * es <= kMaxSliceBytes && slice <= kMaxSliceTokens) return kMaxCluster;
-  return 0;
-}
-
 static Layout make_layout(int32_t vocab, int32_t es, int cs) {
   Layout L{};
   L.slice_len = static_cast<int32_t>(((static_cast<int64_t>(vocab) + cs - 1) / cs + 31) / 32 * 32);
@@ -2833,6 +2823,27 @@ static Layout make_layout(int32_t vocab, int32_t es, int cs) {
   L.total = static_cast<int32_t>((off + 127) / 128 * 128);
   return L;
 }
+
+// Largest shared memory one CTA may hold on this GPU family (227 KiB, dynamic
+// and static together).
+constexpr int64_t kSmemPerCta = 232448;
+
+static bool layout_fits(int32_t vocab, int32_t es, int cs) {
+  // the kernel's static context, and a margin for what the compiler adds
+  return make_layout(vocab, es, cs).total + static_cast<int64_t>(sizeof(Ctx)) + 256 <= kSmemPerCta;
+}
+
+static int choose_cluster(int32_t vocab, int32_t es) {
+  for (int cs = 1; cs <= kMaxCluster; cs <<= 1) {
+    const int64_t slice = ((static_cast<int64_t>(vocab) + cs - 1) / cs + 31) / 32 * 32;
+    if (slice * es <= kTargetSliceBytes) return cs;
+  }
+  const int64_t slice = ((static_cast<int64_t>(vocab) + kMaxCluster - 1) / kMaxCluster + 31) / 32 * 32;
+  if (slice * es <= kMaxSliceBytes && slice <= kMaxSliceTokens && layout_fits(vocab, es, kMaxCluster))
+    return kMaxCluster;
+  return 0;
+}
+
 
 template <int DT>
 static cudaError_t launch(const KArgs& ka, int cs, cudaStream_t stream) {

@@ -39,11 +39,13 @@ def test_host_only_queries(lib):
     assert ss.ss_cluster_size(10, "f32") == 1
     assert ss.ss_cluster_size(0, "f32") == 0
     assert ss.ss_cluster_size(10_000_000, "bf16") == 0
-    # largest supported rows: 8 slices of at most 61,440 tokens / 160 KiB
+    # largest supported rows: 8 slices of at most 61,440 tokens / 160 KiB whose
+    # shared-memory layout fits 227 KiB per CTA
     assert ss.ss_cluster_size(491_520, "bf16") == 8
     assert ss.ss_cluster_size(491_521, "bf16") == 0
-    assert ss.ss_cluster_size(327_680, "f32") == 8
-    assert ss.ss_cluster_size(327_681, "f32") == 0
+    assert ss.ss_cluster_size(321_536, "f32") == 8
+    assert ss.ss_cluster_size(321_537, "f32") == 0
+    assert ss.ss_cluster_size(327_680, "f32") == 0  # 160 KiB slices, but the tables would not fit
     assert ss.ss_workspace_size(32, 4) >= 32 * 5 * 16 + 32 * 4
     assert lib.ss_status_string(0) == b"ok"
 

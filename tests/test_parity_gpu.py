@@ -285,3 +285,19 @@ def test_split_launch_matches_single_launches(ss):
         part = run_gpu(ss, parity.subset_sample(w, list(range(s0, s0 + 8))), debug=False)
         for key in ("token", "status", "kept"):
             assert np.array_equal(part[key], big[key][s0:s0 + 8]), (key, s0)
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 491_520), ("f32", 321_536)])
+def test_maximum_vocabulary(ss, dtype, V):
+    # the largest rows the kernel takes: 8 slices of 61,440 tokens (bf16) or
+    # of 40,192 tokens (fp32, the most that fits 227 KiB with the tables), one
+    # CTA per SM
+    assert ss.ss_cluster_size(V, dtype) == 8
+    rng = np.random.default_rng(V)
+    n = 6
+    z = rng.normal(0, 3.0, size=(n, V)).astype(np.float32)
+    z[np.arange(n), rng.integers(0, V, size=n)] += 10.0
+    w = sample_workload(z, dtype=dtype, temperature=[0.0, 1.0, 0.8, 1.2, 1.0, 0.7], top_k=[0, 0, 50, 1000, 0, 0],
+                        top_p=[1.0, 0.9, 1.0, 0.95, 1.0, 1.0], min_p=[0.0, 0.0, 0.0, 0.0, 0.05, 0.0],
+                        seed=np.arange(n) + 17, position=np.arange(n) * 11)
+    _report("V=%d %s" % (V, dtype), *parity.check_sample(w, run_gpu(ss, w, debug=False)))
