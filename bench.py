@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -56,16 +57,25 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text):
+    """C / CUDA source without its comments and blank lines (the sources hold
+    no comment markers inside string literals), so that editing a comment
+    does not count as changing the kernel."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel="ss_row_kernel"):
-    """Hash of the sources one kernel is compiled from: its translation unit,
-    the shared device headers and the C header."""
+    """Hash of the code one kernel is compiled from: its translation unit,
+    the shared device headers and the C header, comments left out."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_verification_gb300", "csrc")
     for name in (KERNEL_SOURCES[kernel], "ss_philox.cuh", "ss_ptx.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
-    with open(os.path.join(ROOT, "include", "ss.h"), "rb") as f:
-        h.update(f.read())
+        with open(os.path.join(csrc, name)) as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
+    with open(os.path.join(ROOT, "include", "ss.h")) as f:
+        h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

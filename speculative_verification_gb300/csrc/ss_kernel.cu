@@ -1,11 +1,17 @@
 // ss_kernel.cu -- sm_103a kernels and C ABI of libss (see include/ss.h).
 //
-// Execution model (one launch per call, fixed shape):
+// Execution model (fixed shape; one launch per call, or two concurrent
+// launches for a sampling call whose rows split into heavy and light):
 //   * one thread-block cluster of C CTAs per task; a task is one logits row
-//     (ss_process_sample) or one target position (request i, draft j) of
-//     ss_spec_verify.  The row's vocabulary is cut into C slices of
-//     `slice_len` tokens; each CTA stages its slice in shared memory with 1-D
-//     bulk (TMA) copies, once, and every later pass runs on shared memory.
+//     (ss_process_sample), one target position (request i, draft j) of
+//     ss_spec_verify, or one node of a draft tree (ss_tree_verify).  The
+//     row's vocabulary is cut into C slices of `slice_len` tokens; each CTA
+//     stages its slice in shared memory with 1-D bulk (TMA) copies, once, and
+//     every later pass runs on shared memory.
+//   * launches of many tasks are ordered: cluster i takes the i-th task in
+//     decreasing cost, so the longest rows start in the first wave; a sampling
+//     call gives its heavy rows (top-p without top-k) a concurrent launch with
+//     2C CTAs per row.
 //   * penalised / biased tokens live in a per-CTA hash table ("patches") and
 //     are excluded from the raw slice; their processed values are computed
 //     from the global row and visited alongside the slice.
@@ -25,7 +31,8 @@
 //   * the draw is Gumbel-max over the kept set, per thread, then across the
 //     cluster (the argmax decomposes over partitions).  Tokens whose logit
 //     plus the largest possible noise cannot beat the running best skip the
-//     RNG, whole vectors at a time.
+//     RNG, whole vectors at a time.  A position that tests drafts sums the
+//     mass of the kept set instead and draws only from a residual.
 //   * CTAs exchange partial results by writing them into every CTA of the
 //     cluster (distributed shared memory) before a cluster barrier, so each
 //     exchange costs one barrier and every CTA derives identical decisions.
