@@ -67,6 +67,30 @@ def subset_sample(w, rows):
     return out
 
 
+def subset_tree(w, reqs):
+    """The requests `reqs` of a tree-verification workload, with their nodes,
+    rows and per-request parameters."""
+    reqs = np.asarray(reqs)
+    off = w["node_offsets"]
+    out = dict(w)
+    out["num_requests"] = len(reqs)
+    nodes = np.concatenate([np.arange(off[r], off[r + 1]) for r in reqs]) if len(reqs) else np.zeros(0, int)
+    new_off = np.zeros(len(reqs) + 1, np.int32)
+    new_off[1:] = np.cumsum([off[r + 1] - off[r] for r in reqs])
+    out["node_offsets"] = new_off
+    out["parents"] = w["parents"][nodes]
+    out["node_tokens"] = w["node_tokens"][nodes]
+    out["target_logits"] = w["target_logits"][nodes]
+    out["draft_probs"] = w["draft_probs"][nodes]
+    per_req = subset_sample(dict(w, num_rows=int(w["num_requests"]), logits=w["target_logits"], row_stride=0), reqs)
+    for key in ("temperature", "top_k", "top_p", "min_p", "repetition", "frequency", "presence", "use_bitmask",
+                "seed", "position", "row_id", "bitmask", "hist_offsets", "hist_ids", "bias_offsets", "bias_ids",
+                "bias_vals"):
+        if w.get(key) is not None:
+            out[key] = per_req[key]
+    return out
+
+
 def check_verify(w, gpu):
     """gpu: out_tokens/num_accepted/status/kept[/processed].  Returns
     (checked requests, sub-margin requests)."""

@@ -1,9 +1,10 @@
 """Row-sharded (data-parallel) host logic, on CPU with two gloo ranks.
 
-Each rank samples its own shard of one batch with the CPU oracle; the
-gathered tokens must equal those of the whole batch sampled at once (rows
-are independent, so the data path needs no collective), and the elapsed
-time reduction is the maximum over ranks, as the benchmark reports it.
+Each rank samples its own shard of one batch with the CPU oracle (and
+verifies its share of a batch of draft trees); the gathered tokens must equal
+those of the whole batch at once (rows and requests are independent and their
+noise is keyed by their ids, so the data path needs no collective), and the
+elapsed time reduction is the maximum over ranks, as the benchmark reports it.
 """
 import os
 import socket
@@ -17,13 +18,17 @@ import torch.multiprocessing as mp
 from oracle import oracle as O
 from speculative_verification_gb300 import dp as DP
 from speculative_verification_gb300 import workloads as W
-from tests.parity import subset_sample
+from tests.parity import subset_sample, subset_tree
 
 ROWS = 10
 
 
 def _batch():
     return W.make(2, rows=ROWS)
+
+
+def _trees():
+    return W.tree(seed=8, requests=7, vocab=3000, max_nodes=6)
 
 
 def _free_port():
@@ -44,12 +49,21 @@ def _rank_main(rank, world, port, out_dir):
         ref = O.process_sample(shard)
         tokens = [None] * world
         dist.all_gather_object(tokens, (start, stop, ref["token"].tolist(), ref["status"].tolist()))
+        # draft trees, split by request the same way
+        tw = _trees()
+        t0, t1 = DP.shard_rows(tw["num_requests"], rank, world)
+        tshard = subset_tree(tw, list(range(t0, t1)))
+        tshard["row_id"] = np.arange(t0, t1, dtype=np.uint32)
+        tref = O.tree_verify(tshard)
+        trees = [None] * world
+        dist.all_gather_object(trees, (t0, t1, tref["out_tokens"].tolist(), tref["out_path"].tolist()))
         t = torch.tensor([10.0 * (rank + 1)])  # a stand-in elapsed time per rank
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         seeds = [None] * world
         dist.all_gather_object(seeds, [DP.ring_seed(2, rank, i) for i in range(4)])
         if rank == 0:
             np.save(os.path.join(out_dir, "gathered.npy"), np.array(tokens, dtype=object), allow_pickle=True)
+            np.save(os.path.join(out_dir, "trees.npy"), np.array(trees, dtype=object), allow_pickle=True)
             np.save(os.path.join(out_dir, "tmax.npy"), t.numpy())
             np.save(os.path.join(out_dir, "seeds.npy"), np.array(seeds))
     finally:
@@ -86,6 +100,16 @@ def test_two_gloo_ranks_match_whole_batch(tmp_path):
         tok[start:stop] = t
         st[start:stop] = s
     assert np.array_equal(tok, whole["token"]) and np.array_equal(st, whole["status"])
+    trees = np.load(tmp_path / "trees.npy", allow_pickle=True)
+    whole_t = O.tree_verify(_trees())
+    R = int(whole_t["num_accepted"].size)
+    got_tok = np.full(whole_t["out_tokens"].shape, -2, np.int64)
+    got_path = np.full(whole_t["out_path"].shape, -2, np.int64)
+    for t0, t1, tt, pp in trees:
+        got_tok[t0:t1] = tt
+        got_path[t0:t1] = pp
+    assert np.array_equal(got_tok, whole_t["out_tokens"]) and np.array_equal(got_path, whole_t["out_path"])
+    assert R == 7 and (whole_t["num_accepted"] > 0).any()
     assert float(np.load(tmp_path / "tmax.npy")[0]) == 20.0
     seeds = np.load(tmp_path / "seeds.npy")
     assert len(np.unique(seeds)) == seeds.size  # every rank samples its own batches
