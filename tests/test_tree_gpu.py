@@ -124,3 +124,15 @@ def test_tree_graph_capture_and_repeat(ss):
     torch.cuda.synchronize()
     for key in ("out_tokens", "out_path", "num_accepted", "status", "kept"):
         assert torch.equal(o1[key], o2[key]), key
+
+
+def test_tree_requests_split_with_row_ids(ss):
+    # requests split over two calls (as over two GPUs), keyed by their ids,
+    # give what the whole batch gives
+    w = W.tree(seed=15, requests=18, vocab=20000, max_nodes=8)
+    w["row_id"] = np.arange(18, dtype=np.uint32)
+    whole = run_gpu(ss, w)
+    a = run_gpu(ss, parity.subset_tree(w, list(range(0, 9))))
+    b = run_gpu(ss, parity.subset_tree(w, list(range(9, 18))))
+    for key in ("out_tokens", "out_path", "num_accepted", "status"):
+        assert np.array_equal(np.concatenate([a[key], b[key]]), whole[key]), key
