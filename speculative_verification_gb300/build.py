@@ -1,6 +1,6 @@
 """Compile libss.so (the sm_103a CUDA kernels + C ABI) in-tree with nvcc.
 
-Two translation units, one -gencode (sm_103a), no cmake; the output goes to
+Three translation units compiled in parallel, one -gencode (sm_103a), no cmake; the output goes to
 speculative_verification_gb300/_build/libss.so.
 """
 import os
@@ -12,14 +12,15 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libss.so")
-SOURCES = ["ss_kernel.cu", "ss_fused.cu"]
-DEPS = ["ss_kernel.cu", "ss_fused.cu", "ss_philox.cuh", "ss_ptx.cuh"]
+SOURCES = ["ss_kernel.cu", "ss_hist.cu", "ss_fused.cu"]
+DEPS = ["ss_kernel.cu", "ss_hist.cu", "ss_hist.h", "ss_fused.cu", "ss_philox.cuh", "ss_ptx.cuh"]
 
 NVCC_FLAGS = [
     "-std=c++17", "-O3", "-lineinfo",
     "-gencode", "arch=compute_103a,code=sm_103a",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
 ]
+LINK_FLAGS = ["-shared", "-gencode", "arch=compute_103a,code=sm_103a"]
 
 
 def nvcc():
@@ -32,11 +33,20 @@ def build(force: bool = False, verbose: bool = False) -> str:
     inputs = [os.path.join(CSRC, d) for d in DEPS] + [os.path.join(INCLUDE, "ss.h")]
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= max(map(os.path.getmtime, inputs)):
         return LIB
+    # one object per translation unit, compiled in parallel, then one link
+    procs, objs = [], []
+    for src in SOURCES:
+        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        cmd = [nvcc()] + NVCC_FLAGS + ["-I" + INCLUDE, "-c", "-o", obj, os.path.join(CSRC, src)]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        procs.append((src, subprocess.Popen(cmd)))
+        objs.append(obj)
+    failed = [src for src, p in procs if p.wait() != 0]
+    if failed:
+        raise subprocess.CalledProcessError(1, "nvcc " + " ".join(failed))
     tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [nvcc()] + NVCC_FLAGS + ["-I" + INCLUDE, "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.check_call(cmd)
+    subprocess.check_call([nvcc()] + LINK_FLAGS + ["-o", tmp] + objs)
     os.replace(tmp, LIB)
     return LIB
 

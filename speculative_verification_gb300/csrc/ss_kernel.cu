@@ -50,6 +50,7 @@
 #include <mutex>
 
 #include "ss.h"
+#include "ss_hist.h"
 #include "ss_philox.cuh"
 #include "ss_ptx.cuh"
 
@@ -69,6 +70,8 @@ constexpr int kMaxChunks = 20;
 constexpr uint32_t kTargetSliceBytes = 66000u;
 constexpr uint32_t kMaxSliceBytes = kMaxChunks * kChunkBytes;
 constexpr int kMaxCluster = 8;
+// Largest max_draft a verification call takes (tree calls: SS_TREE_MAX_NODES).
+constexpr int32_t kMaxDraft = 1 << 20;
 constexpr uint32_t kWaitPolls = 1u << 22;
 constexpr float kFixedScale = 1099511627776.0f;  // 2^40
 // A token's fixed-point mass (<= 2^40) is histogrammed as two 32-bit halves,
@@ -2975,13 +2978,81 @@ static ss_status run_sample(const KArgs& ka, int32_t dtype, cudaStream_t stream)
   return sh != SS_OK ? sh : sl;
 }
 
+// Host-side checks of a verification call (everything but the workspace).
+static ss_status check_verify(const ss_verify_args* args) {
+  if (!args) return SS_ERR_INVALID_ARG;
+  const ss_verify_args& A = *args;
+  if (A.num_requests < 0 || A.vocab < 1 || A.max_draft < 0 || A.max_draft > kMaxDraft) return SS_ERR_INVALID_ARG;
+  if (A.dtype != SS_DTYPE_F32 && A.dtype != SS_DTYPE_BF16) return SS_ERR_INVALID_ARG;
+  if (A.num_requests == 0) return SS_OK;
+  const int es = (A.dtype == SS_DTYPE_BF16) ? 2 : 4;
+  if (!A.target_logits || (reinterpret_cast<uintptr_t>(A.target_logits) % es) != 0 || !A.draft_offsets)
+    return SS_ERR_INVALID_ARG;
+  if (A.max_draft > 0 && (!A.draft_tokens || !A.draft_probs)) return SS_ERR_INVALID_ARG;
+  if (A.row_stride < A.vocab) return SS_ERR_INVALID_ARG;
+  if (A.max_draft > 0 && A.draft_stride < A.vocab) return SS_ERR_INVALID_ARG;
+  if (!A.out_tokens || !A.out_num_accepted || !A.out_status) return SS_ERR_INVALID_ARG;
+  if (check_params(A.params) != SS_OK) return SS_ERR_INVALID_ARG;
+  if (A.params.bitmask && A.params.bitmask_stride < (static_cast<int64_t>(A.vocab) + 31) / 32) return SS_ERR_INVALID_ARG;
+  const int64_t tasks = static_cast<int64_t>(A.num_requests) * (static_cast<int64_t>(A.max_draft) + 1);
+  if (tasks > 0x7fffffff / kMaxCluster) return SS_ERR_UNSUPPORTED;
+  return SS_OK;
+}
+
+// The per-request arrival counters sit at the end of the workspace and the
+// per-position results at its start.  A workspace sized for (R, max_draft)
+// then never holds a counter of one call where another call of a different
+// shape put its results, so the counters stay at zero between calls (each
+// call leaves its counters at zero) whatever the calls' shapes.
+static int32_t* counters_at_end(void* workspace, size_t bytes, int32_t num_requests) {
+  const uintptr_t end = reinterpret_cast<uintptr_t>(workspace) + bytes;
+  return reinterpret_cast<int32_t*>((end - 4u * static_cast<uintptr_t>(num_requests)) & ~static_cast<uintptr_t>(15));
+}
+
+// One verification launch on a checked call and a large enough workspace.
+static ss_status verify_launch(const ss_verify_args& A, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+  const int64_t tasks = static_cast<int64_t>(A.num_requests) * (static_cast<int64_t>(A.max_draft) + 1);
+  int4* results = reinterpret_cast<int4*>(workspace);
+  int32_t* counters = counters_at_end(workspace, workspace_bytes, A.num_requests);
+  if (hist_cluster_size(A.vocab, A.dtype) > 0) {
+    // bf16 logits: the histogram kernel
+    const ss_status s = hist_verify(A, results, counters, stream);
+    if (s == SS_ERR_CUDA) g_last_cuda_error = hist_last_error();
+    return s;
+  }
+  KArgs k{};
+  k.mode = kModeVerify;
+  k.num_tasks = static_cast<int32_t>(tasks);
+  k.vocab = A.vocab;
+  k.max_draft = A.max_draft;
+  k.dtype = A.dtype;
+  k.row_stride = A.row_stride;
+  k.logits = A.target_logits;
+  k.draft_offsets = A.draft_offsets;
+  k.draft_tokens = A.draft_tokens;
+  k.draft_probs = A.draft_probs;
+  k.draft_stride = A.draft_stride;
+  k.p = A.params;
+  k.out_token = A.out_tokens;
+  k.out_num_accepted = A.out_num_accepted;
+  k.out_status = A.out_status;
+  k.out_kept = A.out_kept;
+  k.debug_processed = A.debug_processed;
+  k.ws_results = results;
+  k.ws_counters = counters;
+  // many positions run in several waves: start the costliest first
+  if (tasks >= 16 && tasks <= kMaxOrderedTasks) k.row_class = 3;
+  return run(k, A.dtype, stream);
+}
+
 }  // namespace ss
 
 extern "C" {
 
 size_t ss_workspace_size(int32_t max_requests, int32_t max_draft) {
-  if (max_requests < 0 || max_draft < 0) return 0;
-  const size_t results = static_cast<size_t>(max_requests) * static_cast<size_t>(max_draft + 1) * sizeof(int4);
+  if (max_requests < 0 || max_draft < 0 || max_draft > ss::kMaxDraft) return 0;
+  const size_t results = static_cast<size_t>(max_requests) * (static_cast<size_t>(max_draft) + 1) * sizeof(int4);
   return results + static_cast<size_t>(max_requests) * sizeof(int32_t) + 256;
 }
 
@@ -3021,6 +3092,12 @@ ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream) {
   k.out_status = A.out_status;
   k.out_kept = A.out_kept;
   k.debug_processed = A.debug_processed;
+  if (hist_cluster_size(A.vocab, A.dtype) > 0) {
+    // bf16 logits: the histogram kernel
+    const ss_status s = hist_sample(A, reinterpret_cast<cudaStream_t>(stream));
+    if (s == SS_ERR_CUDA) g_last_cuda_error = hist_last_error();
+    return s;
+  }
   return run_sample(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -3123,48 +3200,11 @@ ss_status ss_merge_shards(const ss_sample_args* args, int32_t num_shards, void* 
 
 ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t workspace_bytes, ss_stream_t stream) {
   using namespace ss;
-  if (!args) return SS_ERR_INVALID_ARG;
-  const ss_verify_args& A = *args;
-  if (A.num_requests < 0 || A.vocab < 1 || A.max_draft < 0) return SS_ERR_INVALID_ARG;
-  if (A.dtype != SS_DTYPE_F32 && A.dtype != SS_DTYPE_BF16) return SS_ERR_INVALID_ARG;
-  if (A.num_requests == 0) return SS_OK;
-  const int es = (A.dtype == SS_DTYPE_BF16) ? 2 : 4;
-  if (!A.target_logits || (reinterpret_cast<uintptr_t>(A.target_logits) % es) != 0 || !A.draft_offsets)
-    return SS_ERR_INVALID_ARG;
-  if (A.max_draft > 0 && (!A.draft_tokens || !A.draft_probs)) return SS_ERR_INVALID_ARG;
-  if (A.row_stride < A.vocab) return SS_ERR_INVALID_ARG;
-  if (A.max_draft > 0 && A.draft_stride < A.vocab) return SS_ERR_INVALID_ARG;
-  if (!A.out_tokens || !A.out_num_accepted || !A.out_status) return SS_ERR_INVALID_ARG;
-  if (check_params(A.params) != SS_OK) return SS_ERR_INVALID_ARG;
-  if (A.params.bitmask && A.params.bitmask_stride < (static_cast<int64_t>(A.vocab) + 31) / 32) return SS_ERR_INVALID_ARG;
-  const int64_t tasks = static_cast<int64_t>(A.num_requests) * (A.max_draft + 1);
-  if (tasks > 0x7fffffff / kMaxCluster) return SS_ERR_UNSUPPORTED;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < ss_workspace_size(A.num_requests, A.max_draft))
+  const ss_status chk = check_verify(args);
+  if (chk != SS_OK || args->num_requests == 0) return chk;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < ss_workspace_size(args->num_requests, args->max_draft))
     return SS_ERR_WORKSPACE;
-  KArgs k{};
-  k.mode = kModeVerify;
-  k.num_tasks = static_cast<int32_t>(tasks);
-  k.vocab = A.vocab;
-  k.max_draft = A.max_draft;
-  k.dtype = A.dtype;
-  k.row_stride = A.row_stride;
-  k.logits = A.target_logits;
-  k.draft_offsets = A.draft_offsets;
-  k.draft_tokens = A.draft_tokens;
-  k.draft_probs = A.draft_probs;
-  k.draft_stride = A.draft_stride;
-  k.p = A.params;
-  k.out_token = A.out_tokens;
-  k.out_num_accepted = A.out_num_accepted;
-  k.out_status = A.out_status;
-  k.out_kept = A.out_kept;
-  k.debug_processed = A.debug_processed;
-  k.ws_results = reinterpret_cast<int4*>(workspace);
-  k.ws_counters = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
-                                             static_cast<size_t>(tasks) * sizeof(int4));
-  // many positions run in several waves: start the costliest first
-  if (tasks >= 16 && tasks <= kMaxOrderedTasks) k.row_class = 3;
-  return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
+  return verify_launch(*args, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t workspace_bytes, ss_stream_t stream) {
@@ -3210,8 +3250,7 @@ ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t works
   k.out_kept = A.out_kept;
   k.debug_processed = A.debug_processed;
   k.ws_results = reinterpret_cast<int4*>(workspace);
-  k.ws_counters = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) +
-                                             static_cast<size_t>(tasks) * sizeof(int4));
+  k.ws_counters = counters_at_end(workspace, workspace_bytes, A.num_requests);
   if (tasks >= 16 && tasks <= kMaxOrderedTasks) k.row_class = 3;
   return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -3227,15 +3266,20 @@ void* g_noalloc_ptr[64] = {};  // device address of g_noalloc_scratch, per devic
 }  // namespace
 
 ss_status ss_spec_verify_noalloc(const ss_verify_args* args, ss_stream_t stream) {
+  using namespace ss;
+  // every argument is checked before the shared scratch is touched: first
+  // the batch against the scratch's size, then the rest
   if (!args) return SS_ERR_INVALID_ARG;
+  if (args->num_requests < 0 || args->max_draft < 0 || args->max_draft > kMaxDraft) return SS_ERR_INVALID_ARG;
   const size_t need = ss_workspace_size(args->num_requests, args->max_draft);
-  if (args->num_requests < 0 || args->max_draft < 0) return SS_ERR_INVALID_ARG;
   if (need > SS_NOALLOC_SCRATCH_BYTES) return SS_ERR_SCRATCH_LIMIT;
+  const ss_status chk = check_verify(args);
+  if (chk != SS_OK) return chk;
   if (args->num_requests == 0) return SS_OK;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= 64) {
-    ss::g_last_cuda_error = static_cast<int32_t>(e);
+    g_last_cuda_error = static_cast<int32_t>(e);
     return SS_ERR_CUDA;
   }
   void* scratch = nullptr;
@@ -3247,26 +3291,30 @@ ss_status ss_spec_verify_noalloc(const ss_verify_args* args, ss_stream_t stream)
       e = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch);
       if (e != cudaSuccess) {
         g_noalloc_ptr[dev] = nullptr;
-        ss::g_last_cuda_error = static_cast<int32_t>(e);
+        g_last_cuda_error = static_cast<int32_t>(e);
         return SS_ERR_CUDA;
       }
     }
     scratch = g_noalloc_ptr[dev];
   }
-  // The per-request arrival counters must start at zero; the array keeps
-  // whatever the previous call left, so clear them on every call.
-  const size_t results = static_cast<size_t>(args->num_requests) * static_cast<size_t>(args->max_draft + 1) * 16u;
-  e = cudaMemsetAsync(static_cast<char*>(scratch) + results, 0, static_cast<size_t>(args->num_requests) * 4u,
-                      reinterpret_cast<cudaStream_t>(stream));
+  // The per-request arrival counters (at the end of the scratch) must start
+  // at zero; the array keeps whatever the previous call left, so clear them
+  // on every call.
+  int32_t* counters = counters_at_end(scratch, SS_NOALLOC_SCRATCH_BYTES, args->num_requests);
+  const size_t clear = static_cast<size_t>(static_cast<char*>(scratch) + SS_NOALLOC_SCRATCH_BYTES -
+                                           reinterpret_cast<char*>(counters));
+  e = cudaMemsetAsync(counters, 0, clear, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
-    ss::g_last_cuda_error = static_cast<int32_t>(e);
+    g_last_cuda_error = static_cast<int32_t>(e);
     return SS_ERR_CUDA;
   }
-  return ss_spec_verify(args, scratch, SS_NOALLOC_SCRATCH_BYTES, stream);
+  return verify_launch(*args, scratch, SS_NOALLOC_SCRATCH_BYTES, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int32_t ss_cluster_size(int32_t vocab, int32_t dtype) {
   if (vocab < 1 || (dtype != SS_DTYPE_F32 && dtype != SS_DTYPE_BF16)) return 0;
+  const int h = ss::hist_cluster_size(vocab, dtype);
+  if (h > 0) return h;
   return ss::choose_cluster(vocab, dtype == SS_DTYPE_BF16 ? 2 : 4);
 }
 
