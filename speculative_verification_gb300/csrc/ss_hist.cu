@@ -19,22 +19,26 @@
 // tokens [r * slice, (r + 1) * slice) of the row.
 //   1. set-up: bulk (TMA) copies of the slice into shared memory in 16 KB
 //      chunks; meanwhile the row's parameters, its penalised / biased tokens
-//      ("patched": processed in fp32 from the global row, kept as exact
-//      entries) and the grammar mask's allow bits.
-//   2. staging pass, chunk by chunk as the copies land: excluded tokens
-//      (mask, patched) are overwritten with -inf in place, tiny non-zero
-//      values are moved to the exact entries, each 8-token vector's maximum is
-//      stored, and the slice maximum is kept (packed bf16x2 maxima).
+//      ("patched") in a table and the grammar mask's allow bits.
+//   2. staging pass, chunk by chunk as the copies land: the patched tokens'
+//      raw logits go to the table, excluded tokens (mask, patched) are
+//      overwritten with -inf in place, tiny non-zero values are moved to the
+//      exact entries, each 16-token pair of vectors' maximum is stored.  Then
+//      the patched tokens are processed in fp32 into exact entries.
 //   3. cluster exchange 1 (distributed shared memory, one cluster barrier):
-//      row maximum, status, entry counts, the draft token's value, and for
-//      greedy rows the lowest index of the maximum.
-//   4. rows with a top-k or top-p cut: one pass counts the tokens per slot
-//      (slot = distinct value, counted from the row maximum down); every CTA
-//      sums its counts and masses into 64 coarse groups and pushes them, and
-//      its entries, to every CTA (exchange 2).  Every CTA then locates the
-//      cuts identically: coarse groups first, then the slots of one group read
-//      from all CTAs, merged with the sorted entries.  Ties at the cut value
-//      are resolved by index in the CTA where the cut falls (exchange 3).
+//      slice maxima, statuses, the draft token's value, greedy arguments, and
+//      for top-k rows each CTA's count of 16-token pairs per binade below its
+//      maximum.  Summed over the cluster, those counts certify a value tau
+//      with at least k tokens at or above it: only tokens >= tau can be in
+//      the top-k.
+//   4. rows with a top-k or top-p cut: one pass counts the candidate tokens
+//      per slot (slot = distinct value, counted from the row maximum down);
+//      every CTA sums its counts and masses into 64 coarse groups and pushes
+//      them to every CTA (exchange 2).  Every CTA then locates the cuts
+//      identically: coarse groups first, then the slots of one group read
+//      from all CTAs, merged with the group's entries gathered from all CTAs.
+//      Ties at the cut value are resolved by index in the CTA where the cut
+//      falls.
 //   5. the draw over the kept set with Philox noise keyed by token, pruned by
 //      the largest possible noise and by a cheap bound before any logarithm;
 //      the best (score, token) of each CTA is reduced over the cluster.
@@ -67,6 +71,8 @@ constexpr int kGatherCap = 512;   // entries of one coarse group, over the clust
 constexpr int kFineMax = 256;     // slots one coarse group may span (runs of equal y extend a group)
 constexpr int kEntCap = 1024;     // exact entries per CTA (patched tokens and tiny values)
 constexpr int kHashCap = 1024;    // patch table slots
+constexpr int kCertBins = 32;     // binades below the maximum counted for the top-k certificate
+constexpr int kTieEnt = 64;       // entries tied at a cut value, per CTA
 constexpr int kChunkTokens = 8192;
 constexpr int kMaxChunks = 8;
 constexpr int kMaxCluster = 8;
@@ -80,7 +86,33 @@ constexpr uint32_t kTinyA = 0x3780u;  // |z| below 2^-16: tiny (exact entries un
 constexpr float kMassRange = 28.2f;
 
 static_assert(kSlots % kGroups == 0, "groups tile the slots");
-static_assert(kSliceMax / 8 <= 8 * kThreads * 2 + 8192, "vectors per thread");
+
+// Phase timestamps for tracing (built only with -DSS_HIST_STAMPS): the
+// global timer at the end of each phase, per CTA, read back with
+// ss_hist_stamps_copy.
+#ifdef SS_HIST_STAMPS
+constexpr int kStampCtas = 16384, kStampPhases = 24;
+__device__ unsigned long long g_stamps[kStampCtas][kStampPhases];
+#define SS_STAMP(k)                                                                \
+  do {                                                                             \
+    if (threadIdx.x == 0 && blockIdx.x < kStampCtas) {                             \
+      unsigned long long t_;                                                       \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                       \
+      g_stamps[blockIdx.x][k] = t_;                                                \
+    }                                                                              \
+  } while (0)
+#define SS_TRACE(k, v)                                                             \
+  do {                                                                             \
+    if (threadIdx.x == 0 && blockIdx.x < kStampCtas) g_stamps[blockIdx.x][k] = (v); \
+  } while (0)
+#else
+#define SS_STAMP(k) \
+  do {            \
+  } while (0)
+#define SS_TRACE(k, v) \
+  do {               \
+  } while (0)
+#endif
 
 // ---------------------------------------------------------------- helpers --
 
@@ -232,13 +264,14 @@ struct HArgs {
 // Per-CTA partial of exchange 1.
 struct alignas(16) Part1 {
   float zmax;     // largest staged logit (bf16 value, NaN if any)
-  float emax;     // largest entry y
+  float emax;     // largest entry y (z for greedy rows)
   int32_t arg;    // greedy: lowest index of the CTA's largest item
   int32_t status;
   int32_t nent;
   float xy;       // processed value of the draft token (its CTA)
   int32_t xhere;
-  int32_t pad;
+  int32_t zbin;   // binade of zmax (16-bit order key >> 7)
+  uint32_t cert[kCertBins];  // 16-token pairs whose maximum lies d binades below zbin
 };
 
 // Per-CTA partial of a draw / mass exchange.
@@ -263,7 +296,7 @@ struct Ctx {
   int32_t h0, h1, b0, b1;
   int32_t status;   // local, then cluster-wide
   int32_t nent;     // local entries appended
-  int32_t ne;       // local entries kept (sorted for histogram rows)
+  int32_t ne;       // local entries kept
   int32_t n_g;      // entries gathered for one coarse group
   int32_t npatch;
   // after exchange 1
@@ -271,6 +304,7 @@ struct Ctx {
   int32_t arg;
   float xy;
   int32_t xhere;
+  uint32_t tau_key;  // top-k candidates: tokens whose 16-bit order key is >= this
   SlotMap M;
   // cut: K = {y > cut_v} U {y == cut_v, token <= cut_t}
   float cut_v;
@@ -286,26 +320,31 @@ struct Ctx {
   int32_t pick;
   int32_t tcut_in;  // tie cutoff, written by the CTA that resolves it
   int32_t xpar;     // buffer of the next draw / mass exchange
-  float fbest;
-  int32_t farg;
+  uint32_t fail_key;
 };
 
 __shared__ Ctx g;
 __shared__ Part1 g_p1[kMaxCluster];
+__shared__ Part1 g_mine;
 __shared__ PartD g_pd[2][kMaxCluster];
 __shared__ unsigned char g_red[kWarps * 16];
+__shared__ unsigned long long g_scan[2 * kWarps];
 __shared__ int32_t g_gb[kGroups + 2];                // coarse group bounds (slots)
-__shared__ int32_t g_ge[kGroups + 2];                // first local entry of each group
-__shared__ int32_t g_goff[kMaxCluster + 1], g_gbeg[kMaxCluster];
 __shared__ uint32_t g_gcnt[kGroups + 1];
 __shared__ unsigned long long g_gmass[kGroups + 1];
+__shared__ uint32_t g_ecnt[kGroups + 1];             // this CTA's entries per group
+__shared__ unsigned long long g_emass[kGroups + 1];
 __shared__ uint32_t g_fc[kFineMax];                  // one group's slot counts (all CTAs)
-__shared__ int16_t g_epos[kEntCap];                  // slot position of each sorted local entry
-__shared__ int32_t g_rtie[kMaxCluster];
-__shared__ float g_rfail[kMaxCluster];
-__shared__ unsigned long long g_scan[2 * kWarps];
+__shared__ int16_t g_epos[kEntCap];                  // slot position of each local entry
+__shared__ int32_t g_goff[kMaxCluster + 1];
+__shared__ uint32_t g_rtie[kMaxCluster];
+__shared__ uint32_t g_cert[kCertBins];
+__shared__ int32_t g_tietok[kTieEnt];
 
 extern __shared__ __align__(128) uint8_t g_dyn[];
+
+__device__ __forceinline__ uint32_t key16(uint32_t h) { return (h & 0x8000u) ? (~h & 0xffffu) : (h | 0x8000u); }
+__device__ __forceinline__ uint32_t key16_bits(uint32_t k) { return (k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu); }
 
 // ------------------------------------------------------ block reductions --
 
@@ -385,6 +424,95 @@ __device__ __forceinline__ int32_t block_excl_scan(int32_t v, int32_t* total) {
   }
   *total = tot;
   return before + x - v;
+}
+
+// Inclusive prefix over the block of a (count, mass) pair (thread order);
+// the totals land in *tc / *tm.  Called by all threads.
+__device__ __forceinline__ void block_scan2(unsigned long long& c, unsigned long long& m, unsigned long long* tc,
+                                            unsigned long long* tm) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long yc = __shfl_up_sync(0xffffffffu, c, o);
+    const unsigned long long ym = __shfl_up_sync(0xffffffffu, m, o);
+    if (lane >= o) {
+      c += yc;
+      m += ym;
+    }
+  }
+  unsigned long long* r = reinterpret_cast<unsigned long long*>(g_scan);
+  __syncthreads();
+  if (lane == 31) {
+    r[wid] = c;
+    r[kWarps + wid] = m;
+  }
+  __syncthreads();
+  unsigned long long bc = 0, bm = 0, sc = 0, sm = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < wid) {
+      bc += r[w];
+      bm += r[kWarps + w];
+    }
+    sc += r[w];
+    sm += r[kWarps + w];
+  }
+  c += bc;
+  m += bm;
+  *tc = sc;
+  *tm = sm;
+}
+
+// The coarse group where the running count (by_mass = 0) or mass (1) first
+// reaches `target`, and the count / mass before it; one warp.  Returns the
+// group (-1 if none) in g.pick and the sums in g.w_cc / g.w_cm.
+__device__ void coarse_locate(int by_mass, unsigned long long target) {
+  Ctx& c = g;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    constexpr int kPer = (kGroups + 1 + 31) / 32;  // groups per lane, in order
+    unsigned long long cc = 0, cm = 0;
+    for (int i = 0; i < kPer; ++i) {
+      const int q = lane * kPer + i;
+      if (q <= kGroups) {
+        cc += g_gcnt[q];
+        cm += g_gmass[q];
+      }
+    }
+    unsigned long long ic = cc, im = cm;  // inclusive over lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long yc = __shfl_up_sync(0xffffffffu, ic, o);
+      const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, o);
+      if (lane >= o) {
+        ic += yc;
+        im += ym;
+      }
+    }
+    unsigned long long bc = ic - cc, bm = im - cm;  // before this lane's groups
+    int found = -1;
+    unsigned long long fc = 0, fm = 0;
+    for (int i = 0; i < kPer; ++i) {
+      const int q = lane * kPer + i;
+      if (q > kGroups) break;
+      const unsigned long long add = by_mass ? g_gmass[q] : g_gcnt[q];
+      if (found < 0 && add > 0 && (by_mass ? bm : bc) + add >= target) {
+        found = q;
+        fc = bc;
+        fm = bm;
+      }
+      bc += g_gcnt[q];
+      bm += g_gmass[q];
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
+    if (ball == 0) {
+      if (lane == 0) c.pick = -1;
+    } else if (lane == __ffs(ball) - 1) {
+      c.pick = found;
+      c.w_cc = fc;
+      c.w_cm = fm;
+    }
+  }
+  __syncthreads();
 }
 
 // ------------------------------------------------------------- the task --
@@ -505,13 +633,14 @@ __device__ void read_params(const HArgs& a) {
   c.use_mask = p.bitmask && (!p.use_bitmask || p.use_bitmask[i]);
 }
 
-// ------------------------------------------------------------------ kernel --
+// ----------------------------------------------------------- patch table --
 
 __device__ __forceinline__ int hash_slot(int32_t t) { return static_cast<int>((static_cast<uint32_t>(t) * 2654435761u) >> 22); }
 
 // The patch table (in the histogram region during set-up): token ids with
-// their occurrence count | kBiasFlag and bias value.  Returns the slot, or -1
-// when the table is full.
+// their occurrence count | kBiasFlag, bias value (later the processed value)
+// and raw logit | allowed flag.  Returns the slot, or -1 when the table is
+// full.
 __device__ __forceinline__ int patch_insert(int32_t* keys, int32_t t) {
   int h = hash_slot(t);
   for (int probe = 0; probe < kHashCap; ++probe) {
@@ -695,11 +824,11 @@ __device__ void count_pass(const HArgs& a, bool want_mass, const unsigned long l
 
 // ----------------------------------------------------------- the locator --
 // Items are the staged tokens (counted per slot, in every CTA) and the exact
-// entries (sorted in each CTA's list).  Entry e sits at slot position
-// epos[e] = the first slot whose value is <= its y: before that slot's tokens
-// when its y is larger, tied with them when equal.  Coarse group q holds the
-// slots [gb[q], gb[q + 1]) and the entries positioned there; the tail group
-// kGroups holds the entries past the last slot.
+// entries (each CTA's list).  Entry e sits at slot position epos[e] = the
+// first slot whose value is <= its y: before that slot's tokens when its y is
+// larger, tied with them when equal.  Coarse group q holds the slots
+// [gb[q], gb[q + 1]) and the entries positioned there; the tail group kGroups
+// holds the entries past the last slot.
 
 __device__ __forceinline__ float slot_y(int32_t s) {
   const float z = slot_z(g.M, s);
@@ -731,19 +860,6 @@ __device__ __forceinline__ int group_of(int32_t p) {
   return lo;
 }
 
-// First entry of a sorted list whose y is <= v.
-__device__ __forceinline__ int first_entry_le(const unsigned long long* el, int n, float v) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (ekey_y(el[mid]) <= v)
-      hi = mid;
-    else
-      lo = mid + 1;
-  }
-  return lo;
-}
-
 // First entry of a sorted list whose y is < v (the number of entries >= v).
 __device__ __forceinline__ int first_entry_lt(const unsigned long long* el, int n, float v) {
   int lo = 0, hi = n;
@@ -758,10 +874,10 @@ __device__ __forceinline__ int first_entry_lt(const unsigned long long* el, int 
 }
 
 // Reads the slot counts of coarse group `grp` from every CTA into g_fc, and
-// gathers the group's entries from every CTA into (gk, gp), merged in
-// (y desc, token asc) order; g.n_g is their number (-1 if more than
-// kGatherCap).  The gather buffer is the exchange-2 region, free once the
-// coarse sums are read.  Called by all threads; ends with a block barrier.
+// gathers the group's entries from every CTA's list into (gk, gp), sorted
+// (y desc, token asc); g.n_g is their number (-1 if more than kGatherCap).
+// The gather buffer is the exchange-2 region, free once the coarse sums are
+// read.  Called by all threads; ends with a block barrier.
 __device__ void load_group(const HArgs& a, int grp) {
   cg::cluster_group cl = cg::this_cluster();
   const int C = static_cast<int>(cl.num_blocks());
@@ -771,40 +887,42 @@ __device__ void load_group(const HArgs& a, int grp) {
   unsigned long long* gk = reinterpret_cast<unsigned long long*>(g_dyn + a.o_xm);
   int16_t* gp = reinterpret_cast<int16_t*>(gk + kGatherCap);
   __syncthreads();  // the previous readers of g_fc and of the buffer are done
+  if (threadIdx.x == 0) g.n_g = 0;
   for (int i = threadIdx.x; i < s1 - s0; i += kThreads) {
     uint32_t cnt = 0;
     const int q = s0 + i;
     for (int r = 0; r < C; ++r) cnt += (*cl.map_shared_rank(hist + (q >> 1), r) >> ((q & 1) << 4)) & 0xffffu;
     g_fc[i] = cnt;
   }
-  if (threadIdx.x == 0) {
-    int tot = 0;
-    for (int r = 0; r < C; ++r) {
-      const int32_t* ge = cl.map_shared_rank(g_ge, r);
-      const int b = ge[grp], e = ge[grp + 1];
-      g_goff[r] = tot;
-      g_gbeg[r] = b;
-      tot += e - b;
+  __syncthreads();
+  // every (CTA, entry) pair: the entries of this group, appended
+  const int total = g_goff[C];
+  for (int i = threadIdx.x; i < total; i += kThreads) {
+    int r = 0;
+    while (i >= g_goff[r + 1]) ++r;
+    const int e = i - g_goff[r];
+    const int16_t p = *cl.map_shared_rank(g_epos + e, r);
+    if (group_of(p) != grp) continue;
+    const int at = atomicAdd(&g.n_g, 1);
+    if (at < kGatherCap) {
+      gk[at] = *cl.map_shared_rank(el + e, r);
+      gp[at] = p;
     }
-    g_goff[C] = tot;
-    g.n_g = tot > kGatherCap ? -1 : tot;
   }
   __syncthreads();
   const int n = g.n_g;
-  if (n > 0) {
+  __syncthreads();
+  if (n > kGatherCap) {
+    if (threadIdx.x == 0) g.n_g = -1;
+    __syncthreads();
+    return;
+  }
+  if (n > 1) {
     int np2 = 1;
     while (np2 < n) np2 <<= 1;
-    for (int i = threadIdx.x; i < np2; i += kThreads) {
-      if (i < n) {
-        int r = 0;
-        while (i >= g_goff[r + 1]) ++r;
-        const int src = g_gbeg[r] + (i - g_goff[r]);
-        gk[i] = *cl.map_shared_rank(el + src, r);
-        gp[i] = *cl.map_shared_rank(g_epos + src, r);
-      } else {
-        gk[i] = ~0ull;
-        gp[i] = 0x7fff;
-      }
+    for (int i = n + threadIdx.x; i < np2; i += kThreads) {
+      gk[i] = ~0ull;
+      gp[i] = 0x7fff;
     }
     __syncthreads();
     for (int k = 2; k <= np2; k <<= 1)
@@ -823,95 +941,6 @@ __device__ void load_group(const HArgs& a, int grp) {
         __syncthreads();
       }
   }
-}
-
-// Inclusive prefix over the block of a (count, mass) pair (thread order);
-// the totals land in *tc / *tm.  Called by all threads.
-__device__ __forceinline__ void block_scan2(unsigned long long& c, unsigned long long& m, unsigned long long* tc,
-                                            unsigned long long* tm) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long yc = __shfl_up_sync(0xffffffffu, c, o);
-    const unsigned long long ym = __shfl_up_sync(0xffffffffu, m, o);
-    if (lane >= o) {
-      c += yc;
-      m += ym;
-    }
-  }
-  unsigned long long* r = reinterpret_cast<unsigned long long*>(g_scan);
-  __syncthreads();
-  if (lane == 31) {
-    r[wid] = c;
-    r[kWarps + wid] = m;
-  }
-  __syncthreads();
-  unsigned long long bc = 0, bm = 0, sc = 0, sm = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < wid) {
-      bc += r[w];
-      bm += r[kWarps + w];
-    }
-    sc += r[w];
-    sm += r[kWarps + w];
-  }
-  c += bc;
-  m += bm;
-  *tc = sc;
-  *tm = sm;
-}
-
-// The coarse group where the running count (by_mass = 0) or mass (1) first
-// reaches `target`, and the count / mass before it; one warp.  Returns the
-// group (-1 if none) in g.pick and the sums in g.w_cc / g.w_cm.
-__device__ void coarse_locate(int by_mass, unsigned long long target) {
-  Ctx& c = g;
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    constexpr int kPer = (kGroups + 1 + 31) / 32;  // groups per lane, in order
-    unsigned long long cc = 0, cm = 0;
-    for (int i = 0; i < kPer; ++i) {
-      const int q = lane * kPer + i;
-      if (q <= kGroups) {
-        cc += g_gcnt[q];
-        cm += g_gmass[q];
-      }
-    }
-    unsigned long long ic = cc, im = cm;  // inclusive over lanes
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long yc = __shfl_up_sync(0xffffffffu, ic, o);
-      const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, o);
-      if (lane >= o) {
-        ic += yc;
-        im += ym;
-      }
-    }
-    unsigned long long bc = ic - cc, bm = im - cm;  // before this lane's groups
-    int found = -1;
-    unsigned long long fc = 0, fm = 0;
-    for (int i = 0; i < kPer; ++i) {
-      const int q = lane * kPer + i;
-      if (q > kGroups) break;
-      const unsigned long long add = by_mass ? g_gmass[q] : g_gcnt[q];
-      if (found < 0 && add > 0 && (by_mass ? bm : bc) + add >= target) {
-        found = q;
-        fc = bc;
-        fm = bm;
-      }
-      bc += g_gcnt[q];
-      bm += g_gmass[q];
-    }
-    const unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
-    if (ball == 0) {
-      if (lane == 0) c.pick = -1;
-    } else if (lane == __ffs(ball) - 1) {
-      c.pick = found;
-      c.w_cc = fc;
-      c.w_cm = fm;
-    }
-  }
-  __syncthreads();
 }
 
 // Where the running count (by_mass = 0) or mass (1) of the items first
@@ -1082,11 +1111,14 @@ __device__ void above_value(const HArgs& a, float v) {
 }
 
 // Index cutoff for the items of value v when `take` of them (by index) are
-// kept: every CTA learns the index of the take-th one (exchange 3; the CTAs
-// hold increasing index ranges, so the cut falls in one of them).  Sets
-// g.cut_t (-1: none of them, 0x7fffffff: all).  Called by all threads of
-// every CTA.
-__device__ void resolve_ties(const HArgs& a, float v, unsigned long long take) {
+// kept.  The CTAs hold increasing index ranges, so the take-th item lies in
+// one CTA (tie_rank): CTAs before it keep all their items of value v, CTAs
+// after it none, and it finds its own cutoff with one ordered scan of its
+// slice.  With `broadcast` every CTA learns that cutoff (one cluster barrier;
+// verification needs it for the draft token).  Sets g.cut_t, the cutoff that
+// this CTA applies (-1: none of its items of value v, 0x7fffffff: all).
+// Called by all threads of every CTA.
+__device__ void resolve_ties(const HArgs& a, float v, unsigned long long take, bool broadcast) {
   Ctx& c = g;
   cg::cluster_group cl = cg::this_cluster();
   const int C = static_cast<int>(cl.num_blocks());
@@ -1094,95 +1126,137 @@ __device__ void resolve_ties(const HArgs& a, float v, unsigned long long take) {
   const uint32_t* hist = reinterpret_cast<const uint32_t*>(g_dyn + a.o_hist);
   const unsigned long long* el = reinterpret_cast<const unsigned long long*>(g_dyn + a.o_el);
   // per-CTA counts of the items of value v: its run of slots and its entries
+  if (threadIdx.x < C) g_rtie[threadIdx.x] = 0;
+  __syncthreads();
   if (threadIdx.x < C) {
     const int r = threadIdx.x;
     uint32_t n = 0;
     for (int q = first_slot_le(v, 0, c.M.ns); q < c.M.ns && slot_y(q) == v; ++q)
       n += (*cl.map_shared_rank(hist + (q >> 1), r) >> ((q & 1) << 4)) & 0xffffu;
-    const unsigned long long* er = cl.map_shared_rank(el, r);
-    const int ne = *cl.map_shared_rank(&g.ne, r);
-    for (int e = first_entry_le(er, ne, v); e < ne && ekey_y(er[e]) == v; ++e) ++n;
-    g_rtie[r] = static_cast<int32_t>(n);
+    atomicAdd(&g_rtie[r], n);
+  }
+  const int total_e = g_goff[C];
+  for (int i = threadIdx.x; i < total_e; i += kThreads) {
+    int r = 0;
+    while (i >= g_goff[r + 1]) ++r;
+    if (ekey_y(*cl.map_shared_rank(el + (i - g_goff[r]), r)) == v) atomicAdd(&g_rtie[r], 1u);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     unsigned long long before = 0, total = 0;
-    for (int r = 0; r < C; ++r) total += static_cast<unsigned long long>(g_rtie[r]);
+    for (int r = 0; r < C; ++r) total += g_rtie[r];
     c.tie_rank = C;  // all of them
     c.tie_local = 0;
     if (take == 0) {
       c.tie_rank = -1;
     } else if (take < total) {
       for (int r = 0; r < C; ++r) {
-        if (before + static_cast<unsigned long long>(g_rtie[r]) >= take) {
+        if (before + g_rtie[r] >= take) {
           c.tie_rank = r;
           c.tie_local = static_cast<int32_t>(take - before);
           break;
         }
-        before += static_cast<unsigned long long>(g_rtie[r]);
+        before += g_rtie[r];
       }
     }
-    c.cut_t = -1;
-    const int e0 = first_entry_le(el, c.ne, v);
-    int e1 = e0;
-    while (e1 < c.ne && ekey_y(el[e1]) == v) ++e1;
-    c.w_slot = e0;
-    c.pick = e1;
+    c.cut_t = (rank < c.tie_rank) ? 0x7fffffff : -1;
   }
   __syncthreads();
   const int tr = c.tie_rank;
   if (rank == tr) {
-    // the tie_local-th item of value v in this slice, by index: rounds of
-    // kThreads vectors in index order, a block prefix of the matches
+    // this CTA's entries of value v (few): their tokens, sorted
+    int32_t* tie_tok = g_tietok;
+    if (threadIdx.x == 0) c.n_g = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < c.ne; e += kThreads)
+      if (ekey_y(el[e]) == v) {
+        const int at = atomicAdd(&c.n_g, 1);
+        if (at < kTieEnt) tie_tok[at] = ekey_t(el[e]);
+      }
+    __syncthreads();
+    const bool many = c.n_g > kTieEnt;  // then every entry is checked (slow, rare)
+    const int nt = min(c.n_g, kTieEnt);
+    if (threadIdx.x == 0)  // a handful of tokens: insertion sort
+      for (int i = 1; i < nt; ++i) {
+        const int32_t x = tie_tok[i];
+        int j = i - 1;
+        while (j >= 0 && tie_tok[j] > x) {
+          tie_tok[j + 1] = tie_tok[j];
+          --j;
+        }
+        tie_tok[j + 1] = x;
+      }
+    __syncthreads();
+    // each thread takes a contiguous block of vectors, so that one block
+    // prefix of the per-thread match counts orders them by index
     const uint4* data = reinterpret_cast<const uint4*>(g_dyn);
+    const uint16_t* vb = reinterpret_cast<const uint16_t*>(g_dyn + a.o_vb);
+    const int per = (c.nvec + kThreads - 1) / kThreads;
+    const int v0 = threadIdx.x * per, v1 = min(v0 + per, c.nvec);
+    const int32_t t_lo = c.lo + v0 * 8, t_hi = c.lo + v1 * 8;
+    uint32_t mine = 0;
+    for (int vv = v0; vv < v1; ++vv) {
+      if (__fmul_rn(bf16_to_f(vb[vv >> 1]), c.inv_t) < v) continue;
+      const uint4 d = data[vv];
+      const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t word = w[e >> 1];
+        const float y = __fmul_rn((e & 1) ? __uint_as_float(word & 0xffff0000u) : __uint_as_float(word << 16), c.inv_t);
+        mine += (y == v) ? 1u : 0u;
+      }
+    }
+    if (!many) {
+      for (int e = 0; e < nt; ++e) mine += (tie_tok[e] >= t_lo && tie_tok[e] < t_hi) ? 1u : 0u;
+    } else {
+      for (int e = 0; e < c.ne; ++e) {
+        const int32_t t = ekey_t(el[e]);
+        if (t >= t_lo && t < t_hi && ekey_y(el[e]) == v) ++mine;
+      }
+    }
+    int32_t total = 0;
+    const int32_t before = block_excl_scan(static_cast<int32_t>(mine), &total);
     const int want = c.tie_local;
-    const int te0 = c.w_slot, te1 = c.pick;
-    int seen = 0;
-    for (int base = 0; base < c.nvec; base += kThreads) {
-      const int vv = base + static_cast<int>(threadIdx.x);
-      uint32_t hits = 0;
-      const int32_t t0 = c.lo + vv * 8;
-      if (vv < c.nvec) {
+    if (before < want && before + static_cast<int32_t>(mine) >= want) {
+      // the crossing thread walks its tokens in index order
+      int need = want - before;
+      int q = 0;
+      while (q < nt && tie_tok[q] < t_lo) ++q;
+      for (int vv = v0; vv < v1 && need > 0; ++vv) {
         const uint4 d = data[vv];
         const uint32_t w[4] = {d.x, d.y, d.z, d.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 8 && need > 0; ++e) {
+          const int32_t t = c.lo + vv * 8 + e;
           const uint32_t word = w[e >> 1];
-          const float y = __fmul_rn((e & 1) ? __uint_as_float(word & 0xffff0000u) : __uint_as_float(word << 16),
-                                    c.inv_t);
-          if (y == v) hits |= 1u << e;
-        }
-        for (int e = te0; e < te1; ++e) {  // entries of value v among this vector's tokens
-          const int32_t t = ekey_t(el[e]);
-          if (t >= t0 && t < t0 + 8) hits |= 1u << (t - t0);
+          bool hit = __fmul_rn((e & 1) ? __uint_as_float(word & 0xffff0000u) : __uint_as_float(word << 16),
+                               c.inv_t) == v;
+          if (!many) {
+            while (q < nt && tie_tok[q] < t) ++q;
+            if (q < nt && tie_tok[q] == t) hit = true;
+          } else if (!hit) {
+            for (int e2 = 0; e2 < c.ne; ++e2)
+              if (ekey_t(el[e2]) == t && ekey_y(el[e2]) == v) hit = true;
+          }
+          if (hit && --need == 0) c.cut_t = t;
         }
       }
-      const int32_t mine = __popc(hits);
-      int32_t total = 0;
-      const int32_t before = block_excl_scan(mine, &total);
-      if (seen + before < want && seen + before + mine >= want) {
-        int need = want - seen - before;
-        for (int e = 0; e < 8; ++e)
-          if (((hits >> e) & 1u) && --need == 0) c.cut_t = t0 + e;
-      }
-      seen += total;
-      __syncthreads();
-      if (seen >= want) break;
     }
+    __syncthreads();
   }
-  // every CTA learns the cutoff
-  if (rank == tr && threadIdx.x == 0)
-    for (int r = 0; r < C; ++r) *cl.map_shared_rank(&g.tcut_in, r) = c.cut_t;
-  cl.sync();
-  if (threadIdx.x == 0) {
-    if (tr < 0)
-      c.cut_t = -1;
-    else if (tr >= C)
-      c.cut_t = 0x7fffffff;
-    else
-      c.cut_t = c.tcut_in;
+  if (broadcast) {
+    if (rank == tr && threadIdx.x == 0)
+      for (int r = 0; r < C; ++r) *cl.map_shared_rank(&g.tcut_in, r) = c.cut_t;
+    cl.sync();
+    if (threadIdx.x == 0) {
+      if (tr < 0)
+        c.cut_t = -1;
+      else if (tr >= C)
+        c.cut_t = 0x7fffffff;
+      else
+        c.cut_t = c.tcut_in;
+    }
+    __syncthreads();
   }
-  __syncthreads();
 }
 
 // ------------------------------------------------------------------ kernel --
@@ -1199,11 +1273,15 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   uint32_t* hist = reinterpret_cast<uint32_t*>(g_dyn + a.o_hist);
   unsigned long long* el = reinterpret_cast<unsigned long long*>(g_dyn + a.o_el);
   uint32_t* xm = reinterpret_cast<uint32_t*>(g_dyn + a.o_xm);
+  uint32_t* pbits = reinterpret_cast<uint32_t*>(g_dyn + a.o_mg);  // patched tokens, until the locator
   uint64_t* mbar = reinterpret_cast<uint64_t*>(g_dyn + a.o_mbar);
+  // the patch table shares the histogram region during set-up
   int32_t* hkey = reinterpret_cast<int32_t*>(hist);
   int32_t* hcnt = hkey + kHashCap;
   float* hval = reinterpret_cast<float*>(hcnt + kHashCap);
+  uint32_t* hraw = reinterpret_cast<uint32_t*>(hval + kHashCap);  // raw bf16 bits | allowed << 16
 
+  SS_STAMP(0);
   if (tid == 0) decode_and_copy(a, task, rank);
   __syncthreads();
   if (!c.valid) return;  // the same for the whole cluster
@@ -1220,17 +1298,17 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     return;
   }
   if (tid == 0) read_params(a);
-  // patch table and allow bits
   for (int s = tid; s < kHashCap; s += kThreads) {
     hkey[s] = -1;
     hcnt[s] = 0;
     hval[s] = 0.0f;
+    hraw[s] = 0;
   }
   __syncthreads();
   const int32_t V = a.vocab, lo = c.lo, n = c.n;
   const uint16_t* row = a.logits + c.row_off;
+  const int words = a.slice / 32;
   {
-    const int words = a.slice / 32;
     const int32_t* mrow = c.use_mask ? a.p.bitmask + static_cast<int64_t>(c.req) * a.p.bitmask_stride + (lo >> 5) : nullptr;
     for (int w = tid; w < words; w += kThreads) {
       const int first = w * 32;
@@ -1240,6 +1318,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         if (first + 32 > n) allow &= (1u << (n - first)) - 1u;
       }
       xm[w] = allow;
+      pbits[w] = 0;
     }
   }
   // tokens past the bulk copies: plain loads; padding past the row: -inf
@@ -1248,9 +1327,20 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     const int from = (a.bulk ? c.n8 : 0);
     for (int e = from + tid; e < c.nvec * 8; e += kThreads) d16[e] = (e < n) ? row[lo + e] : 0xff80u;
   }
+  __syncthreads();
+  // patched tokens: the table, the patched bits, and (from the first insert of
+  // each) whether the mask allows it; its staged copy is excluded
   int st = c.status;
   const bool row_ok = st == SS_ROW_OK;
   auto in_slice = [&](int32_t t) { return t >= lo && t < lo + n; };
+  auto mark = [&](int32_t t, int s) {
+    const uint32_t bit = 1u << ((t - lo) & 31);
+    const int w = (t - lo) >> 5;
+    if (!(atomicOr(pbits + w, bit) & bit)) {
+      atomicAdd(&c.npatch, 1);
+      if (atomicAnd(xm + w, ~bit) & bit) atomicOr(hraw + s, 1u << 16);
+    }
+  };
   if (row_ok) {
     for (int e = c.h0 + tid; e < c.h1; e += kThreads) {
       const int32_t t = a.p.hist_ids[e];
@@ -1258,10 +1348,12 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         st = max(st, SS_ROW_BAD_INDEX);
       } else if (in_slice(t)) {
         const int s = patch_insert(hkey, t);
-        if (s < 0)
+        if (s < 0) {
           st = max(st, SS_ROW_LIMIT);
-        else
+        } else {
           atomicAdd(hcnt + s, 1);
+          mark(t, s);
+        }
       }
     }
     if (a.mode == 1) {
@@ -1274,10 +1366,12 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           st = max(st, SS_ROW_BAD_INDEX);
         } else if (e < c.j && in_slice(t)) {
           const int s = patch_insert(hkey, t);
-          if (s < 0)
+          if (s < 0) {
             st = max(st, SS_ROW_LIMIT);
-          else
+          } else {
             atomicAdd(hcnt + s, 1);
+            mark(t, s);
+          }
         }
       }
     }
@@ -1294,37 +1388,16 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         } else {
           if (atomicOr(hcnt + s, kBiasFlag) & kBiasFlag) st = max(st, SS_ROW_BAD_INDEX);  // duplicate id
           hval[s] = b;
+          mark(t, s);
         }
       }
     }
   }
   if (st != SS_ROW_OK) atomicMax(&c.status, st);
   __syncthreads();
-  // processed values of the patched tokens: exact entries; their staged
-  // copies are excluded
-  for (int s = tid; s < kHashCap; s += kThreads) {
-    const int32_t t = hkey[s];
-    if (t < 0) continue;
-    atomicAdd(&c.npatch, 1);
-    float z = bf16_to_f(row[t]);
-    const int32_t hc = hcnt[s];
-    const int32_t cnt = hc & ~kBiasFlag;
-    if (cnt > 0) {
-      z = (z > 0.0f) ? __fdiv_rn(z, c.rep) : __fmul_rn(z, c.rep);
-      z = __fsub_rn(z, __fmul_rn(c.freq, static_cast<float>(cnt)));
-      z = __fsub_rn(z, c.pres);
-    }
-    if (hc & kBiasFlag) z = __fadd_rn(z, hval[s]);
-    const uint32_t bit = 1u << ((t - lo) & 31);
-    const bool allowed = (atomicAnd(xm + ((t - lo) >> 5), ~bit) & bit) != 0;
-    const float y = !allowed ? ninf() : (c.greedy ? z : __fmul_rn(z, c.inv_t));
-    hval[s] = y;  // kept for the draft-token lookup
-    if (y != y || y == pinf()) atomicMax(&c.status, SS_ROW_NONFINITE);
-    else if (y != ninf()) add_entry(el, y, t);
-  }
-  __syncthreads();
   if (tid == 0) c.has_excl = c.use_mask || c.npatch > 0;
   __syncthreads();
+  SS_STAMP(1);
 
   // -------------------------------------------------- staging pass
   const bool excl = c.has_excl != 0, tiny = c.need_hist != 0;
@@ -1335,6 +1408,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   bool timed_out = false;
   {
     const uint8_t* xb = reinterpret_cast<const uint8_t*>(xm);
+    const uint8_t* pb = reinterpret_cast<const uint8_t*>(pbits);
     int waited = -1;
     const int nbulk = a.bulk ? c.n8 / 8 : 0;  // vectors landed by bulk copies
     // every thread runs the same number of iterations (the pair exchange
@@ -1352,7 +1426,16 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       }
       uint4 d = act ? data[v] : make_uint4(kNegInfPair, kNegInfPair, kNegInfPair, kNegInfPair);
       bool dirty = false;
-      if (excl) {
+      if (excl && act) {
+        const uint32_t P = pb[v];
+        if (P) {  // the raw logits of the patched tokens, into the table
+          const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+          for (int e = 0; e < 8; ++e)
+            if ((P >> e) & 1u) {
+              const int s = patch_find(hkey, lo + v * 8 + e);
+              if (s >= 0) hraw[s] |= (w[e >> 1] >> ((e & 1) ? 16 : 0)) & 0xffffu;
+            }
+        }
         const uint32_t A = xb[v];
         if (A != 0xffu) {
           d = apply_allow(d, A);
@@ -1361,7 +1444,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       }
       if (tiny) {
         const uint32_t tm = tiny_pair(d.x) | (tiny_pair(d.y) >> 1) | (tiny_pair(d.z) >> 2) | (tiny_pair(d.w) >> 3);
-        if (tm) {
+        if (tm && act) {
           uint32_t w[4] = {d.x, d.y, d.z, d.w};
           for (int e = 0; e < 8; ++e) {
             const uint32_t sh = (e & 1) ? 16u : 0u;
@@ -1396,6 +1479,29 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   }
   if (timed_out) atomicMax(&c.status, SS_ROW_TIMEOUT);
   __syncthreads();
+  SS_STAMP(11);
+  // processed values of the patched tokens: exact entries (penalties, bias,
+  // mask, temperature, each an individually rounded fp32 operation)
+  for (int s = tid; s < kHashCap; s += kThreads) {
+    const int32_t t = hkey[s];
+    if (t < 0) continue;
+    const uint32_t raw = hraw[s];
+    float z = bf16_to_f(raw & 0xffffu);
+    const int32_t hc = hcnt[s];
+    const int32_t cnt = hc & ~kBiasFlag;
+    if (cnt > 0) {
+      z = (z > 0.0f) ? __fdiv_rn(z, c.rep) : __fmul_rn(z, c.rep);
+      z = __fsub_rn(z, __fmul_rn(c.freq, static_cast<float>(cnt)));
+      z = __fsub_rn(z, c.pres);
+    }
+    if (hc & kBiasFlag) z = __fadd_rn(z, hval[s]);
+    const float y = !(raw >> 16) ? ninf() : (c.greedy ? z : __fmul_rn(z, c.inv_t));
+    hval[s] = y;  // kept for the draft-token lookup and the debug output
+    if (y != y || y == pinf()) atomicMax(&c.status, SS_ROW_NONFINITE);
+    else if (y != ninf()) add_entry(el, y, t);
+  }
+  __syncthreads();
+  SS_STAMP(2);
 
   // -------------------------------------------------- debug output
   if (a.debug) {
@@ -1416,6 +1522,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   {
     const uint32_t rmax = bmax2(run, run >> 16) & 0xffffu;
     const float zmax = block_max_nan(bf16_to_f(rmax));
+    SS_STAMP(12);
     // greedy: lowest index of the CTA's largest staged value
     int32_t garg = 0x7fffffff;
     if (c.greedy) {
@@ -1428,6 +1535,31 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         for (int e = 7; e >= 0; --e) {
           const uint32_t h = (w[e >> 1] >> ((e & 1) ? 16 : 0)) & 0xffffu;
           if (bf16_to_f(h) == zmax) garg = lo + t * 8 + e;
+        }
+      }
+    }
+    // top-k rows: pairs per binade below this CTA's maximum (the certificate)
+    const uint32_t zbin = key16(__float_as_uint(zmax) >> 16) >> 7;
+    if (c.k_on) {
+      if (tid < kCertBins) g_cert[tid] = 0;
+      __syncthreads();
+      const int lane = tid & 31;
+      for (int p0 = 0; p0 < c.nvec / 2; p0 += kThreads) {
+        const int p = p0 + tid;
+        int d = -1;
+        if (p < c.nvec / 2) {
+          const uint32_t h = vb[p];
+          if (h != 0xff80u) d = static_cast<int>(zbin) - static_cast<int>(key16(h) >> 7);
+        }
+        if (d >= kCertBins) d = -1;
+        // warp-aggregated counts: one atomic per distinct binade in the warp
+        uint32_t todo = __ballot_sync(0xffffffffu, d >= 0);
+        while (todo) {
+          const int leader = __ffs(todo) - 1;
+          const int dl = __shfl_sync(0xffffffffu, d, leader);
+          const uint32_t same = __ballot_sync(0xffffffffu, d == dl);
+          if (lane == leader) atomicAdd(&g_cert[dl], static_cast<uint32_t>(__popc(same)));
+          todo &= ~same;
         }
       }
     }
@@ -1456,16 +1588,14 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         } else {
           const uint16_t h = reinterpret_cast<const uint16_t*>(g_dyn)[c.x - lo];
           xy = c.greedy ? bf16_to_f(h) : __fmul_rn(bf16_to_f(h), inv_t);
-          const uint32_t aa = h & 0x7fffu;
           if (h == 0xff80u)  // excluded, or moved to the entries as a tiny value
             for (int i = 0; i < ne; ++i)
               if (ekey_t(el[i]) == c.x) xy = ekey_y(el[i]);
-          (void)aa;
         }
       }
     }
     if (tid == 0) {
-      Part1 p;
+      Part1& p = g_mine;
       p.zmax = zmax;
       p.emax = es;
       // greedy: lowest index among this CTA's items of its largest value
@@ -1479,14 +1609,19 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       p.nent = ne;
       p.xy = xy;
       p.xhere = xhere;
-      p.pad = 0;
-      for (int r = 0; r < C; ++r) *cl.map_shared_rank(&g_p1[rank], r) = p;
+      p.zbin = static_cast<int32_t>(zbin);
+      for (int b = 0; b < kCertBins; ++b) p.cert[b] = c.k_on ? g_cert[b] : 0u;
     }
+    __syncthreads();
+    SS_STAMP(13);
+    if (tid < C) *cl.map_shared_rank(&g_p1[rank], tid) = g_mine;
     cl.sync();
+    SS_STAMP(14);
     if (tid == 0) {
       float zm = ninf(), em = ninf();
-      int32_t st1 = SS_ROW_OK;
+      int32_t st1 = SS_ROW_OK, zb = -1;
       bool nan = false;
+      g_goff[0] = 0;
       for (int r = 0; r < C; ++r) {
         const Part1& p = g_p1[r];
         if (p.zmax != p.zmax) nan = true;
@@ -1494,6 +1629,8 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         em = fmaxf(em, p.emax);
         st1 = max(st1, p.status);
         if (p.xhere) c.xy = p.xy;
+        if (p.zmax != ninf()) zb = max(zb, p.zbin);
+        g_goff[r + 1] = g_goff[r] + p.nent;
       }
       const float ysm = c.greedy ? zm : __fmul_rn(zm, c.inv_t);
       float m = fmax_nan(ysm, em);
@@ -1506,15 +1643,40 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           const Part1& p = g_p1[r];
           if (fmaxf(p.zmax, p.emax) == m && p.arg < arg) arg = p.arg;
         }
+      c.tau_key = 0;
+      c.pick = zb;
       c.arg = arg;
       c.status = st1;
       c.m = m;
       c.zmax = zm;
-      c.ne = min(c.nent, kEntCap);
+      c.ne = ne;
       if (c.x < 0) c.xy = ninf();
     }
     __syncthreads();
+    // top-k: the highest binade boundary with at least k tokens at or above
+    // it (pairs whose maximum is at or above it, summed over the cluster);
+    // one lane per binade, then a warp prefix
+    if (c.k_on && tid < 32) {
+      const int zb = c.pick, d = tid;
+      uint32_t cnt = 0;
+      if (zb >= 0 && d < kCertBins && d < zb)
+        for (int r = 0; r < C; ++r) {
+          const Part1& p = g_p1[r];
+          const int dd = d - (zb - p.zbin);  // the same binade in rank r's counts
+          if (p.zmax != ninf() && dd >= 0 && dd < kCertBins) cnt += p.cert[dd];
+        }
+      unsigned long long cum = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, cum, o);
+        if (tid >= o) cum += y;
+      }
+      const unsigned ball = __ballot_sync(0xffffffffu, cum >= static_cast<unsigned long long>(c.top_k));
+      if (ball && tid == __ffs(ball) - 1) c.tau_key = static_cast<uint32_t>(zb - d) << 7;
+    }
+    __syncthreads();
   }
+  SS_STAMP(3);
 
   // -------------------------------------------------- decisions
   const int32_t status = c.status;
@@ -1545,24 +1707,11 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         // ---------------------------------------------- histogram
         if (tid == 0) c.M = make_slot_map(c.zmax);
         for (int s = tid; s < kSlots / 2; s += kThreads) hist[s] = 0;
-        // the local entries, sorted (y desc, token asc)
-        const int ne = c.ne;
-        int np2 = 1;
-        while (np2 < ne) np2 <<= 1;
-        for (int i = ne + tid; i < np2; i += kThreads) el[i] = ~0ull;
+        if (tid <= kGroups) {
+          g_ecnt[tid] = 0;
+          g_emass[tid] = 0;
+        }
         __syncthreads();
-        for (int k = 2; k <= np2; k <<= 1)
-          for (int jj = k >> 1; jj > 0; jj >>= 1) {
-            for (int q = tid; q < (np2 >> 1); q += kThreads) {
-              const int i = ((q & ~(jj - 1)) << 1) | (q & (jj - 1));
-              const unsigned long long x = el[i], y = el[i + jj];
-              if ((x > y) == ((i & k) == 0)) {
-                el[i] = y;
-                el[i + jj] = x;
-              }
-            }
-            __syncthreads();
-          }
         const SlotMap M = c.M;
         // group bounds at run boundaries of equal y
         if (tid <= kGroups) {
@@ -1571,17 +1720,20 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           g_gb[tid] = (tid == kGroups) ? M.ns : b;
           if (tid == kGroups) g_gb[kGroups + 1] = M.ns;  // the tail group: entries only
         }
-        // tokens with zero fixed-point mass cannot move a top-p cut
+        // candidates: top-k rows the tokens at or above the certificate;
+        // top-p rows the tokens with a non-zero fixed-point mass
+        const uint32_t tau = c.tau_key;
         const float skip = (c.k_on) ? ninf() : __fsub_rn(c.m, kMassRange);
         uint32_t below = 0;
         for (int v = tid; v < c.nvec; v += kThreads) {
-          const float vz = bf16_to_f(vb[v >> 1]);
-          if (vz == ninf() || __fmul_rn(vz, inv_t) < skip) continue;
+          const uint32_t hb = vb[v >> 1];
+          if (hb == 0xff80u || key16(hb) < tau || __fmul_rn(bf16_to_f(hb), inv_t) < skip) continue;
           const uint4 d = data[v];
           const uint32_t w[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const uint32_t h = (w[e >> 1] >> ((e & 1) ? 16 : 0)) & 0xffffu;
+            if (key16(h) < tau) continue;
             const int32_t s = slot_of(M, h);
             if (static_cast<uint32_t>(s) < static_cast<uint32_t>(M.ns))
               atomicAdd(hist + (s >> 1), 1u << ((s & 1) << 4));
@@ -1590,67 +1742,56 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           }
         }
         __syncthreads();  // group bounds and histogram complete
-        // slot position and group of every local entry; first entry per group
-        for (int e = tid; e < ne; e += kThreads) g_epos[e] = static_cast<int16_t>(first_slot_le(ekey_y(el[e]), 0, M.ns));
-        __syncthreads();
-        if (tid <= kGroups + 1) {
-          int lo_e = 0, hi_e = ne;  // entries are in slot-position order
-          while (lo_e < hi_e) {
-            const int mid = (lo_e + hi_e) >> 1;
-            if (group_of(g_epos[mid]) >= tid)
-              hi_e = mid;
-            else
-              lo_e = mid + 1;
-          }
-          g_ge[tid] = (tid == kGroups + 1) ? ne : lo_e;
+        SS_STAMP(4);
+        // slot position and group of every local entry
+        for (int e = tid; e < c.ne; e += kThreads) {
+          const float y = ekey_y(el[e]);
+          const int32_t p = first_slot_le(y, 0, M.ns);
+          g_epos[e] = static_cast<int16_t>(p);
+          const int q = group_of(p);
+          atomicAdd(&g_ecnt[q], 1u);
+          atomicAdd(&g_emass[q], fmass(y, c.m));
         }
         __syncthreads();
         // coarse counts and masses of this CTA (slots and entries), pushed to
-        // every CTA (exchange 2)
+        // every CTA (exchange 2); the tail group also carries the count of
+        // uncounted tokens below the slots
         uint32_t* pc = xm;  // [C][kGroups + 1] counts, then masses
         unsigned long long* pm = reinterpret_cast<unsigned long long*>(xm + ((kMaxCluster * (kGroups + 1) + 1) & ~1));
         {
-          const int grp = tid >> 3, sub = tid & 7;
+          const int grp = tid >> 3, sub = tid & 7;  // 8 threads per group
           uint32_t cnt = 0;
           unsigned long long mass = 0;
-          for (int s = g_gb[grp] + sub; s < g_gb[grp + 1]; s += 8) {  // grp < kGroups: 8 threads per group
+          for (int s = g_gb[grp] + sub; s < g_gb[grp + 1]; s += 8) {
             const uint32_t h = (hist[s >> 1] >> ((s & 1) << 4)) & 0xffffu;
             if (h) {
               cnt += h;
               mass += static_cast<unsigned long long>(h) * fmass(slot_y(s), c.m);
             }
           }
-          for (int e = g_ge[grp] + sub; e < g_ge[grp + 1]; e += 8) {
-            ++cnt;
-            mass += fmass(ekey_y(el[e]), c.m);
-          }
 #pragma unroll
           for (int o = 1; o < 8; o <<= 1) {
             cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
             mass += __shfl_xor_sync(0xffffffffu, mass, o);
           }
-          // the tail group: entries past the slots, and the uncounted tokens
-          uint32_t tcnt = 0;
-          unsigned long long tmass = 0;
-          for (int e = g_ge[kGroups] + tid; e < ne; e += kThreads) {
-            ++tcnt;
-            tmass += fmass(ekey_y(el[e]), c.m);
-          }
-          tcnt = block_sum<uint32_t>(tcnt);
-          tmass = block_sum<unsigned long long>(tmass);
+          cnt += g_ecnt[grp];
+          mass += g_emass[grp];
           const uint32_t bsum = block_sum<uint32_t>(below);
           if (sub < C) {
             *cl.map_shared_rank(pc + rank * (kGroups + 1) + grp, sub) = cnt;
             *cl.map_shared_rank(pm + rank * (kGroups + 1) + grp, sub) = mass;
           }
           if (tid < C) {
-            // counts of the tail group and the uncounted tokens, packed
-            *cl.map_shared_rank(pc + rank * (kGroups + 1) + kGroups, tid) = tcnt;
+            // the tail group's entries, and the uncounted tokens in the top
+            // byte of its mass (saturating)
+            *cl.map_shared_rank(pc + rank * (kGroups + 1) + kGroups, tid) = g_ecnt[kGroups];
             *cl.map_shared_rank(pm + rank * (kGroups + 1) + kGroups, tid) =
-                (tmass & 0x00ffffffffffffffull) | (static_cast<unsigned long long>(min(bsum, 255u)) << 56);
+                (g_emass[kGroups] & 0x00ffffffffffffffull) | (static_cast<unsigned long long>(min(bsum, 255u)) << 56);
           }
         }
+        SS_STAMP(15);
         cl.sync();
+        SS_STAMP(16);
         if (tid <= kGroups) {
           uint32_t cnt = 0;
           unsigned long long mass = 0, bel = 0;
@@ -1669,6 +1810,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           g_gmass[tid] = mass;
         }
         __syncthreads();
+        SS_STAMP(5);
 
         // ---------------------------------------------- the cuts
         // K = the shortest of the top-k, top-p and min-p prefixes of the
@@ -1689,11 +1831,17 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
             bcm = c.w_cm;
             Sk = bcm + btake * fmass(bv, c.m);
           }
+          SS_TRACE(19, c.tau_key);
+          SS_TRACE(20, __float_as_uint(bv));
+          SS_TRACE(21, btake | (bcc << 32));
+          SS_TRACE(22, c.pick);
         }
         if (!have_cut && !unknown) {
           // every item (top-k off or larger than the item count): all must
           // have been counted
-          if (c.below && (c.k_on || M.ns == 0 || __fmul_rn(slot_z(M, M.ns - 1), inv_t) > skip)) unknown = true;
+          if ((c.below || (c.k_on && c.tau_key)) &&
+              (c.k_on || M.ns == 0 || __fmul_rn(slot_z(M, M.ns - 1), inv_t) > skip))
+            unknown = true;
           Sk = 0;
           for (int q = 0; q <= kGroups; ++q) Sk += g_gmass[q];
           if (tid == 0) {
@@ -1702,6 +1850,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
             c.kcount = cnt;
           }
         }
+        SS_STAMP(6);
         if (c.p_on && !unknown) {
           const unsigned long long T = mass_target(c.top_p, Sk);
           locate(a, 1, T);
@@ -1716,19 +1865,15 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         }
         if (c.mp_on && !unknown) {
           // the largest value failing the min-p test: among the slots (they
-          // fall monotonically) and every CTA's sorted entries
-          if (tid < C) {
-            const unsigned long long* er = cl.map_shared_rank(el, tid);
-            const int ner = *cl.map_shared_rank(&g.ne, tid);
-            int lo_e = 0, hi_e = ner;  // failing entries are a suffix
-            while (lo_e < hi_e) {
-              const int mid = (lo_e + hi_e) >> 1;
-              if (!(__fsub_rn(ekey_y(er[mid]), c.m) >= c.lmp))
-                hi_e = mid;
-              else
-                lo_e = mid + 1;
-            }
-            g_rfail[tid] = (lo_e < ner) ? ekey_y(er[lo_e]) : ninf();
+          // fall monotonically) and every CTA's entries
+          if (tid == 0) c.fail_key = 0;
+          __syncthreads();
+          const int total_e = g_goff[C];
+          for (int i = tid; i < total_e; i += kThreads) {
+            int r = 0;
+            while (i >= g_goff[r + 1]) ++r;
+            const float y = ekey_y(*cl.map_shared_rank(el + (i - g_goff[r]), r));
+            if (!(__fsub_rn(y, c.m) >= c.lmp)) atomicMax(&c.fail_key, okey(y));
           }
           __syncthreads();
           if (tid == 0) {
@@ -1741,14 +1886,15 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
                 lo_s = mid + 1;
             }
             float vf = (lo_s < M.ns) ? slot_y(lo_s) : ninf();
-            for (int r = 0; r < C; ++r) vf = fmaxf(vf, g_rfail[r]);
+            if (c.fail_key) vf = fmaxf(vf, okey_value(c.fail_key));
             // every counted slot passes, but uncounted tokens below them may
             // not: the min-p cut is unknown unless a shorter cut exists
-            c.pick = (lo_s == M.ns && c.below && !have_cut) ? 1 : 0;
+            c.pick = (lo_s == M.ns && (c.below || c.tau_key) && !have_cut) ? 1 : 0;
             c.w_v = vf;
           }
           __syncthreads();
           const float vf = c.w_v;
+          SS_TRACE(23, __float_as_uint(vf) | (static_cast<unsigned long long>(__float_as_uint(c.m)) << 32));
           if (c.pick) unknown = true;
           if (!unknown && vf != ninf() && (!have_cut || vf > bv || (vf == bv && btake > 0))) {
             above_value(a, vf);
@@ -1763,6 +1909,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
             }
           }
         }
+        SS_STAMP(7);
         if (unknown) {
           if (tid == 0) c.status = SS_ROW_LIMIT;
         } else if (have_cut) {
@@ -1772,7 +1919,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
             c.kmass = bcm + btake * fmass(bv, c.m);
           }
           __syncthreads();
-          resolve_ties(a, bv, btake);
+          resolve_ties(a, bv, btake, tests_draft);
           cv = c.cut_v;
           ct = c.cut_t;
         } else {
@@ -1796,6 +1943,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           }
           __syncthreads();
         }
+        SS_STAMP(8);
         kept = c.kcount;
         bool need_draw = !tests_draft;
         if (tests_draft) {
@@ -1831,8 +1979,10 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       }
     }
   }
+  SS_STAMP(9);
   // every CTA of the cluster is done with the others' shared memory
   cl.sync();
+  SS_STAMP(10);
   if (rank != 0 || tid != 0) return;
   const int32_t fst = c.status;
   const bool ok = fst == SS_ROW_OK;
@@ -1900,7 +2050,7 @@ static void layout(HArgs& a) {
   a.o_vb = take(static_cast<int64_t>(a.slice / 16) * 2, 16);
   // slot counts as 16-bit halves of 32-bit words (a slot holds at most
   // kSliceMax tokens); the patch table shares the region during set-up
-  a.o_hist = take(std::max<int64_t>(kSlots * 2, kHashCap * 12), 16);
+  a.o_hist = take(std::max<int64_t>(kSlots * 2, kHashCap * 16), 16);
   a.o_el = take(kEntCap * 8, 16);
   // one region, in turn: the allow bits, the exchange-2 push, a group's
   // gathered entries
@@ -1908,7 +2058,8 @@ static void layout(HArgs& a) {
   const int64_t push_bytes = ((kMaxCluster * (kGroups + 1) + 1) & ~1) * 4 + kMaxCluster * (kGroups + 1) * 8;
   const int64_t gather_bytes = kGatherCap * 10;
   a.o_xm = take(std::max(xm_bytes, std::max(push_bytes, gather_bytes)), 16);
-  a.o_mg = take((kFineMax + kGatherCap) * 8, 16);
+  // the patched-token bits during set-up, then a group's items merged by value
+  a.o_mg = take(std::max<int64_t>((kFineMax + kGatherCap) * 8, a.slice / 8), 16);
   a.o_mbar = take(kMaxChunks * 8, 16);
   a.total = static_cast<int32_t>((off + 127) / 128 * 128);
 }
@@ -1960,6 +2111,16 @@ int hist_cluster_size(int32_t vocab, int32_t dtype) {
 }
 
 int32_t hist_last_error() { return hist::t_err; }
+
+}  // namespace ss
+
+#ifdef SS_HIST_STAMPS
+extern "C" int ss_hist_stamps_copy(void* host, size_t bytes) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, ss::hist::g_stamps, bytes));
+}
+#endif
+
+namespace ss {
 
 ss_status hist_sample(const ss_sample_args& A, cudaStream_t stream) {
   hist::HArgs a{};
