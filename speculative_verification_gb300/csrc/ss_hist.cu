@@ -81,24 +81,35 @@ constexpr int kSliceMax = 49152;
 constexpr uint32_t kWaitPolls = 1u << 22;
 constexpr int kBiasFlag = 1 << 30;
 constexpr uint32_t kNegInfPair = 0xff80ff80u;
-constexpr uint32_t kTinyA = 0x3780u;  // |z| below 2^-16: tiny (exact entries unless zero)
+constexpr uint32_t kTinyA = 0x3780u;
+// A rejection at draft position j is recorded as kRejBase - j in the
+// request's rejection word (atomic maximum): the word exceeds kRejBase - j
+// exactly when a position before j has rejected.
+constexpr int32_t kRejBase = kMaxDraft + 2;  // |z| below 2^-16: tiny (exact entries unless zero)
 // Fixed-point masses of tokens more than this far below the maximum are 0.
 constexpr float kMassRange = 28.2f;
 
 static_assert(kSlots % kGroups == 0, "groups tile the slots");
+// the entries' group offsets and order sit behind the slot counts, in the
+// part of the region the patch table no longer needs
+static_assert(kSlots * 2 + (kGroups + 2) * 4 + kEntCap * 2 <= kHashCap * 16, "entry order fits the region");
+static_assert(kEntCap % kThreads == 0, "entries per thread");
 
 // Phase timestamps for tracing (built only with -DSS_HIST_STAMPS): the
 // global timer at the end of each phase, per CTA, read back with
 // ss_hist_stamps_copy.
 #ifdef SS_HIST_STAMPS
-constexpr int kStampCtas = 16384, kStampPhases = 24;
+constexpr int kStampCtas = 16384, kStampPhases = 48;
 __device__ unsigned long long g_stamps[kStampCtas][kStampPhases];
 #define SS_STAMP(k)                                                                \
   do {                                                                             \
     if (threadIdx.x == 0 && blockIdx.x < kStampCtas) {                             \
-      unsigned long long t_;                                                       \
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                       \
-      g_stamps[blockIdx.x][k] = t_;                                                \
+      if ((k) == 0) {                                                              \
+        unsigned long long t_;                                                     \
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                     \
+        g_stamps[blockIdx.x][kStampPhases - 1] = t_;                               \
+      }                                                                            \
+      g_stamps[blockIdx.x][k] = static_cast<unsigned long long>(clock64());        \
     }                                                                              \
   } while (0)
 #define SS_TRACE(k, v)                                                             \
@@ -137,9 +148,16 @@ __device__ __forceinline__ int32_t ekey_t(unsigned long long e) { return static_
 
 // Fixed-point mass trunc(exp(y - m) * 2^40) (0 for y = -inf); a function of
 // y alone for a given row, so every CTA computes the same integers.
+// The truncation of e * 2^40 (e in [0, 1]) is taken from e's bits with
+// integer shifts: the same integer as the float -> 64-bit conversion, which
+// sm_103 issues at a fraction of the integer rate.
 __device__ __forceinline__ unsigned long long fmass(float y, float m) {
   const float e = fminf(__expf(__fsub_rn(y, m)), 1.0f);
-  return static_cast<unsigned long long>(__fmul_rn(e, 1099511627776.0f));
+  const uint32_t b = __float_as_uint(e);
+  const int sh = static_cast<int>(b >> 23) - 127 + 40 - 23;  // e * 2^40 = (1.f as an integer) * 2^sh
+  const unsigned long long mant = (b & 0x7fffffu) | 0x800000u;
+  if (sh >= 0) return mant << sh;  // sh <= 17
+  return (sh > -24) ? (mant >> (-sh)) : 0ull;  // zero and subnormal e give 0
 }
 __device__ __forceinline__ unsigned long long mass_target(float p, unsigned long long S) {
   return static_cast<unsigned long long>(ceil(static_cast<double>(p) * static_cast<double>(S)));
@@ -271,6 +289,8 @@ struct alignas(16) Part1 {
   float xy;       // processed value of the draft token (its CTA)
   int32_t xhere;
   int32_t zbin;   // binade of zmax (16-bit order key >> 7)
+  int32_t rej;    // verification: the request's rejection word as this CTA read it
+  int32_t pad[3];
   uint32_t cert[kCertBins];  // 16-token pairs whose maximum lies d binades below zbin
 };
 
@@ -286,7 +306,8 @@ struct alignas(16) PartD {
 
 struct Ctx {
   // task
-  int32_t valid, row, req, j, k, bad_k, d0, x, drow;
+  int32_t valid, row, req, j, k, bad_k, d0, x, drow, nreq;
+  int32_t skip_draw;  // verification: a position before this one has rejected
   int64_t row_off;
   int32_t lo, n, nvec, nch, n8;
   // parameters
@@ -295,6 +316,7 @@ struct Ctx {
   uint32_t seed_lo, seed_hi, pos, rowid;
   int32_t h0, h1, b0, b1;
   int32_t status;   // local, then cluster-wide
+  int32_t pstatus;  // what the parameters alone give
   int32_t nent;     // local entries appended
   int32_t ne;       // local entries kept
   int32_t n_g;      // entries gathered for one coarse group
@@ -311,24 +333,27 @@ struct Ctx {
   int32_t cut_t;
   unsigned long long kcount, kmass;  // |K| and its fixed-point mass
   // locate results
-  int32_t w_found, w_slot;
+  int32_t w_found, w_slot, w_grp;
   float w_v;
   unsigned long long w_take, w_cc, w_cm;
   int32_t tie_rank, tie_local;
   unsigned long long below;
+  unsigned long long ntot, stot;  // count and mass of every counted item
   // scratch
   int32_t pick;
   int32_t tcut_in;  // tie cutoff, written by the CTA that resolves it
   int32_t xpar;     // buffer of the next draw / mass exchange
-  uint32_t fail_key;
+  uint32_t fail_key;  // the largest entry key failing min-p (cluster), and this CTA's
+  uint32_t fail_loc;
 };
 
 __shared__ Ctx g;
 __shared__ Part1 g_p1[kMaxCluster];
 __shared__ Part1 g_mine;
 __shared__ PartD g_pd[2][kMaxCluster];
-__shared__ unsigned char g_red[kWarps * 16];
-__shared__ unsigned long long g_scan[2 * kWarps];
+__shared__ __align__(16) unsigned char g_red[(kWarps + 1) * 8];
+__shared__ unsigned long long g_scan[2 * (kWarps + 1)];
+__shared__ __align__(16) unsigned char g_red2[(kWarps + 1) * 16];
 __shared__ int32_t g_gb[kGroups + 2];                // coarse group bounds (slots)
 __shared__ uint32_t g_gcnt[kGroups + 1];
 __shared__ unsigned long long g_gmass[kGroups + 1];
@@ -337,9 +362,13 @@ __shared__ unsigned long long g_emass[kGroups + 1];
 __shared__ uint32_t g_fc[kFineMax];                  // one group's slot counts (all CTAs)
 __shared__ int16_t g_epos[kEntCap];                  // slot position of each local entry
 __shared__ int32_t g_goff[kMaxCluster + 1];
+__shared__ int32_t g_gr0[kMaxCluster];       // one group's entry range in every CTA
+__shared__ int32_t g_grc[kMaxCluster + 1];
 __shared__ uint32_t g_rtie[kMaxCluster];
 __shared__ uint32_t g_cert[kCertBins];
 __shared__ int32_t g_tietok[kTieEnt];
+__shared__ uint32_t g_prm[32];
+__shared__ unsigned long long g_dbest;  // the draw's best key so far  // the request's parameter words
 
 extern __shared__ __align__(128) uint8_t g_dyn[];
 
@@ -347,6 +376,10 @@ __device__ __forceinline__ uint32_t key16(uint32_t h) { return (h & 0x8000u) ? (
 __device__ __forceinline__ uint32_t key16_bits(uint32_t k) { return (k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu); }
 
 // ------------------------------------------------------ block reductions --
+// Warp partials go through shared memory; 32-bit partials are read back by
+// every thread as four 16-byte loads, wider ones are combined by warp 0 and
+// broadcast.  Either way the combine over the 16 warps is not a 16-step loop
+// in every thread.
 
 __device__ __forceinline__ float block_max_nan(float v) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -356,16 +389,14 @@ __device__ __forceinline__ float block_max_nan(float v) {
   __syncthreads();
   if (lane == 0) r[wid] = v;
   __syncthreads();
-  v = r[0];
-  for (int w = 1; w < kWarps; ++w) v = fmax_nan(v, r[w]);
-  return v;
+  const float4* r4 = reinterpret_cast<const float4*>(r);
+  const float4 a = r4[0], b = r4[1], c = r4[2], d = r4[3];
+  return fmax_nan(fmax_nan(fmax_nan(fmax_nan(a.x, a.y), fmax_nan(a.z, a.w)), fmax_nan(fmax_nan(b.x, b.y), fmax_nan(b.z, b.w))),
+                  fmax_nan(fmax_nan(fmax_nan(c.x, c.y), fmax_nan(c.z, c.w)), fmax_nan(fmax_nan(d.x, d.y), fmax_nan(d.z, d.w))));
 }
 
-// (score desc, token asc) arg-reduction over the block; every thread gets it.
-__device__ __forceinline__ void block_best(float& s, int32_t& t) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
+__device__ __forceinline__ void warp_best(float& s, int32_t& t, int width) {
+  for (int o = width >> 1; o; o >>= 1) {
     const float os = __shfl_xor_sync(0xffffffffu, s, o);
     const int32_t ot = __shfl_xor_sync(0xffffffffu, t, o);
     if (beats(os, ot, s, t)) {
@@ -373,21 +404,68 @@ __device__ __forceinline__ void block_best(float& s, int32_t& t) {
       t = ot;
     }
   }
+}
+
+// (score desc, token asc) arg-reduction over the block; every thread gets it.
+__device__ __forceinline__ void block_best(float& s, int32_t& t) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  warp_best(s, t, 32);
   float* rs = reinterpret_cast<float*>(g_red);
-  int32_t* rt = reinterpret_cast<int32_t*>(g_red) + kWarps;
+  int32_t* rt = reinterpret_cast<int32_t*>(g_red) + (kWarps + 1);
   __syncthreads();
   if (lane == 0) {
     rs[wid] = s;
     rt[wid] = t;
   }
   __syncthreads();
-  s = rs[0];
-  t = rt[0];
-  for (int w = 1; w < kWarps; ++w)
-    if (beats(rs[w], rt[w], s, t)) {
-      s = rs[w];
-      t = rt[w];
+  if (wid == 0) {
+    float x = (lane < kWarps) ? rs[lane] : ninf();
+    int32_t y = (lane < kWarps) ? rt[lane] : 0x7fffffff;
+    warp_best(x, y, kWarps);
+    if (lane == 0) {
+      rs[kWarps] = x;
+      rt[kWarps] = y;
     }
+  }
+  __syncthreads();
+  s = rs[kWarps];
+  t = rt[kWarps];
+}
+
+// Two (score desc, token asc) arg-reductions over the block in one pass.
+__device__ __forceinline__ void block_best2(float& s1, int32_t& t1, float& s2, int32_t& t2) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  warp_best(s1, t1, 32);
+  warp_best(s2, t2, 32);
+  float* rs1 = reinterpret_cast<float*>(g_red2);
+  int32_t* rt1 = reinterpret_cast<int32_t*>(rs1 + (kWarps + 1));
+  float* rs2 = reinterpret_cast<float*>(rt1 + (kWarps + 1));
+  int32_t* rt2 = reinterpret_cast<int32_t*>(rs2 + (kWarps + 1));
+  __syncthreads();
+  if (lane == 0) {
+    rs1[wid] = s1;
+    rt1[wid] = t1;
+    rs2[wid] = s2;
+    rt2[wid] = t2;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    float x1 = (lane < kWarps) ? rs1[lane] : ninf(), x2 = (lane < kWarps) ? rs2[lane] : ninf();
+    int32_t y1 = (lane < kWarps) ? rt1[lane] : 0x7fffffff, y2 = (lane < kWarps) ? rt2[lane] : 0x7fffffff;
+    warp_best(x1, y1, kWarps);
+    warp_best(x2, y2, kWarps);
+    if (lane == 0) {
+      rs1[kWarps] = x1;
+      rt1[kWarps] = y1;
+      rs2[kWarps] = x2;
+      rt2[kWarps] = y2;
+    }
+  }
+  __syncthreads();
+  s1 = rs1[kWarps];
+  t1 = rt1[kWarps];
+  s2 = rs2[kWarps];
+  t2 = rt2[kWarps];
 }
 
 template <typename T>
@@ -399,9 +477,25 @@ __device__ __forceinline__ T block_sum(T v) {
   __syncthreads();
   if (lane == 0) r[wid] = v;
   __syncthreads();
-  v = r[0];
-  for (int w = 1; w < kWarps; ++w) v += r[w];
-  return v;
+  if constexpr (sizeof(T) == 4) {
+    const uint4* r4 = reinterpret_cast<const uint4*>(r);
+    T acc = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 q = r4[i];
+      acc += (static_cast<T>(q.x) + static_cast<T>(q.y)) + (static_cast<T>(q.z) + static_cast<T>(q.w));
+    }
+    return acc;
+  } else {
+    if (wid == 0) {
+      T x = (lane < kWarps) ? r[lane] : T(0);
+#pragma unroll
+      for (int o = kWarps >> 1; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      if (lane == 0) r[kWarps] = x;
+    }
+    __syncthreads();
+    return r[kWarps];
+  }
 }
 
 // Exclusive prefix over the block (thread order); *total gets the sum.
@@ -417,13 +511,21 @@ __device__ __forceinline__ int32_t block_excl_scan(int32_t v, int32_t* total) {
   __syncthreads();
   if (lane == 31) r[wid] = x;
   __syncthreads();
-  int32_t before = 0, tot = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < wid) before += r[w];
-    tot += r[w];
+  if (wid == 0) {  // exclusive prefix of the warp totals, and the total
+    const int32_t w = (lane < kWarps) ? r[lane] : 0;
+    int32_t inc = w;
+#pragma unroll
+    for (int o = 1; o < kWarps; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    __syncwarp();
+    if (lane < kWarps) r[lane] = inc - w;
+    if (lane == kWarps - 1) r[kWarps] = inc;
   }
-  *total = tot;
-  return before + x - v;
+  __syncthreads();
+  *total = r[kWarps];
+  return r[wid] + x - v;
 }
 
 // Inclusive prefix over the block of a (count, mass) pair (thread order);
@@ -444,22 +546,36 @@ __device__ __forceinline__ void block_scan2(unsigned long long& c, unsigned long
   __syncthreads();
   if (lane == 31) {
     r[wid] = c;
-    r[kWarps + wid] = m;
+    r[(kWarps + 1) + wid] = m;
   }
   __syncthreads();
-  unsigned long long bc = 0, bm = 0, sc = 0, sm = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < wid) {
-      bc += r[w];
-      bm += r[kWarps + w];
+  if (wid == 0) {
+    const unsigned long long wc = (lane < kWarps) ? r[lane] : 0, wm = (lane < kWarps) ? r[(kWarps + 1) + lane] : 0;
+    unsigned long long ic = wc, im = wm;
+#pragma unroll
+    for (int o = 1; o < kWarps; o <<= 1) {
+      const unsigned long long yc = __shfl_up_sync(0xffffffffu, ic, o);
+      const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, o);
+      if (lane >= o) {
+        ic += yc;
+        im += ym;
+      }
     }
-    sc += r[w];
-    sm += r[kWarps + w];
+    __syncwarp();
+    if (lane < kWarps) {
+      r[lane] = ic - wc;
+      r[(kWarps + 1) + lane] = im - wm;
+    }
+    if (lane == kWarps - 1) {
+      r[kWarps] = ic;
+      r[(kWarps + 1) + kWarps] = im;
+    }
   }
-  c += bc;
-  m += bm;
-  *tc = sc;
-  *tm = sm;
+  __syncthreads();
+  c += r[wid];
+  m += r[(kWarps + 1) + wid];
+  *tc = r[kWarps];
+  *tm = r[(kWarps + 1) + kWarps];
 }
 
 // The coarse group where the running count (by_mass = 0) or mass (1) first
@@ -529,15 +645,20 @@ __device__ void decode_and_copy(const HArgs& a, int task, int rank) {
   c.xpar = 0;
   c.kcount = 0;
   c.kmass = 0;
+  c.nreq = 0;
+  c.skip_draw = 0;
   c.x = -1;
   c.drow = -1;
   c.d0 = 0;
   int req = task, j = 0, k = 0;
   int64_t row = task;
   if (a.mode == 1) {
-    const int width = a.max_draft + 1;
-    req = task / width;
-    j = task - req * width;
+    // position-major: every request's position 0 first, so that later
+    // positions tend to start after the earlier ones have decided
+    const int nreq = a.num_tasks / (a.max_draft + 1);
+    c.nreq = nreq;
+    j = task / nreq;
+    req = task - j * nreq;
     c.d0 = a.draft_offsets[req];
     k = a.draft_offsets[req + 1] - c.d0;
     if (k < 0 || k > a.max_draft) {
@@ -581,36 +702,80 @@ __device__ void decode_and_copy(const HArgs& a, int task, int rank) {
   }
 }
 
-__device__ void read_params(const HArgs& a) {
-  Ctx& c = g;
+__device__ void read_params(const HArgs& a, int task);
+
+// Warp 1: the request's parameter words, one global load per lane (all in
+// flight at once), into g_prm; then its lane 0 checks them (read_params),
+// while thread 0 issues the bulk copies.
+__device__ void load_params(const HArgs& a, int task) {
   const ss_params& p = a.p;
-  const int i = c.req;
-  int st = c.status;
-  const float T = p.temperature[i];
+  const int lane = threadIdx.x & 31;
+  int i = task;
+  if (a.mode == 1) {
+    const int nreq = a.num_tasks / (a.max_draft + 1);
+    i = task - (task / nreq) * nreq;
+  }
+  uint32_t v = 0;
+  switch (lane) {
+    case 0: v = __float_as_uint(p.temperature[i]); break;
+    case 1: v = p.top_k ? static_cast<uint32_t>(p.top_k[i]) : 0u; break;
+    case 2: v = __float_as_uint(p.top_p ? p.top_p[i] : 1.0f); break;
+    case 3: v = __float_as_uint(p.min_p ? p.min_p[i] : 0.0f); break;
+    case 4: v = __float_as_uint(p.repetition ? p.repetition[i] : 1.0f); break;
+    case 5: v = __float_as_uint(p.frequency ? p.frequency[i] : 0.0f); break;
+    case 6: v = __float_as_uint(p.presence ? p.presence[i] : 0.0f); break;
+    case 7: v = static_cast<uint32_t>(p.seed[i]); break;
+    case 8: v = static_cast<uint32_t>(p.seed[i] >> 32); break;
+    case 9: v = p.row_id ? p.row_id[i] : static_cast<uint32_t>(i); break;
+    case 10: v = static_cast<uint32_t>(p.position[i]); break;
+    case 11: v = static_cast<uint32_t>(static_cast<uint64_t>(p.position[i]) >> 32); break;
+    case 12: v = p.hist_offsets ? static_cast<uint32_t>(p.hist_offsets[i]) : 0u; break;
+    case 13: v = p.hist_offsets ? static_cast<uint32_t>(p.hist_offsets[i + 1]) : 0u; break;
+    case 14: v = p.bias_offsets ? static_cast<uint32_t>(p.bias_offsets[i]) : 0u; break;
+    case 15: v = p.bias_offsets ? static_cast<uint32_t>(p.bias_offsets[i + 1]) : 0u; break;
+    case 16: v = (p.bitmask && (!p.use_bitmask || p.use_bitmask[i])) ? 1u : 0u; break;
+    case 17: v = (a.mode == 1) ? static_cast<uint32_t>(a.draft_offsets[i]) : 0u; break;
+    case 18: v = (a.mode == 1) ? static_cast<uint32_t>(a.draft_offsets[i + 1]) : 0u; break;
+    default: break;
+  }
+  // the loads are issued: let thread 0 queue the bulk copies behind them
+  asm volatile("bar.arrive 1, 64;" ::: "memory");
+  if (lane < 19) g_prm[lane] = v;
+  __syncwarp();
+  if (lane == 0) read_params(a, task);
+}
+
+// Lane 0 of warp 1, after load_params: the parameters, checked (the status
+// they give goes to c.pstatus; decode_and_copy runs meanwhile).
+__device__ void read_params(const HArgs& a, int task) {
+  Ctx& c = g;
+  int st = SS_ROW_OK;
+  int j = 0;
+  int32_t k = 0;
+  if (a.mode == 1) {
+    const int nreq = a.num_tasks / (a.max_draft + 1);
+    j = task / nreq;
+    k = static_cast<int32_t>(g_prm[18]) - static_cast<int32_t>(g_prm[17]);
+  }
+  const float T = __uint_as_float(g_prm[0]);
   c.T = T;
-  c.top_k = p.top_k ? p.top_k[i] : 0;
-  c.top_p = p.top_p ? p.top_p[i] : 1.0f;
-  c.min_p = p.min_p ? p.min_p[i] : 0.0f;
-  c.rep = p.repetition ? p.repetition[i] : 1.0f;
-  c.freq = p.frequency ? p.frequency[i] : 0.0f;
-  c.pres = p.presence ? p.presence[i] : 0.0f;
-  const uint64_t seed = p.seed[i];
-  c.seed_lo = static_cast<uint32_t>(seed);
-  c.seed_hi = static_cast<uint32_t>(seed >> 32);
-  c.rowid = p.row_id ? p.row_id[i] : static_cast<uint32_t>(i);
-  const int64_t pos64 = p.position[i];
-  const int64_t last = pos64 + (a.mode == 1 ? c.k : 0);
+  c.top_k = static_cast<int32_t>(g_prm[1]);
+  c.top_p = __uint_as_float(g_prm[2]);
+  c.min_p = __uint_as_float(g_prm[3]);
+  c.rep = __uint_as_float(g_prm[4]);
+  c.freq = __uint_as_float(g_prm[5]);
+  c.pres = __uint_as_float(g_prm[6]);
+  c.seed_lo = g_prm[7];
+  c.seed_hi = g_prm[8];
+  c.rowid = g_prm[9];
+  const int64_t pos64 = static_cast<int64_t>((static_cast<uint64_t>(g_prm[11]) << 32) | g_prm[10]);
+  const int64_t last = pos64 + k;
   if (pos64 < 0 || last > 0xFFFFFFFFLL) st = max(st, SS_ROW_BAD_PARAM);
-  c.pos = static_cast<uint32_t>(pos64) + static_cast<uint32_t>(c.j);
-  c.h0 = c.h1 = c.b0 = c.b1 = 0;
-  if (p.hist_offsets) {
-    c.h0 = p.hist_offsets[i];
-    c.h1 = p.hist_offsets[i + 1];
-  }
-  if (p.bias_offsets) {
-    c.b0 = p.bias_offsets[i];
-    c.b1 = p.bias_offsets[i + 1];
-  }
+  c.pos = static_cast<uint32_t>(pos64) + static_cast<uint32_t>(j);
+  c.h0 = static_cast<int32_t>(g_prm[12]);
+  c.h1 = static_cast<int32_t>(g_prm[13]);
+  c.b0 = static_cast<int32_t>(g_prm[14]);
+  c.b1 = static_cast<int32_t>(g_prm[15]);
   if (!(T >= 0.0f) || isinf(T)) st = max(st, SS_ROW_BAD_PARAM);
   if (c.top_k < 0) st = max(st, SS_ROW_BAD_PARAM);
   if (!(c.top_p > 0.0f)) st = max(st, SS_ROW_BAD_PARAM);
@@ -622,7 +787,7 @@ __device__ void read_params(const HArgs& a) {
     c.h1 = c.h0;
     c.b1 = c.b0;
   }
-  c.status = st;
+  c.pstatus = st;
   c.greedy = (T == 0.0f);
   c.inv_t = (c.greedy || !(T > 0.0f)) ? 1.0f : __frcp_rn(T);
   c.k_on = (!c.greedy && c.top_k > 0 && c.top_k < a.vocab);
@@ -630,7 +795,7 @@ __device__ void read_params(const HArgs& a) {
   c.mp_on = (!c.greedy && c.min_p > 0.0f);
   c.lmp = c.mp_on ? logf(c.min_p) : 0.0f;
   c.need_hist = c.k_on || c.p_on;
-  c.use_mask = p.bitmask && (!p.use_bitmask || p.use_bitmask[i]);
+  c.use_mask = g_prm[16] != 0;
 }
 
 // ----------------------------------------------------------- patch table --
@@ -678,15 +843,26 @@ __device__ __forceinline__ bool in_cut(float y, int32_t t, float cv, int32_t ct)
 
 // Writes this CTA's PartD into every CTA, cluster barrier, and
 // combines the C partials in rank order (identical in every CTA): best
-// (score desc, token asc), count and mass summed.  Called by all threads.
+// (score desc, token asc), and with SUMS the counts and masses summed.
+// Called by all threads.
+// With REDUCED the caller's (best, arg) is already the CTA's (the same in
+// every thread).
+template <bool SUMS, bool REDUCED>
 __device__ PartD exchange_d(float best, int32_t arg, int32_t count, unsigned long long mass) {
   cg::cluster_group cl = cg::this_cluster();
-  block_best(best, arg);  // (a block barrier: g.xpar below is current)
-  // consecutive exchanges alternate between two buffers: a CTA still reading
-  // the previous result is never overwritten
+  if (SUMS) {
+    count = block_sum<int32_t>(count);
+    mass = block_sum<unsigned long long>(mass);
+  } else if (REDUCED) {
+    __syncthreads();
+  } else {
+    block_best(best, arg);
+  }
+  SS_STAMP(37);
+  // (a block barrier above: g.xpar is current) consecutive exchanges
+  // alternate between two buffers, so a CTA still reading the previous result
+  // is never overwritten
   const int par = g.xpar;
-  count = block_sum<int32_t>(count);
-  mass = block_sum<unsigned long long>(mass);
   const int C = static_cast<int>(cl.num_blocks());
   if (threadIdx.x < C) {
     PartD d;
@@ -703,59 +879,109 @@ __device__ PartD exchange_d(float best, int32_t arg, int32_t count, unsigned lon
   PartD r = g_pd[par][0];
   for (int q = 1; q < C; ++q) {
     const PartD& o = g_pd[par][q];
-    if (beats(o.best, o.arg, r.best, r.arg)) {
+    if (SUMS) {
+      r.count += o.count;
+      r.mass += o.mass;
+    } else if (beats(o.best, o.arg, r.best, r.arg)) {
       r.best = o.best;
       r.arg = o.arg;
     }
-    r.count += o.count;
-    r.mass += o.mass;
   }
   return r;
 }
 
 // ---------------------------------------------------------------- passes --
 
+// The score of a token that passed the cheap noise bound: base + Gumbel
+// noise, base = y (the draw over K) or log(P - q) (the residual); -inf when
+// the residual is empty there or the token cannot beat `bs`.  Out of line:
+// most tokens never get here.
+template <bool RES>
+__device__ __noinline__ float draw_score(float y, int32_t t, uint32_t num, float ub, float m, float inv_s,
+                                         const float* qrow, float bs) {
+  float base = y;
+  if (RES) {
+    const float P = __fmul_rn(__expf(__fsub_rn(y, m)), inv_s);
+    const float r = __fsub_rn(P, qrow[t]);
+    if (!(r > 0.0f)) return ninf();
+    base = logf(r);
+    if (base + ub < bs) return ninf();
+  }
+  return __fadd_rn(base, gumbel_from_numerator(num));
+}
+
 // The draw over K (stream 0) or, with RES, over the residual
-// max(P - q, 0) (stream 2, log r + g); P(t) = exp(y - m) / S.  Returns this
-// thread's best (score, token); entries are visited by the CTA that owns
-// their token.
+// max(P - q, 0) (stream 2, log r + g); P(t) = exp(y - m) / S.  The CTA's
+// best (score, token) so far lives in g_dbest as one 64-bit key (score order
+// key, then the token's complement: the maximum is the best score, lowest
+// token among equals); every thread prunes against it, so a token whose
+// score bound is below the best of the whole CTA costs no logarithm.  g_dbest
+// must be 0 on entry (then a block barrier); cta_best() reads the result.
+// Entries are visited by the CTA that owns their token.
+__device__ __forceinline__ unsigned long long score_key(float s, int32_t t) {
+  return (static_cast<unsigned long long>(okey(s)) << 32) | static_cast<uint32_t>(~t);
+}
+
+__device__ __forceinline__ void cta_best(float& bs, int32_t& bt) {
+  __syncthreads();
+  const unsigned long long k = g_dbest;
+  bs = k ? okey_value(static_cast<uint32_t>(k >> 32)) : ninf();
+  bt = k ? static_cast<int32_t>(~static_cast<uint32_t>(k)) : 0x7fffffff;
+}
+
 template <bool RES>
 __device__ void draw_pass(const HArgs& a, float cv, int32_t ct, bool mp_on, float inv_s, float log_s,
-                          const float* qrow, const unsigned long long* ents, int n_ents, float& bs, int32_t& bt) {
+                          const float* qrow, const unsigned long long* ents, int n_ents) {
   const Ctx& c = g;
   const uint4* data = reinterpret_cast<const uint4*>(g_dyn);
   const uint16_t* vb = reinterpret_cast<const uint16_t*>(g_dyn + a.o_vb);
   const float inv_t = c.inv_t, m = c.m, lmp = c.lmp;
   const uint32_t k0 = c.seed_lo, k1 = c.seed_hi, pos = c.pos, rid = c.rowid;
   const uint32_t stream = RES ? 2u : 0u;
-  // the largest score a token of processed value y can reach
+  float bs = ninf();                 // a lower bound of the CTA's best score
+  unsigned long long mine = 0;       // this thread's best key
+  auto refresh = [&]() {
+    const unsigned long long k = *reinterpret_cast<volatile unsigned long long*>(&g_dbest);
+    if (k) bs = fmaxf(bs, okey_value(static_cast<uint32_t>(k >> 32)));
+  };
   auto reach = [&](float y) -> float {
     return RES ? (y - m - log_s + kGumbelMax + 1e-3f + fabsf(y) * 1e-6f) : (y + kGumbelMax);
   };
   auto member = [&](float y, int32_t t) -> bool {
     return y != ninf() && in_cut(y, t, cv, ct) && (!mp_on || __fsub_rn(y, m) >= lmp);
   };
+#ifdef SS_HIST_STAMPS
+  int n_score = 0, n_philox = 0, n_vec = 0;
+#endif
   auto consider = [&](float y, int32_t t, uint32_t word) {
     const uint32_t num = uniform_numerator(word);
-    float base = y;
-    if (RES) {
-      const float P = __fmul_rn(__expf(__fsub_rn(y, m)), inv_s);
-      const float r = __fsub_rn(P, qrow[t]);
-      if (!(r > 0.0f)) return;
-      base = logf(r);
-    }
-    if (base + gumbel_upper_bound(num) < bs) return;
-    const float s = __fadd_rn(base, gumbel_from_numerator(num));
-    if (beats(s, t, bs, bt)) {
-      bs = s;
-      bt = t;
+    const float ub = gumbel_upper_bound(num);
+    // an upper bound of the base (for the residual log r <= log P), before
+    // any logarithm or read of the draft's q
+    const float base_ub = RES ? (y - m - log_s + 1e-3f + fabsf(y) * 1e-6f) : y;
+    if (base_ub + ub < bs) return;
+#ifdef SS_HIST_STAMPS
+    ++n_score;
+#endif
+    const float s = draw_score<RES>(y, t, num, ub, m, inv_s, qrow, bs);
+    if (s > ninf()) {
+      const unsigned long long k = score_key(s, t);
+      if (k > mine) {
+        mine = k;
+        atomicMax(&g_dbest, k);
+        bs = fmaxf(bs, s);
+      }
     }
   };
   const int nvec = c.nvec;
   for (int v = threadIdx.x; v < nvec; v += kThreads) {
     const float vy = __fmul_rn(bf16_to_f(vb[v >> 1]), inv_t);
+    refresh();
     if (vy < cv || vy == ninf() || reach(vy) < bs) continue;
     if (mp_on && !(__fsub_rn(vy, m) >= lmp)) continue;
+#ifdef SS_HIST_STAMPS
+    ++n_vec;
+#endif
     const uint4 d = data[v];
     const uint32_t w[4] = {d.x, d.y, d.z, d.w};
     const int32_t t0 = c.lo + v * 8;
@@ -774,6 +1000,9 @@ __device__ void draw_pass(const HArgs& a, float cv, int32_t ct, bool mp_on, floa
       }
       if (!any) continue;
       const int32_t tq = t0 + half * 4;
+#ifdef SS_HIST_STAMPS
+      ++n_philox;
+#endif
       const Philox4 r = philox4x32_10(static_cast<uint32_t>(tq) >> 2, pos, rid, stream, k0, k1);
 #pragma unroll
       for (int e = 0; e < 4; ++e)
@@ -789,6 +1018,15 @@ __device__ void draw_pass(const HArgs& a, float cv, int32_t ct, bool mp_on, floa
     const Philox4 r = philox4x32_10(static_cast<uint32_t>(t) >> 2, pos, rid, stream, k0, k1);
     consider(y, t, r.w[t & 3]);
   }
+#ifdef SS_HIST_STAMPS
+  if (blockIdx.x < kStampCtas) {
+    if (threadIdx.x == 0) {
+      g_stamps[blockIdx.x][43] = n_vec;
+      g_stamps[blockIdx.x][44] = n_philox;
+      g_stamps[blockIdx.x][45] = n_score;
+    }
+  }
+#endif
 }
 
 // |K| and its fixed-point mass for rows whose K is a plain predicate (no
@@ -873,74 +1111,88 @@ __device__ __forceinline__ int first_entry_lt(const unsigned long long* el, int 
   return lo;
 }
 
+// The range of coarse group `grp` in every CTA's group-ordered entry list:
+// g_gr0[r] its start, g_grc[r] the entries of the group in CTAs before r
+// (g_grc[C] the total).  Called by all threads; ends with a block barrier.
+__device__ void group_ranges(const HArgs& a, int grp) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int C = static_cast<int>(cl.num_blocks());
+  const int32_t* eoff = reinterpret_cast<const int32_t*>(g_dyn + a.o_hist + kSlots * 2);
+  if (threadIdx.x < 32) {
+    const int r = threadIdx.x;
+    int32_t lo = 0, n = 0;
+    if (r < C) {
+      const int32_t* ro = cl.map_shared_rank(eoff, r);
+      lo = ro[grp];
+      n = ro[grp + 1] - lo;
+    }
+    int32_t inc = n;
+#pragma unroll
+    for (int o = 1; o < kMaxCluster; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (r >= o) inc += y;
+    }
+    if (r < C) {
+      g_gr0[r] = lo;
+      g_grc[r] = inc - n;
+    }
+    if (r == C - 1) g_grc[C] = inc;
+  }
+  __syncthreads();
+}
+
 // Reads the slot counts of coarse group `grp` from every CTA into g_fc, and
 // gathers the group's entries from every CTA's list into (gk, gp), sorted
-// (y desc, token asc); g.n_g is their number (-1 if more than kGatherCap).
-// The gather buffer is the exchange-2 region, free once the coarse sums are
-// read.  Called by all threads; ends with a block barrier.
+// (y desc, token asc) by rank; g.n_g is their number (-1 if more than
+// kGatherCap).  The entries are gathered unsorted into the merge region and
+// ranked into the exchange-2 region (free once the coarse sums are read).
+// Called by all threads; ends with a block barrier.
 __device__ void load_group(const HArgs& a, int grp) {
   cg::cluster_group cl = cg::this_cluster();
   const int C = static_cast<int>(cl.num_blocks());
   const int s0 = g_gb[grp], s1 = g_gb[grp + 1];
   const uint32_t* hist = reinterpret_cast<const uint32_t*>(g_dyn + a.o_hist);
   const unsigned long long* el = reinterpret_cast<const unsigned long long*>(g_dyn + a.o_el);
+  const int16_t* eord = reinterpret_cast<const int16_t*>(g_dyn + a.o_hist + kSlots * 2 + (kGroups + 2) * 4);
   unsigned long long* gk = reinterpret_cast<unsigned long long*>(g_dyn + a.o_xm);
   int16_t* gp = reinterpret_cast<int16_t*>(gk + kGatherCap);
-  __syncthreads();  // the previous readers of g_fc and of the buffer are done
-  if (threadIdx.x == 0) g.n_g = 0;
+  unsigned long long* uk = reinterpret_cast<unsigned long long*>(g_dyn + a.o_mg);
+  int16_t* up = reinterpret_cast<int16_t*>(uk + kGatherCap);
+  __syncthreads();  // the previous readers of g_fc and of the buffers are done
+  group_ranges(a, grp);
   for (int i = threadIdx.x; i < s1 - s0; i += kThreads) {
     uint32_t cnt = 0;
     const int q = s0 + i;
-    for (int r = 0; r < C; ++r) cnt += (*cl.map_shared_rank(hist + (q >> 1), r) >> ((q & 1) << 4)) & 0xffffu;
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < C) cnt += (*cl.map_shared_rank(hist + (q >> 1), r) >> ((q & 1) << 4)) & 0xffffu;
     g_fc[i] = cnt;
   }
-  __syncthreads();
-  // every (CTA, entry) pair: the entries of this group, appended
-  const int total = g_goff[C];
-  for (int i = threadIdx.x; i < total; i += kThreads) {
-    int r = 0;
-    while (i >= g_goff[r + 1]) ++r;
-    const int e = i - g_goff[r];
-    const int16_t p = *cl.map_shared_rank(g_epos + e, r);
-    if (group_of(p) != grp) continue;
-    const int at = atomicAdd(&g.n_g, 1);
-    if (at < kGatherCap) {
-      gk[at] = *cl.map_shared_rank(el + e, r);
-      gp[at] = p;
-    }
-  }
-  __syncthreads();
-  const int n = g.n_g;
-  __syncthreads();
+  const int n = g_grc[C];
   if (n > kGatherCap) {
+    __syncthreads();
     if (threadIdx.x == 0) g.n_g = -1;
     __syncthreads();
     return;
   }
-  if (n > 1) {
-    int np2 = 1;
-    while (np2 < n) np2 <<= 1;
-    for (int i = n + threadIdx.x; i < np2; i += kThreads) {
-      gk[i] = ~0ull;
-      gp[i] = 0x7fff;
-    }
-    __syncthreads();
-    for (int k = 2; k <= np2; k <<= 1)
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int q = threadIdx.x; q < (np2 >> 1); q += kThreads) {
-          const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1));
-          const unsigned long long x = gk[i], y = gk[i + j];
-          if ((x > y) == ((i & k) == 0)) {
-            gk[i] = y;
-            gk[i + j] = x;
-            const int16_t t = gp[i];
-            gp[i] = gp[i + j];
-            gp[i + j] = t;
-          }
-        }
-        __syncthreads();
-      }
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    int r = 0;
+    while (i >= g_grc[r + 1]) ++r;
+    const int e = *cl.map_shared_rank(eord + g_gr0[r] + (i - g_grc[r]), r);
+    uk[i] = *cl.map_shared_rank(el + e, r);
+    up[i] = *cl.map_shared_rank(g_epos + e, r);
   }
+  __syncthreads();
+  // rank sort: the keys are distinct (one entry per token)
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const unsigned long long k = uk[i];
+    int rk = 0;
+    for (int j = 0; j < n; ++j) rk += (uk[j] < k) ? 1 : 0;
+    gk[rk] = k;
+    gp[rk] = up[i];
+  }
+  if (threadIdx.x == 0) g.n_g = n;
+  __syncthreads();
 }
 
 // Where the running count (by_mass = 0) or mass (1) of the items first
@@ -965,11 +1217,13 @@ __device__ void locate(const HArgs& a, int by_mass, unsigned long long target) {
   if (c.w_found != 1) return;
   const int grp = c.pick;
   load_group(a, grp);
+  SS_STAMP(28);
   if (c.n_g < 0) {
     if (threadIdx.x == 0) c.w_found = -1;
     __syncthreads();
     return;
   }
+  if (threadIdx.x == 0) c.w_grp = grp;
   const unsigned long long* gk = reinterpret_cast<const unsigned long long*>(g_dyn + a.o_xm);
   const int16_t* gp = reinterpret_cast<const int16_t*>(gk + kGatherCap);
   const int s0 = g_gb[grp], ns = g_gb[grp + 1] - s0, ng = c.n_g;
@@ -997,6 +1251,7 @@ __device__ void locate(const HArgs& a, int by_mass, unsigned long long target) {
     g_mc[at] = static_cast<uint32_t>(cnt);
   }
   __syncthreads();
+  SS_STAMP(29);
   const unsigned long long before_c = c.w_cc, before_m = c.w_cm;
   // block prefix: kItemsPer merged items per thread, in order
   constexpr int kItemsPer = (kFineMax + kGatherCap + kThreads - 1) / kThreads;
@@ -1011,6 +1266,7 @@ __device__ void locate(const HArgs& a, int by_mass, unsigned long long target) {
   }
   unsigned long long ic = tc, im = tm, totc, totm;
   block_scan2(ic, im, &totc, &totm);
+  SS_STAMP(30);
   // the first item whose running total reaches the target
   unsigned long long rc = before_c + ic - tc, rm = before_m + im - tm;
   if (threadIdx.x == 0) c.pick = 0x7fffffff;
@@ -1118,16 +1374,24 @@ __device__ void above_value(const HArgs& a, float v) {
 // verification needs it for the draft token).  Sets g.cut_t, the cutoff that
 // this CTA applies (-1: none of its items of value v, 0x7fffffff: all).
 // Called by all threads of every CTA.
-__device__ void resolve_ties(const HArgs& a, float v, unsigned long long take, bool broadcast) {
+__device__ void resolve_ties(const HArgs& a, float v, unsigned long long take, int grp, bool broadcast) {
   Ctx& c = g;
   cg::cluster_group cl = cg::this_cluster();
   const int C = static_cast<int>(cl.num_blocks());
   const int rank = static_cast<int>(cl.block_rank());
   const uint32_t* hist = reinterpret_cast<const uint32_t*>(g_dyn + a.o_hist);
   const unsigned long long* el = reinterpret_cast<const unsigned long long*>(g_dyn + a.o_el);
-  // per-CTA counts of the items of value v: its run of slots and its entries
+  const int16_t* eord = reinterpret_cast<const int16_t*>(g_dyn + a.o_hist + kSlots * 2 + (kGroups + 2) * 4);
+  if (take == 0) {  // none of them (the same in every CTA)
+    __syncthreads();
+    if (threadIdx.x == 0) c.cut_t = -1;
+    __syncthreads();
+    return;
+  }
+  // per-CTA counts of the items of value v: its run of slots, and its
+  // entries of v (all in coarse group grp)
   if (threadIdx.x < C) g_rtie[threadIdx.x] = 0;
-  __syncthreads();
+  group_ranges(a, grp);
   if (threadIdx.x < C) {
     const int r = threadIdx.x;
     uint32_t n = 0;
@@ -1135,11 +1399,12 @@ __device__ void resolve_ties(const HArgs& a, float v, unsigned long long take, b
       n += (*cl.map_shared_rank(hist + (q >> 1), r) >> ((q & 1) << 4)) & 0xffffu;
     atomicAdd(&g_rtie[r], n);
   }
-  const int total_e = g_goff[C];
+  const int total_e = g_grc[C];
   for (int i = threadIdx.x; i < total_e; i += kThreads) {
     int r = 0;
-    while (i >= g_goff[r + 1]) ++r;
-    if (ekey_y(*cl.map_shared_rank(el + (i - g_goff[r]), r)) == v) atomicAdd(&g_rtie[r], 1u);
+    while (i >= g_grc[r + 1]) ++r;
+    const int e = *cl.map_shared_rank(eord + g_gr0[r] + (i - g_grc[r]), r);
+    if (ekey_y(*cl.map_shared_rank(el + e, r)) == v) atomicAdd(&g_rtie[r], 1u);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -1147,9 +1412,7 @@ __device__ void resolve_ties(const HArgs& a, float v, unsigned long long take, b
     for (int r = 0; r < C; ++r) total += g_rtie[r];
     c.tie_rank = C;  // all of them
     c.tie_local = 0;
-    if (take == 0) {
-      c.tie_rank = -1;
-    } else if (take < total) {
+    if (take < total) {
       for (int r = 0; r < C; ++r) {
         if (before + g_rtie[r] >= take) {
           c.tie_rank = r;
@@ -1282,8 +1545,16 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   uint32_t* hraw = reinterpret_cast<uint32_t*>(hval + kHashCap);  // raw bf16 bits | allowed << 16
 
   SS_STAMP(0);
-  if (tid == 0) decode_and_copy(a, task, rank);
+  // the parameter loads go out before the bulk copies (a global load issued
+  // after 16 KB copies of every CTA waits behind them)
+  if (tid < 32) {
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    if (tid == 0) decode_and_copy(a, task, rank);
+  } else if (tid < 64) {
+    load_params(a, task);
+  }
   __syncthreads();
+  SS_STAMP(17);
   if (!c.valid) return;  // the same for the whole cluster
   if (c.bad_k) {
     // a draft count outside [0, max_draft]: the request's outputs, from its
@@ -1297,14 +1568,21 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     }
     return;
   }
-  if (tid == 0) read_params(a);
+  int32_t rej_seen = 0;  // thread 0: the rejection word, read early (used at exchange 1)
+  if (tid == 0) {
+    c.status = max(c.status, c.pstatus);
+    if (a.mode == 1) rej_seen = ld_cg_s32(a.ws_counters + c.nreq + c.req);
+  }
+  SS_STAMP(19);
   for (int s = tid; s < kHashCap; s += kThreads) {
     hkey[s] = -1;
     hcnt[s] = 0;
     hval[s] = 0.0f;
     hraw[s] = 0;
   }
+  if (tid < kCertBins) g_cert[tid] = 0;
   __syncthreads();
+  SS_STAMP(20);
   const int32_t V = a.vocab, lo = c.lo, n = c.n;
   const uint16_t* row = a.logits + c.row_off;
   const int words = a.slice / 32;
@@ -1321,6 +1599,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       pbits[w] = 0;
     }
   }
+  SS_STAMP(21);
   // tokens past the bulk copies: plain loads; padding past the row: -inf
   {
     uint16_t* d16 = reinterpret_cast<uint16_t*>(g_dyn);
@@ -1328,6 +1607,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     for (int e = from + tid; e < c.nvec * 8; e += kThreads) d16[e] = (e < n) ? row[lo + e] : 0xff80u;
   }
   __syncthreads();
+  SS_STAMP(18);
   // patched tokens: the table, the patched bits, and (from the first insert of
   // each) whether the mask allows it; its staged copy is excluded
   int st = c.status;
@@ -1337,8 +1617,8 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     const uint32_t bit = 1u << ((t - lo) & 31);
     const int w = (t - lo) >> 5;
     if (!(atomicOr(pbits + w, bit) & bit)) {
-      atomicAdd(&c.npatch, 1);
-      if (atomicAnd(xm + w, ~bit) & bit) atomicOr(hraw + s, 1u << 16);
+      c.npatch = 1;  // a flag: some token of the slice is patched
+      if (xm[w] & bit) atomicOr(hraw + s, 1u << 16);
     }
   };
   if (row_ok) {
@@ -1395,16 +1675,16 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   }
   if (st != SS_ROW_OK) atomicMax(&c.status, st);
   __syncthreads();
-  if (tid == 0) c.has_excl = c.use_mask || c.npatch > 0;
+  if (tid == 0) c.has_excl = c.use_mask;
   __syncthreads();
   SS_STAMP(1);
 
   // -------------------------------------------------- staging pass
+  // Patched tokens stay as staged here; the fix-up after the compaction
+  // excludes them and mends their pairs' bounds.
   const bool excl = c.has_excl != 0, tiny = c.need_hist != 0;
   const float inv_t = c.inv_t;
   uint32_t run = kNegInfPair;
-  float gbest = ninf();  // greedy: this thread's largest vector maximum and its first vector
-  int gvec = 0x7fffffff;
   bool timed_out = false;
   {
     const uint8_t* xb = reinterpret_cast<const uint8_t*>(xm);
@@ -1422,20 +1702,15 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           for (int q = waited + 1; q <= ch; ++q)
             if (!mbar_wait_bounded(mbar + q, 0, kWaitPolls)) timed_out = true;
           waited = ch;
+          if (ch == 0) SS_STAMP(22);
+          if (ch == 1) SS_STAMP(32);
+          if (ch == 2) SS_STAMP(33);
+          if (ch == 3) SS_STAMP(34);
         }
       }
       uint4 d = act ? data[v] : make_uint4(kNegInfPair, kNegInfPair, kNegInfPair, kNegInfPair);
       bool dirty = false;
       if (excl && act) {
-        const uint32_t P = pb[v];
-        if (P) {  // the raw logits of the patched tokens, into the table
-          const uint32_t w[4] = {d.x, d.y, d.z, d.w};
-          for (int e = 0; e < 8; ++e)
-            if ((P >> e) & 1u) {
-              const int s = patch_find(hkey, lo + v * 8 + e);
-              if (s >= 0) hraw[s] |= (w[e >> 1] >> ((e & 1) ? 16 : 0)) & 0xffffu;
-            }
-        }
         const uint32_t A = xb[v];
         if (A != 0xffu) {
           d = apply_allow(d, A);
@@ -1445,12 +1720,14 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       if (tiny) {
         const uint32_t tm = tiny_pair(d.x) | (tiny_pair(d.y) >> 1) | (tiny_pair(d.z) >> 2) | (tiny_pair(d.w) >> 3);
         if (tm && act) {
+          // tiny values move to the entries (patched ones are the fix-up's)
           uint32_t w[4] = {d.x, d.y, d.z, d.w};
+          const uint32_t P = pb[v];
           for (int e = 0; e < 8; ++e) {
             const uint32_t sh = (e & 1) ? 16u : 0u;
             const uint32_t h = (w[e >> 1] >> sh) & 0xffffu;
             const uint32_t aa = h & 0x7fffu;
-            if (aa != 0 && aa < kTinyA) {
+            if (aa != 0 && aa < kTinyA && !((P >> e) & 1u)) {
               add_entry(el, c.greedy ? bf16_to_f(h) : __fmul_rn(bf16_to_f(h), inv_t), lo + v * 8 + e);
               w[e >> 1] = (w[e >> 1] & ~(0xffffu << sh)) | (0xff80u << sh);
             }
@@ -1467,12 +1744,8 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       const uint32_t other = __shfl_xor_sync(0xffffffffu, mh, 1);
       if (act && !(v & 1)) vb[v >> 1] = static_cast<uint16_t>(bmax2(mh, other) & 0xffffu);
       run = bmax2(run, mx);
-      const float vm = bf16_to_f(mh);
-      if (act && vm > gbest) {
-        gbest = vm;
-        gvec = v;
-      }
     }
+    SS_STAMP(23);
     if (tid == 0)
       for (int q = waited + 1; q < c.nch; ++q)
         if (!mbar_wait_bounded(mbar + q, 0, kWaitPolls)) timed_out = true;
@@ -1482,25 +1755,61 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   SS_STAMP(11);
   // processed values of the patched tokens: exact entries (penalties, bias,
   // mask, temperature, each an individually rounded fp32 operation)
+  // (every warp runs the loop uniformly: one entry-counter atomic per warp)
   for (int s = tid; s < kHashCap; s += kThreads) {
     const int32_t t = hkey[s];
-    if (t < 0) continue;
-    const uint32_t raw = hraw[s];
-    float z = bf16_to_f(raw & 0xffffu);
-    const int32_t hc = hcnt[s];
-    const int32_t cnt = hc & ~kBiasFlag;
-    if (cnt > 0) {
-      z = (z > 0.0f) ? __fdiv_rn(z, c.rep) : __fmul_rn(z, c.rep);
-      z = __fsub_rn(z, __fmul_rn(c.freq, static_cast<float>(cnt)));
-      z = __fsub_rn(z, c.pres);
+    float y = ninf();
+    if (t >= 0) {
+      const uint32_t raw = hraw[s] | reinterpret_cast<const uint16_t*>(g_dyn)[t - lo];
+      float z = bf16_to_f(raw & 0xffffu);
+      const int32_t hc = hcnt[s];
+      const int32_t cnt = hc & ~kBiasFlag;
+      if (cnt > 0) {
+        z = (z > 0.0f) ? __fdiv_rn(z, c.rep) : __fmul_rn(z, c.rep);
+        z = __fsub_rn(z, __fmul_rn(c.freq, static_cast<float>(cnt)));
+        z = __fsub_rn(z, c.pres);
+      }
+      if (hc & kBiasFlag) z = __fadd_rn(z, hval[s]);
+      y = !(raw >> 16) ? ninf() : (c.greedy ? z : __fmul_rn(z, c.inv_t));
+      hval[s] = y;  // kept for the draft-token lookup and the debug output
+      if (y != y || y == pinf()) {
+        atomicMax(&c.status, SS_ROW_NONFINITE);
+        y = ninf();
+      }
     }
-    if (hc & kBiasFlag) z = __fadd_rn(z, hval[s]);
-    const float y = !(raw >> 16) ? ninf() : (c.greedy ? z : __fmul_rn(z, c.inv_t));
-    hval[s] = y;  // kept for the draft-token lookup and the debug output
-    if (y != y || y == pinf()) atomicMax(&c.status, SS_ROW_NONFINITE);
-    else if (y != ninf()) add_entry(el, y, t);
+    const bool add = y != ninf();
+    const uint32_t ball = __ballot_sync(0xffffffffu, add);
+    if (ball) {
+      const int lane = tid & 31;
+      int base = 0;
+      if (lane == __ffs(ball) - 1) base = atomicAdd(&c.nent, __popc(ball));
+      base = __shfl_sync(0xffffffffu, base, __ffs(ball) - 1);
+      if (add) {
+        const int i = base + __popc(ball & ((1u << lane) - 1u));
+        if (i < kEntCap)
+          el[i] = ekey(y, t);
+        else
+          atomicMax(&c.status, SS_ROW_LIMIT);
+      }
+    }
   }
   __syncthreads();
+  // fix-up: the patched tokens' staged copies are excluded (they are
+  // entries now), then the bounds of their 16-token pairs are recomputed
+  if (c.npatch) {
+    uint16_t* d16 = reinterpret_cast<uint16_t*>(g_dyn);
+    for (int s = tid; s < kHashCap; s += kThreads)
+      if (hkey[s] >= 0) d16[hkey[s] - lo] = 0xff80u;
+    __syncthreads();
+    for (int s = tid; s < kHashCap; s += kThreads)
+      if (hkey[s] >= 0) {
+        const int pr = (hkey[s] - lo) >> 4;
+        const uint4 d0 = data[2 * pr], d1 = data[2 * pr + 1];
+        const uint32_t mx = bmax2(bmax2(bmax2(d0.x, d0.y), bmax2(d0.z, d0.w)), bmax2(bmax2(d1.x, d1.y), bmax2(d1.z, d1.w)));
+        vb[pr] = static_cast<uint16_t>(bmax2(mx, mx >> 16) & 0xffffu);
+      }
+    __syncthreads();
+  }
   SS_STAMP(2);
 
   // -------------------------------------------------- debug output
@@ -1520,29 +1829,46 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
 
   // -------------------------------------------------- exchange 1
   {
-    const uint32_t rmax = bmax2(run, run >> 16) & 0xffffu;
-    const float zmax = block_max_nan(bf16_to_f(rmax));
+    // one reduction: the CTA's largest staged value with the first pair
+    // holding it (a NaN anywhere counts as +inf: the row is non-finite
+    // either way), and its largest entry (lowest token among equals)
+    float gbest = ninf();
+    int gvec = 0x7fffffff;  // the first pair holding it
+    for (int p = tid; p < c.nvec / 2; p += kThreads) {
+      const float vm = bf16_to_f(vb[p]);
+      if (vm > gbest) {
+        gbest = vm;
+        gvec = p;
+      }
+    }
+    if ((bmax2(run, run >> 16) & 0x7fffu) > 0x7f80u) {
+      gbest = pinf();
+      gvec = 0;
+    }
+    float es = ninf();
+    int32_t et = 0x7fffffff;
+    const int ne = min(c.nent, kEntCap);
+    for (int i = tid; i < ne; i += kThreads) {
+      const float y = ekey_y(el[i]);
+      const int32_t t = ekey_t(el[i]);
+      if (beats(y, t, es, et)) {
+        es = y;
+        et = t;
+      }
+    }
+    block_best2(gbest, gvec, es, et);
+    const float zmax = gbest;
     SS_STAMP(12);
     // greedy: lowest index of the CTA's largest staged value
     int32_t garg = 0x7fffffff;
-    if (c.greedy) {
-      float s = (gbest == zmax) ? 0.0f : ninf();
-      int32_t t = (gbest == zmax) ? gvec : 0x7fffffff;
-      block_best(s, t);  // smallest vector index among those holding the maximum
-      if (t != 0x7fffffff && tid == 0) {
-        const uint4 d = data[t];
-        const uint32_t w[4] = {d.x, d.y, d.z, d.w};
-        for (int e = 7; e >= 0; --e) {
-          const uint32_t h = (w[e >> 1] >> ((e & 1) ? 16 : 0)) & 0xffffu;
-          if (bf16_to_f(h) == zmax) garg = lo + t * 8 + e;
-        }
-      }
+    if (c.greedy && gvec != 0x7fffffff && zmax != pinf() && tid == 0) {
+      const uint16_t* d16 = reinterpret_cast<const uint16_t*>(g_dyn) + gvec * 16;
+      for (int e = 15; e >= 0; --e)
+        if (bf16_to_f(d16[e]) == zmax) garg = lo + gvec * 16 + e;
     }
     // top-k rows: pairs per binade below this CTA's maximum (the certificate)
     const uint32_t zbin = key16(__float_as_uint(zmax) >> 16) >> 7;
     if (c.k_on) {
-      if (tid < kCertBins) g_cert[tid] = 0;
-      __syncthreads();
       const int lane = tid & 31;
       for (int p0 = 0; p0 < c.nvec / 2; p0 += kThreads) {
         const int p = p0 + tid;
@@ -1563,19 +1889,6 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         }
       }
     }
-    // largest entry (lowest token among equals)
-    float es = ninf();
-    int32_t et = 0x7fffffff;
-    const int ne = min(c.nent, kEntCap);
-    for (int i = tid; i < ne; i += kThreads) {
-      const float y = ekey_y(el[i]);
-      const int32_t t = ekey_t(el[i]);
-      if (beats(y, t, es, et)) {
-        es = y;
-        et = t;
-      }
-    }
-    block_best(es, et);
     // the draft token's processed value, in the CTA that owns it
     float xy = ninf();
     int32_t xhere = 0;
@@ -1594,6 +1907,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         }
       }
     }
+    if (c.k_on) __syncthreads();  // the certificate counts are complete
     if (tid == 0) {
       Part1& p = g_mine;
       p.zmax = zmax;
@@ -1610,6 +1924,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       p.xy = xy;
       p.xhere = xhere;
       p.zbin = static_cast<int32_t>(zbin);
+      p.rej = rej_seen;
       for (int b = 0; b < kCertBins; ++b) p.cert[b] = c.k_on ? g_cert[b] : 0u;
     }
     __syncthreads();
@@ -1643,6 +1958,11 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           const Part1& p = g_p1[r];
           if (fmaxf(p.zmax, p.emax) == m && p.arg < arg) arg = p.arg;
         }
+      if (a.mode == 1) {
+        int32_t rj = 0;
+        for (int r = 0; r < C; ++r) rj = max(rj, g_p1[r].rej);
+        c.skip_draw = rj > kRejBase - c.j;  // the same in every CTA
+      }
       c.tau_key = 0;
       c.pick = zb;
       c.arg = arg;
@@ -1698,6 +2018,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         const float P = (c.x == c.arg) ? 1.0f : 0.0f;
         accept = (__fmul_rn(u, q) < P) ? 1 : 0;
         token = accept ? c.x : c.arg;
+        if (!accept && rank == 0 && tid == 0) atomicMax(a.ws_counters + c.nreq + c.req, kRejBase - c.j);
       }
     } else {
       float cv = ninf();
@@ -1705,7 +2026,12 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       bool mp_on = c.mp_on != 0;
       if (c.need_hist) {
         // ---------------------------------------------- histogram
-        if (tid == 0) c.M = make_slot_map(c.zmax);
+        if (tid == 0) {
+          c.M = make_slot_map(c.zmax);
+          c.ntot = 0;
+          c.stot = 0;
+          c.fail_loc = 0;
+        }
         for (int s = tid; s < kSlots / 2; s += kThreads) hist[s] = 0;
         if (tid <= kGroups) {
           g_ecnt[tid] = 0;
@@ -1720,6 +2046,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           g_gb[tid] = (tid == kGroups) ? M.ns : b;
           if (tid == kGroups) g_gb[kGroups + 1] = M.ns;  // the tail group: entries only
         }
+        SS_STAMP(27);
         // candidates: top-k rows the tokens at or above the certificate;
         // top-p rows the tokens with a non-zero fixed-point mass
         const uint32_t tau = c.tau_key;
@@ -1743,21 +2070,65 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         }
         __syncthreads();  // group bounds and histogram complete
         SS_STAMP(4);
-        // slot position and group of every local entry
-        for (int e = tid; e < c.ne; e += kThreads) {
-          const float y = ekey_y(el[e]);
-          const int32_t p = first_slot_le(y, 0, M.ns);
-          g_epos[e] = static_cast<int16_t>(p);
-          const int q = group_of(p);
-          atomicAdd(&g_ecnt[q], 1u);
-          atomicAdd(&g_emass[q], fmass(y, c.m));
+        // slot position and group of every local entry, its place within the
+        // group (the list is then ordered by group: every CTA reads one
+        // group's entries of another CTA as one range), and for min-p the
+        // largest entry failing the test
+        int32_t* eoff = reinterpret_cast<int32_t*>(g_dyn + a.o_hist + kSlots * 2);
+        int16_t* eord = reinterpret_cast<int16_t*>(eoff + (kGroups + 2));
+        int eq[kEntCap / kThreads], er[kEntCap / kThreads];
+        uint32_t fk = 0;  // min-p: the largest failing entry key of this thread
+#pragma unroll
+        for (int k = 0; k < kEntCap / kThreads; ++k) {
+          const int e = tid + k * kThreads;
+          eq[k] = -1;
+          if (e < c.ne) {
+            const float y = ekey_y(el[e]);
+            const int32_t p = first_slot_le(y, 0, M.ns);
+            g_epos[e] = static_cast<int16_t>(p);
+            const int q = group_of(p);
+            eq[k] = q;
+            er[k] = static_cast<int>(atomicAdd(&g_ecnt[q], 1u));
+            atomicAdd(&g_emass[q], fmass(y, c.m));
+            if (mp_on && !(__fsub_rn(y, c.m) >= c.lmp)) fk = max(fk, okey(y));
+          }
+        }
+        if (mp_on) {  // one atomic per warp
+          fk = __reduce_max_sync(0xffffffffu, fk);
+          if ((tid & 31) == 0 && fk) atomicMax(&c.fail_loc, fk);
         }
         __syncthreads();
+        SS_STAMP(24);
+        if (tid < 32) {  // group offsets of the ordered list
+          constexpr int kPer = (kGroups + 1 + 31) / 32;
+          int32_t loc[kPer], sum = 0;
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) {
+            const int q = tid * kPer + i;
+            loc[i] = (q <= kGroups) ? static_cast<int32_t>(g_ecnt[q]) : 0;
+            sum += loc[i];
+          }
+          int32_t inc = sum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (tid >= o) inc += y;
+          }
+          int32_t run_off = inc - sum;
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) {
+            const int q = tid * kPer + i;
+            if (q <= kGroups) eoff[q] = run_off;
+            run_off += loc[i];
+          }
+          if (tid == 31) eoff[kGroups + 1] = inc;
+        }
         // coarse counts and masses of this CTA (slots and entries), pushed to
         // every CTA (exchange 2); the tail group also carries the count of
-        // uncounted tokens below the slots
-        uint32_t* pc = xm;  // [C][kGroups + 1] counts, then masses
+        // uncounted tokens below the slots, and each CTA its min-p fail key
+        uint32_t* pc = xm;  // [C][kGroups + 1] counts, then masses, then fail keys
         unsigned long long* pm = reinterpret_cast<unsigned long long*>(xm + ((kMaxCluster * (kGroups + 1) + 1) & ~1));
+        uint32_t* pf = reinterpret_cast<uint32_t*>(pm + kMaxCluster * (kGroups + 1));
         {
           const int grp = tid >> 3, sub = tid & 7;  // 8 threads per group
           uint32_t cnt = 0;
@@ -1776,7 +2147,12 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           }
           cnt += g_ecnt[grp];
           mass += g_emass[grp];
-          const uint32_t bsum = block_sum<uint32_t>(below);
+          SS_STAMP(25);
+          const uint32_t bsum = block_sum<uint32_t>(below);  // (a block barrier: eoff is complete)
+          SS_STAMP(26);
+#pragma unroll
+          for (int k = 0; k < kEntCap / kThreads; ++k)
+            if (eq[k] >= 0) eord[eoff[eq[k]] + er[k]] = static_cast<int16_t>(tid + k * kThreads);
           if (sub < C) {
             *cl.map_shared_rank(pc + rank * (kGroups + 1) + grp, sub) = cnt;
             *cl.map_shared_rank(pm + rank * (kGroups + 1) + grp, sub) = mass;
@@ -1787,27 +2163,42 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
             *cl.map_shared_rank(pc + rank * (kGroups + 1) + kGroups, tid) = g_ecnt[kGroups];
             *cl.map_shared_rank(pm + rank * (kGroups + 1) + kGroups, tid) =
                 (g_emass[kGroups] & 0x00ffffffffffffffull) | (static_cast<unsigned long long>(min(bsum, 255u)) << 56);
+            *cl.map_shared_rank(pf + rank, tid) = c.fail_loc;
           }
         }
         SS_STAMP(15);
         cl.sync();
         SS_STAMP(16);
-        if (tid <= kGroups) {
+        if (tid < 96) {  // the groups, and (warp-reduced) their totals
           uint32_t cnt = 0;
           unsigned long long mass = 0, bel = 0;
-          for (int r = 0; r < C; ++r) {
-            cnt += pc[r * (kGroups + 1) + tid];
-            const unsigned long long mm = pm[r * (kGroups + 1) + tid];
-            if (tid == kGroups) {
-              bel += mm >> 56;
-              mass += mm & 0x00ffffffffffffffull;
-            } else {
-              mass += mm;
+          if (tid <= kGroups) {
+            for (int r = 0; r < C; ++r) {
+              cnt += pc[r * (kGroups + 1) + tid];
+              const unsigned long long mm = pm[r * (kGroups + 1) + tid];
+              if (tid == kGroups) {
+                bel += mm >> 56;
+                mass += mm & 0x00ffffffffffffffull;
+              } else {
+                mass += mm;
+              }
             }
+            if (tid == kGroups) {
+              c.below = bel;  // uncounted tokens below the slots (saturating per CTA)
+              uint32_t fk = 0;
+              for (int r = 0; r < C; ++r) fk = max(fk, pf[r]);
+              c.fail_key = fk;
+            }
+            g_gcnt[tid] = cnt;
+            g_gmass[tid] = mass;
           }
-          if (tid == kGroups) c.below = bel;  // uncounted tokens below the slots (saturating per CTA)
-          g_gcnt[tid] = cnt;
-          g_gmass[tid] = mass;
+          const uint32_t wc = __reduce_add_sync(0xffffffffu, cnt);
+#pragma unroll
+          for (int o = 16; o; o >>= 1) mass += __shfl_xor_sync(0xffffffffu, mass, o);
+          if ((tid & 31) == 0) {
+            atomicAdd(&c.ntot, static_cast<unsigned long long>(wc));
+            atomicAdd(&c.stot, mass);
+          }
         }
         __syncthreads();
         SS_STAMP(5);
@@ -1818,6 +2209,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         bool unknown = false;
         float bv = ninf();                     // best (shortest) cut so far
         unsigned long long btake = 0, bcc = 0, bcm = 0;
+        int bgrp = 0;
         bool have_cut = false;
         unsigned long long Sk = 0;
         if (c.k_on) {
@@ -1829,12 +2221,9 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
             btake = c.w_take;
             bcc = c.w_cc;
             bcm = c.w_cm;
+            bgrp = c.w_grp;
             Sk = bcm + btake * fmass(bv, c.m);
           }
-          SS_TRACE(19, c.tau_key);
-          SS_TRACE(20, __float_as_uint(bv));
-          SS_TRACE(21, btake | (bcc << 32));
-          SS_TRACE(22, c.pick);
         }
         if (!have_cut && !unknown) {
           // every item (top-k off or larger than the item count): all must
@@ -1842,13 +2231,8 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           if ((c.below || (c.k_on && c.tau_key)) &&
               (c.k_on || M.ns == 0 || __fmul_rn(slot_z(M, M.ns - 1), inv_t) > skip))
             unknown = true;
-          Sk = 0;
-          for (int q = 0; q <= kGroups; ++q) Sk += g_gmass[q];
-          if (tid == 0) {
-            unsigned long long cnt = 0;
-            for (int q = 0; q <= kGroups; ++q) cnt += g_gcnt[q];
-            c.kcount = cnt;
-          }
+          Sk = c.stot;
+          if (tid == 0) c.kcount = c.ntot;
         }
         SS_STAMP(6);
         if (c.p_on && !unknown) {
@@ -1861,21 +2245,12 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
             btake = c.w_take;
             bcc = c.w_cc;
             bcm = c.w_cm;
+            bgrp = c.w_grp;
           }
         }
         if (c.mp_on && !unknown) {
           // the largest value failing the min-p test: among the slots (they
           // fall monotonically) and every CTA's entries
-          if (tid == 0) c.fail_key = 0;
-          __syncthreads();
-          const int total_e = g_goff[C];
-          for (int i = tid; i < total_e; i += kThreads) {
-            int r = 0;
-            while (i >= g_goff[r + 1]) ++r;
-            const float y = ekey_y(*cl.map_shared_rank(el + (i - g_goff[r]), r));
-            if (!(__fsub_rn(y, c.m) >= c.lmp)) atomicMax(&c.fail_key, okey(y));
-          }
-          __syncthreads();
           if (tid == 0) {
             int lo_s = 0, hi_s = M.ns;
             while (lo_s < hi_s) {
@@ -1894,7 +2269,6 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           }
           __syncthreads();
           const float vf = c.w_v;
-          SS_TRACE(23, __float_as_uint(vf) | (static_cast<unsigned long long>(__float_as_uint(c.m)) << 32));
           if (c.pick) unknown = true;
           if (!unknown && vf != ninf() && (!have_cut || vf > bv || (vf == bv && btake > 0))) {
             above_value(a, vf);
@@ -1919,7 +2293,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
             c.kmass = bcm + btake * fmass(bv, c.m);
           }
           __syncthreads();
-          resolve_ties(a, bv, btake, tests_draft);
+          resolve_ties(a, bv, btake, bgrp, tests_draft);
           cv = c.cut_v;
           ct = c.cut_t;
         } else {
@@ -1936,7 +2310,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           int32_t cnt = 0;
           unsigned long long mass = 0;
           count_pass(a, tests_draft, ents, n_ents, cnt, mass);
-          const PartD r = exchange_d(ninf(), 0x7fffffff, cnt, mass);
+          const PartD r = exchange_d<true, false>(ninf(), 0x7fffffff, cnt, mass);
           if (tid == 0) {
             c.kcount = static_cast<unsigned long long>(r.count);
             c.kmass = r.mass;
@@ -1956,24 +2330,36 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           const float q = qrow[c.x];
           const float u = uniform_from_numerator(uniform_numerator(philox4x32_10(0u, c.pos, c.rowid, 1u, k0, k1).w[0]));
           accept = (__fmul_rn(u, q) < Px) ? 1 : 0;
+          if (!accept && rank == 0 && tid == 0) atomicMax(a.ws_counters + c.nreq + c.req, kRejBase - c.j);
           if (accept) {
             token = c.x;
+          } else if (c.skip_draw) {
+            token = -1;  // an earlier position rejected: this draw is never used
           } else {
-            float bs = ninf();
-            int32_t bt = 0x7fffffff;
-            draw_pass<true>(a, cv, ct, mp_on, inv_s, logf(SK), qrow, ents, n_ents, bs, bt);
-            const PartD r = exchange_d(bs, bt, 0, 0);
+            float bs;
+            int32_t bt;
+            if (tid == 0) g_dbest = 0;
+            __syncthreads();
+            draw_pass<true>(a, cv, ct, mp_on, inv_s, logf(SK), qrow, ents, n_ents);
+            cta_best(bs, bt);
+            const PartD r = exchange_d<false, true>(bs, bt, 0, 0);
             if (r.arg != 0x7fffffff && r.best > ninf())
               token = r.arg;
             else
               need_draw = true;  // an empty residual (rounding): the stream-0 draw
           }
         }
-        if (need_draw) {
-          float bs = ninf();
-          int32_t bt = 0x7fffffff;
-          draw_pass<false>(a, cv, ct, mp_on, 0.0f, 0.0f, nullptr, ents, n_ents, bs, bt);
-          const PartD r = exchange_d(bs, bt, 0, 0);
+        if (need_draw && c.skip_draw) {
+          token = -1;
+        } else if (need_draw) {
+          float bs;
+          int32_t bt;
+          if (tid == 0) g_dbest = 0;
+          __syncthreads();
+          draw_pass<false>(a, cv, ct, mp_on, 0.0f, 0.0f, nullptr, ents, n_ents);
+          SS_STAMP(36);
+          cta_best(bs, bt);
+          const PartD r = exchange_d<false, true>(bs, bt, 0, 0);
           token = r.arg;
         }
       }
@@ -2026,6 +2412,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   a.out_num_accepted[c.req] = nacc;
   a.out_status[c.req] = wst;
   a.ws_counters[c.req] = 0;  // ready for the next call
+  a.ws_counters[c.nreq + c.req] = 0;
 }
 
 // ------------------------------------------------------------------ host --
@@ -2055,7 +2442,8 @@ static void layout(HArgs& a) {
   // one region, in turn: the allow bits, the exchange-2 push, a group's
   // gathered entries
   const int64_t xm_bytes = a.slice / 8;
-  const int64_t push_bytes = ((kMaxCluster * (kGroups + 1) + 1) & ~1) * 4 + kMaxCluster * (kGroups + 1) * 8;
+  const int64_t push_bytes =
+      ((kMaxCluster * (kGroups + 1) + 1) & ~1) * 4 + kMaxCluster * (kGroups + 1) * 8 + kMaxCluster * 4;
   const int64_t gather_bytes = kGatherCap * 10;
   a.o_xm = take(std::max(xm_bytes, std::max(push_bytes, gather_bytes)), 16);
   // the patched-token bits during set-up, then a group's items merged by value
@@ -2117,6 +2505,9 @@ int32_t hist_last_error() { return hist::t_err; }
 #ifdef SS_HIST_STAMPS
 extern "C" int ss_hist_stamps_copy(void* host, size_t bytes) {
   return static_cast<int>(cudaMemcpyFromSymbol(host, ss::hist::g_stamps, bytes));
+}
+extern "C" int ss_hist_stamps_set(const void* host, size_t bytes) {
+  return static_cast<int>(cudaMemcpyToSymbol(ss::hist::g_stamps, host, bytes));
 }
 #endif
 

@@ -8,6 +8,9 @@
 
 namespace ss {
 
+// Largest draft length a verification call may declare.
+constexpr int32_t kMaxDraft = 1 << 20;
+
 // CTAs per row the histogram kernel uses for this vocabulary (bf16 only),
 // or 0 when it does not take it (the general kernel does).
 int hist_cluster_size(int32_t vocab, int32_t dtype);
@@ -19,8 +22,8 @@ int32_t hist_last_error();
 ss_status hist_sample(const ss_sample_args& args, cudaStream_t stream);
 
 // Linear verification; `results` holds R * (max_draft + 1) int4 and
-// `counters` R arrival counters that are zero on entry (the kernel leaves
-// them at zero).
+// `counters` 2R words that are zero on entry (the kernel leaves them at
+// zero): R arrival counters, then R rejection words.
 ss_status hist_verify(const ss_verify_args& args, int4* results, int32_t* counters, cudaStream_t stream);
 
 }  // namespace ss

@@ -71,7 +71,6 @@ constexpr uint32_t kTargetSliceBytes = 66000u;
 constexpr uint32_t kMaxSliceBytes = kMaxChunks * kChunkBytes;
 constexpr int kMaxCluster = 8;
 // Largest max_draft a verification call takes (tree calls: SS_TREE_MAX_NODES).
-constexpr int32_t kMaxDraft = 1 << 20;
 constexpr uint32_t kWaitPolls = 1u << 22;
 constexpr float kFixedScale = 1099511627776.0f;  // 2^40
 // A token's fixed-point mass (<= 2^40) is histogrammed as two 32-bit halves,
@@ -2999,14 +2998,14 @@ static ss_status check_verify(const ss_verify_args* args) {
   return SS_OK;
 }
 
-// The per-request arrival counters sit at the end of the workspace and the
-// per-position results at its start.  A workspace sized for (R, max_draft)
+// The per-request words (arrival counters, then rejection words) sit at the
+// end of the workspace and the per-position results at its start.  A workspace sized for (R, max_draft)
 // then never holds a counter of one call where another call of a different
 // shape put its results, so the counters stay at zero between calls (each
 // call leaves its counters at zero) whatever the calls' shapes.
 static int32_t* counters_at_end(void* workspace, size_t bytes, int32_t num_requests) {
   const uintptr_t end = reinterpret_cast<uintptr_t>(workspace) + bytes;
-  return reinterpret_cast<int32_t*>((end - 4u * static_cast<uintptr_t>(num_requests)) & ~static_cast<uintptr_t>(15));
+  return reinterpret_cast<int32_t*>((end - 8u * static_cast<uintptr_t>(num_requests)) & ~static_cast<uintptr_t>(15));
 }
 
 // One verification launch on a checked call and a large enough workspace.
@@ -3053,7 +3052,7 @@ extern "C" {
 size_t ss_workspace_size(int32_t max_requests, int32_t max_draft) {
   if (max_requests < 0 || max_draft < 0 || max_draft > ss::kMaxDraft) return 0;
   const size_t results = static_cast<size_t>(max_requests) * (static_cast<size_t>(max_draft) + 1) * sizeof(int4);
-  return results + static_cast<size_t>(max_requests) * sizeof(int32_t) + 256;
+  return results + 2 * static_cast<size_t>(max_requests) * sizeof(int32_t) + 256;
 }
 
 ss_status ss_workspace_init(void* workspace, size_t workspace_bytes, ss_stream_t stream) {
