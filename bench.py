@@ -39,7 +39,8 @@ from speculative_verification_gb300 import workloads as W  # noqa: E402
 METRIC = "sampled rows/s and logits HBM GB/s (% of peak) at V=128k B=64; spec-verify rows/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_NAME = "ss_row_kernel"
+KERNEL_NAME = "ss_hist_kernel"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 def progress(msg):
@@ -52,8 +53,9 @@ _T0 = time.time()
 
 
 KERNEL_SOURCES = {
-    "ss_row_kernel": "ss_kernel.cu",
-    "ss_fused_kernel": "ss_fused.cu",
+    "ss_hist_kernel": ("ss_hist.cu", "ss_hist.h"),
+    "ss_row_kernel": ("ss_kernel.cu",),
+    "ss_fused_kernel": ("ss_fused.cu",),
 }
 
 
@@ -66,12 +68,12 @@ def _code_only(text):
     return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
-def kernel_source_hash(kernel="ss_row_kernel"):
-    """Hash of the code one kernel is compiled from: its translation unit,
+def kernel_source_hash(kernel=KERNEL_NAME):
+    """Hash of the code one kernel is compiled from: its translation unit(s),
     the shared device headers and the C header, comments left out."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_verification_gb300", "csrc")
-    for name in (KERNEL_SOURCES[kernel], "ss_philox.cuh", "ss_ptx.cuh"):
+    for name in KERNEL_SOURCES[kernel] + ("ss_philox.cuh", "ss_ptx.cuh"):
         with open(os.path.join(csrc, name)) as f:
             h.update(name.encode() + _code_only(f.read()).encode())
     with open(os.path.join(ROOT, "include", "ss.h")) as f:
@@ -89,26 +91,24 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(workload_key, kernel="ss_row_kernel"):
-    """Per-launch DRAM bytes from the committed ncu summary
-    (profiles/<kernel>_traffic.md), if it was taken on the current source of
-    that kernel; otherwise None."""
-    path = os.path.join(ROOT, "profiles", kernel + "_traffic.md")
-    if not os.path.exists(path):
+def recorded_traffic(workload_key, kernel=KERNEL_NAME):
+    """Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum)
+    recorded from an ncu capture in profiles/traffic.json, if that capture
+    was taken on the current source of the kernel and on this workload;
+    otherwise None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            entries = json.load(f)["entries"]
+    except (OSError, ValueError, KeyError):
         return None
     want = kernel_source_hash(kernel)
-    cur = {}
-    for line in open(path):
-        line = line.strip().strip("`")
-        if ":" in line:
-            k, v = line.split(":", 1)
-            cur[k.strip().lstrip("- ")] = v.strip()
-    if cur.get("kernel_sha256") != want or cur.get("workload") != workload_key:
-        return None
-    try:
-        return int(cur["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("kernel_sha256") == want and e.get("workload") == workload_key:
+            try:
+                return int(e["traffic_bytes_per_launch"])
+            except (KeyError, ValueError, TypeError):
+                return None
+    return None
 
 
 class ClockSampler:
@@ -169,6 +169,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def kernel_for(w):
+    """The kernel a call on workload w runs: bf16 logits take the histogram
+    kernel, fp32 logits the general row kernel."""
+    return "ss_hist_kernel" if w["dtype"] == "bf16" else "ss_row_kernel"
+
+
+def launches_per_call(w, cs):
+    """Kernel launches one call makes: one for bf16 logits; the fp32 kernel
+    gives the heavy rows (top-p without top-k) a concurrent launch of their
+    own when there are 16 rows or more and the cluster can double."""
+    if w["dtype"] == "bf16":
+        return 1
+    return 2 if (w["kind"] == "sample" and 16 <= int(w["num_rows"]) <= 4096 and 2 <= cs <= 4) else 1
+
+
 def workload_for(cfg, rank, idx):
     return W.make(cfg, seed=DP.ring_seed(cfg, rank, idx))
 
@@ -194,7 +209,7 @@ def run_ours(args, rank, world, dist):
     # that can double, the heavy rows (top-p without top-k) get a concurrent
     # launch of their own with twice the CTAs per row
     cs = ss.ss_cluster_size(int(ring_host[0]["vocab"]), ring_host[0]["dtype"])
-    per_call = 2 if (ring_host[0]["kind"] == "sample" and 16 <= int(ring_host[0]["num_rows"]) <= 4096 and 2 <= cs <= 4) else 1
+    per_call = launches_per_call(ring_host[0], cs)
     rows_per_call = int(ring_host[0]["num_rows"]) if ring_host[0]["kind"] == "sample" else int(
         ring_host[0]["draft_offsets"][-1]) + int(ring_host[0]["num_requests"])
     ring = [ss.to_device(w, dev) for w in ring_host]
@@ -281,8 +296,18 @@ def run_ours(args, rank, world, dist):
                "median_replay": statistics.median(per_replay) if per_replay else None,
                "single_call_no_graph_median": statistics.median(single)}
 
-    # end-to-end through the public API with host buffers (pinned)
     progress("timed region done: %.3f ms" % ms)
+    # untimed: the GPU's outputs on the first input set, checked against the
+    # oracle (all rows)
+    chk = ss.alloc_outputs(ring[0], dev)
+    ss.run(ring[0], chk, stream=stream)
+    stream.synchronize()
+    gpu0 = {k: v.cpu().numpy() for k, v in chk.items() if k not in ("workspace", "processed")}
+    n_check = int(ring_host[0]["num_rows"]) if ring_host[0]["kind"] == "sample" else int(ring_host[0]["num_requests"])
+    parity = cpu_leg_check(ring_host[0], gpu0, range(n_check))["parity"] if not args.no_cpu_baseline else None
+    progress("parity check done")
+
+    # end-to-end through the public API with host buffers (pinned)
     e2e = run_e2e(args, ss, ring_host, dev, stream, rows_per_call, dist)
     progress("end-to-end done")
 
@@ -295,8 +320,17 @@ def run_ours(args, rank, world, dist):
     progress("sharded done")
     fused = run_fused(args, ss, dev, stream, measured_peak()[0]) if args.fused_steps > 0 else None
     progress("fused done")
-
     peak, peak_kind = measured_peak()
+    grammar = mixed = None
+    if args.grammar_calls > 0:
+        grammar = run_config_block(args, ss, 3, rank, dev, stream, peak, 8, args.grammar_calls,
+                                   range(128) if not args.no_cpu_baseline else [])
+        progress("grammar done")
+    if args.mixed_calls > 0:
+        mixed = run_config_block(args, ss, 5, rank, dev, stream, peak, 1, args.mixed_calls,
+                                 range(0, 256, 4) if not args.no_cpu_baseline else [])
+        progress("mixed stress done")
+
     achieved = bytes_per_call / per_call_s / 1e9
     res = {
         "metric": METRIC,
@@ -320,7 +354,7 @@ def run_ours(args, rank, world, dist):
             "launch": "CUDA graph of %d calls, replayed" % per_graph,
             "parallelism": "dp%d replicas" % world,
             "cluster_ctas_per_row": cs,
-            "heavy_row_ctas": 2 * cs if per_call == 2 else cs,
+            "launches_per_call": per_call,
         },
         "roofline": {
             "bound": "hbm",
@@ -331,9 +365,9 @@ def run_ours(args, rank, world, dist):
             "frac_of_nominal_7900": achieved / 7900.0,
             "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured" else "fallback",
             "algorithmic_bytes_per_launch": bytes_per_call,
-            "traffic": recorded_traffic(W.CONFIG_NAMES[cfg]),
-            "kernel": KERNEL_NAME,
-            "kernel_sha256": kernel_source_hash(),
+            "traffic": recorded_traffic(W.CONFIG_NAMES[cfg], kernel_for(ring_host[0])),
+            "kernel": kernel_for(ring_host[0]),
+            "kernel_sha256": kernel_source_hash(kernel_for(ring_host[0])),
         },
         "e2e": e2e,
         "us_per_call": call_us,
@@ -348,6 +382,12 @@ def run_ours(args, rank, world, dist):
         res["vocab_sharded"] = sharded
     if fused is not None:
         res["fused_lmhead"] = fused
+    if parity is not None:
+        res["parity"] = parity
+    if grammar is not None:
+        res["grammar"] = grammar
+    if mixed is not None:
+        res["mixed_stress"] = mixed
     return res
 
 
@@ -666,7 +706,126 @@ def run_fused(args, ss, dev, stream, peak):
                          "kernel_sha256": kernel_source_hash("ss_fused_kernel")}}
 
 
+def run_config_block(args, ss, cfg, rank, dev, stream, peak, ring_n, calls_wanted, check_reqs):
+    """Throughput of one more workload (3: grammar-constrained, 5: mixed
+    stress), timed like the headline: a ring of input sets larger than twice
+    the L2 cache (or one set larger than it), calls replayed from a CUDA graph,
+    CUDA events on the launching stream.  Afterwards (untimed) the GPU's
+    outputs on the first set are checked against the oracle on `check_reqs`."""
+    import torch
+    progress("config %d: generating %d input sets" % (cfg, ring_n))
+    ring_host = [workload_for(cfg, rank, i) for i in range(ring_n)]
+    ring = [ss.to_device(w, dev) for w in ring_host]
+    out = ss.alloc_outputs(ring[0], dev)
+    w0 = ring_host[0]
+    rows = int(w0["num_rows"]) if w0["kind"] == "sample" else int(w0["draft_offsets"][-1]) + int(w0["num_requests"])
+    alg = W.algorithmic_bytes(w0)
+    cs = ss.ss_cluster_size(int(w0["vocab"]), w0["dtype"])
+    with torch.cuda.stream(stream):
+        if "workspace" in out:
+            ss.ss_workspace_init(out["workspace"], stream=stream)
+        for dw in ring:
+            ss.run(dw, out, stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for dw in ring:
+                ss.run(dw, out, stream=stream)
+    reps = max(1, calls_wanted // ring_n)
+    for _ in range(3):
+        g.replay()
+    stream.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    calls = reps * ring_n
+    per_call_s = ms / 1e3 / calls
+    achieved = alg / per_call_s / 1e9
+    # untimed: one more call on the first set, for the check
+    chk = ss.alloc_outputs(ring[0], dev)
+    ss.run(ring[0], chk, stream=stream)
+    stream.synchronize()
+    gpu = {k: v.cpu().numpy() for k, v in chk.items() if k not in ("workspace", "processed")}
+    kernel = kernel_for(w0)
+    block = {
+        "workload": W.CONFIG_NAMES[cfg],
+        "rows_per_call": rows,
+        "rows_per_s": rows / per_call_s,
+        "us_per_call": per_call_s * 1e6,
+        "calls": calls,
+        "gpu_launches": calls * launches_per_call(w0, cs),
+        "l2": "ring of %d input set(s), %.0f MB%s" % (ring_n, ring_n * alg / 1e6,
+                                                       " > 2x L2" if ring_n * alg > 2 * L2_BYTES else " > L2"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "algorithmic_bytes_per_launch": alg, "traffic": recorded_traffic(W.CONFIG_NAMES[cfg], kernel),
+                     "kernel": kernel, "kernel_sha256": kernel_source_hash(kernel)},
+    }
+    if len(check_reqs):
+        block.update(cpu_leg_check(w0, gpu, check_reqs))
+    return block
+
+
 # -------------------------------------------------------- oracle timing --
+
+
+def cpu_leg_check(w, gpu, reqs):
+    """The CPU-baseline leg on a checked sample: the oracle run on the
+    requests `reqs` of input set w (timed: its rows/s on one thread), and the
+    GPU's outputs for them compared with it as the parity tests do -- tokens,
+    statuses and accepted counts must match except where the oracle marks the
+    decision as within the 1e-5 margin; a GPU kept-set size inside the
+    oracle's margin range is adopted (forced_kept counts those).  Reports
+    counts; never raises on a mismatch."""
+    from oracle import oracle as O
+    reqs = list(reqs)
+    sub = W.subset_requests(w, reqs)
+    if w["kind"] == "sample":
+        g = {k: gpu[k][reqs] for k in ("token", "status", "kept")}
+        t0 = time.perf_counter()
+        ref = O.process_sample(sub, force_kept=g["kept"])
+        el = time.perf_counter() - t0
+        ok = ref["status"] == 0
+        forced = ok & (g["kept"] != ref["kept_own"])
+        outside = ok & ((g["kept"] < ref["kept_lo"]) | (g["kept"] > ref["kept_hi"]))
+        sm = ok & (ref["sub_margin"] != 0)
+        mism = (g["status"] != ref["status"]) | (ok & ~sm & (g["token"] != ref["token"])) | outside
+        rows = len(reqs)
+    else:
+        d = w["draft_offsets"]
+        trows = np.concatenate([np.arange(int(d[r]) + r, int(d[r + 1]) + r + 1) for r in reqs])
+        g = {"out_tokens": gpu["out_tokens"][reqs], "num_accepted": gpu["num_accepted"][reqs],
+             "status": gpu["status"][reqs], "kept": gpu["kept"][trows]}
+        t0 = time.perf_counter()
+        ref = O.spec_verify(sub, force_kept=g["kept"])
+        el = time.perf_counter() - t0
+        ok = ref["status"] == 0
+        off = sub["draft_offsets"]
+        forced = np.zeros(len(reqs), bool)
+        outside = np.zeros(len(reqs), bool)
+        for i in range(len(reqs)):
+            rr = np.arange(int(off[i]) + i, int(off[i + 1]) + i + 1)
+            forced[i] = ok[i] and np.any(g["kept"][rr] != ref["kept_own"][rr])
+            outside[i] = ok[i] and np.any((g["kept"][rr] < ref["kept_lo"][rr]) | (g["kept"][rr] > ref["kept_hi"][rr]))
+        sm = ok & (ref["sub_margin"] != 0)
+        tok_bad = np.array([not np.array_equal(g["out_tokens"][i], ref["out_tokens"][i]) for i in range(len(reqs))])
+        mism = (g["status"] != ref["status"]) | (ok & ~sm & ((g["num_accepted"] != ref["num_accepted"]) | tok_bad)) | outside
+        rows = int(len(trows))
+    return {"parity": {"checked": len(reqs), "unit": "rows" if w["kind"] == "sample" else "requests",
+                       "status_ok": int(ok.sum()), "mismatches": int(mism.sum()), "sub_margin": int(sm.sum()),
+                       "forced_kept": int(forced.sum()),
+                       "what": "GPU outputs of one input set against the CPU oracle, outside the timed region"},
+            "cpu_oracle": {"value": rows / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                           "sample": "%d target rows of the checked sample, one thread" % rows}}
+
+
+
 
 
 def time_oracle(cfg, seconds, max_steps=None):
@@ -771,16 +930,23 @@ def main():
     ap.add_argument("--steps", type=int, default=100000)
     ap.add_argument("--warmup", type=int, default=500)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, help="workload 2 (headline) or 1/3")
+    ap.add_argument("--config", type=int, default=2, help="workload of the headline line: 2 (default), 1, 3 or 5")
     ap.add_argument("--ring", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--spec-steps", type=int, default=4000)
     ap.add_argument("--tree-steps", type=int, default=1500)
     ap.add_argument("--shard-steps", type=int, default=2000)
     ap.add_argument("--fused-steps", type=int, default=400)
+    ap.add_argument("--grammar-calls", type=int, default=400, help="calls timed on workload 3 (0: skip)")
+    ap.add_argument("--mixed-calls", type=int, default=20, help="calls timed on workload 5 (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # not started by torchrun: start one process per GPU here, with the
+        # same rendezvous variables torchrun would set
+        return DP.launch_local(args.gpus, [sys.executable, os.path.abspath(__file__)] + sys.argv[1:])
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

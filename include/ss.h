@@ -193,6 +193,16 @@ ss_status ss_workspace_init(void* workspace, size_t workspace_bytes, ss_stream_t
  * starts before the thread's first such call records the single launch. */
 ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream);
 
+/* Self-test of the kernels' bounded waits (no counterpart in the pages; it
+ * exists so that the timeout path can be exercised without a fault).  Runs
+ * ss_process_sample on bf16 logits with one extra wait in every CTA, on a
+ * barrier that nothing completes, given up after `polls` polls (each poll
+ * sleeps a hardware-chosen interval, so keep it small: 100 to 1000).  Every
+ * valid row then reports SS_ROW_TIMEOUT and token -1; the context stays
+ * usable.  SS_ERR_UNSUPPORTED for fp32 logits or polls == 0; the other
+ * errors are ss_process_sample's. */
+ss_status ss_selftest_wait_timeout(const ss_sample_args* args, uint32_t polls, ss_stream_t stream);
+
 /* Batched speculative verification; one kernel launch.  The workspace must
  * have been zeroed once (ss_workspace_init). */
 ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t workspace_bytes,

@@ -63,6 +63,7 @@ class _SampleOut(C.Structure):
         ("sub_margin", C.c_void_p),
         ("kept_lo", C.c_void_p),
         ("kept_hi", C.c_void_p),
+        ("kept_own", C.c_void_p),
     ]
 
 
@@ -93,6 +94,7 @@ class _VerifyOut(C.Structure):
         ("sub_margin", C.c_void_p),
         ("kept_lo", C.c_void_p),
         ("kept_hi", C.c_void_p),
+        ("kept_own", C.c_void_p),
     ]
 
 
@@ -236,6 +238,7 @@ def process_sample(w, want_processed=False, force_kept=None):
         "sub_margin": np.zeros(n, np.uint8),
         "kept_lo": np.zeros(n, np.int32),
         "kept_hi": np.zeros(n, np.int32),
+        "kept_own": np.zeros(n, np.int32),
     }
     if want_processed:
         res["processed"] = np.zeros((n, V), np.float32)
@@ -247,6 +250,7 @@ def process_sample(w, want_processed=False, force_kept=None):
     o.sub_margin = _ptr(res["sub_margin"])
     o.kept_lo = _ptr(res["kept_lo"])
     o.kept_hi = _ptr(res["kept_hi"])
+    o.kept_own = _ptr(res["kept_own"])
     lib().or_process_sample(C.byref(s), C.byref(o))
     return res
 
@@ -286,6 +290,7 @@ def spec_verify(w, want_processed=False, force_kept=None):
         "sub_margin": np.zeros(R, np.uint8),
         "kept_lo": np.zeros(rows, np.int32),
         "kept_hi": np.zeros(rows, np.int32),
+        "kept_own": np.zeros(rows, np.int32),
     }
     if want_processed:
         res["processed"] = np.zeros((rows, V), np.float32)
@@ -298,6 +303,7 @@ def spec_verify(w, want_processed=False, force_kept=None):
     o.sub_margin = _ptr(res["sub_margin"])
     o.kept_lo = _ptr(res["kept_lo"])
     o.kept_hi = _ptr(res["kept_hi"])
+    o.kept_own = _ptr(res["kept_own"])
     lib().or_spec_verify(C.byref(v), C.byref(o))
     return res
 

@@ -270,8 +270,11 @@ static void row_prepare(const row_in* in, row_state* s) {
   }
 
   /* 7. filters.  Besides L, record the range [L_lo, L_hi] of prefix lengths
-   * that the top-p and min-p comparisons give when every probability moves
-   * by at most 1e-5 relative (the decision margin). */
+   * the comparisons can give within the decision margin (1e-5 relative):
+   * for top-p, each renormalised probability of the top-k prefix may move by
+   * that much (so every prefix mass C may lie anywhere in [C(1-d), C(1+d)]);
+   * for min-p, each ratio w = exp(y - ymax) may (the maximum's own w = 1 is
+   * exact: its y - ymax is 0 in any arithmetic). */
   {
     int32_t Lk = (in->top_k > 0 && in->top_k < n) ? in->top_k : n;
     int32_t Lp = Lk, Lp_lo = Lk, Lp_hi = Lk, Lm = n, Lm_lo = n, Lm_hi = n;
@@ -285,17 +288,19 @@ static void row_prepare(const row_in* in, row_state* s) {
       for (i = 0; i < Lk; ++i) {
         cum += s->w[i];
         c = cum / Sk; /* C_{i+1}: mass of the first i+1 tokens */
-        if (!got_lo && c >= p * (1.0 - REL_MARGIN)) { Lp_lo = i + 1; got_lo = 1; }
+        /* shortest: every mass at its largest, C(1+d) >= p; longest: C(1-d) >= p */
+        if (!got_lo && c * (1.0 + REL_MARGIN) >= p) { Lp_lo = i + 1; got_lo = 1; }
         if (!got && c >= p) { Lp = i + 1; got = 1; }
-        if (!got_hi && c >= p * (1.0 + REL_MARGIN)) { Lp_hi = i + 1; got_hi = 1; break; }
+        if (!got_hi && c * (1.0 - REL_MARGIN) >= p) { Lp_hi = i + 1; got_hi = 1; break; }
       }
     }
     if (in->min_p > 0.0f) {
       double mp = (double)in->min_p;
       Lm = Lm_lo = Lm_hi = 0;
       while (Lm < n && s->w[Lm] >= mp) ++Lm;
-      while (Lm_lo < n && s->w[Lm_lo] >= mp * (1.0 + REL_MARGIN)) ++Lm_lo;
-      while (Lm_hi < n && s->w[Lm_hi] >= mp * (1.0 - REL_MARGIN)) ++Lm_hi;
+      /* shortest: every w (but the exact 1s) at w(1-d); longest: at w(1+d) */
+      while (Lm_lo < n && (s->w[Lm_lo] == 1.0 ? 1.0 >= mp : s->w[Lm_lo] * (1.0 - REL_MARGIN) >= mp)) ++Lm_lo;
+      while (Lm_hi < n && (s->w[Lm_hi] == 1.0 ? 1.0 >= mp : s->w[Lm_hi] * (1.0 + REL_MARGIN) >= mp)) ++Lm_hi;
     }
     s->L = Lk < Lp ? Lk : Lp;
     if (Lm < s->L) s->L = Lm;
@@ -330,33 +335,35 @@ static double row_prob(const row_state* s, int32_t t) {
   return 0.0;
 }
 
-/* Step 8.  Gumbel-max over K; sets *flag when the two best scores are within
- * the relative margin. */
+/* Step 8.  Gumbel-max over K.  Sets *flag when the decision is within the
+ * margin: each y_t and each g_t may move by 1e-5 * max(1, |value|), and some
+ * other token's highest score reaches the winner's lowest. */
+static double margin_of(double v) { return REL_MARGIN * fmax(1.0, fabs(v)); }
+
 static int32_t row_draw(const row_state* s, uint64_t seed, int32_t row, uint32_t pos, int* flag) {
-  int32_t i, best = -1, second = -1;
-  double sb = -INFINITY, ss = -INFINITY, gb = 0.0, gs = 0.0;
+  int32_t i, best = -1;
+  double sb = -INFINITY, lo_best = 0.0;
   if (s->greedy) return s->order[0];
   for (i = 0; i < s->L; ++i) {
     int32_t t = s->order[i];
     double g = or_gumbel(seed, row, pos, t, OR_STREAM_DRAW);
     double sc = (double)s->y[t] + g;
     if (best < 0 || sc > sb || (sc == sb && t < best)) {
-      second = best;
-      ss = sb;
-      gs = gb;
       best = t;
       sb = sc;
-      gb = g;
-    } else if (second < 0 || sc > ss || (sc == ss && t < second)) {
-      second = t;
-      ss = sc;
-      gs = g;
+      lo_best = sc - margin_of((double)s->y[t]) - margin_of(g);
     }
   }
-  if (second >= 0) {
-    double ys = fmax(1.0, fmax(fabs((double)s->y[best]), fabs((double)s->y[second])));
-    double gsc = fmax(1.0, fmax(fabs(gb), fabs(gs)));
-    if (sb - ss < REL_MARGIN * (ys + gsc)) *flag = 1;
+  for (i = 0; i < s->L; ++i) {
+    int32_t t = s->order[i];
+    double g, hi;
+    if (t == best) continue;
+    g = or_gumbel(seed, row, pos, t, OR_STREAM_DRAW);
+    hi = (double)s->y[t] + g + margin_of((double)s->y[t]) + margin_of(g);
+    if (hi >= lo_best) {
+      *flag = 1;
+      break;
+    }
   }
   return best;
 }
@@ -407,6 +414,7 @@ int or_process_sample(const or_sample_in* in, or_sample_out* out) {
     row_prepare(&ri, &s);
     if (out->kept_lo) out->kept_lo[r] = (s.status == OR_ROW_OK) ? s.L_lo : 0;
     if (out->kept_hi) out->kept_hi[r] = (s.status == OR_ROW_OK) ? s.L_hi : 0;
+    if (out->kept_own) out->kept_own[r] = (s.status == OR_ROW_OK) ? s.L : 0;
     if (in->force_kept && in->force_kept[r] > 0) row_force_L(&s, in->force_kept[r]);
     if (s.status == OR_ROW_OK) {
       /* Philox counter word 2: the caller's row id, else the row's index */
@@ -460,8 +468,9 @@ int32_t or_residual_probs(int32_t vocab, const double* P, const float* q, double
 
 /* Residual draw on a rejected position: argmax over t with r_t > 0 of
  * log r_t + g_t (stream 2).  Returns -1 when no r_t > 0.  The sub-margin test
- * perturbs P_t and q_t by 1e-5 relative and asks whether any other candidate's
- * best case reaches the winner's worst case. */
+ * lets each P_t move by 1e-5 relative and each g_t by 1e-5 * max(1, |g_t|)
+ * (q_t is an input, exact) and asks whether any other candidate's best case
+ * reaches the winner's worst case, or the winner's residual can vanish. */
 static int32_t residual_draw(const row_state* s, const float* qrow, uint64_t seed, int32_t row,
                              uint32_t pos, int* flag) {
   int32_t i, best = -1;
@@ -475,9 +484,9 @@ static int32_t residual_draw(const row_state* s, const float* qrow, uint64_t see
     double P = s->greedy ? 1.0 : s->w[i] / s->SK;
     double q = (double)qrow[t];
     double r = P - q;
-    double d = REL_MARGIN * (P + fabs(q));
+    double d = REL_MARGIN * P; /* P may move by the margin; q is an input */
     double g = or_gumbel(seed, row, pos, t, OR_STREAM_RESIDUAL);
-    double geps = REL_MARGIN * fmax(1.0, fabs(g));
+    double geps = margin_of(g);
     tok[i] = t;
     hi[i] = (r + d > 0.0) ? log(r + d) + g + geps : -INFINITY;
     lo[i] = (r - d > 0.0) ? log(r - d) + g - geps : -INFINITY;
@@ -547,6 +556,7 @@ int or_spec_verify(const or_verify_in* in, or_verify_out* out) {
       row_prepare(&ri, &rows[j]);
       if (out->kept_lo) out->kept_lo[trow] = (rows[j].status == OR_ROW_OK) ? rows[j].L_lo : 0;
       if (out->kept_hi) out->kept_hi[trow] = (rows[j].status == OR_ROW_OK) ? rows[j].L_hi : 0;
+      if (out->kept_own) out->kept_own[trow] = (rows[j].status == OR_ROW_OK) ? rows[j].L : 0;
       if (in->force_kept && in->force_kept[trow] > 0) row_force_L(&rows[j], in->force_kept[trow]);
       if (rows[j].status > status) status = rows[j].status;
       if (out->kept) out->kept[trow] = (rows[j].status == OR_ROW_OK) ? rows[j].L : 0;
@@ -566,7 +576,8 @@ int or_spec_verify(const or_verify_in* in, or_verify_out* out) {
         double u = (double)or_uniform(seed, rid, pos + (uint32_t)j, 0, OR_STREAM_ACCEPT);
         double uq = u * q;
         flag |= rows[j].flag_k;
-        if (fabs(uq - P) <= REL_MARGIN * fmax(P, uq) + ABS_FLOOR) flag = 1;
+        /* accept iff u q < P; P may move by the margin, u and q are exact */
+        if (uq >= P * (1.0 - REL_MARGIN) && uq < P * (1.0 + REL_MARGIN)) flag = 1;
         if (uq < P) {
           o[j] = x;
           ++n_acc;

@@ -87,6 +87,7 @@ typedef struct {
   uint8_t* sub_margin;           /* [n] or NULL: a decision was within 1e-5    */
   int32_t* kept_lo;              /* [n] or NULL: smallest |K| within margin    */
   int32_t* kept_hi;              /* [n] or NULL: largest |K| within margin     */
+  int32_t* kept_own;             /* [n] or NULL: |K| before force_kept         */
 } or_sample_out;
 
 typedef struct {
@@ -111,6 +112,7 @@ typedef struct {
   uint8_t* sub_margin;           /* [R] or NULL                                */
   int32_t* kept_lo;              /* [rows] or NULL                             */
   int32_t* kept_hi;              /* [rows] or NULL                             */
+  int32_t* kept_own;             /* [rows] or NULL: |K| before force_kept      */
 } or_verify_out;
 
 /* Philox4x32-10 block function (Salmon, Moraes, Dror, Shaw, "Parallel random

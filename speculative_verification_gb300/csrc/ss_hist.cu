@@ -94,6 +94,7 @@ static_assert(kSlots % kGroups == 0, "groups tile the slots");
 // part of the region the patch table no longer needs
 static_assert(kSlots * 2 + (kGroups + 2) * 4 + kEntCap * 2 <= kHashCap * 16, "entry order fits the region");
 static_assert(kEntCap % kThreads == 0, "entries per thread");
+static_assert((kSliceMax + kChunkTokens - 1) / kChunkTokens < kMaxChunks, "a barrier slot stays free for the self-test");
 
 // Phase timestamps for tracing (built only with -DSS_HIST_STAMPS): the
 // global timer at the end of each phase, per CTA, read back with
@@ -277,6 +278,7 @@ struct HArgs {
   int32_t* ws_counters;
   int32_t ncta, slice, bulk;
   int32_t o_vb, o_hist, o_el, o_xm, o_mg, o_mbar, total;
+  uint32_t stall_polls;  // self-test: a bounded wait on a barrier nothing completes
 };
 
 // Per-CTA partial of exchange 1.
@@ -1749,6 +1751,14 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     if (tid == 0)
       for (int q = waited + 1; q < c.nch; ++q)
         if (!mbar_wait_bounded(mbar + q, 0, kWaitPolls)) timed_out = true;
+    if (a.stall_polls && tid == 0) {
+      // the self-test: the last barrier slot (no chunk uses it) is armed for
+      // one arrival that never comes
+      uint64_t* bar = mbar + (kMaxChunks - 1);
+      mbar_init(bar, 1);
+      fence_barrier_init();
+      if (!mbar_wait_bounded(bar, 0, a.stall_polls)) timed_out = true;
+    }
   }
   if (timed_out) atomicMax(&c.status, SS_ROW_TIMEOUT);
   __syncthreads();
@@ -2513,8 +2523,9 @@ extern "C" int ss_hist_stamps_set(const void* host, size_t bytes) {
 
 namespace ss {
 
-ss_status hist_sample(const ss_sample_args& A, cudaStream_t stream) {
+ss_status hist_sample(const ss_sample_args& A, cudaStream_t stream, uint32_t stall_polls) {
   hist::HArgs a{};
+  a.stall_polls = stall_polls;
   a.mode = 0;
   a.num_tasks = A.num_rows;
   a.vocab = A.vocab;

@@ -18,8 +18,10 @@ int hist_cluster_size(int32_t vocab, int32_t dtype);
 // cudaError_t of the last failed launch on this thread.
 int32_t hist_last_error();
 
-// Batched sampling; arguments already validated by the caller.
-ss_status hist_sample(const ss_sample_args& args, cudaStream_t stream);
+// Batched sampling; arguments already validated by the caller.  With
+// stall_polls > 0 every CTA also waits, for at most that many polls, on a
+// barrier nothing completes (the bounded-wait self-test).
+ss_status hist_sample(const ss_sample_args& args, cudaStream_t stream, uint32_t stall_polls = 0);
 
 // Linear verification; `results` holds R * (max_draft + 1) int4 and
 // `counters` 2R words that are zero on entry (the kernel leaves them at

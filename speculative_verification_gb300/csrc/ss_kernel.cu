@@ -3065,7 +3065,8 @@ ss_status ss_workspace_init(void* workspace, size_t workspace_bytes, ss_stream_t
   return SS_OK;
 }
 
-ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream) {
+// Checks of a sampling call (everything the launch needs).
+static ss_status check_sample(const ss_sample_args* args) {
   using namespace ss;
   if (!args) return SS_ERR_INVALID_ARG;
   const ss_sample_args& A = *args;
@@ -3078,6 +3079,24 @@ ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream) {
   if (A.row_stride != 0 && A.row_stride < A.vocab) return SS_ERR_INVALID_ARG;
   if (check_params(A.params) != SS_OK) return SS_ERR_INVALID_ARG;
   if (A.params.bitmask && A.params.bitmask_stride < (static_cast<int64_t>(A.vocab) + 31) / 32) return SS_ERR_INVALID_ARG;
+  return SS_OK;
+}
+
+ss_status ss_selftest_wait_timeout(const ss_sample_args* args, uint32_t polls, ss_stream_t stream) {
+  using namespace ss;
+  const ss_status chk = check_sample(args);
+  if (chk != SS_OK || args->num_rows == 0) return chk;
+  if (polls == 0 || hist_cluster_size(args->vocab, args->dtype) <= 0) return SS_ERR_UNSUPPORTED;
+  const ss_status s = hist_sample(*args, reinterpret_cast<cudaStream_t>(stream), polls);
+  if (s == SS_ERR_CUDA) g_last_cuda_error = hist_last_error();
+  return s;
+}
+
+ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream) {
+  using namespace ss;
+  const ss_status chk = check_sample(args);
+  if (chk != SS_OK || args->num_rows == 0) return chk;
+  const ss_sample_args& A = *args;
   KArgs k{};
   k.mode = kModeSample;
   k.num_tasks = A.num_rows;

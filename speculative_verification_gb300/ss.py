@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libss.so")
 
 SS_OK = 0
 SS_ERR_SCRATCH_LIMIT = 5
+SS_ROW_TIMEOUT = 5
 SS_DTYPE = {"f32": 0, "bf16": 1}
 ROW_STATUS = {0: "ok", 1: "empty_set", 2: "nonfinite", 3: "bad_index", 4: "bad_param", 5: "timeout", 6: "limit"}
 
@@ -129,6 +130,7 @@ SIGNATURES = {
     "ss_workspace_size": ([C.c_int32, C.c_int32], C.c_size_t),
     "ss_workspace_init": ([C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "ss_process_sample": ([C.POINTER(ss_sample_args), C.c_void_p], C.c_int),
+    "ss_selftest_wait_timeout": ([C.POINTER(ss_sample_args), C.c_uint32, C.c_void_p], C.c_int),
     "ss_spec_verify": ([C.POINTER(ss_verify_args), C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "ss_spec_verify_noalloc": ([C.POINTER(ss_verify_args), C.c_void_p], C.c_int),
     "ss_tree_verify": ([C.POINTER(ss_tree_args), C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
@@ -223,9 +225,7 @@ def ss_workspace_init(workspace, stream=None):
                                     _stream_handle(stream)))
 
 
-def ss_process_sample(logits, params, out_token, out_status, *, vocab, dtype, row_stride=None, out_kept=None,
-                      debug_processed=None, stream=None):
-    """Sample one token per row of `logits` (device tensor, [rows, row_stride])."""
+def _sample_args(logits, params, out_token, out_status, vocab, dtype, row_stride, out_kept, debug_processed):
     a = ss_sample_args()
     a.num_rows = int(out_token.numel())
     a.vocab = int(vocab)
@@ -237,7 +237,22 @@ def ss_process_sample(logits, params, out_token, out_status, *, vocab, dtype, ro
     a.out_status = _ptr(out_status)
     a.out_kept = _ptr(out_kept)
     a.debug_processed = _ptr(debug_processed)
+    return a
+
+
+def ss_process_sample(logits, params, out_token, out_status, *, vocab, dtype, row_stride=None, out_kept=None,
+                      debug_processed=None, stream=None):
+    """Sample one token per row of `logits` (device tensor, [rows, row_stride])."""
+    a = _sample_args(logits, params, out_token, out_status, vocab, dtype, row_stride, out_kept, debug_processed)
     _check(load().ss_process_sample(C.byref(a), _stream_handle(stream)))
+
+
+def ss_selftest_wait_timeout(logits, params, out_token, out_status, *, vocab, dtype, polls, row_stride=None,
+                             out_kept=None, stream=None):
+    """ss_process_sample with one bounded wait per CTA that nothing completes
+    (the timeout self-test): every valid row reports SS_ROW_TIMEOUT."""
+    a = _sample_args(logits, params, out_token, out_status, vocab, dtype, row_stride, out_kept, None)
+    _check(load().ss_selftest_wait_timeout(C.byref(a), int(polls), _stream_handle(stream)))
 
 
 def ss_commit_accepted(out_tokens, num_accepted, status, tokens, seq_len, position, next_token, commit_status,

@@ -384,3 +384,60 @@ def lmhead(batch=64, hidden=4096, vocab=128256, seed=6):
                 vocab=vocab, hidden_states=h, weight=w, temperature=temp,
                 seed=(1000 + np.arange(batch)).astype(np.uint64),
                 position=rng.integers(0, 4096, batch).astype(np.int64))
+
+
+_PER_REQUEST = ("temperature", "top_k", "top_p", "min_p", "repetition", "frequency", "presence", "use_bitmask",
+                "seed", "position", "row_id")
+
+
+def _subset_csr(w, out, reqs, off_key, val_keys):
+    if w.get(off_key) is None:
+        return
+    o = w[off_key]
+    new_off = np.zeros(len(reqs) + 1, np.int32)
+    parts = {v: [] for v in val_keys}
+    for i, r in enumerate(reqs):
+        a, b = int(o[r]), int(o[r + 1])
+        new_off[i + 1] = new_off[i] + (b - a)
+        for v in val_keys:
+            parts[v].append(w[v][a:b])
+    out[off_key] = new_off
+    for v in val_keys:
+        out[v] = np.concatenate(parts[v]) if parts[v] else w[v][:0]
+
+
+def subset_requests(w, reqs):
+    """The requests `reqs` (in that order) of a sampling or linear
+    verification workload, with their rows, drafts and per-request
+    parameters, and row ids equal to their original indices (so every draw
+    is the one it is in the whole batch): a smaller workload of the same
+    kind."""
+    reqs = [int(r) for r in reqs]
+    out = dict(w)
+    for key in _PER_REQUEST:
+        if w.get(key) is not None:
+            out[key] = np.asarray(w[key])[reqs]
+    if w.get("row_id") is None:  # the noise stays keyed by the original index
+        out["row_id"] = np.asarray(reqs, np.uint32)
+    if w.get("bitmask") is not None:
+        out["bitmask"] = w["bitmask"][reqs]
+    _subset_csr(w, out, reqs, "hist_offsets", ("hist_ids",))
+    _subset_csr(w, out, reqs, "bias_offsets", ("bias_ids", "bias_vals"))
+    if w["kind"] == "sample":
+        out["num_rows"] = len(reqs)
+        out["logits"] = w["logits"][reqs]
+        return out
+    d = w["draft_offsets"]
+    rows, drafts = [], []
+    new_d = np.zeros(len(reqs) + 1, np.int32)
+    for i, r in enumerate(reqs):
+        k = int(d[r + 1] - d[r])
+        rows.extend(range(int(d[r]) + r, int(d[r]) + r + k + 1))
+        drafts.extend(range(int(d[r]), int(d[r + 1])))
+        new_d[i + 1] = new_d[i] + k
+    out["num_requests"] = len(reqs)
+    out["draft_offsets"] = new_d
+    out["target_logits"] = w["target_logits"][rows]
+    out["draft_tokens"] = np.asarray(w["draft_tokens"])[drafts]
+    out["draft_probs"] = w["draft_probs"][drafts] if len(drafts) else w["draft_probs"][:0]
+    return out

@@ -11,10 +11,31 @@ def _bits_equal(a, b):
     return np.all((a.view(np.uint32) == b.view(np.uint32)) | both_nan)
 
 
+class Counts:
+    """What a parity check compared: `total` rows (requests) with status OK;
+    `exact` of them compared exactly (tokens, kept sizes, accepted counts);
+    `forced` of those where the GPU's kept-set size differs from the oracle's
+    own and lies inside the oracle's margin range (the oracle then drew from
+    the GPU's kept set); `sub` rows whose draw / accept / residual decision is
+    within the 1e-5 margin (counted, not compared)."""
+
+    def __init__(self, total, exact, forced, sub):
+        self.total, self.exact, self.forced, self.sub = int(total), int(exact), int(forced), int(sub)
+
+    def as_dict(self):
+        return dict(rows=self.total, exact=self.exact, forced_kept=self.forced, sub_margin=self.sub)
+
+    def __iter__(self):  # (checked, sub), as the older callers unpack it
+        return iter((self.exact, self.sub))
+
+    def __repr__(self):
+        return "Counts(%r)" % self.as_dict()
+
+
 def check_sample(w, gpu, rows=None):
-    """gpu: dict of numpy arrays token/status/kept[/processed].  Returns
-    (checked rows, sub-margin rows).  `rows` restricts the check (and the
-    oracle run) to a subset, for full-size workloads."""
+    """gpu: dict of numpy arrays token/status/kept[/processed].  Returns a
+    Counts.  `rows` restricts the check (and the oracle run) to a subset, for
+    full-size workloads."""
     if rows is not None:
         w = subset_sample(w, rows)
         gpu = {k: (v[rows] if isinstance(v, np.ndarray) else v) for k, v in gpu.items()}
@@ -33,7 +54,8 @@ def check_sample(w, gpu, rows=None):
     chk = ok & ~sub
     mism = np.flatnonzero(chk & (gpu["token"] != ref["token"]))
     assert mism.size == 0, ("token mismatch", mism, gpu["token"][mism], ref["token"][mism])
-    return int(chk.sum()), int(sub.sum())
+    forced = ok & (gpu["kept"] != ref["kept_own"])
+    return Counts(ok.sum(), chk.sum(), forced.sum(), sub.sum())
 
 
 def subset_sample(w, rows):
@@ -92,8 +114,9 @@ def subset_tree(w, reqs):
 
 
 def check_verify(w, gpu):
-    """gpu: out_tokens/num_accepted/status/kept[/processed].  Returns
-    (checked requests, sub-margin requests)."""
+    """gpu: out_tokens/num_accepted/status/kept[/processed].  Returns a
+    Counts over requests (a request is `forced` when any of its target rows
+    is)."""
     ref = O.spec_verify(w, want_processed="processed" in gpu, force_kept=gpu["kept"])
     assert np.array_equal(gpu["status"], ref["status"]), (gpu["status"], ref["status"])
     ok = ref["status"] == 0
@@ -112,7 +135,11 @@ def check_verify(w, gpu):
     for i in np.flatnonzero(chk):
         assert gpu["num_accepted"][i] == ref["num_accepted"][i], ("accepted", i, gpu["num_accepted"][i], ref["num_accepted"][i])
         assert np.array_equal(gpu["out_tokens"][i], ref["out_tokens"][i]), ("tokens", i, gpu["out_tokens"][i], ref["out_tokens"][i])
-    return int(chk.sum()), int(sub.sum())
+    forced = np.zeros(R, bool)
+    for i in np.flatnonzero(ok):
+        rows = np.arange(int(d_off[i]) + i, int(d_off[i + 1]) + i + 1)
+        forced[i] = np.any(gpu["kept"][rows] != ref["kept_own"][rows])
+    return Counts(ok.sum(), chk.sum(), forced.sum(), sub.sum())
 
 
 def check_tree(w, gpu):

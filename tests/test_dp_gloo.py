@@ -113,3 +113,44 @@ def test_two_gloo_ranks_match_whole_batch(tmp_path):
     assert float(np.load(tmp_path / "tmax.npy")[0]) == 20.0
     seeds = np.load(tmp_path / "seeds.npy")
     assert len(np.unique(seeds)) == seeds.size  # every rank samples its own batches
+
+
+_RANK_SCRIPT = r"""
+import os, sys
+import torch
+import torch.distributed as dist
+dist.init_process_group("gloo")
+rank, world = dist.get_rank(), dist.get_world_size()
+assert rank == int(os.environ["RANK"]) == int(os.environ["LOCAL_RANK"])
+if len(sys.argv) > 2 and int(sys.argv[2]) == rank:
+    sys.exit(3)  # this rank fails before the collective
+t = torch.tensor([float(rank + 1)])
+dist.all_reduce(t)
+with open(os.path.join(sys.argv[1], "rank%d" % rank), "w") as f:
+    f.write("%d %d %.0f" % (rank, world, t.item()))
+dist.destroy_process_group()
+"""
+
+
+def test_launch_local_starts_every_rank(tmp_path):
+    """bench.py --gpus N without torchrun starts its ranks with
+    DP.launch_local: every rank gets torchrun's variables, joins the same
+    process group and exits 0."""
+    import sys
+    script = tmp_path / "rank.py"
+    script.write_text(_RANK_SCRIPT)
+    world = 3
+    assert DP.launch_local(world, [sys.executable, str(script), str(tmp_path)], timeout=300) == 0
+    for r in range(world):
+        rank, w, total = (tmp_path / ("rank%d" % r)).read_text().split()
+        assert (int(rank), int(w), int(total)) == (r, world, world * (world + 1) // 2)
+
+
+def test_launch_local_reports_a_failed_rank(tmp_path):
+    """A rank that exits non-zero: the launcher returns its code and stops the
+    rank left waiting in the collective."""
+    import sys
+    script = tmp_path / "rank.py"
+    script.write_text(_RANK_SCRIPT)
+    assert DP.launch_local(2, [sys.executable, str(script), str(tmp_path), "1"], timeout=300) == 3
+    assert not (tmp_path / "rank1").exists()

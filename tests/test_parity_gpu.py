@@ -39,9 +39,16 @@ def run_gpu(ss, w, debug=True):
     return res
 
 
-def _report(name, checked, sub):
-    print("%s: %d checked exactly, %d within the 1e-5 draw margin" % (name, checked, sub))
-    assert checked > 0
+def _report(name, counts):
+    """Prints what the margin excused and bounds it: at most 1% of the rows
+    (plus one) may be drawn from a GPU kept set inside the oracle's margin
+    range, and at most as many may be sub-margin."""
+    c = counts
+    print("%s: %d rows OK, %d compared exactly (%d of them on the GPU's kept set), %d within the 1e-5 margin"
+          % (name, c.total, c.exact, c.forced, c.sub))
+    assert c.exact > 0
+    assert c.forced <= 0.01 * c.total + 1, c
+    assert c.sub <= 0.01 * c.total + 1, c
 
 
 # ----------------------------------------------------------- workloads
@@ -49,49 +56,78 @@ def _report(name, checked, sub):
 
 def test_tiny_sampling_full_size(ss):
     w = W.make(1)
-    _report("tiny", *parity.check_sample(w, run_gpu(ss, w)))
+    _report("tiny", parity.check_sample(w, run_gpu(ss, w)))
 
 
 @pytest.mark.parametrize("rows,vocab", [(32, 5003), (12, 128256)])
 def test_heterogeneous_decode(ss, rows, vocab):
     w = W.make(2, rows=rows, vocab=vocab)
-    _report("decode", *parity.check_sample(w, run_gpu(ss, w)))
+    _report("decode", parity.check_sample(w, run_gpu(ss, w)))
 
 
 def test_heterogeneous_decode_full_size(ss):
     w = W.make(2)  # 64 x 128256 bf16: the benchmarked launch
     g = run_gpu(ss, w, debug=False)
-    _report("decode full", *parity.check_sample(w, g))
+    _report("decode full", parity.check_sample(w, g))
 
 
 def test_grammar_constrained(ss):
     w = W.make(3, rows=24, vocab=20011)
-    _report("grammar", *parity.check_sample(w, run_gpu(ss, w)))
+    _report("grammar", parity.check_sample(w, run_gpu(ss, w)))
 
 
 def test_grammar_constrained_full_size(ss):
     w = W.make(3)
-    _report("grammar full", *parity.check_sample(w, run_gpu(ss, w, debug=False)))
+    _report("grammar full", parity.check_sample(w, run_gpu(ss, w, debug=False)))
 
 
 def test_spec_verify_linear(ss):
     w = W.make(4, requests=12, k=4, vocab=7001)
-    _report("verify", *parity.check_verify(w, run_gpu(ss, w)))
+    _report("verify", parity.check_verify(w, run_gpu(ss, w)))
 
 
 def test_spec_verify_full_size(ss):
     w = W.make(4)
-    _report("verify full", *parity.check_verify(w, run_gpu(ss, w, debug=False)))
+    _report("verify full", parity.check_verify(w, run_gpu(ss, w, debug=False)))
 
 
 def test_mixed_stress_small(ss):
     w = W.make(5, requests=32, vocab=9001, max_draft=7, plain_top_k_max=600)
-    _report("mixed", *parity.check_verify(w, run_gpu(ss, w)))
+    _report("mixed", parity.check_verify(w, run_gpu(ss, w)))
 
 
 def test_mixed_stress_full_vocab(ss):
     w = W.make(5, requests=24)
-    _report("mixed full V", *parity.check_verify(w, run_gpu(ss, w, debug=False)))
+    _report("mixed full V", parity.check_verify(w, run_gpu(ss, w, debug=False)))
+
+
+def test_workspace_reuse_across_batch_shapes(ss):
+    """One workspace, sized for the larger batch, serves a larger call, a
+    smaller one and the larger again: every call's outputs equal those of a
+    fresh workspace (the per-request words sit at the workspace's end, so no
+    shape puts them where another shape left its results)."""
+    large = W.make(5, requests=20, vocab=9001, max_draft=7, plain_top_k_max=500)
+    small = W.make(4, requests=12, k=4, vocab=7001)
+    shared = torch.zeros((ss.ss_workspace_size(20, 7) + 15) // 16 * 4, dtype=torch.int32, device="cuda")
+    for w in (large, small, large, small):
+        dw = ss.to_device(w)
+        ref = ss.alloc_outputs(dw)
+        ss.run(dw, ref)
+        got = ss.alloc_outputs(dw)
+        got["workspace"] = shared
+        ss.run(dw, got)
+        torch.cuda.synchronize()
+        for key in ("out_tokens", "num_accepted", "status", "kept"):
+            assert np.array_equal(ref[key].cpu().numpy(), got[key].cpu().numpy()), key
+    assert int(shared[-(2 * 20 + 4):].abs().sum()) == 0  # the words are back at zero
+
+
+def test_mixed_stress_full_size(ss):
+    """Workload 5 as specified: 256 requests (128 plain rows on flat logits
+    with top-k up to 4096, 128 verifications with 1..7 drafts), V = 262144,
+    every request checked."""
+    w = W.make(5)
+    _report("mixed full", parity.check_verify(w, run_gpu(ss, w, debug=False)))
 
 
 def test_row_ids(ss):
@@ -102,7 +138,7 @@ def test_row_ids(ss):
     same = run_gpu(ss, dict(w, row_id=np.arange(12, dtype=np.uint32)), debug=False)
     assert np.array_equal(base["token"], same["token"])
     wid = dict(w, row_id=np.random.default_rng(3).integers(0, 2**32, 12, dtype=np.uint64).astype(np.uint32))
-    _report("row ids", *parity.check_sample(wid, run_gpu(ss, wid)))
+    _report("row ids", parity.check_sample(wid, run_gpu(ss, wid)))
 
 
 def test_commit_accepted_random(ss):
@@ -165,7 +201,7 @@ def test_small_and_ragged_vocab(ss, V):
     w = sample_workload(z, dtype="bf16", temperature=rng.choice([0.0, 0.7, 1.0], size=n),
                         top_k=rng.choice([0, 1, 3, V, V + 2], size=n), top_p=rng.choice([1.0, 0.5, 0.9], size=n),
                         min_p=rng.choice([0.0, 0.1], size=n), seed=5)
-    _report("V=%d" % V, *parity.check_sample(w, run_gpu(ss, w)))
+    _report("V=%d" % V, parity.check_sample(w, run_gpu(ss, w)))
 
 
 def test_ties_everywhere(ss):
@@ -177,6 +213,23 @@ def test_ties_everywhere(ss):
     g = run_gpu(ss, w)
     parity.check_sample(w, g)
     assert g["kept"][:4].tolist() == [1, 5, 100, 585]
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(ss):
+    """A wait that nothing completes gives up after its poll limit: every row
+    reports the timeout status and token -1, and the next ordinary call on
+    the same inputs is correct (no fault, no hang)."""
+    w = W.make(2, rows=6, vocab=9001)
+    dw = ss.to_device(w)
+    o = ss.alloc_outputs(dw)
+    params = {k: dw.get(k) for k in ss.PARAM_FIELDS}
+    params["bitmask_stride"] = dw.get("bitmask_stride", 0)
+    ss.ss_selftest_wait_timeout(dw["logits"], params, o["token"], o["status"], vocab=dw["vocab"], dtype=dw["dtype"],
+                                polls=200, row_stride=dw["row_stride"], out_kept=o["kept"])
+    torch.cuda.synchronize()
+    assert np.all(o["status"].cpu().numpy() == ss.SS_ROW_TIMEOUT)
+    assert np.all(o["token"].cpu().numpy() == -1)
+    _report("after timeout", parity.check_sample(w, run_gpu(ss, w)))
 
 
 def test_statuses(ss):
@@ -206,7 +259,7 @@ def test_broadcast_rows_and_long_history(ss):
                         top_p=rng.choice([1.0, 0.9], size=n), repetition=1.3, frequency=0.1, presence=0.2,
                         history=hist, row_stride=0, num_rows=n, seed=np.arange(n),
                         position=rng.integers(0, 1000, size=n))
-    _report("broadcast", *parity.check_sample(w, run_gpu(ss, w)))
+    _report("broadcast", parity.check_sample(w, run_gpu(ss, w)))
 
 
 def test_patch_table_overflow_reports_limit(ss):
@@ -300,4 +353,4 @@ def test_maximum_vocabulary(ss, dtype, V):
     w = sample_workload(z, dtype=dtype, temperature=[0.0, 1.0, 0.8, 1.2, 1.0, 0.7], top_k=[0, 0, 50, 1000, 0, 0],
                         top_p=[1.0, 0.9, 1.0, 0.95, 1.0, 1.0], min_p=[0.0, 0.0, 0.0, 0.0, 0.05, 0.0],
                         seed=np.arange(n) + 17, position=np.arange(n) * 11)
-    _report("V=%d %s" % (V, dtype), *parity.check_sample(w, run_gpu(ss, w, debug=False)))
+    _report("V=%d %s" % (V, dtype), parity.check_sample(w, run_gpu(ss, w, debug=False)))

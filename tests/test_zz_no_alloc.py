@@ -46,16 +46,18 @@ def _outputs(o):
 
 
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(ss):
-    workloads = [W.make(4, requests=12, k=4, vocab=7001),
-                 W.make(5, requests=20, vocab=9001, max_draft=7, plain_top_k_max=500)]
-    for w in workloads:  # two calls in a row, different batches
+    # the larger batch first: the smaller batch's counters then fall on the
+    # bytes where the larger one left its per-position results, which a
+    # missing reset would show; then both shapes again
+    large = W.make(5, requests=20, vocab=9001, max_draft=7, plain_top_k_max=500)
+    small = W.make(4, requests=12, k=4, vocab=7001)
+    for w in (large, small, large, small):
         dw = ss.to_device(w)
         ref = ss.alloc_outputs(dw)
         ss.run(dw, ref)
         got = ss.alloc_outputs(dw)
-        for o in (got,):
-            for key in ("out_tokens", "num_accepted", "status", "kept"):
-                o[key].fill_(-99)
+        for key in ("out_tokens", "num_accepted", "status", "kept"):
+            got[key].fill_(-99)
         _call_noalloc(ss, dw, got)
         torch.cuda.synchronize()
         a, b = _outputs(ref), _outputs(got)
