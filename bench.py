@@ -404,7 +404,8 @@ def run_e2e(args, ss, ring_host, dev, stream, rows_per_call, dist):
     pinned = [ss.pack_pinned(w, lay, total) for w in sets]
     bufs = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
     staging = [ss.views(b, lay, sets[0]) for b in bufs]
-    outs = [ss.alloc_outputs(st, dev) for st in staging]
+    # output sizes from the host copy: the staging buffers are not filled yet
+    outs = [ss.alloc_outputs(sets[0], dev) for _ in staging]
     keys = [k for k in ("token", "status", "kept", "out_tokens", "num_accepted") if k in outs[0]]
     host_out = [{k: torch.empty(o[k].shape, dtype=o[k].dtype, pin_memory=True) for k in keys} for o in outs]
     h2d = sum(lay[k][1] for k in lay)

@@ -490,7 +490,8 @@ class Outputs(dict):
 
 
 def alloc_outputs(dw, device="cuda", debug=False):
-    """Output tensors for a device workload."""
+    """Output tensors for a workload (host or device arrays: only its sizes
+    are read, and a device workload's offsets must already hold its data)."""
     import torch
     o = Outputs()
     V = int(dw["vocab"])
