@@ -71,8 +71,12 @@ constexpr int kGatherCap = 512;   // entries of one coarse group, over the clust
 constexpr int kFineMax = 256;     // slots one coarse group may span (runs of equal y extend a group)
 constexpr int kEntCap = 1024;     // exact entries per CTA (patched tokens and tiny values)
 constexpr int kHashCap = 1024;    // patch table slots
-constexpr int kCertBins = 32;     // binades below the maximum counted for the top-k certificate
+constexpr int kCertBins = 64;     // bins below the maximum counted for the top-k certificate
+constexpr int kCertShift = 3;     // certificate bin = 16-bit order key >> 3 (16 bins per binade)
 constexpr int kTieEnt = 64;       // entries tied at a cut value, per CTA
+constexpr int kFastK = 1024;      // short path: top-k rows up to this k
+constexpr int kFastCap = 2048;    // short path: candidates gathered into rank 0 (the histogram region)
+constexpr int kRankSortMax = 768; // short path: a rank sort up to this many candidates, else bitonic
 constexpr int kChunkTokens = 8192;
 constexpr int kMaxChunks = 8;
 constexpr int kMaxCluster = 8;
@@ -290,10 +294,10 @@ struct alignas(16) Part1 {
   int32_t nent;
   float xy;       // processed value of the draft token (its CTA)
   int32_t xhere;
-  int32_t zbin;   // binade of zmax (16-bit order key >> 7)
+  int32_t zbin;   // certificate bin of zmax (16-bit order key >> kCertShift)
   int32_t rej;    // verification: the request's rejection word as this CTA read it
   int32_t pad[3];
-  uint32_t cert[kCertBins];  // 16-token pairs whose maximum lies d binades below zbin
+  uint32_t cert[kCertBins / 2];  // 16-token pairs whose maximum lies d bins below zbin (16-bit halves)
 };
 
 // Per-CTA partial of a draw / mass exchange.
@@ -329,6 +333,7 @@ struct Ctx {
   float xy;
   int32_t xhere;
   uint32_t tau_key;  // top-k candidates: tokens whose 16-bit order key is >= this
+  unsigned long long tau_pairs;  // pairs at or above tau (summed over the cluster)
   SlotMap M;
   // cut: K = {y > cut_v} U {y == cut_v, token <= cut_t}
   float cut_v;
@@ -367,10 +372,13 @@ __shared__ int32_t g_goff[kMaxCluster + 1];
 __shared__ int32_t g_gr0[kMaxCluster];       // one group's entry range in every CTA
 __shared__ int32_t g_grc[kMaxCluster + 1];
 __shared__ uint32_t g_rtie[kMaxCluster];
-__shared__ uint32_t g_cert[kCertBins];
+__shared__ uint32_t g_cert[kCertBins / 2];  // two 16-bit bin counts per word
 __shared__ int32_t g_tietok[kTieEnt];
-__shared__ uint32_t g_prm[32];
-__shared__ unsigned long long g_dbest;  // the draw's best key so far  // the request's parameter words
+__shared__ uint32_t g_prm[32];           // the request's parameter words
+__shared__ unsigned long long g_dbest;   // the draw's best key so far
+__shared__ int32_t g_fcount;             // short path: candidates gathered (rank 0's copy)
+__shared__ int32_t g_fpos[3];            // short path: first failing positions (top-p, min-p), draft position
+__shared__ int32_t g_runs[kMaxCluster][2];  // short path (rank 0): every CTA's run (start, length)
 
 extern __shared__ __align__(128) uint8_t g_dyn[];
 
@@ -647,6 +655,7 @@ __device__ void decode_and_copy(const HArgs& a, int task, int rank) {
   c.xpar = 0;
   c.kcount = 0;
   c.kmass = 0;
+  g_fcount = 0;
   c.nreq = 0;
   c.skip_draw = 0;
   c.x = -1;
@@ -1020,15 +1029,7 @@ __device__ void draw_pass(const HArgs& a, float cv, int32_t ct, bool mp_on, floa
     const Philox4 r = philox4x32_10(static_cast<uint32_t>(t) >> 2, pos, rid, stream, k0, k1);
     consider(y, t, r.w[t & 3]);
   }
-#ifdef SS_HIST_STAMPS
-  if (blockIdx.x < kStampCtas) {
-    if (threadIdx.x == 0) {
-      g_stamps[blockIdx.x][43] = n_vec;
-      g_stamps[blockIdx.x][44] = n_philox;
-      g_stamps[blockIdx.x][45] = n_score;
-    }
-  }
-#endif
+
 }
 
 // |K| and its fixed-point mass for rows whose K is a plain predicate (no
@@ -1368,6 +1369,324 @@ __device__ void above_value(const HArgs& a, float v) {
   __syncthreads();
 }
 
+// Sorts kFastCap (2048) keys ascending: a bitonic network with four keys per
+// thread in registers; strides 1 and 2 stay in the thread, strides 4 to 64 go
+// through warp shuffles, and only strides of 128 and more through shared
+// memory (10 of the network's 66 stages, two block barriers each).  Called by
+// all threads; ends with a block barrier.
+__device__ __noinline__ void sort_fast_cap(unsigned long long* key) {
+  static_assert(kFastCap == 4 * kThreads, "four keys per thread");
+  const int tid = threadIdx.x;
+  const int e0 = 4 * tid;  // this thread's first element
+  unsigned long long v0 = key[e0], v1 = key[e0 + 1], v2 = key[e0 + 2], v3 = key[e0 + 3];
+  auto cas = [](unsigned long long& lo, unsigned long long& hi, bool asc) {
+    if ((lo > hi) == asc) {
+      const unsigned long long t = lo;
+      lo = hi;
+      hi = t;
+    }
+  };
+  auto merge = [](unsigned long long mine, unsigned long long other, bool keep_min) {
+    return keep_min ? (mine < other ? mine : other) : (mine > other ? mine : other);
+  };
+  for (int k = 2; k <= kFastCap; k <<= 1) {
+    const bool asc = (e0 & k) == 0;  // k >= 4: the same for the thread's four elements
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= 128) {
+        __syncthreads();  // the previous stage's reads are done
+        key[e0] = v0;
+        key[e0 + 1] = v1;
+        key[e0 + 2] = v2;
+        key[e0 + 3] = v3;
+        __syncthreads();
+        const bool keep_min = ((e0 & j) == 0) == asc;  // the lower of the pair keeps the minimum when ascending
+        v0 = merge(v0, key[e0 ^ j], keep_min);
+        v1 = merge(v1, key[(e0 + 1) ^ j], keep_min);
+        v2 = merge(v2, key[(e0 + 2) ^ j], keep_min);
+        v3 = merge(v3, key[(e0 + 3) ^ j], keep_min);
+      } else if (j >= 4) {
+        const int lj = j >> 2;
+        const bool keep_min = ((e0 & j) == 0) == asc;
+        v0 = merge(v0, __shfl_xor_sync(0xffffffffu, v0, lj), keep_min);
+        v1 = merge(v1, __shfl_xor_sync(0xffffffffu, v1, lj), keep_min);
+        v2 = merge(v2, __shfl_xor_sync(0xffffffffu, v2, lj), keep_min);
+        v3 = merge(v3, __shfl_xor_sync(0xffffffffu, v3, lj), keep_min);
+      } else if (j == 2) {
+        const bool a = (k == 2) ? true : asc;
+        cas(v0, v2, a);
+        cas(v1, v3, a);
+      } else {
+        // k == 2: pairs (0,1) ascending, (2,3) descending; k >= 4: both by asc
+        cas(v0, v1, (k == 2) ? true : asc);
+        cas(v2, v3, (k == 2) ? false : asc);
+      }
+    }
+  }
+  __syncthreads();
+  key[e0] = v0;
+  key[e0 + 1] = v1;
+  key[e0 + 2] = v2;
+  key[e0 + 3] = v3;
+  __syncthreads();
+}
+
+// ------------------------------------------------------------ short path --
+// Rows with 0 < top_k <= kFastK and a top-k certificate: every item of K has
+// y >= y(tau) (at least k staged tokens are >= tau), so the candidates --
+// staged tokens at or above tau and entries at or above y(tau) -- hold K.
+// Every CTA pushes its candidates into rank 0; when they fit, rank 0 sorts
+// them by (y desc, token asc) and takes every cut (top-k, top-p over the
+// top-k's fixed-point masses, min-p) and the draw itself: the items of K are
+// then the first L of that order, ties included.  Returns false (in every CTA
+// alike) when the candidates do not fit and the row takes the histogram path.
+// Called by all threads of every CTA; ends with rank 0's decisions in
+// token / accept / kept.
+__device__ bool short_path(const HArgs& a, bool tests_draft, const float* qrow, int32_t& token, int32_t& accept,
+                           unsigned long long& kept) {
+  Ctx& c = g;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = static_cast<int>(cl.block_rank());
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint4* data = reinterpret_cast<const uint4*>(g_dyn);
+  const uint16_t* vb = reinterpret_cast<const uint16_t*>(g_dyn + a.o_vb);
+  const unsigned long long* el = reinterpret_cast<const unsigned long long*>(g_dyn + a.o_el);
+  // candidates, first in this CTA's histogram region, then its sorted run
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(g_dyn + a.o_hist);
+  unsigned long long* run = reinterpret_cast<unsigned long long*>(g_dyn + a.o_xm);  // xm and mg, contiguous
+  int32_t* rcount = cl.map_shared_rank(&g_fcount, 0);
+  const uint32_t tau = c.tau_key;
+  const float inv_t = c.inv_t;
+  const float ytau = __fmul_rn(bf16_to_f(key16_bits(tau)), inv_t);
+  if (tid == 0) g.n_g = 0;
+  __syncthreads();
+  // append: one reservation per warp and round
+  auto append = [&](int n_mine, auto&& item) {
+    int inc = n_mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const int tot = __shfl_sync(0xffffffffu, inc, 31);
+    int base = 0;
+    if (lane == 31 && tot) base = atomicAdd(&g.n_g, tot);
+    base = __shfl_sync(0xffffffffu, base, 31) + inc - n_mine;
+    for (int i = 0; i < n_mine; ++i)
+      if (base + i < kFastCap) cand[base + i] = item(i);
+  };
+  for (int p0 = 0; p0 < c.nvec / 2; p0 += kThreads) {
+    const int p = p0 + tid;
+    uint32_t hit = 0;  // bit e: token e of the pair is a candidate
+    uint4 d0 = make_uint4(0, 0, 0, 0), d1 = d0;
+    if (p < c.nvec / 2 && vb[p] != 0xff80u && key16(vb[p]) >= tau) {
+      d0 = data[2 * p];
+      d1 = data[2 * p + 1];
+      const uint32_t w[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const uint32_t h = (w[e >> 1] >> ((e & 1) ? 16 : 0)) & 0xffffu;
+        if (h != 0xff80u && key16(h) >= tau) hit |= 1u << e;
+      }
+    }
+    const uint32_t wds[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+    append(__popc(hit), [&](int i) {
+      uint32_t m = hit;
+      for (int j = 0; j < i; ++j) m &= m - 1;
+      const int e = __ffs(m) - 1;
+      const uint32_t h = (wds[e >> 1] >> ((e & 1) ? 16 : 0)) & 0xffffu;
+      return ekey(__fmul_rn(bf16_to_f(h), inv_t), c.lo + p * 16 + e);
+    });
+  }
+  for (int i0 = 0; i0 < c.ne; i0 += kThreads) {
+    const int i = i0 + tid;
+    const bool take = i < c.ne && ekey_y(el[i]) >= ytau;
+    append(take ? 1 : 0, [&](int) { return el[i]; });
+  }
+  __syncthreads();
+  const int nr = g.n_g;  // this CTA's candidates
+  // this CTA's sorted run: a rank sort while small, else the bitonic network
+  const unsigned long long* srun = run;
+  if (nr <= kRankSortMax) {
+    for (int i = tid; i < nr; i += kThreads) {
+      const unsigned long long k = cand[i];
+      int r = 0;
+      for (int j = 0; j < nr; ++j) r += (cand[j] < k) ? 1 : 0;
+      run[r] = k;
+    }
+  } else if (nr <= kFastCap) {
+    for (int i = nr + tid; i < kFastCap; i += kThreads) cand[i] = ~0ull;
+    __syncthreads();
+    sort_fast_cap(cand);
+    srun = cand;
+  }
+  // this CTA's run, recorded in rank 0 (its length and which region holds it)
+  if (tid == 0) {
+    if (nr > 0) atomicAdd(rcount, nr);
+    *cl.map_shared_rank(&g_runs[rank][0], 0) = (srun == cand) ? 1 : 0;
+    *cl.map_shared_rank(&g_runs[rank][1], 0) = nr;
+  }
+  SS_STAMP(38);
+  cl.sync();  // every CTA has its sorted run, and rank 0 its slice no more
+  SS_STAMP(42);
+  const int n = *rcount;
+  SS_TRACE(43, n);
+  if (n > kFastCap) return false;
+  if (rank != 0) return true;  // (its run stays put until the kernel's last cluster barrier)
+  // rank 0 pulls every run into its slice region, one after the other
+  const int C = static_cast<int>(cl.num_blocks());
+  unsigned long long* mbuf = reinterpret_cast<unsigned long long*>(g_dyn);
+  SS_STAMP(41);
+  if (tid == 0) {
+    int off = 0;
+    for (int r = 0; r < C; ++r) {
+      g_runs[r][0] |= off << 1;  // bit 0: the region; the rest: the run's start in mbuf
+      off += g_runs[r][1];
+    }
+  }
+  __syncthreads();
+  // (one pass over all items: every remote load in flight at once)
+  for (int i = tid; i < n; i += kThreads) {
+    int r = 0;
+    while (r + 1 < C && (g_runs[r + 1][0] >> 1) <= i) ++r;
+    const unsigned long long* src = cl.map_shared_rank((g_runs[r][0] & 1) ? cand : run, r);
+    mbuf[i] = src[i - (g_runs[r][0] >> 1)];
+  }
+  __syncthreads();
+  SS_STAMP(44);
+
+  // ---- rank 0: merge the runs by rank: an item's place is its index in its
+  // run plus, for every other run, how many of its items are smaller (a few
+  // items: counted against all of them; else binary searches in all runs at
+  // once, their steps interleaved so that the loads overlap)
+  unsigned long long* sorted = cand;
+  if (n <= 256) {
+    for (int i = tid; i < n; i += kThreads) {
+      const unsigned long long k = mbuf[i];
+      int place = 0;
+      for (int j = 0; j < n; ++j) place += (mbuf[j] < k) ? 1 : 0;
+      sorted[place] = k;
+    }
+  } else {
+    int rs[kMaxCluster + 1];
+#pragma unroll
+    for (int q = 0; q <= kMaxCluster; ++q) rs[q] = (q < C) ? (g_runs[q][0] >> 1) : n;
+    for (int i = tid; i < n; i += kThreads) {
+      const unsigned long long k = mbuf[i];
+      int lo[kMaxCluster], hi[kMaxCluster];
+#pragma unroll
+      for (int q = 0; q < kMaxCluster; ++q) {
+        lo[q] = rs[q];
+        hi[q] = (q < C) ? rs[q + 1] : rs[q];
+        if (i >= lo[q] && i < hi[q]) hi[q] = lo[q] = i;  // its own run: its index there
+      }
+      for (int step = 0; step < 12; ++step) {  // runs hold at most 2048 items
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q)
+          if (lo[q] < hi[q]) {
+            const int mid = (lo[q] + hi[q]) >> 1;
+            if (mbuf[mid] < k)
+              lo[q] = mid + 1;
+            else
+              hi[q] = mid;
+          }
+      }
+      int place = 0;
+#pragma unroll
+      for (int q = 0; q < kMaxCluster; ++q) place += lo[q] - rs[q];
+      sorted[place] = k;
+    }
+  }
+  SS_STAMP(45);
+  if (tid == 0) {
+    g_fpos[0] = 0x7fffffff;
+    g_fpos[1] = 0x7fffffff;
+    g_fpos[2] = -1;
+  }
+  __syncthreads();
+  SS_STAMP(46);
+
+  // ---- the cuts: prefix masses of the top k (two items per thread, in order)
+  const int kk = min(c.top_k, n);
+  const float m = c.m;
+  const int i0 = 2 * tid;
+  unsigned long long w0 = 0, w1 = 0;
+  if (i0 < kk) w0 = fmass(ekey_y(sorted[i0]), m);
+  if (i0 + 1 < kk) w1 = fmass(ekey_y(sorted[i0 + 1]), m);
+  unsigned long long ic = 0, im = w0 + w1, tc, tm;
+  block_scan2(ic, im, &tc, &tm);
+  const unsigned long long before = im - (w0 + w1);
+  const unsigned long long Sk = tm;
+  const unsigned long long T = c.p_on ? mass_target(c.top_p, Sk) : ~0ull;
+  if (c.p_on) {
+    if (i0 < kk && before + w0 >= T) atomicMin(&g_fpos[0], i0 + 1);
+    else if (i0 + 1 < kk && before + w0 + w1 >= T) atomicMin(&g_fpos[0], i0 + 2);
+  }
+  if (c.mp_on) {
+    for (int i = i0; i < min(i0 + 2, kk); ++i)
+      if (!(__fsub_rn(ekey_y(sorted[i]), m) >= c.lmp)) {
+        atomicMin(&g_fpos[1], i);
+        break;
+      }
+  }
+  __syncthreads();
+  const int L = max(1, min(kk, min(g_fpos[0], g_fpos[1])));
+  // the kept mass: the prefix through item L - 1
+  if (i0 == L - 1) c.kmass = before + w0;
+  if (i0 + 1 == L - 1) c.kmass = before + w0 + w1;
+  if (tests_draft)
+    for (int i = tid; i < L; i += kThreads)
+      if (ekey_t(sorted[i]) == c.x) g_fpos[2] = i;
+  __syncthreads();
+  kept = static_cast<unsigned long long>(L);
+  if (tid == 0) c.kcount = kept;
+  SS_STAMP(40);
+
+  // ---- the draw, over the first L items
+  const uint32_t k0 = c.seed_lo, k1 = c.seed_hi;
+  auto draw = [&](bool res, float inv_s) -> int32_t {
+    float bs = ninf();
+    int32_t bt = 0x7fffffff;
+    for (int i = tid; i < L; i += kThreads) {
+      const float y = ekey_y(sorted[i]);
+      const int32_t t = ekey_t(sorted[i]);
+      const uint32_t num = uniform_numerator(
+          philox4x32_10(static_cast<uint32_t>(t) >> 2, c.pos, c.rowid, res ? 2u : 0u, k0, k1).w[t & 3]);
+      const float sc = res ? draw_score<true>(y, t, num, kGumbelMax, m, inv_s, qrow, ninf())
+                           : draw_score<false>(y, t, num, kGumbelMax, m, 0.0f, nullptr, ninf());
+      if (sc > ninf() && beats(sc, t, bs, bt)) {
+        bs = sc;
+        bt = t;
+      }
+    }
+    block_best(bs, bt);
+    return bt;
+  };
+  bool need_draw = !tests_draft;
+  if (tests_draft) {
+    const float SK = static_cast<float>(static_cast<double>(c.kmass) * (1.0 / 1099511627776.0));
+    const float inv_s = __frcp_rn(SK);
+    const int xi = g_fpos[2];
+    const float Px = (xi >= 0) ? __fmul_rn(__expf(__fsub_rn(ekey_y(sorted[xi]), m)), inv_s) : 0.0f;
+    const float q = qrow[c.x];
+    const float u = uniform_from_numerator(uniform_numerator(philox4x32_10(0u, c.pos, c.rowid, 1u, k0, k1).w[0]));
+    accept = (__fmul_rn(u, q) < Px) ? 1 : 0;
+    if (!accept && tid == 0) atomicMax(a.ws_counters + c.nreq + c.req, kRejBase - c.j);
+    if (accept) {
+      token = c.x;
+    } else if (c.skip_draw) {
+      token = -1;
+    } else {
+      const int32_t t = draw(true, inv_s);
+      if (t != 0x7fffffff)
+        token = t;
+      else
+        need_draw = true;  // an empty residual (rounding): the stream-0 draw
+    }
+  }
+  if (need_draw) token = c.skip_draw ? -1 : draw(false, 0.0f);
+  return true;
+}
+
 // Index cutoff for the items of value v when `take` of them (by index) are
 // kept.  The CTAs hold increasing index ranges, so the take-th item lies in
 // one CTA (tie_rank): CTAs before it keep all their items of value v, CTAs
@@ -1582,7 +1901,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     hval[s] = 0.0f;
     hraw[s] = 0;
   }
-  if (tid < kCertBins) g_cert[tid] = 0;
+  if (tid < kCertBins / 2) g_cert[tid] = 0;
   __syncthreads();
   SS_STAMP(20);
   const int32_t V = a.vocab, lo = c.lo, n = c.n;
@@ -1877,7 +2196,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         if (bf16_to_f(d16[e]) == zmax) garg = lo + gvec * 16 + e;
     }
     // top-k rows: pairs per binade below this CTA's maximum (the certificate)
-    const uint32_t zbin = key16(__float_as_uint(zmax) >> 16) >> 7;
+    const uint32_t zbin = key16(__float_as_uint(zmax) >> 16) >> kCertShift;
     if (c.k_on) {
       const int lane = tid & 31;
       for (int p0 = 0; p0 < c.nvec / 2; p0 += kThreads) {
@@ -1885,18 +2204,13 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         int d = -1;
         if (p < c.nvec / 2) {
           const uint32_t h = vb[p];
-          if (h != 0xff80u) d = static_cast<int>(zbin) - static_cast<int>(key16(h) >> 7);
+          if (h != 0xff80u) d = static_cast<int>(zbin) - static_cast<int>(key16(h) >> kCertShift);
         }
         if (d >= kCertBins) d = -1;
-        // warp-aggregated counts: one atomic per distinct binade in the warp
-        uint32_t todo = __ballot_sync(0xffffffffu, d >= 0);
-        while (todo) {
-          const int leader = __ffs(todo) - 1;
-          const int dl = __shfl_sync(0xffffffffu, d, leader);
-          const uint32_t same = __ballot_sync(0xffffffffu, d == dl);
-          if (lane == leader) atomicAdd(&g_cert[dl], static_cast<uint32_t>(__popc(same)));
-          todo &= ~same;
-        }
+        // warp-aggregated counts: one atomic per distinct bin in the warp
+        const uint32_t same = __match_any_sync(0xffffffffu, d);
+        if (d >= 0 && lane == __ffs(same) - 1)
+          atomicAdd(&g_cert[d >> 1], static_cast<uint32_t>(__popc(same)) << ((d & 1) << 4));
       }
     }
     // the draft token's processed value, in the CTA that owns it
@@ -1935,7 +2249,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       p.xhere = xhere;
       p.zbin = static_cast<int32_t>(zbin);
       p.rej = rej_seen;
-      for (int b = 0; b < kCertBins; ++b) p.cert[b] = c.k_on ? g_cert[b] : 0u;
+      for (int b = 0; b < kCertBins / 2; ++b) p.cert[b] = c.k_on ? g_cert[b] : 0u;
     }
     __syncthreads();
     SS_STAMP(13);
@@ -1974,6 +2288,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         c.skip_draw = rj > kRejBase - c.j;  // the same in every CTA
       }
       c.tau_key = 0;
+      c.tau_pairs = 0;
       c.pick = zb;
       c.arg = arg;
       c.status = st1;
@@ -1983,26 +2298,35 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       if (c.x < 0) c.xy = ninf();
     }
     __syncthreads();
-    // top-k: the highest binade boundary with at least k tokens at or above
-    // it (pairs whose maximum is at or above it, summed over the cluster);
-    // one lane per binade, then a warp prefix
+    // top-k: the highest bin boundary with at least k tokens at or above it
+    // (pairs whose maximum is at or above it, summed over the cluster); lane
+    // l takes bins 2l and 2l + 1, then a warp prefix
     if (c.k_on && tid < 32) {
-      const int zb = c.pick, d = tid;
-      uint32_t cnt = 0;
-      if (zb >= 0 && d < kCertBins && d < zb)
-        for (int r = 0; r < C; ++r) {
-          const Part1& p = g_p1[r];
-          const int dd = d - (zb - p.zbin);  // the same binade in rank r's counts
-          if (p.zmax != ninf() && dd >= 0 && dd < kCertBins) cnt += p.cert[dd];
-        }
-      unsigned long long cum = cnt;
+      const int zb = c.pick;
+      uint32_t cnt[2] = {0, 0};
+      for (int h = 0; h < 2; ++h) {
+        const int d = 2 * tid + h;
+        if (zb >= 0 && d < zb)
+          for (int r = 0; r < C; ++r) {
+            const Part1& p = g_p1[r];
+            const int dd = d - (zb - p.zbin);  // the same bin in rank r's counts
+            if (p.zmax != ninf() && dd >= 0 && dd < kCertBins) cnt[h] += (p.cert[dd >> 1] >> ((dd & 1) << 4)) & 0xffffu;
+          }
+      }
+      unsigned long long cum = cnt[0] + cnt[1];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const unsigned long long y = __shfl_up_sync(0xffffffffu, cum, o);
         if (tid >= o) cum += y;
       }
-      const unsigned ball = __ballot_sync(0xffffffffu, cum >= static_cast<unsigned long long>(c.top_k));
-      if (ball && tid == __ffs(ball) - 1) c.tau_key = static_cast<uint32_t>(zb - d) << 7;
+      const unsigned long long lo = cum - cnt[1];  // through bin 2l
+      const unsigned long long k = static_cast<unsigned long long>(c.top_k);
+      const unsigned ball = __ballot_sync(0xffffffffu, cum >= k);
+      if (ball && tid == __ffs(ball) - 1) {
+        const int d = (lo >= k) ? 2 * tid : 2 * tid + 1;
+        c.tau_key = static_cast<uint32_t>(zb - d) << kCertShift;
+        c.tau_pairs = (lo >= k) ? lo : cum;
+      }
     }
     __syncthreads();
   }
@@ -2030,7 +2354,8 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         token = accept ? c.x : c.arg;
         if (!accept && rank == 0 && tid == 0) atomicMax(a.ws_counters + c.nreq + c.req, kRejBase - c.j);
       }
-    } else {
+    } else if (!(c.k_on && c.tau_key != 0 && c.top_k <= kFastK && c.tau_pairs <= kFastCap &&
+                 short_path(a, tests_draft, qrow, token, accept, kept))) {
       float cv = ninf();
       int32_t ct = -1;
       bool mp_on = c.mp_on != 0;
