@@ -588,45 +588,67 @@ def run_tree(args, ss, rank, dev, stream):
 
 
 def run_sharded(args, ss, rank, dev, stream, parts=4):
-    """The vocabulary-sharded path on one GPU: `parts` shard launches and
-    one merge per call, on the headline workload with a top-k of 200 given
-    to its top-p / min-p rows (the sharded path needs one)."""
+    """The vocabulary-sharded path on one GPU, on the headline workload as it
+    is: `parts` shard launches and one merge for the top-k rows (the list
+    path), then four rounds of `parts` shard launches and one merge for the
+    top-p / min-p rows without top-k, all into the same outputs.  The shards
+    of a step run on one stream each (on P GPUs they would run at the same
+    time), forked from and joined back into the call's stream."""
     import torch
-    ring_host = [W.shardable(workload_for(2, rank, i)) for i in range(max(2, args.ring // 2))]
+    ring_host = [workload_for(2, rank, i) for i in range(max(2, args.ring // 2))]
     ring = [ss.to_device(w, dev) for w in ring_host]
     n = int(ring_host[0]["num_rows"])
     V = int(ring_host[0]["vocab"])
     cap = 1024
     bounds = W.even_shards(V, parts)
     recs = [torch.empty(n * ss.ss_shard_record_bytes(cap), dtype=torch.uint8, device=dev) for _ in bounds]
+    rrecs = [torch.empty(n * ss.ss_shard_round_record_bytes(), dtype=torch.uint8, device=dev) for _ in bounds]
+    state = torch.empty(ss.ss_shard_round_state_bytes(n), dtype=torch.uint8, device=dev)
     tok = torch.empty(n, dtype=torch.int32, device=dev)
     st = torch.empty(n, dtype=torch.int32, device=dev)
     kept = torch.empty(n, dtype=torch.int32, device=dev)
-
-    # the shards are independent (on P GPUs they would run at the same time):
-    # one stream each, forked from and joined back into the call's stream
     shard_streams = [torch.cuda.Stream(device=dev) for _ in bounds]
     fork = torch.cuda.Event()
     joins = [torch.cuda.Event() for _ in bounds]
 
-    def call(dw):
-        params = {k: dw.get(k) for k in ss.PARAM_FIELDS}
-        params["bitmask_stride"] = dw.get("bitmask_stride", 0)
+    def shards(launch):
         fork.record(stream)
-        for (off, length), rec, sst, jn in zip(bounds, recs, shard_streams, joins):
+        for i, (sst, jn) in enumerate(zip(shard_streams, joins)):
             sst.wait_event(fork)
-            ss.ss_sample_shard(dw["logits"][:, off:], params, rec, vocab=V, vocab_offset=off, shard_len=length,
-                               list_cap=cap, num_rows=n, dtype=dw["dtype"], row_stride=int(dw["row_stride"]),
-                               stream=sst)
+            launch(i, sst)
             jn.record(sst)
         for jn in joins:
             stream.wait_event(jn)
+
+    def call(dw):
+        params = {k: dw.get(k) for k in ss.PARAM_FIELDS}
+        params["bitmask_stride"] = dw.get("bitmask_stride", 0)
+        stride = int(dw["row_stride"])
+
+        def list_shard(i, sst):
+            off, length = bounds[i]
+            ss.ss_sample_shard(dw["logits"][:, off:], params, recs[i], vocab=V, vocab_offset=off, shard_len=length,
+                               list_cap=cap, num_rows=n, dtype=dw["dtype"], row_stride=stride, stream=sst)
+        shards(list_shard)
         ss.ss_merge_shards(recs, params, tok, st, vocab=V, list_cap=cap, out_kept=kept, stream=stream)
+        for rnd in range(4):
+            def round_shard(i, sst, rnd=rnd):
+                off, length = bounds[i]
+                ss.ss_shard_round(dw["logits"][:, off:], params, state, rrecs[i], round=rnd, vocab=V,
+                                  vocab_offset=off, shard_len=length, num_rows=n, dtype=dw["dtype"],
+                                  row_stride=stride, stream=sst)
+            shards(round_shard)
+            ss.ss_merge_round(rrecs, params, state, tok, st, round=rnd, vocab=V, out_kept=kept, stream=stream)
 
     with torch.cuda.stream(stream):
         for dw in ring:
             call(dw)
     stream.synchronize()
+    # the sharded outputs of the last input set equal a single call's
+    ref = ss.alloc_outputs(ring[-1], dev)
+    ss.run(ring[-1], ref, stream=stream)
+    stream.synchronize()
+    same = all(torch.equal(x, ref[k]) for x, k in ((tok, "token"), (st, "status"), (kept, "kept")))
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
@@ -646,9 +668,12 @@ def run_sharded(args, ss, rank, dev, stream, parts=4):
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
     calls = reps * len(ring)
-    return {"workload": W.CONFIG_NAMES[2] + ", top-p / min-p rows with top-k 200", "shards": len(bounds),
+    return {"workload": W.CONFIG_NAMES[2], "shards": len(bounds),
             "rows_per_s": n * calls / (ms / 1e3), "ms_per_call": ms / calls, "calls": calls,
-            "launches_per_call": len(bounds) + 1, "shard_launches": "concurrent, one stream each"}
+            "launches_per_call": 5 * (len(bounds) + 1),
+            "equal_to_single_call": bool(same),
+            "path": "top-k rows: one shard launch each + merge; top-p / min-p rows without top-k: four rounds "
+                    "of one launch per shard + merge; shard launches concurrent, one stream each"}
 
 
 def run_fused(args, ss, dev, stream, peak):

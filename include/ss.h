@@ -99,8 +99,11 @@ enum {
                             frequency / presence / bias value non-finite, negative list
                             length, position outside [0, 2^32 - 1 - k], k > max_draft */
   SS_ROW_TIMEOUT = 5,    /* a bounded wait for an asynchronous copy gave up         */
-  SS_ROW_LIMIT = 6,      /* more distinct penalised/biased tokens in one vocabulary
-                            slice than the slice's table holds (SS_MAX_PATCHED)     */
+  SS_ROW_LIMIT = 6,      /* an implementation capacity: more distinct penalised /
+                            biased tokens in one vocabulary slice than its table
+                            holds (SS_MAX_PATCHED), or (bf16 logits) a cut the
+                            kernel cannot place within its slot window or gather
+                            buffers; never seen on the benchmark workloads       */
   SS_ROW_UNSUPPORTED = 7 /* vocabulary-sharded path only: top-p or min-p without
                             top-k, or top_k above the records' list capacity      */
 };
@@ -174,23 +177,31 @@ typedef struct {
 } ss_verify_args;
 
 /* Bytes of caller-owned device workspace ss_spec_verify needs for up to
- * `max_requests` requests with up to `max_draft` drafts each (per-position
- * results and one arrival counter per request). */
+ * `max_requests` requests with up to `max_draft` drafts each: per-position
+ * results (16 B each) at its start, and two words per request at its end (an
+ * arrival counter and a rejection word).  Returns 0 for a negative argument or
+ * max_draft above 2^20.  A buffer sized for (R, k) serves any call with at
+ * most R requests and k drafts, in any order of shapes: the per-request words
+ * are placed from the buffer's end, so no shape puts them where another shape
+ * left its results. */
 size_t ss_workspace_size(int32_t max_requests, int32_t max_draft);
 
 /* Zero a workspace before its first use (cudaMemsetAsync on `stream`).  Every
- * ss_spec_verify call leaves the counters at zero again, so this is needed
- * once per buffer.  Calls sharing one workspace must not overlap in time. */
+ * ss_spec_verify call leaves its per-request words at zero again, so this is
+ * needed once per buffer.  Calls sharing one workspace must not overlap in
+ * time. */
 ss_status ss_workspace_init(void* workspace, size_t workspace_bytes, ss_stream_t stream);
 
-/* Batched sampling.  With 16 to 4096 rows and a vocabulary whose cluster
- * can double (ss_cluster_size <= 4), the rows with a top-p cut and no top-k
- * run on a second launch with twice the CTAs per row, on a library-owned
- * stream (one per host thread and device, created by the first such call)
- * forked from and joined back into `stream` with events; otherwise one
- * launch.  Either way the call is asynchronous on `stream`, capturable in a
- * CUDA graph, and its results do not depend on the split.  A capture that
- * starts before the thread's first such call records the single launch. */
+/* Batched sampling.  bf16 logits: one launch of the histogram kernel (one
+ * thread-block cluster per row).  fp32 logits: with 16 to 4096 rows and a
+ * vocabulary whose cluster can double (ss_cluster_size <= 4), the rows with a
+ * top-p cut and no top-k run on a second launch with twice the CTAs per row,
+ * on a library-owned stream (one per host thread and device, created by the
+ * first such call) forked from and joined back into `stream` with events;
+ * otherwise one launch.  Either way the call is asynchronous on `stream`,
+ * capturable in a CUDA graph, and its results do not depend on the split.  A
+ * capture that starts before the thread's first such call records the single
+ * launch. */
 ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream);
 
 /* Self-test of the kernels' bounded waits (no counterpart in the pages; it
@@ -228,7 +239,7 @@ ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t wor
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
  *     stream capture.
- *   - Every call clears the per-request counters with cudaMemsetAsync on
+ *   - Every call clears the per-request words with cudaMemsetAsync on
  *     `stream`, then launches the verification kernel; the results are
  *     identical to ss_spec_verify's.
  *   - All calls on one device share the array: calls that overlap on the GPU
@@ -351,6 +362,43 @@ ss_status ss_sample_shard(const ss_sample_args* args, int32_t vocab_offset, int3
                           void* records, ss_stream_t stream);
 ss_status ss_merge_shards(const ss_sample_args* args, int32_t num_shards, void* const* records, int32_t list_cap,
                           ss_stream_t stream);
+
+/* ---------------------------------- shards: top-p / min-p without top-k --
+ * Rows whose kept set needs the whole distribution (top-p and / or min-p
+ * without a top-k; also greedy and unfiltered rows) over vocabulary shards,
+ * in four rounds.  Round i (0..3) is one ss_shard_round call per shard, then
+ * one ss_merge_round call over every shard's records; on P GPUs the records
+ * of a round are all-gathered before its merge.  What the rounds carry (the
+ * FlashSampling news page's grouped variants need this much because a top-p
+ * cut depends on the whole row's mass):
+ *   0. the shard's largest processed logit, greedy argument, allowed count
+ *      and status                    -> merge: the row maximum m; greedy and
+ *                                       failed rows are finished here
+ *   1. (top-p rows) the shard's fixed-point mass sum trunc(exp(y-m) 2^40)
+ *      and a count / mass histogram over 1024 buckets of y below m
+ *                                    -> merge: S, ceil(p S), the cut's bucket
+ *   2. (top-p rows) the shard's tokens in that bucket (at most 1024)
+ *                                    -> merge: the exact cut item, or the
+ *                                       min-p threshold when that is shorter
+ *   3. the shard's count of kept tokens and its best y + Gumbel noise
+ *                                    -> merge: token, status and |K| to
+ *                                       out_token / out_status / out_kept
+ * The outputs equal ss_process_sample's on the whole rows.  args as for
+ * ss_sample_shard (logits hold tokens [vocab_offset, vocab_offset +
+ * shard_len) of every row, row_stride >= shard_len; ids are global).  Rows
+ * with a top-k cut are left to ss_sample_shard / ss_merge_shards: the rounds
+ * do not write their outputs, so a batch mixing both kinds runs the list
+ * path's merge first, then the four rounds.  A row whose cut bucket holds
+ * more than 1024 tokens in one shard reports SS_ROW_LIMIT.  records: ss_shard_round_record_bytes() per row, 16-byte
+ * aligned, one buffer per shard (reused by every round); state:
+ * ss_shard_round_state_bytes(num_rows), written by the merges and read by
+ * the next round's shard calls.  All calls are asynchronous on `stream`. */
+size_t ss_shard_round_record_bytes(void);
+size_t ss_shard_round_state_bytes(int32_t num_rows);
+ss_status ss_shard_round(const ss_sample_args* args, int32_t vocab_offset, int32_t shard_len, int32_t round,
+                         const void* state, void* records, ss_stream_t stream);
+ss_status ss_merge_round(const ss_sample_args* args, int32_t num_shards, void* const* records, int32_t round,
+                         void* state, ss_stream_t stream);
 
 /* ------------------------------------------------ fused LM head + draw --
  * The LM-head matrix multiply fused with the draw (FlashSampling news page:

@@ -12,8 +12,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libss.so")
-SOURCES = ["ss_kernel.cu", "ss_hist.cu", "ss_fused.cu"]
-DEPS = ["ss_kernel.cu", "ss_hist.cu", "ss_hist.h", "ss_fused.cu", "ss_philox.cuh", "ss_ptx.cuh"]
+SOURCES = ["ss_kernel.cu", "ss_hist.cu", "ss_shard.cu", "ss_fused.cu"]
+DEPS = ["ss_kernel.cu", "ss_hist.cu", "ss_hist.h", "ss_shard.cu", "ss_fused.cu", "ss_philox.cuh", "ss_ptx.cuh"]
 
 NVCC_FLAGS = [
     "-std=c++17", "-O3", "-lineinfo",

@@ -130,6 +130,12 @@ SIGNATURES = {
     "ss_workspace_size": ([C.c_int32, C.c_int32], C.c_size_t),
     "ss_workspace_init": ([C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "ss_process_sample": ([C.POINTER(ss_sample_args), C.c_void_p], C.c_int),
+    "ss_shard_round_record_bytes": ([], C.c_size_t),
+    "ss_shard_round_state_bytes": ([C.c_int32], C.c_size_t),
+    "ss_shard_round": ([C.POINTER(ss_sample_args), C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                        C.c_void_p], C.c_int),
+    "ss_merge_round": ([C.POINTER(ss_sample_args), C.c_int32, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p],
+                       C.c_int),
     "ss_selftest_wait_timeout": ([C.POINTER(ss_sample_args), C.c_uint32, C.c_void_p], C.c_int),
     "ss_spec_verify": ([C.POINTER(ss_verify_args), C.c_void_p, C.c_size_t, C.c_void_p], C.c_int),
     "ss_spec_verify_noalloc": ([C.POINTER(ss_verify_args), C.c_void_p], C.c_int),
@@ -315,6 +321,41 @@ def ss_merge_shards(records, params, out_token, out_status, *, vocab, list_cap, 
     a.out_kept = _ptr(out_kept)
     ptrs = (C.c_void_p * len(records))(*[r.data_ptr() for r in records])
     _check(load().ss_merge_shards(C.byref(a), len(records), ptrs, int(list_cap), _stream_handle(stream)))
+
+
+def ss_shard_round_record_bytes():
+    return int(load().ss_shard_round_record_bytes())
+
+
+def ss_shard_round_state_bytes(num_rows):
+    return int(load().ss_shard_round_state_bytes(int(num_rows)))
+
+
+def ss_shard_round(logits, params, state, records, *, round, vocab, vocab_offset, shard_len, num_rows, dtype,
+                   row_stride=None, stream=None):
+    """One round of one vocabulary shard (rows without a top-k cut)."""
+    a = ss_sample_args()
+    a.num_rows = int(num_rows)
+    a.vocab = int(vocab)
+    a.row_stride = int(shard_len if row_stride is None else row_stride)
+    a.dtype = SS_DTYPE[dtype]
+    a.logits = _ptr(logits)
+    a.params = make_params(params)
+    _check(load().ss_shard_round(C.byref(a), int(vocab_offset), int(shard_len), int(round), _ptr(state),
+                                 _ptr(records), _stream_handle(stream)))
+
+
+def ss_merge_round(records, params, state, out_token, out_status, *, round, vocab, out_kept=None, stream=None):
+    """The merge of one round over every shard's records."""
+    a = ss_sample_args()
+    a.num_rows = int(out_token.numel())
+    a.vocab = int(vocab)
+    a.params = make_params(params)
+    a.out_token = _ptr(out_token)
+    a.out_status = _ptr(out_status)
+    a.out_kept = _ptr(out_kept)
+    ptrs = (C.c_void_p * len(records))(*[r.data_ptr() for r in records])
+    _check(load().ss_merge_round(C.byref(a), len(records), ptrs, int(round), _ptr(state), _stream_handle(stream)))
 
 
 def _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
