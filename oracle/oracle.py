@@ -136,6 +136,8 @@ def lib():
         L.or_uniform.restype = C.c_float
         L.or_gumbel.argtypes = [C.c_uint64, C.c_int32, C.c_uint32, C.c_int32, C.c_uint32]
         L.or_gumbel.restype = C.c_double
+        L.or_gumbel_row.argtypes = [C.c_uint64, C.c_int32, C.c_uint32, C.c_uint32, C.c_int32, C.c_void_p]
+        L.or_gumbel_row.restype = None
         L.or_process_sample.argtypes = [C.POINTER(_SampleIn), C.POINTER(_SampleOut)]
         L.or_process_sample.restype = C.c_int
         L.or_spec_verify.argtypes = [C.POINTER(_VerifyIn), C.POINTER(_VerifyOut)]
@@ -206,6 +208,13 @@ def uniform(seed, row, position, token, stream):
 
 def gumbel(seed, row, position, token, stream):
     return float(lib().or_gumbel(seed, row, position, token, stream))
+
+
+def gumbel_row(seed, row, position, vocab, stream=0):
+    """The Gumbel noise of every token of one row (fp64), stream 0 = the draw."""
+    out = np.zeros(int(vocab), np.float64)
+    lib().or_gumbel_row(seed, row, position, stream, int(vocab), out.ctypes.data)
+    return out
 
 
 def _sample_in(w, keep, force_kept=None):
@@ -392,6 +401,44 @@ def lmhead_logits(hidden_bits, weight_bits):
     h = (np.asarray(hidden_bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     w = (np.asarray(weight_bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return (h @ w.T).astype(np.float32)
+
+
+REL_MARGIN = 1e-5  # the decision margin of the C oracle (ss_oracle.c)
+
+
+def interval_flags(logits, bound, temperature, seed, position, row_id=None):
+    """Rows whose draw (temperature only: K is every token) can change when
+    each logit z_t may lie anywhere in [z_t - bound_t, z_t + bound_t]: logits
+    known only up to an error bound, such as an fp32 sum of many products.
+
+    The draw is Gumbel-max, argmax_t y_t + g_t with y_t = z_t * fp32(1/T)
+    (greedy, T = 0: argmax_t z_t), the lowest index among equals.  Each score
+    is an interval: the logit's bound scaled by 1/T, plus the oracle's own
+    margin of 1e-5 * max(1, |v|) on y_t and on g_t.  A row is flagged when
+    some other token's highest score reaches the winner's lowest (the same
+    test as the oracle's draw margin, with wider intervals)."""
+    z = np.asarray(logits, np.float32)
+    B, V = z.shape
+    bound = np.broadcast_to(np.asarray(bound, np.float64), (B, V))
+    flags = np.zeros(B, np.uint8)
+    margin = lambda v: REL_MARGIN * np.maximum(1.0, np.abs(v))
+    for r in range(B):
+        T = np.float32(temperature[r])
+        if T == 0:
+            sc = z[r].astype(np.float64)
+            unc = bound[r] + margin(sc)
+        else:
+            inv_t = np.float32(1.0) / T
+            y = (z[r] * inv_t).astype(np.float64)
+            rid = int(row_id[r]) if row_id is not None else r
+            g = gumbel_row(int(seed[r]), rid, int(position[r]), V)
+            sc = y + g
+            unc = bound[r] * float(inv_t) + margin(y) + margin(g)
+        b = int(np.argmax(sc))  # the first maximum: the lowest index
+        hi = sc + unc
+        hi[b] = -np.inf
+        flags[r] = 1 if np.any(hi >= sc[b] - unc[b]) else 0
+    return flags
 
 
 def lmhead_sample(w):

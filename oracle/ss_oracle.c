@@ -84,6 +84,12 @@ double or_gumbel(uint64_t seed, int32_t row, uint32_t position, int32_t token, u
   return -log(-log(u));
 }
 
+/* The Gumbel noise of tokens 0 .. vocab-1 of one row, position and stream. */
+void or_gumbel_row(uint64_t seed, int32_t row, uint32_t position, uint32_t stream, int32_t vocab, double* out) {
+  int32_t t;
+  for (t = 0; t < vocab; ++t) out[t] = or_gumbel(seed, row, position, t, stream);
+}
+
 /* ---------------------------------------------------------------- helpers -- */
 
 static float ld_logit(const void* base, int32_t dtype, int64_t idx) {

@@ -125,6 +125,9 @@ float or_uniform(uint64_t seed, int32_t row, uint32_t position, int32_t token, u
 /* Gumbel noise of that uniform, in fp64: -log(-log u). */
 double or_gumbel(uint64_t seed, int32_t row, uint32_t position, int32_t token, uint32_t stream);
 
+/* or_gumbel of tokens 0 .. vocab-1 (one row, position and stream) into out. */
+void or_gumbel_row(uint64_t seed, int32_t row, uint32_t position, uint32_t stream, int32_t vocab, double* out);
+
 /* Batched sampling over [num_rows, vocab] logits.  Returns 0.
  * When force_kept[r] > 0 lies in [kept_lo[r], kept_hi[r]] -- a kept-set size
  * that the top-p / min-p comparisons reach under a 1e-5 relative change of the

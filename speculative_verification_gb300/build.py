@@ -13,14 +13,14 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libss.so")
 SOURCES = ["ss_kernel.cu", "ss_hist.cu", "ss_shard.cu", "ss_fused.cu"]
-DEPS = ["ss_kernel.cu", "ss_hist.cu", "ss_hist.h", "ss_shard.cu", "ss_fused.cu", "ss_philox.cuh", "ss_ptx.cuh"]
+DEPS = ["ss_kernel.cu", "ss_hist.cu", "ss_hist.h", "ss_shard.cu", "ss_fused.cu", "ss_philox.cuh", "ss_ptx.cuh", "ss_nvtx.h"]
 
 NVCC_FLAGS = [
     "-std=c++17", "-O3", "-lineinfo",
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-Xcompiler", "-fPIC",
 ]
-LINK_FLAGS = ["-shared", "-gencode", "arch=compute_103a,code=sm_103a"]
+LINK_FLAGS = ["-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-ldl"]
 
 
 def nvcc():

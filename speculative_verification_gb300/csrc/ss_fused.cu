@@ -28,6 +28,7 @@
 #include <string.h>
 
 #include "ss.h"
+#include "ss_nvtx.h"
 #include "ss_philox.cuh"
 #include "ss_ptx.cuh"
 
@@ -392,6 +393,7 @@ size_t ss_fused_scratch_bytes(int32_t batch) {
 }
 
 ss_status ss_fused_lmhead_sample(const ss_fused_args* args, ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_fused_lmhead_sample");
   using namespace ssf;
   if (!args) return SS_ERR_INVALID_ARG;
   const ss_fused_args& A = *args;

@@ -52,6 +52,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "ss.h"
 #include "ss_hist.h"
@@ -375,7 +376,8 @@ __shared__ uint32_t g_rtie[kMaxCluster];
 __shared__ uint32_t g_cert[kCertBins / 2];  // two 16-bit bin counts per word
 __shared__ int32_t g_tietok[kTieEnt];
 __shared__ uint32_t g_prm[32];           // the request's parameter words
-__shared__ unsigned long long g_dbest;   // the draw's best key so far
+__shared__ uint32_t g_dscore;            // the draw's best score so far (order key; 0: none)
+__shared__ int32_t g_dtok;               // the lowest token holding it
 __shared__ int32_t g_fcount;             // short path: candidates gathered (rank 0's copy)
 __shared__ int32_t g_fpos[3];            // short path: first failing positions (top-p, min-p), draft position
 __shared__ int32_t g_runs[kMaxCluster][2];  // short path (rank 0): every CTA's run (start, length)
@@ -858,12 +860,14 @@ __device__ __forceinline__ bool in_cut(float y, int32_t t, float cv, int32_t ct)
 // Called by all threads.
 // With REDUCED the caller's (best, arg) is already the CTA's (the same in
 // every thread).
+// With SUMS and REDUCED both, the counts are summed (not the masses) and the
+// bests combined.
 template <bool SUMS, bool REDUCED>
 __device__ PartD exchange_d(float best, int32_t arg, int32_t count, unsigned long long mass) {
   cg::cluster_group cl = cg::this_cluster();
   if (SUMS) {
     count = block_sum<int32_t>(count);
-    mass = block_sum<unsigned long long>(mass);
+    if (!REDUCED) mass = block_sum<unsigned long long>(mass);
   } else if (REDUCED) {
     __syncthreads();
   } else {
@@ -893,7 +897,8 @@ __device__ PartD exchange_d(float best, int32_t arg, int32_t count, unsigned lon
     if (SUMS) {
       r.count += o.count;
       r.mass += o.mass;
-    } else if (beats(o.best, o.arg, r.best, r.arg)) {
+    }
+    if ((!SUMS || REDUCED) && beats(o.best, o.arg, r.best, r.arg)) {
       r.best = o.best;
       r.arg = o.arg;
     }
@@ -923,26 +928,32 @@ __device__ __noinline__ float draw_score(float y, int32_t t, uint32_t num, float
 
 // The draw over K (stream 0) or, with RES, over the residual
 // max(P - q, 0) (stream 2, log r + g); P(t) = exp(y - m) / S.  The CTA's
-// best (score, token) so far lives in g_dbest as one 64-bit key (score order
-// key, then the token's complement: the maximum is the best score, lowest
-// token among equals); every thread prunes against it, so a token whose
-// score bound is below the best of the whole CTA costs no logarithm.  g_dbest
-// must be 0 on entry (then a block barrier); cta_best() reads the result.
-// Entries are visited by the CTA that owns their token.
-__device__ __forceinline__ unsigned long long score_key(float s, int32_t t) {
-  return (static_cast<unsigned long long>(okey(s)) << 32) | static_cast<uint32_t>(~t);
+// best score so far lives in g_dscore as a 32-bit order key (a native shared
+// atomic maximum: a 64-bit (score, token) key would need a compare-and-swap
+// loop, and every thread's first candidate lands at once); every thread
+// prunes against it, so a token whose score bound is below the best of the
+// whole CTA costs no logarithm.  Each thread keeps its own best (score,
+// lowest token); after the pass the threads holding the CTA's best score
+// take the lowest token among them.  draw_reset() before the pass (then a
+// block barrier); cta_best() reads the result.  Entries are visited by the
+// CTA that owns their token.
+__device__ __forceinline__ void draw_reset() {
+  g_dscore = 0;
+  g_dtok = 0x7fffffff;
 }
 
 __device__ __forceinline__ void cta_best(float& bs, int32_t& bt) {
   __syncthreads();
-  const unsigned long long k = g_dbest;
-  bs = k ? okey_value(static_cast<uint32_t>(k >> 32)) : ninf();
-  bt = k ? static_cast<int32_t>(~static_cast<uint32_t>(k)) : 0x7fffffff;
+  const uint32_t k = g_dscore;
+  bs = k ? okey_value(k) : ninf();
+  bt = g_dtok;
 }
 
-template <bool RES>
+// With COUNT the pass also counts this thread's members of K (rows whose K
+// is a plain predicate: the count needs no pass of its own).
+template <bool RES, bool COUNT = false>
 __device__ void draw_pass(const HArgs& a, float cv, int32_t ct, bool mp_on, float inv_s, float log_s,
-                          const float* qrow, const unsigned long long* ents, int n_ents) {
+                          const float* qrow, const unsigned long long* ents, int n_ents, int32_t* count = nullptr) {
   const Ctx& c = g;
   const uint4* data = reinterpret_cast<const uint4*>(g_dyn);
   const uint16_t* vb = reinterpret_cast<const uint16_t*>(g_dyn + a.o_vb);
@@ -950,10 +961,11 @@ __device__ void draw_pass(const HArgs& a, float cv, int32_t ct, bool mp_on, floa
   const uint32_t k0 = c.seed_lo, k1 = c.seed_hi, pos = c.pos, rid = c.rowid;
   const uint32_t stream = RES ? 2u : 0u;
   float bs = ninf();                 // a lower bound of the CTA's best score
-  unsigned long long mine = 0;       // this thread's best key
+  float ms = ninf();                 // this thread's best (score, token)
+  int32_t mt = 0x7fffffff;
   auto refresh = [&]() {
-    const unsigned long long k = *reinterpret_cast<volatile unsigned long long*>(&g_dbest);
-    if (k) bs = fmaxf(bs, okey_value(static_cast<uint32_t>(k >> 32)));
+    const uint32_t k = *reinterpret_cast<volatile uint32_t*>(&g_dscore);
+    if (k) bs = fmaxf(bs, okey_value(k));
   };
   auto reach = [&](float y) -> float {
     return RES ? (y - m - log_s + kGumbelMax + 1e-3f + fabsf(y) * 1e-6f) : (y + kGumbelMax);
@@ -970,25 +982,28 @@ __device__ void draw_pass(const HArgs& a, float cv, int32_t ct, bool mp_on, floa
     // an upper bound of the base (for the residual log r <= log P), before
     // any logarithm or read of the draft's q
     const float base_ub = RES ? (y - m - log_s + 1e-3f + fabsf(y) * 1e-6f) : y;
-    if (base_ub + ub < bs) return;
+    if (base_ub + ub < bs || !member(y, t)) return;
 #ifdef SS_HIST_STAMPS
     ++n_score;
 #endif
     const float s = draw_score<RES>(y, t, num, ub, m, inv_s, qrow, bs);
-    if (s > ninf()) {
-      const unsigned long long k = score_key(s, t);
-      if (k > mine) {
-        mine = k;
-        atomicMax(&g_dbest, k);
-        bs = fmaxf(bs, s);
+    if (s > ninf() && beats(s, t, ms, mt)) {
+      ms = s;
+      mt = t;
+      // only a score at or above the CTA's best so far can still win (bs
+      // is always a score already published)
+      if (s >= bs) {
+        atomicMax(&g_dscore, okey(s));
+        bs = s;
       }
     }
   };
   const int nvec = c.nvec;
+  int32_t cnt = 0;
   for (int v = threadIdx.x; v < nvec; v += kThreads) {
     const float vy = __fmul_rn(bf16_to_f(vb[v >> 1]), inv_t);
     refresh();
-    if (vy < cv || vy == ninf() || reach(vy) < bs) continue;
+    if (vy < cv || vy == ninf() || (!COUNT && reach(vy) < bs)) continue;
     if (mp_on && !(__fsub_rn(vy, m) >= lmp)) continue;
 #ifdef SS_HIST_STAMPS
     ++n_vec;
@@ -996,28 +1011,67 @@ __device__ void draw_pass(const HArgs& a, float cv, int32_t ct, bool mp_on, floa
     const uint4 d = data[v];
     const uint32_t w[4] = {d.x, d.y, d.z, d.w};
     const int32_t t0 = c.lo + v * 8;
+    if (COUNT) {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float y[4];
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t word = w[e >> 1];
+        const float y = __fmul_rn((e & 1) ? __uint_as_float(word & 0xffff0000u) : __uint_as_float(word << 16), inv_t);
+        cnt += member(y, t0 + e) ? 1 : 0;
+      }
+      if (reach(vy) < bs) continue;
+    }
+    auto y_of = [&](int e) {
+      const uint32_t word = w[e >> 1];
+      return __fmul_rn((e & 1) ? __uint_as_float(word & 0xffff0000u) : __uint_as_float(word << 16), inv_t);
+    };
+    const uint32_t q0 = static_cast<uint32_t>(t0) >> 2;
+    if (RES) {
+      float y[8];
       bool any = false;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t word = w[half * 2 + (e >> 1)];
-        y[e] = __fmul_rn((e & 1) ? __uint_as_float(word & 0xffff0000u) : __uint_as_float(word << 16), inv_t);
-        const int32_t t = t0 + half * 4 + e;
-        const bool ok = member(y[e], t) && reach(y[e]) >= bs;
+      for (int e = 0; e < 8; ++e) {
+        y[e] = y_of(e);
+        const bool ok = member(y[e], t0 + e) && reach(y[e]) >= bs;
         if (!ok) y[e] = ninf();
         any |= ok;
       }
       if (!any) continue;
-      const int32_t tq = t0 + half * 4;
-#ifdef SS_HIST_STAMPS
-      ++n_philox;
-#endif
-      const Philox4 r = philox4x32_10(static_cast<uint32_t>(tq) >> 2, pos, rid, stream, k0, k1);
+      const Philox4 r0 = philox4x32_10(q0, pos, rid, stream, k0, k1);
+      const Philox4 r1 = philox4x32_10(q0 + 1u, pos, rid, stream, k0, k1);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (y[e] != ninf()) consider(y[e], tq + e, r.w[e]);
+      for (int e = 0; e < 8; ++e)
+        if (y[e] != ninf()) consider(y[e], t0 + e, (e < 4) ? r0.w[e] : r1.w[e - 4]);
+    } else {
+      // One noise threshold for the vector, from its largest y: a token can
+      // win only if its noise bound ln2 * (clz(2^24 - n) - 7) reaches
+      // D = bs - vy (less a slack far above the fp32 rounding), i.e. only if
+      // clz(2^24 - n) >= c = ceil(7 + D / ln2), i.e. 2^24 - n < 2^(32 - c);
+      // with n = 2 * (x >> 9) + 1 that is one comparison of the raw Philox
+      // word x.  Tokens past it get the exact tests (their own y, K).
+      uint32_t x_thr = 0;
+      if (bs > ninf()) {
+        const float D = bs - vy - 1e-3f * fmaxf(1.0f, fabsf(bs));
+        if (D > 0.0f) {
+          const float cf = ceilf(7.0f + D * 1.44269504f);
+          if (cf >= 32.0f) continue;  // no token of the vector can win
+          const int cc = static_cast<int>(cf);  // 8 .. 31
+          if (cc > 8) {
+            const uint32_t mthr = 1u << (32 - cc);  // <= 2^23
+            x_thr = (((1u << 24) - mthr - 1u) / 2u + 1u) << 9;
+          }
+        }
+      }
+#ifdef SS_HIST_STAMPS
+      n_philox += 2;
+#endif
+      // both halves' noise words at once: two independent Philox chains
+      const Philox4 r0 = philox4x32_10(q0, pos, rid, stream, k0, k1);
+      const Philox4 r1 = philox4x32_10(q0 + 1u, pos, rid, stream, k0, k1);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t x = (e < 4) ? r0.w[e] : r1.w[e - 4];
+        if (x >= x_thr) consider(y_of(e), t0 + e, x);
+      }
     }
   }
   for (int i = threadIdx.x; i < n_ents; i += kThreads) {
@@ -1025,11 +1079,16 @@ __device__ void draw_pass(const HArgs& a, float cv, int32_t ct, bool mp_on, floa
     const int32_t t = ekey_t(e);
     if (t < c.lo || t >= c.lo + c.n) continue;
     const float y = ekey_y(e);
+    if (COUNT) cnt += member(y, t) ? 1 : 0;
     if (!member(y, t) || reach(y) < bs) continue;
     const Philox4 r = philox4x32_10(static_cast<uint32_t>(t) >> 2, pos, rid, stream, k0, k1);
     consider(y, t, r.w[t & 3]);
   }
-
+  if (COUNT) *count = cnt;
+  // the lowest token among the threads holding the CTA's best score
+  __syncthreads();
+  const uint32_t best = g_dscore;
+  if (best && mt != 0x7fffffff && okey(ms) == best) atomicMin(&g_dtok, mt);
 }
 
 // |K| and its fixed-point mass for rows whose K is a plain predicate (no
@@ -2387,22 +2446,29 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         const uint32_t tau = c.tau_key;
         const float skip = (c.k_on) ? ninf() : __fsub_rn(c.m, kMassRange);
         uint32_t below = 0;
-        for (int v = tid; v < c.nvec; v += kThreads) {
-          const uint32_t hb = vb[v >> 1];
-          if (hb == 0xff80u || key16(hb) < tau || __fmul_rn(bf16_to_f(hb), inv_t) < skip) continue;
-          const uint4 d = data[v];
-          const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+        // (top-p rows have no certificate: their loop skips the key test)
+        auto count_pass_b = [&](auto with_tau) {
+          for (int v = tid; v < c.nvec; v += kThreads) {
+            const uint32_t hb = vb[v >> 1];
+            if (hb == 0xff80u || (with_tau.value && key16(hb) < tau) || __fmul_rn(bf16_to_f(hb), inv_t) < skip) continue;
+            const uint4 d = data[v];
+            const uint32_t w[4] = {d.x, d.y, d.z, d.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint32_t h = (w[e >> 1] >> ((e & 1) ? 16 : 0)) & 0xffffu;
-            if (key16(h) < tau) continue;
-            const int32_t s = slot_of(M, h);
-            if (static_cast<uint32_t>(s) < static_cast<uint32_t>(M.ns))
-              atomicAdd(hist + (s >> 1), 1u << ((s & 1) << 4));
-            else if (h != 0xff80u)
-              ++below;
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t h = (w[e >> 1] >> ((e & 1) ? 16 : 0)) & 0xffffu;
+              if (with_tau.value && key16(h) < tau) continue;
+              const int32_t s = slot_of(M, h);
+              if (static_cast<uint32_t>(s) < static_cast<uint32_t>(M.ns))
+                atomicAdd(hist + (s >> 1), 1u << ((s & 1) << 4));
+              else if (h != 0xff80u)
+                ++below;
+            }
           }
-        }
+        };
+        if (tau != 0)
+          count_pass_b(std::true_type{});
+        else
+          count_pass_b(std::false_type{});
         __syncthreads();  // group bounds and histogram complete
         SS_STAMP(4);
         // slot position and group of every local entry, its place within the
@@ -2640,8 +2706,10 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       if (c.status == SS_ROW_OK) {
         const unsigned long long* ents = el;
         const int n_ents = c.ne;
-        // |K| (and its mass) for rows without a histogram
-        if (!c.need_hist && (a.out_kept || tests_draft)) {
+        // |K| (and its mass) for rows without a histogram; a plain draw
+        // counts K itself
+        const bool fold_count = !c.need_hist && a.out_kept && !tests_draft && !c.skip_draw;
+        if (!c.need_hist && (a.out_kept || tests_draft) && !fold_count) {
           int32_t cnt = 0;
           unsigned long long mass = 0;
           count_pass(a, tests_draft, ents, n_ents, cnt, mass);
@@ -2673,7 +2741,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           } else {
             float bs;
             int32_t bt;
-            if (tid == 0) g_dbest = 0;
+            if (tid == 0) draw_reset();
             __syncthreads();
             draw_pass<true>(a, cv, ct, mp_on, inv_s, logf(SK), qrow, ents, n_ents);
             cta_best(bs, bt);
@@ -2689,13 +2757,23 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
         } else if (need_draw) {
           float bs;
           int32_t bt;
-          if (tid == 0) g_dbest = 0;
+          if (tid == 0) draw_reset();
           __syncthreads();
-          draw_pass<false>(a, cv, ct, mp_on, 0.0f, 0.0f, nullptr, ents, n_ents);
-          SS_STAMP(36);
-          cta_best(bs, bt);
-          const PartD r = exchange_d<false, true>(bs, bt, 0, 0);
-          token = r.arg;
+          if (fold_count) {
+            int32_t cnt = 0;
+            draw_pass<false, true>(a, cv, ct, mp_on, 0.0f, 0.0f, nullptr, ents, n_ents, &cnt);
+            SS_STAMP(36);
+            cta_best(bs, bt);
+            const PartD r = exchange_d<true, true>(bs, bt, cnt, 0);
+            token = r.arg;
+            kept = static_cast<unsigned long long>(r.count);
+          } else {
+            draw_pass<false>(a, cv, ct, mp_on, 0.0f, 0.0f, nullptr, ents, n_ents);
+            SS_STAMP(36);
+            cta_best(bs, bt);
+            const PartD r = exchange_d<false, true>(bs, bt, 0, 0);
+            token = r.arg;
+          }
         }
       }
     }

@@ -50,6 +50,7 @@
 #include <mutex>
 
 #include "ss.h"
+#include "ss_nvtx.h"
 #include "ss_hist.h"
 #include "ss_philox.cuh"
 #include "ss_ptx.cuh"
@@ -3056,6 +3057,7 @@ size_t ss_workspace_size(int32_t max_requests, int32_t max_draft) {
 }
 
 ss_status ss_workspace_init(void* workspace, size_t workspace_bytes, ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_workspace_init");
   if (!workspace) return SS_ERR_WORKSPACE;
   const cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
@@ -3083,6 +3085,7 @@ static ss_status check_sample(const ss_sample_args* args) {
 }
 
 ss_status ss_selftest_wait_timeout(const ss_sample_args* args, uint32_t polls, ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_selftest_wait_timeout");
   using namespace ss;
   const ss_status chk = check_sample(args);
   if (chk != SS_OK || args->num_rows == 0) return chk;
@@ -3093,6 +3096,7 @@ ss_status ss_selftest_wait_timeout(const ss_sample_args* args, uint32_t polls, s
 }
 
 ss_status ss_process_sample(const ss_sample_args* args, ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_process_sample");
   using namespace ss;
   const ss_status chk = check_sample(args);
   if (chk != SS_OK || args->num_rows == 0) return chk;
@@ -3123,6 +3127,7 @@ ss_status ss_commit_accepted(int32_t num_requests, int32_t max_draft, const int3
                              const int32_t* num_accepted, const int32_t* status, int32_t* tokens, int32_t capacity,
                              int32_t* seq_len, int64_t* position, int32_t* next_token, int32_t* commit_status,
                              ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_commit_accepted");
   using namespace ss;
   if (num_requests < 0 || max_draft < 0 || capacity < 1) return SS_ERR_INVALID_ARG;
   if (num_requests == 0) return SS_OK;
@@ -3147,6 +3152,7 @@ size_t ss_shard_record_bytes(int32_t list_cap) {
 
 ss_status ss_sample_shard(const ss_sample_args* args, int32_t vocab_offset, int32_t shard_len, int32_t list_cap,
                           void* records, ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_sample_shard");
   using namespace ss;
   if (!args) return SS_ERR_INVALID_ARG;
   const ss_sample_args& A = *args;
@@ -3181,6 +3187,7 @@ ss_status ss_sample_shard(const ss_sample_args* args, int32_t vocab_offset, int3
 
 ss_status ss_merge_shards(const ss_sample_args* args, int32_t num_shards, void* const* records, int32_t list_cap,
                           ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_merge_shards");
   using namespace ss;
   if (!args || !records) return SS_ERR_INVALID_ARG;
   const ss_sample_args& A = *args;
@@ -3217,6 +3224,7 @@ ss_status ss_merge_shards(const ss_sample_args* args, int32_t num_shards, void* 
 }
 
 ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t workspace_bytes, ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_spec_verify");
   using namespace ss;
   const ss_status chk = check_verify(args);
   if (chk != SS_OK || args->num_requests == 0) return chk;
@@ -3226,6 +3234,7 @@ ss_status ss_spec_verify(const ss_verify_args* args, void* workspace, size_t wor
 }
 
 ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t workspace_bytes, ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_tree_verify");
   using namespace ss;
   if (!args) return SS_ERR_INVALID_ARG;
   const ss_tree_args& A = *args;
@@ -3284,6 +3293,7 @@ void* g_noalloc_ptr[64] = {};  // device address of g_noalloc_scratch, per devic
 }  // namespace
 
 ss_status ss_spec_verify_noalloc(const ss_verify_args* args, ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_spec_verify_noalloc");
   using namespace ss;
   // every argument is checked before the shared scratch is touched: first
   // the batch against the scratch's size, then the rest

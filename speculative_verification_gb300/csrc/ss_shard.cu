@@ -26,6 +26,7 @@
 #include <algorithm>
 
 #include "ss.h"
+#include "ss_nvtx.h"
 #include "ss_philox.cuh"
 
 namespace ss {
@@ -602,6 +603,7 @@ size_t ss_shard_round_state_bytes(int32_t num_rows) {
 
 ss_status ss_shard_round(const ss_sample_args* args, int32_t vocab_offset, int32_t shard_len, int32_t round,
                          const void* state, void* records, ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_shard_round");
   using namespace ss::shard;
   if (!args) return SS_ERR_INVALID_ARG;
   const ss_sample_args& A = *args;
@@ -644,6 +646,7 @@ ss_status ss_shard_round(const ss_sample_args* args, int32_t vocab_offset, int32
 
 ss_status ss_merge_round(const ss_sample_args* args, int32_t num_shards, void* const* records, int32_t round,
                          void* state, ss_stream_t stream) {
+  SS_NVTX_RANGE("ss_merge_round");
   using namespace ss::shard;
   if (!args || !records || !state) return SS_ERR_INVALID_ARG;
   const ss_sample_args& A = *args;

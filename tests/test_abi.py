@@ -31,6 +31,22 @@ def test_every_declared_symbol_is_exported(lib):
         assert name in ss.SIGNATURES, name
 
 
+def test_every_call_that_enqueues_work_opens_an_nvtx_range():
+    # each public entry point returning ss_status names itself in one NVTX
+    # range (the calls that only answer a size or a string have none)
+    csrc = os.path.join(ROOT, "speculative_verification_gb300", "csrc")
+    found = {}
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith(".cu"):
+            text = open(os.path.join(csrc, f)).read()
+            for m in re.finditer(r"\nss_status (ss_[a-z0-9_]+)\(.*?\) \{\n(.*?)\n", text, flags=re.S):
+                found[m.group(1)] = m.group(2).strip()
+    declared = [n for n in _declared_functions() if n in found]
+    assert "ss_process_sample" in declared and "ss_spec_verify_noalloc" in declared and "ss_merge_round" in declared
+    for name in declared:
+        assert found[name] == 'SS_NVTX_RANGE("%s");' % name, (name, found[name])
+
+
 def test_host_only_queries(lib):
     assert ss.ss_version().startswith("ss ")
     assert ss.ss_cluster_size(128256, "bf16") == 4

@@ -276,3 +276,71 @@ def test_residual_flag_fires_exactly_when_a_perturbation_flips(k_gap):
         if done == 4:
             break
     assert done > 0
+
+
+# ------------------------------------- logits known within a bound (LM head)
+
+
+def _brute_interval_flag(z, b, T, g):
+    """The winner of argmax((z_t + e_t) / T + g_t), e_t in [-b_t, b_t], with
+    y_t and g_t each moving by their margin as well, differs between vertices
+    of that box (greedy, T = 0: argmax of z_t + e_t, z_t's margin)."""
+    n = len(z)
+    inv_t = float(np.float32(1.0) / np.float32(T)) if T else None
+    winners = set()
+    for se in itertools.product((-1.0, 1.0), repeat=n):
+        for sy in itertools.product((-1.0, 1.0), repeat=n):
+            sgs = itertools.product((-1.0, 1.0), repeat=n) if T else [(0.0,) * n]
+            for sg in sgs:
+                sc = []
+                for t in range(n):
+                    if T:
+                        y = float(np.float32(z[t]) * np.float32(inv_t))
+                        sc.append(y + se[t] * b[t] * inv_t + sy[t] * _m(y) + g[t] + sg[t] * _m(g[t]))
+                    else:
+                        sc.append(z[t] + se[t] * b[t] + sy[t] * _m(z[t]))
+                winners.add(_winner(sc, range(n)))
+    return len(winners) > 1
+
+
+@pytest.mark.parametrize("T", [0.0, 0.7, 1.3])
+@pytest.mark.parametrize("k_gap", [-2.0, -1.2, -0.85, -0.2, 0.2, 0.85, 1.2, 2.0])
+def test_interval_flag_fires_exactly_when_a_logit_in_its_bound_flips(T, k_gap):
+    V = 4
+    for seed in range(4):
+        pos = 40 + seed
+        b = np.array([0.01, 0.004, 0.02, 0.001]) * (1 + seed)
+        g = O.gumbel_row(seed, 0, pos, V) if T else np.zeros(V)
+        inv_t = float(np.float32(1.0) / np.float32(T)) if T else 1.0
+        z0 = np.float32(1.5)
+        # the total uncertainty of tokens 0 and 1 (the two leaders)
+        y0 = float(np.float32(z0) * np.float32(inv_t)) if T else float(z0)
+        unc = (b[0] + b[1]) * inv_t + 2 * _m(y0) + (_m(g[0]) + _m(g[1]) if T else 0.0)
+        # token 1's score sits k_gap uncertainties below token 0's
+        z1 = np.float32(float(z0) + (g[0] - g[1]) / inv_t + k_gap * unc / inv_t)
+        z = np.array([[z0, z1, -30.0, -31.0]], np.float32)
+        flags = O.interval_flags(z, b[None, :], np.array([T], np.float32), np.array([seed], np.uint64),
+                                 np.array([pos], np.int64))
+        want = _brute_interval_flag([float(v) for v in z[0]], b, T, g)
+        assert bool(flags[0]) == want, (seed, T, k_gap, flags[0], want)
+
+
+def test_interval_flags_reduce_to_the_draw_margin_at_zero_bound():
+    # with exact logits the interval test is the oracle's own draw margin
+    rng = np.random.default_rng(5)
+    z = rng.normal(0, 2, (24, 7)).astype(np.float32)
+    z[:, 2:] -= 30.0
+    T = rng.uniform(0.5, 1.5, 24).astype(np.float32)
+    seed = rng.integers(0, 2**63, 24, dtype=np.uint64)
+    pos = rng.integers(0, 1000, 24).astype(np.int64)
+    for r in range(0, 24, 2):  # even rows: tokens 0 and 1 tie to within the margin
+        g = O.gumbel_row(int(seed[r]), r, int(pos[r]), 2)
+        z[r, 1] = np.float32(float(z[r, 0]) + (g[0] - g[1]) * float(T[r]))
+    w = sample_workload(z, temperature=T, seed=seed, position=pos)
+    res = O.process_sample(w)
+    flags = O.interval_flags(z, 0.0, T, seed, pos)
+    assert np.array_equal(flags, res["sub_margin"]) and flags.any() and not flags.all()
+    # caller row ids (the Philox counter's row word), above 2^31 too
+    w["row_id"] = rng.integers(0, 2**32, 24, dtype=np.uint64).astype(np.uint32)
+    res = O.process_sample(w)
+    assert np.array_equal(O.interval_flags(z, 0.0, T, seed, pos, w["row_id"]), res["sub_margin"])
