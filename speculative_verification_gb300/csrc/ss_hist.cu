@@ -76,8 +76,8 @@ constexpr int kCertBins = 64;     // bins below the maximum counted for the top-
 constexpr int kCertShift = 3;     // certificate bin = 16-bit order key >> 3 (16 bins per binade)
 constexpr int kTieEnt = 64;       // entries tied at a cut value, per CTA
 constexpr int kFastK = 1024;      // short path: top-k rows up to this k
-constexpr int kFastCap = 2048;    // short path: candidates gathered into rank 0 (the histogram region)
-constexpr int kRankSortMax = 768; // short path: a rank sort up to this many candidates, else bitonic
+constexpr int kFastCap = 2048;    // short path: candidates of a row, merged into rank 0
+constexpr int kRankSortMax = 768; // short path: a CTA's run by rank sort up to this many, else bitonic
 constexpr int kChunkTokens = 8192;
 constexpr int kMaxChunks = 8;
 constexpr int kMaxCluster = 8;
@@ -99,6 +99,7 @@ static_assert(kSlots % kGroups == 0, "groups tile the slots");
 // part of the region the patch table no longer needs
 static_assert(kSlots * 2 + (kGroups + 2) * 4 + kEntCap * 2 <= kHashCap * 16, "entry order fits the region");
 static_assert(kEntCap % kThreads == 0, "entries per thread");
+static_assert(kHashCap * 16 >= kFastCap * 8, "the histogram region holds the short path's candidates");
 static_assert((kSliceMax + kChunkTokens - 1) / kChunkTokens < kMaxChunks, "a barrier slot stays free for the self-test");
 
 // Phase timestamps for tracing (built only with -DSS_HIST_STAMPS): the
@@ -378,9 +379,8 @@ __shared__ int32_t g_tietok[kTieEnt];
 __shared__ uint32_t g_prm[32];           // the request's parameter words
 __shared__ uint32_t g_dscore;            // the draw's best score so far (order key; 0: none)
 __shared__ int32_t g_dtok;               // the lowest token holding it
-__shared__ int32_t g_fcount;             // short path: candidates gathered (rank 0's copy)
 __shared__ int32_t g_fpos[3];            // short path: first failing positions (top-p, min-p), draft position
-__shared__ int32_t g_runs[kMaxCluster][2];  // short path (rank 0): every CTA's run (start, length)
+__shared__ int32_t g_runs[kMaxCluster][2];  // short path: every CTA's run (region flag, length)
 
 extern __shared__ __align__(128) uint8_t g_dyn[];
 
@@ -657,7 +657,6 @@ __device__ void decode_and_copy(const HArgs& a, int task, int rank) {
   c.xpar = 0;
   c.kcount = 0;
   c.kmass = 0;
-  g_fcount = 0;
   c.nreq = 0;
   c.skip_draw = 0;
   c.x = -1;
@@ -1489,14 +1488,61 @@ __device__ __noinline__ void sort_fast_cap(unsigned long long* key) {
   __syncthreads();
 }
 
+// One step of the short path's merge, in every CTA of a cluster of C: each
+// item of this CTA's sorted run goes to its place in the cluster-wide order,
+// its index in its own run plus, for every other run, the number of that
+// run's items below it (keys are distinct: one per token), found by binary
+// searches in the other CTAs' runs, all runs' steps interleaved so that the
+// remote loads overlap.  Runs live in the candidate region (flag 1 in g_runs)
+// or the run region of their CTA.
+template <int C>
+__device__ void place_run(const unsigned long long* srun, int nr, int rank, const unsigned long long* cand,
+                          const unsigned long long* run, unsigned long long* dst) {
+  cg::cluster_group cl = cg::this_cluster();
+  const unsigned long long* rq[C];
+  int nq[C];
+#pragma unroll
+  for (int q = 0; q < C; ++q) {
+    rq[q] = cl.map_shared_rank(g_runs[q][0] ? cand : run, q);
+    nq[q] = (q == rank) ? 0 : g_runs[q][1];
+  }
+  for (int i = threadIdx.x; i < nr; i += kThreads) {
+    const unsigned long long k = srun[i];
+    int lo[C], hi[C];
+#pragma unroll
+    for (int q = 0; q < C; ++q) {
+      lo[q] = 0;
+      hi[q] = nq[q];
+    }
+    for (bool more = true; more;) {
+      more = false;
+#pragma unroll
+      for (int q = 0; q < C; ++q)
+        if (lo[q] < hi[q]) {
+          const int mid = (lo[q] + hi[q]) >> 1;
+          if (rq[q][mid] < k)
+            lo[q] = mid + 1;
+          else
+            hi[q] = mid;
+          more |= lo[q] < hi[q];
+        }
+    }
+    int place = i;
+#pragma unroll
+    for (int q = 0; q < C; ++q) place += lo[q];
+    dst[place] = k;
+  }
+}
+
 // ------------------------------------------------------------ short path --
 // Rows with 0 < top_k <= kFastK and a top-k certificate: every item of K has
 // y >= y(tau) (at least k staged tokens are >= tau), so the candidates --
 // staged tokens at or above tau and entries at or above y(tau) -- hold K.
-// Every CTA pushes its candidates into rank 0; when they fit, rank 0 sorts
-// them by (y desc, token asc) and takes every cut (top-k, top-p over the
-// top-k's fixed-point masses, min-p) and the draw itself: the items of K are
-// then the first L of that order, ties included.  Returns false (in every CTA
+// Every CTA sorts its candidates by (y desc, token asc); when they fit, the
+// CTAs merge their runs into rank 0 (each places its own items), and rank 0
+// takes every cut (top-k, top-p over the top-k's fixed-point masses, min-p)
+// and the draw itself: the items of K are then the first L of that order,
+// ties included.  Returns false (in every CTA
 // alike) when the candidates do not fit and the row takes the histogram path.
 // Called by all threads of every CTA; ends with rank 0's decisions in
 // token / accept / kept.
@@ -1509,10 +1555,8 @@ __device__ bool short_path(const HArgs& a, bool tests_draft, const float* qrow, 
   const uint4* data = reinterpret_cast<const uint4*>(g_dyn);
   const uint16_t* vb = reinterpret_cast<const uint16_t*>(g_dyn + a.o_vb);
   const unsigned long long* el = reinterpret_cast<const unsigned long long*>(g_dyn + a.o_el);
-  // candidates, first in this CTA's histogram region, then its sorted run
+  // candidates, in this CTA's histogram region
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(g_dyn + a.o_hist);
-  unsigned long long* run = reinterpret_cast<unsigned long long*>(g_dyn + a.o_xm);  // xm and mg, contiguous
-  int32_t* rcount = cl.map_shared_rank(&g_fcount, 0);
   const uint32_t tau = c.tau_key;
   const float inv_t = c.inv_t;
   const float ytau = __fmul_rn(bf16_to_f(key16_bits(tau)), inv_t);
@@ -1564,7 +1608,8 @@ __device__ bool short_path(const HArgs& a, bool tests_draft, const float* qrow, 
   __syncthreads();
   const int nr = g.n_g;  // this CTA's candidates
   // this CTA's sorted run: a rank sort while small, else the bitonic network
-  const unsigned long long* srun = run;
+  unsigned long long* run = reinterpret_cast<unsigned long long*>(g_dyn + a.o_xm);  // xm and mg, contiguous
+  unsigned long long* srun = run;
   if (nr <= kRankSortMax) {
     for (int i = tid; i < nr; i += kThreads) {
       const unsigned long long k = cand[i];
@@ -1578,83 +1623,37 @@ __device__ bool short_path(const HArgs& a, bool tests_draft, const float* qrow, 
     sort_fast_cap(cand);
     srun = cand;
   }
-  // this CTA's run, recorded in rank 0 (its length and which region holds it)
-  if (tid == 0) {
-    if (nr > 0) atomicAdd(rcount, nr);
-    *cl.map_shared_rank(&g_runs[rank][0], 0) = (srun == cand) ? 1 : 0;
-    *cl.map_shared_rank(&g_runs[rank][1], 0) = nr;
+  // every CTA learns every run's length and region
+  const int C = static_cast<int>(cl.num_blocks());
+  if (tid < C) {
+    *cl.map_shared_rank(&g_runs[rank][0], tid) = (srun == cand) ? 1 : 0;
+    *cl.map_shared_rank(&g_runs[rank][1], tid) = nr;
   }
   SS_STAMP(38);
-  cl.sync();  // every CTA has its sorted run, and rank 0 its slice no more
+  cl.sync();  // every run is sorted, and rank 0's slice is free
   SS_STAMP(42);
-  const int n = *rcount;
+  int n = 0;
+  for (int r = 0; r < C; ++r) n += g_runs[r][1];
   SS_TRACE(43, n);
   if (n > kFastCap) return false;
-  if (rank != 0) return true;  // (its run stays put until the kernel's last cluster barrier)
-  // rank 0 pulls every run into its slice region, one after the other
-  const int C = static_cast<int>(cl.num_blocks());
-  unsigned long long* mbuf = reinterpret_cast<unsigned long long*>(g_dyn);
-  SS_STAMP(41);
-  if (tid == 0) {
-    int off = 0;
-    for (int r = 0; r < C; ++r) {
-      g_runs[r][0] |= off << 1;  // bit 0: the region; the rest: the run's start in mbuf
-      off += g_runs[r][1];
-    }
+  const unsigned long long* sorted = srun;  // one CTA: its run is the order
+  if (C > 1) {
+    // the merge, spread over the cluster: every CTA places its own items in
+    // rank 0's slice region (a cluster of two or more has slices of 16384
+    // tokens or more: the region holds kFastCap keys)
+    unsigned long long* dst = cl.map_shared_rank(reinterpret_cast<unsigned long long*>(g_dyn), 0);
+    if (C == 2)
+      place_run<2>(srun, nr, rank, cand, run, dst);
+    else if (C == 4)
+      place_run<4>(srun, nr, rank, cand, run, dst);
+    else
+      place_run<8>(srun, nr, rank, cand, run, dst);
+    SS_STAMP(41);
+    cl.sync();  // the merged order is complete in rank 0
+    if (rank != 0) return true;  // (its run stays put until the kernel's last cluster barrier)
+    sorted = reinterpret_cast<const unsigned long long*>(g_dyn);
   }
-  __syncthreads();
-  // (one pass over all items: every remote load in flight at once)
-  for (int i = tid; i < n; i += kThreads) {
-    int r = 0;
-    while (r + 1 < C && (g_runs[r + 1][0] >> 1) <= i) ++r;
-    const unsigned long long* src = cl.map_shared_rank((g_runs[r][0] & 1) ? cand : run, r);
-    mbuf[i] = src[i - (g_runs[r][0] >> 1)];
-  }
-  __syncthreads();
   SS_STAMP(44);
-
-  // ---- rank 0: merge the runs by rank: an item's place is its index in its
-  // run plus, for every other run, how many of its items are smaller (a few
-  // items: counted against all of them; else binary searches in all runs at
-  // once, their steps interleaved so that the loads overlap)
-  unsigned long long* sorted = cand;
-  if (n <= 256) {
-    for (int i = tid; i < n; i += kThreads) {
-      const unsigned long long k = mbuf[i];
-      int place = 0;
-      for (int j = 0; j < n; ++j) place += (mbuf[j] < k) ? 1 : 0;
-      sorted[place] = k;
-    }
-  } else {
-    int rs[kMaxCluster + 1];
-#pragma unroll
-    for (int q = 0; q <= kMaxCluster; ++q) rs[q] = (q < C) ? (g_runs[q][0] >> 1) : n;
-    for (int i = tid; i < n; i += kThreads) {
-      const unsigned long long k = mbuf[i];
-      int lo[kMaxCluster], hi[kMaxCluster];
-#pragma unroll
-      for (int q = 0; q < kMaxCluster; ++q) {
-        lo[q] = rs[q];
-        hi[q] = (q < C) ? rs[q + 1] : rs[q];
-        if (i >= lo[q] && i < hi[q]) hi[q] = lo[q] = i;  // its own run: its index there
-      }
-      for (int step = 0; step < 12; ++step) {  // runs hold at most 2048 items
-#pragma unroll
-        for (int q = 0; q < kMaxCluster; ++q)
-          if (lo[q] < hi[q]) {
-            const int mid = (lo[q] + hi[q]) >> 1;
-            if (mbuf[mid] < k)
-              lo[q] = mid + 1;
-            else
-              hi[q] = mid;
-          }
-      }
-      int place = 0;
-#pragma unroll
-      for (int q = 0; q < kMaxCluster; ++q) place += lo[q] - rs[q];
-      sorted[place] = k;
-    }
-  }
   SS_STAMP(45);
   if (tid == 0) {
     g_fpos[0] = 0x7fffffff;
@@ -2209,10 +2208,12 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
       out[lo + e] = c.greedy ? z : __fmul_rn(z, inv_t);
     }
     __syncthreads();
-    for (int s = tid; s < kHashCap; s += kThreads)
-      if (hkey[s] >= 0) out[hkey[s]] = hval[s];
     const int ne = min(c.nent, kEntCap);
     for (int i = tid; i < ne; i += kThreads) out[ekey_t(el[i])] = ekey_y(el[i]);
+    __syncthreads();
+    // the patched tokens last, from the table: an entry's key folds -0 to +0
+    for (int s = tid; s < kHashCap; s += kThreads)
+      if (hkey[s] >= 0) out[hkey[s]] = hval[s];
   }
 
   // -------------------------------------------------- exchange 1

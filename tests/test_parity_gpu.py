@@ -204,6 +204,26 @@ def test_small_and_ragged_vocab(ss, V):
     _report("V=%d" % V, parity.check_sample(w, run_gpu(ss, w)))
 
 
+@pytest.mark.parametrize("dtype,V", [("bf16", 700), ("bf16", 1500), ("bf16", 2600), ("bf16", 40000), ("f32", 1500)])
+def test_top_k_short_list_sizes(ss, dtype, V):
+    """Top-k rows whose candidates (tokens at or above the certificate) are
+    gathered and sorted in one CTA: a few (rank sort), hundreds to 2048
+    (sorting network), in a single CTA whose slice is smaller than the list
+    and in a cluster; flat logits put many tokens at the cut.  The coarse
+    rows hold many -0 logits, penalised ones among them (the processed value
+    keeps the sign of zero)."""
+    rng = np.random.default_rng(V)
+    n = 12
+    z = rng.normal(0.0, 0.5, size=(n, V)).astype(np.float32)
+    z[::3] = np.round(z[::3] * 4) / 4  # coarse values: long runs of ties at the cut
+    k = np.array([5, 40, 200, 257, 300, 600, 900, 1000, 1024, 1, 700, 1024])
+    k = np.minimum(k, V - 1)
+    w = sample_workload(z, dtype=dtype, temperature=rng.uniform(0.5, 1.5, n), top_k=k,
+                        top_p=rng.choice([1.0, 0.9, 0.95], size=n), min_p=rng.choice([0.0, 0.05], size=n),
+                        history=[rng.integers(0, V, 64).tolist() for _ in range(n)], repetition=1.1, seed=9)
+    _report("top-k short lists %s V=%d" % (dtype, V), parity.check_sample(w, run_gpu(ss, w)))
+
+
 def test_ties_everywhere(ss):
     V = 4096
     z = np.zeros((8, V), np.float32)
