@@ -1146,17 +1146,41 @@ __device__ int32_t first_slot_le(float v, int32_t lo, int32_t hi) {
   return lo;
 }
 
+// first_slot_le(v, 0, ns) from an estimate: the slot of v's value before the
+// temperature (bf16, truncated), then a walk to the exact answer (slot_y
+// falls with the slot, so the walk is short and always ends right).
+__device__ int32_t first_slot_le_near(float v) {
+  const SlotMap& M = g.M;
+  const float z = __fmul_rn(v, g.T);
+  int32_t s = slot_of(M, __float_as_uint(z) >> 16);
+  s = min(max(s, 0), M.ns);
+  if (s < M.ns && slot_y(s) <= v) {
+    while (s > 0 && slot_y(s - 1) <= v) --s;
+  } else {
+    while (s < M.ns && slot_y(s) > v) ++s;
+  }
+  return s;
+}
+
+// A 64-bit shared-memory sum built from two 32-bit atomics (the low word's
+// carry goes to the high word): much cheaper than a 64-bit shared atomic.
+__device__ __forceinline__ void atomic_add_u64_split(unsigned long long* addr, unsigned long long v) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(addr);
+  const uint32_t lo = static_cast<uint32_t>(v);
+  const uint32_t old = atomicAdd(w, lo);
+  const uint32_t hi = static_cast<uint32_t>(v >> 32) + ((old + lo < old) ? 1u : 0u);
+  if (hi) atomicAdd(w + 1, hi);
+}
+
+// The last group q with gb[q] <= p: group q starts at slot q * (kSlots /
+// kGroups) or later (a run of equal values pushes it on), so start there and
+// walk.
 __device__ __forceinline__ int group_of(int32_t p) {
   if (p >= g.M.ns) return kGroups;
-  int lo = 0, hi = kGroups - 1;  // the last q with gb[q] <= p
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (g_gb[mid] <= p)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  return lo;
+  int q = min(p / (kSlots / kGroups), kGroups - 1);
+  while (q > 0 && g_gb[q] > p) --q;
+  while (q + 1 < kGroups && g_gb[q + 1] <= p) ++q;
+  return q;
 }
 
 // First entry of a sorted list whose y is < v (the number of entries >= v).
@@ -1174,7 +1198,10 @@ __device__ __forceinline__ int first_entry_lt(const unsigned long long* el, int 
 
 // The range of coarse group `grp` in every CTA's group-ordered entry list:
 // g_gr0[r] its start, g_grc[r] the entries of the group in CTAs before r
-// (g_grc[C] the total).  Called by all threads; ends with a block barrier.
+// (g_grc[C] the total).  Called by all threads; warp 0 does the work and,
+// with BARRIER, every thread waits for it (else the caller's next block
+// barrier publishes it).
+template <bool BARRIER = true>
 __device__ void group_ranges(const HArgs& a, int grp) {
   cg::cluster_group cl = cg::this_cluster();
   const int C = static_cast<int>(cl.num_blocks());
@@ -1199,7 +1226,7 @@ __device__ void group_ranges(const HArgs& a, int grp) {
     }
     if (r == C - 1) g_grc[C] = inc;
   }
-  __syncthreads();
+  if (BARRIER) __syncthreads();
 }
 
 // Reads the slot counts of coarse group `grp` from every CTA into g_fc, and
@@ -1220,7 +1247,9 @@ __device__ void load_group(const HArgs& a, int grp) {
   unsigned long long* uk = reinterpret_cast<unsigned long long*>(g_dyn + a.o_mg);
   int16_t* up = reinterpret_cast<int16_t*>(uk + kGatherCap);
   __syncthreads();  // the previous readers of g_fc and of the buffers are done
-  group_ranges(a, grp);
+  // the entry ranges (warp 0) and the slot counts (every thread) are
+  // independent remote reads: both in flight before one barrier
+  group_ranges<false>(a, grp);
   for (int i = threadIdx.x; i < s1 - s0; i += kThreads) {
     uint32_t cnt = 0;
     const int q = s0 + i;
@@ -1229,6 +1258,7 @@ __device__ void load_group(const HArgs& a, int grp) {
       if (r < C) cnt += (*cl.map_shared_rank(hist + (q >> 1), r) >> ((q & 1) << 4)) & 0xffffu;
     g_fc[i] = cnt;
   }
+  __syncthreads();
   const int n = g_grc[C];
   if (n > kGatherCap) {
     __syncthreads();
@@ -2486,12 +2516,12 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           eq[k] = -1;
           if (e < c.ne) {
             const float y = ekey_y(el[e]);
-            const int32_t p = first_slot_le(y, 0, M.ns);
+            const int32_t p = first_slot_le_near(y);
             g_epos[e] = static_cast<int16_t>(p);
             const int q = group_of(p);
             eq[k] = q;
             er[k] = static_cast<int>(atomicAdd(&g_ecnt[q], 1u));
-            atomicAdd(&g_emass[q], fmass(y, c.m));
+            atomic_add_u64_split(&g_emass[q], fmass(y, c.m));
             if (mp_on && !(__fsub_rn(y, c.m) >= c.lmp)) fk = max(fk, okey(y));
           }
         }
