@@ -1134,21 +1134,10 @@ __device__ __forceinline__ float slot_y(int32_t s) {
   return __fmul_rn(z, g.inv_t);
 }
 
-// First slot in [lo, hi) whose y is <= v (hi if none); y falls with s.
-__device__ int32_t first_slot_le(float v, int32_t lo, int32_t hi) {
-  while (lo < hi) {
-    const int32_t mid = (lo + hi) >> 1;
-    if (slot_y(mid) <= v)
-      hi = mid;
-    else
-      lo = mid + 1;
-  }
-  return lo;
-}
-
-// first_slot_le(v, 0, ns) from an estimate: the slot of v's value before the
-// temperature (bf16, truncated), then a walk to the exact answer (slot_y
-// falls with the slot, so the walk is short and always ends right).
+// The first slot whose y is <= v (ns if none), from an estimate: the slot of
+// v's value before the temperature (bf16, truncated), then a walk to the
+// exact answer (slot_y falls with the slot, so the walk is short and always
+// ends right).
 __device__ int32_t first_slot_le_near(float v) {
   const SlotMap& M = g.M;
   const float z = __fmul_rn(v, g.T);
@@ -1414,7 +1403,7 @@ __device__ void above_value(const HArgs& a, float v) {
   Ctx& c = g;
   if (threadIdx.x == 0) {
     // the group holding the first slot <= v
-    const int grp = group_of(first_slot_le(v, 0, c.M.ns));
+    const int grp = group_of(first_slot_le_near(v));
     unsigned long long cc = 0, cm = 0;
     for (int q = 0; q < grp; ++q) {
       cc += g_gcnt[q];
@@ -1804,7 +1793,7 @@ __device__ void resolve_ties(const HArgs& a, float v, unsigned long long take, i
   if (threadIdx.x < C) {
     const int r = threadIdx.x;
     uint32_t n = 0;
-    for (int q = first_slot_le(v, 0, c.M.ns); q < c.M.ns && slot_y(q) == v; ++q)
+    for (int q = first_slot_le_near(v); q < c.M.ns && slot_y(q) == v; ++q)
       n += (*cl.map_shared_rank(hist + (q >> 1), r) >> ((q & 1) << 4)) & 0xffffu;
     atomicAdd(&g_rtie[r], n);
   }
@@ -2684,13 +2673,14 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           // the largest value failing the min-p test: among the slots (they
           // fall monotonically) and every CTA's entries
           if (tid == 0) {
-            int lo_s = 0, hi_s = M.ns;
-            while (lo_s < hi_s) {
-              const int mid = (lo_s + hi_s) >> 1;
-              if (!(__fsub_rn(slot_y(mid), c.m) >= c.lmp))
-                hi_s = mid;
-              else
-                lo_s = mid + 1;
+            // the first slot failing it: from the slot of m + log(min_p),
+            // a walk to the exact boundary (the test falls with the slot)
+            auto fails = [&](int q) { return !(__fsub_rn(slot_y(q), c.m) >= c.lmp); };
+            int lo_s = first_slot_le_near(__fadd_rn(c.m, c.lmp));
+            if (lo_s < M.ns && fails(lo_s)) {
+              while (lo_s > 0 && fails(lo_s - 1)) --lo_s;
+            } else {
+              while (lo_s < M.ns && !fails(lo_s)) ++lo_s;
             }
             float vf = (lo_s < M.ns) ? slot_y(lo_s) : ninf();
             if (c.fail_key) vf = fmaxf(vf, okey_value(c.fail_key));
