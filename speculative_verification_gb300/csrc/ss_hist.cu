@@ -211,6 +211,16 @@ __device__ __forceinline__ uint32_t tiny_pair(uint32_t w) {
   return small & nz;
 }
 
+// The smallest magnitude (16-bit pattern without the sign) among the eight
+// bf16 values of a vector: three 16x2 minima and one of the two halves.
+__device__ __forceinline__ uint32_t min_mag8(uint4 d) {
+  uint32_t a, b, r;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(a) : "r"(d.x & 0x7fff7fffu), "r"(d.y & 0x7fff7fffu));
+  asm("min.u16x2 %0, %1, %2;" : "=r"(b) : "r"(d.z & 0x7fff7fffu), "r"(d.w & 0x7fff7fffu));
+  asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return min(r & 0xffffu, r >> 16);
+}
+
 __device__ __forceinline__ bool beats(float s, int32_t t, float bs, int32_t bt) {
   return s > bs || (s == bs && t < bt);
 }
@@ -2115,7 +2125,9 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           dirty = true;
         }
       }
-      if (tiny) {
+      // (a pre-test first: the smallest magnitude among the eight, zero
+      // included, is below the tiny bound -- rare outside exact zeros)
+      if (tiny && min_mag8(d) < kTinyA) {
         const uint32_t tm = tiny_pair(d.x) | (tiny_pair(d.y) >> 1) | (tiny_pair(d.z) >> 2) | (tiny_pair(d.w) >> 3);
         if (tm && act) {
           // tiny values move to the entries (patched ones are the fix-up's)
