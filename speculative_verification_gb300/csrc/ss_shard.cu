@@ -403,7 +403,8 @@ __global__ void __launch_bounds__(kThreads) ss_shard_round_kernel(const SArgs a)
 
 __global__ void __launch_bounds__(256) ss_merge_round_kernel(const MArgs a) {
   extern __shared__ __align__(16) unsigned long long keys[];  // round 2: the listed tokens
-  __shared__ int32_t s_total;
+  __shared__ int32_t s_total, s_cut;
+  __shared__ unsigned long long s_wsum[8], s_wcnt[8];  // rounds 1 and 2: per-warp sums (256 threads)
   const int r = blockIdx.x, tid = threadIdx.x;
   RowState& st = a.state[r];
   auto rec = [&](int s) { return reinterpret_cast<const Rec*>(a.rec[s] + static_cast<int64_t>(r) * kRecBytes); };
@@ -449,53 +450,66 @@ __global__ void __launch_bounds__(256) ss_merge_round_kernel(const MArgs a) {
     return;
   }
   if (a.round == 1) {
-    // the target and the bucket holding the cut (warp 0: 32 buckets per lane)
-    if (tid >= 32) return;
+    // the target and the bucket holding the cut: each thread sums four
+    // buckets over the shards, a block scan of those sums, and the thread
+    // whose buckets hold the first one reaching the target records it
+    constexpr int kPer = kBuckets / 256;
+    static_assert(kBuckets % 256 == 0, "four buckets per thread");
     unsigned long long S = 0;
     for (int s = 0; s < a.num_shards; ++s) S += rec(s)->S;
     const float top_p = a.p.top_p[r];
     const unsigned long long T = static_cast<unsigned long long>(ceil(static_cast<double>(top_p) * static_cast<double>(S)));
-    constexpr int kPer = kBuckets / 32;
-    unsigned long long cm = 0, cc = 0;
+    unsigned long long mb[kPer], cb[kPer], cm = 0, cc = 0;
+#pragma unroll
     for (int i = 0; i < kPer; ++i) {
       const int b = tid * kPer + i;
+      mb[i] = 0;
+      cb[i] = 0;
       for (int s = 0; s < a.num_shards; ++s) {
         const uint32_t* bc = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(rec(s)) + sizeof(Rec));
         const unsigned long long* bm = reinterpret_cast<const unsigned long long*>(bc + kBuckets);
-        cm += bm[b];
-        cc += bc[b];
+        mb[i] += bm[b];
+        cb[i] += bc[b];
       }
+      cm += mb[i];
+      cc += cb[i];
     }
-    unsigned long long im = cm, ic = cc;
+    const int lane = tid & 31, wid = tid >> 5;
+    unsigned long long im = cm, ic = cc;  // inclusive within the warp
+#pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, o), yc = __shfl_up_sync(0xffffffffu, ic, o);
-      if (tid >= o) {
+      if (lane >= o) {
         im += ym;
         ic += yc;
       }
     }
-    unsigned long long bm_run = im - cm, bc_run = ic - cc;  // before this lane's buckets
+    if (lane == 31) {
+      s_wsum[wid] = im;
+      s_wcnt[wid] = ic;
+    }
+    if (tid == 0) s_cut = 0x7fffffff;
+    __syncthreads();
+    unsigned long long bm_run = im - cm, bc_run = ic - cc;  // before this thread's buckets
+    for (int w = 0; w < wid; ++w) {
+      bm_run += s_wsum[w];
+      bc_run += s_wcnt[w];
+    }
     int found = -1;
     unsigned long long fm = 0, fc = 0;
-    for (int i = 0; i < kPer && found < 0; ++i) {
-      const int b = tid * kPer + i;
-      unsigned long long mb = 0, cb = 0;
-      for (int s = 0; s < a.num_shards; ++s) {
-        const uint32_t* bc = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(rec(s)) + sizeof(Rec));
-        const unsigned long long* bm = reinterpret_cast<const unsigned long long*>(bc + kBuckets);
-        mb += bm[b];
-        cb += bc[b];
-      }
-      if (mb > 0 && bm_run + mb >= T) {
-        found = b;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      if (found < 0 && mb[i] > 0 && bm_run + mb[i] >= T) {
+        found = tid * kPer + i;
         fm = bm_run;
         fc = bc_run;
       }
-      bm_run += mb;
-      bc_run += cb;
+      bm_run += mb[i];
+      bc_run += cb[i];
     }
-    const unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
-    if (ball && tid == __ffs(ball) - 1) {
+    if (found >= 0) atomicMin(&s_cut, found);
+    __syncthreads();
+    if (found >= 0 && found == s_cut) {
       st.S = S;
       st.T = T;
       st.bucket = found;
@@ -546,17 +560,39 @@ __global__ void __launch_bounds__(256) ss_merge_round_kernel(const MArgs a) {
         }
         __syncthreads();
       }
-    if (tid == 0) {
-      unsigned long long run = st.mass_before;
-      int cut = -1;
-      for (int i = 0; i < n; ++i) {
+    // the first item i with a non-zero mass whose running total (from the
+    // mass before the bucket) reaches the target: each thread sums a
+    // contiguous chunk, a block scan of the chunk sums, and the thread whose
+    // chunk holds it walks its chunk
+    {
+      const int per = (n + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+      const int i0 = min(tid * per, n), i1 = min(i0 + per, n);
+      unsigned long long local = 0;
+      for (int i = i0; i < i1; ++i) local += fmass(ekey_y(keys[i]), st.m);
+      unsigned long long inc = local;  // inclusive scan within the warp
+      const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane == 31) s_wsum[wid] = inc;
+      if (tid == 0) s_cut = 0x7fffffff;
+      __syncthreads();
+      unsigned long long run = st.mass_before + inc - local;
+      for (int w = 0; w < wid; ++w) run += s_wsum[w];
+      for (int i = i0; i < i1; ++i) {
         const unsigned long long w = fmass(ekey_y(keys[i]), st.m);
         if (w > 0 && run + w >= st.T) {
-          cut = i;
+          atomicMin(&s_cut, i);
           break;
         }
         run += w;
       }
+      __syncthreads();
+    }
+    if (tid == 0) {
+      const int cut = (s_cut == 0x7fffffff) ? -1 : s_cut;
       if (cut < 0) {
         finish(SS_ROW_LIMIT, -1, 0);
         return;
