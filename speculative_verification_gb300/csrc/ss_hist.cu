@@ -403,20 +403,6 @@ __device__ __forceinline__ uint32_t key16_bits(uint32_t k) { return (k & 0x8000u
 // broadcast.  Either way the combine over the 16 warps is not a 16-step loop
 // in every thread.
 
-__device__ __forceinline__ float block_max_nan(float v) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
-  float* r = reinterpret_cast<float*>(g_red);
-  __syncthreads();
-  if (lane == 0) r[wid] = v;
-  __syncthreads();
-  const float4* r4 = reinterpret_cast<const float4*>(r);
-  const float4 a = r4[0], b = r4[1], c = r4[2], d = r4[3];
-  return fmax_nan(fmax_nan(fmax_nan(fmax_nan(a.x, a.y), fmax_nan(a.z, a.w)), fmax_nan(fmax_nan(b.x, b.y), fmax_nan(b.z, b.w))),
-                  fmax_nan(fmax_nan(fmax_nan(c.x, c.y), fmax_nan(c.z, c.w)), fmax_nan(fmax_nan(d.x, d.y), fmax_nan(d.z, d.w))));
-}
-
 __device__ __forceinline__ void warp_best(float& s, int32_t& t, int width) {
   for (int o = width >> 1; o; o >>= 1) {
     const float os = __shfl_xor_sync(0xffffffffu, s, o);
