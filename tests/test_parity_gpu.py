@@ -224,6 +224,31 @@ def test_top_k_short_list_sizes(ss, dtype, V):
     _report("top-k short lists %s V=%d" % (dtype, V), parity.check_sample(w, run_gpu(ss, w)))
 
 
+@pytest.mark.parametrize("dtype,V", [("bf16", 3001), ("bf16", 128256), ("f32", 3001)])
+def test_extreme_temperatures_and_thresholds(ss, dtype, V):
+    """Corners of the filters: temperatures from 1e-3 (every mass but the
+    top's underflows) to 100 (nearly flat), top-p at 1e-6 (the maximum alone)
+    and at 0.9999, min-p at 1 (the values equal to the maximum) and at 1e-6,
+    top-k at 1 and at V - 1, alone and combined."""
+    rng = np.random.default_rng(V + 7)
+    combos = [
+        (1e-3, 0, 1.0, 0.0), (1e-3, 0, 0.9, 0.0), (1e-3, 50, 0.95, 0.05), (0.05, 0, 0.9999, 0.0),
+        (100.0, 0, 0.9, 0.0), (100.0, 0, 1.0, 1e-6), (100.0, 2000, 0.95, 0.0), (1.0, 0, 1e-6, 0.0),
+        (1.0, 0, 1.0, 1.0), (1.0, 0, 0.9, 0.999), (1.0, 1, 1.0, 0.0), (1.0, V - 1, 1.0, 0.0),
+        (0.7, V - 1, 0.9999, 1e-6), (20.0, 1000, 0.9, 0.05), (1e-3, 1000, 1.0, 0.0), (3.0, 0, 0.5, 0.1),
+    ]
+    n = len(combos)
+    z = rng.normal(0.0, 3.0, size=(n, V)).astype(np.float32)
+    z[::2, : V // 10] = np.round(z[::2, : V // 10])  # runs of equal values among the largest
+    T = np.array([c[0] for c in combos], np.float32)
+    k = np.array([c[1] for c in combos], np.int32)
+    p = np.array([c[2] for c in combos], np.float32)
+    mp = np.array([c[3] for c in combos], np.float32)
+    w = sample_workload(z, dtype=dtype, temperature=T, top_k=k, top_p=p, min_p=mp,
+                        history=[rng.integers(0, V, 32).tolist() for _ in range(n)], repetition=1.2, seed=21)
+    _report("extreme %s V=%d" % (dtype, V), parity.check_sample(w, run_gpu(ss, w)))
+
+
 def test_ties_everywhere(ss):
     V = 4096
     z = np.zeros((8, V), np.float32)
