@@ -249,6 +249,50 @@ def test_extreme_temperatures_and_thresholds(ss, dtype, V):
     _report("extreme %s V=%d" % (dtype, V), parity.check_sample(w, run_gpu(ss, w)))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_verify_draft_corner_cases(ss, dtype):
+    """Drafts at the corners of the accept test: q(x) = 0 (accepted whenever
+    P(x) > 0), q concentrated on a token of small P (rejected, then the
+    residual), a draft outside K (P = 0: rejected), the rows' leader (also
+    under a tiny temperature), and requests with every draft accepted (the
+    bonus token)."""
+    rng = np.random.default_rng(31)
+    V = 4099
+    ks = np.array([3, 3, 2, 4, 1, 5, 3, 2], np.int32)
+    rows = int(ks.sum() + ks.size)
+    z = rng.normal(0.0, 2.0, size=(rows, V)).astype(np.float32)
+    z[:, 7] = z.max(axis=1) + 1.0  # token 7 leads every row (so it is in every K)
+    T = np.array([1.0, 0.8, 1e-3, 1.2, 1.0, 0.9, 1.0, 1.5], np.float32)
+    k = np.array([0, 40, 0, 0, 1, 0, 200, 0], np.int32)
+    p = np.array([1.0, 1.0, 1.0, 0.9, 1.0, 0.95, 1.0, 1.0], np.float32)
+    drafts, q = [], []
+    for r in range(ks.size):
+        for j in range(int(ks[r])):
+            qi = rng.dirichlet(np.full(V, 0.5)).astype(np.float32)
+            x = int(rng.integers(0, V))
+            case = 4 if r >= 6 else (r + j) % 5
+            if r >= 6:         # the last two requests: every draft token 7 with q = 0, so all are accepted
+                x = 7
+                qi[7] = 0.0
+            elif case == 0:    # q(x) = 0
+                qi[x] = 0.0
+            elif case == 1:    # q concentrated on x
+                qi[:] = 0.0
+                qi[x] = 1.0
+            elif case == 2:    # token 7, every row's leader
+                x = 7
+            elif case == 3:    # a token that top-k / top-p drop
+                x = int(np.argmin(z[0]))
+            drafts.append(x)
+            q.append(qi)
+    w = verify_workload(z, ks, drafts, np.stack(q), dtype=dtype, temperature=T, top_k=k, top_p=p,
+                        seed=np.arange(ks.size, dtype=np.uint64) + 5, position=np.arange(ks.size) * 3)
+    g = run_gpu(ss, w)
+    _report("verify corners %s" % dtype, parity.check_verify(w, g))
+    print("accepted", g["num_accepted"].tolist(), "of", ks.tolist())
+    assert (g["num_accepted"][6:] == ks[6:]).all()  # all accepted: the bonus token follows (token 7 is in K)
+
+
 def test_ties_everywhere(ss):
     V = 4096
     z = np.zeros((8, V), np.float32)
