@@ -216,8 +216,13 @@ def run_ours(args, rank, world, dist):
     out = ss.alloc_outputs(ring[0], dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def call(i):
-        ss.run(ring[i % args.ring], out, stream=stream)
+    # consecutive sampling calls over independent batches may overlap (a
+    # call's first rows start on the SMs the previous call's last rows leave:
+    # SS_SAMPLE_OVERLAP_PREVIOUS); no call reads another's outputs here
+    overlap = ring_host[0]["kind"] == "sample" and not args.no_overlap
+
+    def call(i, ov=overlap):
+        ss.run(ring[i % args.ring], out, stream=stream, overlap_previous=ov)
 
     # graphs: one of `per_graph` calls (replayed), one for the remainder
     per_graph = min(args.steps, args.ring * 8)
@@ -226,12 +231,12 @@ def run_ours(args, rank, world, dist):
             call(i)
     stream.synchronize()
 
-    def capture(n):
+    def capture(n, ov=overlap):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
                 for i in range(n):
-                    call(i)
+                    call(i, ov)
         return g
 
     progress("capturing graphs")
@@ -291,9 +296,27 @@ def run_ours(args, rank, world, dist):
         b_ev.record(stream)
         stream.synchronize()
         single.append(a_ev.elapsed_time(b_ev) * 1e3)
+    # the same graph of calls without the overlap: each call alone on the GPU
+    alone_us = None
+    if overlap and per_graph > 0:
+        g_alone = capture(per_graph, False)
+        with torch.cuda.stream(stream):
+            g_alone.replay()
+        stream.synchronize()
+        a_ev = torch.cuda.Event(enable_timing=True)
+        b_ev = torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g_alone.replay()
+        b_ev.record(stream)
+        stream.synchronize()
+        alone_us = a_ev.elapsed_time(b_ev) * 1e3 / (3 * per_graph)
+        del g_alone
     call_us = {"mean": ms * 1e3 / args.steps,
                "best_replay": min(per_replay) if per_replay else None,
                "median_replay": statistics.median(per_replay) if per_replay else None,
+               "one_call_at_a_time_in_graph": alone_us if overlap else ms * 1e3 / args.steps,
                "single_call_no_graph_median": statistics.median(single)}
 
     progress("timed region done: %.3f ms" % ms)
@@ -351,7 +374,9 @@ def run_ours(args, rank, world, dist):
             "vocab": int(ring_host[0]["vocab"]),
             "input_dtype": ring_host[0]["dtype"],
             "l2": "ring of %d input sets, %.0f MB > 2x L2" % (args.ring, args.ring * bytes_per_call / 1e6),
-            "launch": "CUDA graph of %d calls, replayed" % per_graph,
+            "launch": ("CUDA graph of %d calls, replayed; consecutive calls overlap (programmatic dependent "
+                       "launch, SS_SAMPLE_OVERLAP_PREVIOUS)" % per_graph) if overlap else (
+                           "CUDA graph of %d calls, replayed" % per_graph),
             "parallelism": "dp%d replicas" % world,
             "cluster_ctas_per_row": cs,
             "launches_per_call": per_call,
@@ -757,17 +782,18 @@ def run_config_block(args, ss, cfg, rank, dev, stream, peak, ring_n, calls_wante
     rows = int(w0["num_rows"]) if w0["kind"] == "sample" else int(w0["draft_offsets"][-1]) + int(w0["num_requests"])
     alg = W.algorithmic_bytes(w0)
     cs = ss.ss_cluster_size(int(w0["vocab"]), w0["dtype"])
+    overlap = w0["kind"] == "sample" and not args.no_overlap  # as the headline
     with torch.cuda.stream(stream):
         if "workspace" in out:
             ss.ss_workspace_init(out["workspace"], stream=stream)
         for dw in ring:
-            ss.run(dw, out, stream=stream)
+            ss.run(dw, out, stream=stream, overlap_previous=overlap)
     stream.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
             for dw in ring:
-                ss.run(dw, out, stream=stream)
+                ss.run(dw, out, stream=stream, overlap_previous=overlap)
     reps = max(1, calls_wanted // ring_n)
     for _ in range(3):
         g.replay()
@@ -799,6 +825,7 @@ def run_config_block(args, ss, cfg, rank, dev, stream, peak, ring_n, calls_wante
         "gpu_launches": calls * launches_per_call(w0, cs),
         "l2": "ring of %d input set(s), %.0f MB%s" % (ring_n, ring_n * alg / 1e6,
                                                        " > 2x L2" if ring_n * alg > 2 * L2_BYTES else " > L2"),
+        "consecutive_calls_overlap": overlap,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "algorithmic_bytes_per_launch": alg, "traffic": recorded_traffic(W.CONFIG_NAMES[cfg], kernel),
                      "kernel": kernel, "kernel_sha256": kernel_source_hash(kernel)},
@@ -977,6 +1004,8 @@ def main():
     ap.add_argument("--mixed-calls", type=int, default=20, help="calls timed on workload 5 (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="time sampling calls one at a time (no SS_SAMPLE_OVERLAP_PREVIOUS)")
     args = ap.parse_args()
 
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:

@@ -142,6 +142,9 @@ typedef struct {
                                    batch and of how a batch is split over GPUs. */
 } ss_params;
 
+/* ss_sample_args.flags (0 = none). */
+#define SS_SAMPLE_OVERLAP_PREVIOUS 1 /* the call may overlap the sampling call before it (below) */
+
 /* ss_process_sample: one token per row.  Row r is logits + r * row_stride. */
 typedef struct {
   int32_t num_rows;
@@ -155,6 +158,20 @@ typedef struct {
   int32_t* out_kept;            /* [num_rows] |K| (1 greedy, 0 error), or NULL    */
   float* debug_processed;       /* [num_rows, V] processed logits y (z for greedy
                                    rows, -inf where masked), or NULL              */
+  int32_t flags;                /* 0, or SS_SAMPLE_OVERLAP_PREVIOUS: the call may
+                                   begin while the kernel before it on the stream
+                                   -- a bf16 ss_process_sample call -- is still
+                                   running (programmatic dependent launch): it
+                                   reads its inputs at once and orders only its
+                                   writes after that call.  Set it only when no
+                                   input of this call is written by that call
+                                   (its out_token / out_status / out_kept /
+                                   debug_processed); back-to-back calls over
+                                   independent batches then overlap each other's
+                                   first and last rows.  Honoured by bf16
+                                   ss_process_sample; other bits are invalid;
+                                   the other entry points taking this struct
+                                   ignore it. */
 } ss_sample_args;
 
 /* ss_spec_verify: request i owns target rows draft_offsets[i] + i + j,

@@ -134,6 +134,10 @@ __device__ unsigned long long g_stamps[kStampCtas][kStampPhases];
 
 // ---------------------------------------------------------------- helpers --
 
+// Programmatic dependent launch (no-ops in a launch without it).
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
 __device__ __forceinline__ float pinf() { return __int_as_float(0x7f800000); }
 __device__ __forceinline__ float bf16_to_f(uint32_t h) { return __uint_as_float((h & 0xffffu) << 16); }
@@ -295,6 +299,7 @@ struct HArgs {
   int32_t ncta, slice, bulk;
   int32_t o_vb, o_hist, o_el, o_xm, o_mg, o_mbar, total;
   uint32_t stall_polls;  // self-test: a bounded wait on a barrier nothing completes
+  int32_t overlap;       // sampling: launched to overlap the sampling call before it
 };
 
 // Per-CTA partial of exchange 1.
@@ -1939,6 +1944,13 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   uint32_t* hraw = reinterpret_cast<uint32_t*>(hval + kHashCap);  // raw bf16 bits | allowed << 16
 
   SS_STAMP(0);
+  // Programmatic dependent launch (sampling calls): a next sampling call that
+  // allows it may start its CTAs as soon as every CTA of this one has started
+  // (they take the SM slots this call's finished rows give back).  Such a
+  // call reads no output of this one, so only its writes -- outputs and the
+  // debug rows -- wait for this grid (griddepcontrol.wait; a no-op in a
+  // launch without the attribute).
+  if (a.mode == 0) grid_launch_dependents();
   // the parameter loads go out before the bulk copies (a global load issued
   // after 16 KB copies of every CTA waits behind them)
   if (tid < 32) {
@@ -2218,6 +2230,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
 
   // -------------------------------------------------- debug output
   if (a.debug) {
+    grid_dependency_wait();
     float* out = a.debug + static_cast<int64_t>(c.row) * V;
     const uint16_t* d16 = reinterpret_cast<const uint16_t*>(g_dyn);
     for (int e = tid; e < n; e += kThreads) {
@@ -2805,6 +2818,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   const int32_t fst = c.status;
   const bool ok = fst == SS_ROW_OK;
   if (!verify) {
+    grid_dependency_wait();  // the previous call has written its outputs
     a.out_token[c.row] = ok ? token : -1;
     a.out_status[c.row] = fst;
     if (a.out_kept) a.out_kept[c.row] = ok ? static_cast<int32_t>(kept) : 0;
@@ -2907,13 +2921,18 @@ static ss_status launch(HArgs& a, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(a.total);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // with SS_SAMPLE_OVERLAP_PREVIOUS: this launch may begin while the
+    // sampling kernel before it on the stream finishes (the kernel orders its
+    // writes after that grid)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = (a.mode == 0 && a.overlap) ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, ss_hist_kernel, a);
   }
   if (e != cudaSuccess) {
@@ -2959,6 +2978,7 @@ ss_status hist_sample(const ss_sample_args& A, cudaStream_t stream, uint32_t sta
   a.out_status = A.out_status;
   a.out_kept = A.out_kept;
   a.debug = A.debug_processed;
+  a.overlap = (A.flags & SS_SAMPLE_OVERLAP_PREVIOUS) ? 1 : 0;
   a.ncta = hist::cluster_for(A.vocab);
   const int64_t slice = ((static_cast<int64_t>(A.vocab) + a.ncta - 1) / a.ncta + 63) / 64 * 64;
   a.slice = static_cast<int32_t>(slice);

@@ -3074,6 +3074,7 @@ static ss_status check_sample(const ss_sample_args* args) {
   const ss_sample_args& A = *args;
   if (A.num_rows < 0 || A.vocab < 1) return SS_ERR_INVALID_ARG;
   if (A.dtype != SS_DTYPE_F32 && A.dtype != SS_DTYPE_BF16) return SS_ERR_INVALID_ARG;
+  if (A.flags & ~SS_SAMPLE_OVERLAP_PREVIOUS) return SS_ERR_INVALID_ARG;
   if (A.num_rows == 0) return SS_OK;
   const int es = (A.dtype == SS_DTYPE_BF16) ? 2 : 4;
   if (!A.logits || (reinterpret_cast<uintptr_t>(A.logits) % es) != 0 || !A.out_token || !A.out_status)

@@ -78,7 +78,11 @@ class ss_sample_args(C.Structure):
         ("out_status", C.c_void_p),
         ("out_kept", C.c_void_p),
         ("debug_processed", C.c_void_p),
+        ("flags", C.c_int32),
     ]
+
+
+SS_SAMPLE_OVERLAP_PREVIOUS = 1
 
 
 class ss_verify_args(C.Structure):
@@ -231,8 +235,9 @@ def ss_workspace_init(workspace, stream=None):
                                     _stream_handle(stream)))
 
 
-def _sample_args(logits, params, out_token, out_status, vocab, dtype, row_stride, out_kept, debug_processed):
+def _sample_args(logits, params, out_token, out_status, vocab, dtype, row_stride, out_kept, debug_processed, flags=0):
     a = ss_sample_args()
+    a.flags = int(flags)
     a.num_rows = int(out_token.numel())
     a.vocab = int(vocab)
     a.row_stride = int(vocab if row_stride is None else row_stride)
@@ -247,9 +252,12 @@ def _sample_args(logits, params, out_token, out_status, vocab, dtype, row_stride
 
 
 def ss_process_sample(logits, params, out_token, out_status, *, vocab, dtype, row_stride=None, out_kept=None,
-                      debug_processed=None, stream=None):
-    """Sample one token per row of `logits` (device tensor, [rows, row_stride])."""
-    a = _sample_args(logits, params, out_token, out_status, vocab, dtype, row_stride, out_kept, debug_processed)
+                      debug_processed=None, stream=None, overlap_previous=False):
+    """Sample one token per row of `logits` (device tensor, [rows, row_stride]).
+    overlap_previous sets SS_SAMPLE_OVERLAP_PREVIOUS (see include/ss.h): only
+    when no input is an output of the sampling call before it."""
+    a = _sample_args(logits, params, out_token, out_status, vocab, dtype, row_stride, out_kept, debug_processed,
+                     SS_SAMPLE_OVERLAP_PREVIOUS if overlap_previous else 0)
     _check(load().ss_process_sample(C.byref(a), _stream_handle(stream)))
 
 
@@ -567,14 +575,16 @@ def alloc_outputs(dw, device="cuda", debug=False):
     return o
 
 
-def run(dw, o, stream=None, debug=False):
-    """One library call on a device workload `dw` into outputs `o`."""
+def run(dw, o, stream=None, debug=False, overlap_previous=False):
+    """One library call on a device workload `dw` into outputs `o`
+    (overlap_previous: see ss_process_sample; sampling only)."""
     params = {k: dw.get(k) for k in PARAM_FIELDS}
     params["bitmask_stride"] = dw.get("bitmask_stride", 0)
     dbg = o.get("processed") if debug else None
     if dw["kind"] == "sample":
         ss_process_sample(dw["logits"], params, o["token"], o["status"], vocab=dw["vocab"], dtype=dw["dtype"],
-                          row_stride=dw["row_stride"], out_kept=o["kept"], debug_processed=dbg, stream=stream)
+                          row_stride=dw["row_stride"], out_kept=o["kept"], debug_processed=dbg, stream=stream,
+                          overlap_previous=overlap_previous)
     elif dw["kind"] == "tree":
         ss_tree_verify(dw["target_logits"], dw["node_offsets"], dw["parents"], dw["node_tokens"], dw["draft_probs"],
                        params, o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],

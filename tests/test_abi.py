@@ -80,6 +80,10 @@ def test_host_side_argument_errors_launch_nothing(lib):
     assert lib.ss_process_sample(C.byref(a), None) == 1
     a.num_rows = 0  # empty batch: nothing to do
     assert lib.ss_process_sample(C.byref(a), None) == 0
+    a.flags = 2  # an unknown flag bit
+    assert lib.ss_process_sample(C.byref(a), None) == 1
+    a.flags = ss.SS_SAMPLE_OVERLAP_PREVIOUS
+    assert lib.ss_process_sample(C.byref(a), None) == 0
     assert lib.ss_process_sample(None, None) == 1
     v = ss.ss_verify_args()
     v.num_requests = 2

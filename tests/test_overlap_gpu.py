@@ -1,0 +1,109 @@
+"""Back-to-back sampling calls that overlap (SS_SAMPLE_OVERLAP_PREVIOUS,
+programmatic dependent launch): every call's results equal those of the same
+call made alone, including when consecutive calls write the same output
+buffers (the later call's writes land last) and inside a CUDA graph."""
+import numpy as np
+import pytest
+
+from speculative_verification_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+KEYS = ("token", "status", "kept")
+
+
+@pytest.fixture(scope="module")
+def ss():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_verification_gb300 import build as ss_build
+    ss_build.build()
+    from speculative_verification_gb300 import ss as _ss
+    _ss.load()
+    return _ss
+
+
+def _sets(ss, n, rows=32, vocab=128256):
+    return [ss.to_device(W.make(2, rows=rows, vocab=vocab, seed=50 + i)) for i in range(n)]
+
+
+def _alone(ss, sets):
+    ref = []
+    for dw in sets:
+        o = ss.alloc_outputs(dw)
+        ss.run(dw, o)
+        torch.cuda.synchronize()
+        ref.append({k: o[k].clone() for k in KEYS})
+    return ref
+
+
+def test_overlapped_calls_equal_calls_alone(ss):
+    sets = _sets(ss, 6)
+    ref = _alone(ss, sets)
+    outs = [ss.alloc_outputs(dw) for dw in sets]
+    for dw, o in zip(sets, outs):
+        ss.run(dw, o, overlap_previous=True)
+    torch.cuda.synchronize()
+    for r, o in zip(ref, outs):
+        for k in KEYS:
+            assert torch.equal(r[k], o[k]), k
+
+
+def test_overlapped_calls_into_the_same_outputs_keep_the_last(ss):
+    sets = _sets(ss, 5)
+    ref = _alone(ss, sets)
+    o = ss.alloc_outputs(sets[0])
+    dbg = torch.empty((int(sets[0]["num_rows"]), int(sets[0]["vocab"])), dtype=torch.float32, device="cuda")
+    o["processed"] = dbg
+    for rep in range(3):
+        for dw in sets:
+            ss.run(dw, o, debug=True, overlap_previous=True)
+        torch.cuda.synchronize()
+        for k in KEYS:
+            assert torch.equal(ref[-1][k], o[k]), (rep, k)
+    # the debug rows of the last call too
+    last = ss.alloc_outputs(sets[-1], debug=True)
+    ss.run(sets[-1], last, debug=True)
+    torch.cuda.synchronize()
+    assert torch.equal(last["processed"], dbg)
+
+
+def test_overlapped_calls_in_a_graph(ss):
+    sets = _sets(ss, 4)
+    ref = _alone(ss, sets)
+    outs = [ss.alloc_outputs(dw) for dw in sets]
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for dw, o in zip(sets, outs):  # warm-up outside the capture
+            ss.run(dw, o, stream=stream, overlap_previous=True)
+    stream.synchronize()
+    for o in outs:
+        for k in KEYS:
+            o[k].fill_(-7)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for dw, o in zip(sets, outs):
+                ss.run(dw, o, stream=stream, overlap_previous=True)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for r, o in zip(ref, outs):
+        for k in KEYS:
+            assert torch.equal(r[k], o[k]), k
+
+
+def test_overlap_flag_on_fp32_and_verification_is_harmless(ss):
+    # the flag is honoured by bf16 sampling only; fp32 calls run as usual
+    w = W.make(2, rows=8, vocab=5003, seed=3)
+    w32 = dict(w, dtype="f32", logits=W.bf16_bits_to_f32(w["logits"]))
+    dw = ss.to_device(w32)
+    a, b = ss.alloc_outputs(dw), ss.alloc_outputs(dw)
+    ss.run(dw, a)
+    ss.run(dw, b, overlap_previous=True)
+    torch.cuda.synchronize()
+    for k in KEYS:
+        assert torch.equal(a[k], b[k]), k
+    assert np.all(a["status"].cpu().numpy() == 0)
