@@ -361,6 +361,9 @@ struct Ctx {
   float w_v;
   unsigned long long w_take, w_cc, w_cm;
   int32_t tie_rank, tie_local;
+  // this CTA's largest staged pair (index) and largest entry: the draw's seeds
+  int32_t seed_pair, seed_et;
+  float seed_ey;
   unsigned long long below;
   unsigned long long ntot, stot;  // count and mass of every counted item
   // scratch
@@ -998,6 +1001,32 @@ __device__ void draw_pass(const HArgs& a, float cv, int32_t ct, bool mp_on, floa
       }
     }
   };
+  // Seeds (sampling calls): thread 0 scores the CTA's largest staged token
+  // and its largest entry when they are drawn from, so that every thread
+  // prunes from its first vector on.  Only the score is published: the pass
+  // visits both tokens again, and the lowest token holding the best is taken
+  // at its end.  (Measured: a gain for sampling calls, a loss for the
+  // verification launches of many waves, which skip it.)
+  const bool seeded = !RES && a.mode == 0;
+  if (seeded && threadIdx.x == 0) {
+    float best = ninf();
+    auto seed = [&](float y, int32_t t) {
+      if (!member(y, t)) return;
+      const Philox4 r = philox4x32_10(static_cast<uint32_t>(t) >> 2, pos, rid, stream, k0, k1);
+      best = fmaxf(best, __fadd_rn(y, gumbel_from_numerator(uniform_numerator(r.w[t & 3]))));
+    };
+    const int sp = c.seed_pair;
+    if (sp >= 0 && sp < c.nvec / 2) {
+      const uint16_t* d16 = reinterpret_cast<const uint16_t*>(g_dyn) + sp * 16;
+      int eb = -1;
+      for (int e = 0; e < 16; ++e)
+        if (d16[e] != 0xff80u && (eb < 0 || bf16_to_f(d16[e]) > bf16_to_f(d16[eb]))) eb = e;
+      if (eb >= 0) seed(__fmul_rn(bf16_to_f(d16[eb]), inv_t), c.lo + sp * 16 + eb);
+    }
+    if (c.seed_et >= c.lo && c.seed_et < c.lo + c.n) seed(c.seed_ey, c.seed_et);
+    if (best > ninf()) g_dscore = okey(best);
+  }
+  if (seeded) __syncthreads();
   const int nvec = c.nvec;
   int32_t cnt = 0;
   for (int v = threadIdx.x; v < nvec; v += kThreads) {
@@ -2323,6 +2352,9 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     }
     if (c.k_on) __syncthreads();  // the certificate counts are complete
     if (tid == 0) {
+      c.seed_pair = gvec;
+      c.seed_ey = es;
+      c.seed_et = et;
       Part1& p = g_mine;
       p.zmax = zmax;
       p.emax = es;
