@@ -521,14 +521,14 @@ def run_spec(args, ss, rank, dev, stream):
     with torch.cuda.stream(stream):
         ss.ss_workspace_init(out["workspace"], stream=stream)
         for i in range(len(ring)):
-            ss.run(ring[i], out, stream=stream)
+            ss.run(ring[i], out, stream=stream, overlap_previous=not args.no_overlap)
     stream.synchronize()
     n = args.spec_steps
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
             for i in range(len(ring)):
-                ss.run(ring[i], out, stream=stream)
+                ss.run(ring[i], out, stream=stream, overlap_previous=not args.no_overlap)
     reps = max(1, n // len(ring))
     for _ in range(3):
         g.replay()
@@ -576,7 +576,8 @@ def run_spec(args, ss, rank, dev, stream):
             "commit_accepted_us_per_call": commit_us,
             "requests_per_s": int(ring_host[0]["num_requests"]) * calls / (ms / 1e3),
             "ms_per_call": ms / calls, "calls": calls,
-            "logits_GBps": W.algorithmic_bytes(ring_host[0]) * calls / (ms / 1e3) / 1e9}
+            "logits_GBps": W.algorithmic_bytes(ring_host[0]) * calls / (ms / 1e3) / 1e9,
+            "consecutive_calls_overlap": not args.no_overlap}
 
 
 TREE_WORKLOAD = "tree verify R=32 trees of 1-16 nodes V=128256 bf16"
@@ -782,7 +783,7 @@ def run_config_block(args, ss, cfg, rank, dev, stream, peak, ring_n, calls_wante
     rows = int(w0["num_rows"]) if w0["kind"] == "sample" else int(w0["draft_offsets"][-1]) + int(w0["num_requests"])
     alg = W.algorithmic_bytes(w0)
     cs = ss.ss_cluster_size(int(w0["vocab"]), w0["dtype"])
-    overlap = w0["kind"] == "sample" and not args.no_overlap  # as the headline
+    overlap = w0["kind"] in ("sample", "verify") and not args.no_overlap  # as the headline
     with torch.cuda.stream(stream):
         if "workspace" in out:
             ss.ss_workspace_init(out["workspace"], stream=stream)
@@ -1005,7 +1006,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overlap", action="store_true",
-                    help="time sampling calls one at a time (no SS_SAMPLE_OVERLAP_PREVIOUS)")
+                    help="time calls one at a time (no SS_SAMPLE/VERIFY_OVERLAP_PREVIOUS)")
     args = ap.parse_args()
 
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:

@@ -142,8 +142,9 @@ typedef struct {
                                    batch and of how a batch is split over GPUs. */
 } ss_params;
 
-/* ss_sample_args.flags (0 = none). */
-#define SS_SAMPLE_OVERLAP_PREVIOUS 1 /* the call may overlap the sampling call before it (below) */
+/* ss_sample_args.flags / ss_verify_args.flags (0 = none). */
+#define SS_SAMPLE_OVERLAP_PREVIOUS 1 /* the call may overlap the call before it (below) */
+#define SS_VERIFY_OVERLAP_PREVIOUS 1 /* the same for ss_spec_verify / ss_spec_verify_noalloc */
 
 /* ss_process_sample: one token per row.  Row r is logits + r * row_stride. */
 typedef struct {
@@ -160,7 +161,8 @@ typedef struct {
                                    rows, -inf where masked), or NULL              */
   int32_t flags;                /* 0, or SS_SAMPLE_OVERLAP_PREVIOUS: the call may
                                    begin while the kernel before it on the stream
-                                   -- a bf16 ss_process_sample call -- is still
+                                   -- a bf16 sampling or verification call of this
+                                   library -- is still
                                    running (programmatic dependent launch): it
                                    reads its inputs at once and orders only its
                                    writes after that call.  Set it only when no
@@ -195,6 +197,16 @@ typedef struct {
   int32_t* out_status;          /* [R] worst row status of the request            */
   int32_t* out_kept;            /* [sum(k_i + 1)] |K| per target row, or NULL     */
   float* debug_processed;       /* [sum(k_i + 1), V], or NULL                     */
+  int32_t flags;                /* 0, or SS_VERIFY_OVERLAP_PREVIOUS: on bf16
+                                   logits the call may begin while the kernel
+                                   before it on the stream -- a bf16 sampling or
+                                   verification call of this library -- is still
+                                   running, as SS_SAMPLE_OVERLAP_PREVIOUS; its
+                                   workspace is used only once that call has
+                                   finished.  Set it only when no input of this
+                                   call is an output of that call.  Other bits
+                                   are invalid; ss_spec_verify_noalloc ignores
+                                   it (it clears its scratch before the launch). */
 } ss_verify_args;
 
 /* Bytes of caller-owned device workspace ss_spec_verify needs for up to

@@ -1973,13 +1973,13 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   uint32_t* hraw = reinterpret_cast<uint32_t*>(hval + kHashCap);  // raw bf16 bits | allowed << 16
 
   SS_STAMP(0);
-  // Programmatic dependent launch (sampling calls): a next sampling call that
-  // allows it may start its CTAs as soon as every CTA of this one has started
-  // (they take the SM slots this call's finished rows give back).  Such a
-  // call reads no output of this one, so only its writes -- outputs and the
-  // debug rows -- wait for this grid (griddepcontrol.wait; a no-op in a
-  // launch without the attribute).
-  if (a.mode == 0) grid_launch_dependents();
+  // Programmatic dependent launch: a next call that allows it may start its
+  // CTAs as soon as every CTA of this one has started (they take the SM
+  // slots this call's finished rows give back).  Such a call reads no output
+  // of this one, so only its writes -- outputs, debug rows -- and, for
+  // verification, its use of the workspace wait for this grid
+  // (griddepcontrol.wait; a no-op in a launch without the attribute).
+  grid_launch_dependents();
   // the parameter loads go out before the bulk copies (a global load issued
   // after 16 KB copies of every CTA waits behind them)
   if (tid < 32) {
@@ -1994,6 +1994,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   if (c.bad_k) {
     // a draft count outside [0, max_draft]: the request's outputs, from its
     // first position only
+    grid_dependency_wait();
     if (rank == 0 && tid <= a.max_draft) {
       a.out_token[static_cast<int64_t>(c.req) * (a.max_draft + 1) + tid] = -1;
       if (tid == 0) {
@@ -2003,11 +2004,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     }
     return;
   }
-  int32_t rej_seen = 0;  // thread 0: the rejection word, read early (used at exchange 1)
-  if (tid == 0) {
-    c.status = max(c.status, c.pstatus);
-    if (a.mode == 1) rej_seen = ld_cg_s32(a.ws_counters + c.nreq + c.req);
-  }
+  if (tid == 0) c.status = max(c.status, c.pstatus);
   SS_STAMP(19);
   for (int s = tid; s < kHashCap; s += kThreads) {
     hkey[s] = -1;
@@ -2352,6 +2349,13 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     }
     if (c.k_on) __syncthreads();  // the certificate counts are complete
     if (tid == 0) {
+      // verification: the request's rejection word (the workspace is the
+      // previous call's until that grid has finished)
+      int32_t rej_seen = 0;
+      if (a.mode == 1) {
+        grid_dependency_wait();
+        rej_seen = ld_cg_s32(a.ws_counters + c.nreq + c.req);
+      }
       c.seed_pair = gvec;
       c.seed_ey = es;
       c.seed_et = et;
@@ -2958,13 +2962,13 @@ static ss_status launch(HArgs& a, cudaStream_t stream) {
     attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    // with SS_SAMPLE_OVERLAP_PREVIOUS: this launch may begin while the
-    // sampling kernel before it on the stream finishes (the kernel orders its
-    // writes after that grid)
+    // with SS_SAMPLE_OVERLAP_PREVIOUS / SS_VERIFY_OVERLAP_PREVIOUS: this
+    // launch may begin while the kernel before it on the stream finishes (the
+    // kernel orders its writes and its workspace use after that grid)
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = (a.mode == 0 && a.overlap) ? 2 : 1;
+    cfg.numAttrs = a.overlap ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, ss_hist_kernel, a);
   }
   if (e != cudaSuccess) {
@@ -3036,6 +3040,7 @@ ss_status hist_verify(const ss_verify_args& A, int4* results, int32_t* counters,
   a.out_status = A.out_status;
   a.out_kept = A.out_kept;
   a.debug = A.debug_processed;
+  a.overlap = (A.flags & SS_VERIFY_OVERLAP_PREVIOUS) ? 1 : 0;
   a.ws_results = results;
   a.ws_counters = counters;
   a.ncta = hist::cluster_for(A.vocab);

@@ -2984,6 +2984,7 @@ static ss_status check_verify(const ss_verify_args* args) {
   const ss_verify_args& A = *args;
   if (A.num_requests < 0 || A.vocab < 1 || A.max_draft < 0 || A.max_draft > kMaxDraft) return SS_ERR_INVALID_ARG;
   if (A.dtype != SS_DTYPE_F32 && A.dtype != SS_DTYPE_BF16) return SS_ERR_INVALID_ARG;
+  if (A.flags & ~SS_VERIFY_OVERLAP_PREVIOUS) return SS_ERR_INVALID_ARG;
   if (A.num_requests == 0) return SS_OK;
   const int es = (A.dtype == SS_DTYPE_BF16) ? 2 : 4;
   if (!A.target_logits || (reinterpret_cast<uintptr_t>(A.target_logits) % es) != 0 || !A.draft_offsets)
@@ -3337,7 +3338,10 @@ ss_status ss_spec_verify_noalloc(const ss_verify_args* args, ss_stream_t stream)
     g_last_cuda_error = static_cast<int32_t>(e);
     return SS_ERR_CUDA;
   }
-  return verify_launch(*args, scratch, SS_NOALLOC_SCRATCH_BYTES, reinterpret_cast<cudaStream_t>(stream));
+  // (no overlap with the call before: the scratch is cleared in between)
+  ss_verify_args A = *args;
+  A.flags = 0;
+  return verify_launch(A, scratch, SS_NOALLOC_SCRATCH_BYTES, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int32_t ss_cluster_size(int32_t vocab, int32_t dtype) {

@@ -83,6 +83,7 @@ class ss_sample_args(C.Structure):
 
 
 SS_SAMPLE_OVERLAP_PREVIOUS = 1
+SS_VERIFY_OVERLAP_PREVIOUS = 1
 
 
 class ss_verify_args(C.Structure):
@@ -103,6 +104,7 @@ class ss_verify_args(C.Structure):
         ("out_status", C.c_void_p),
         ("out_kept", C.c_void_p),
         ("debug_processed", C.c_void_p),
+        ("flags", C.c_int32),
     ]
 
 
@@ -367,8 +369,9 @@ def ss_merge_round(records, params, state, out_token, out_status, *, round, voca
 
 
 def _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
-                 out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed):
+                 out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed, flags=0):
     a = ss_verify_args()
+    a.flags = int(flags)
     a.num_requests = int(out_num_accepted.numel())
     a.vocab = int(vocab)
     a.max_draft = int(max_draft)
@@ -390,10 +393,12 @@ def _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params
 
 def ss_spec_verify(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
                    out_status, workspace, *, vocab, max_draft, dtype, row_stride=None, draft_stride=None,
-                   out_kept=None, debug_processed=None, stream=None):
-    """Verify the drafts of `out_num_accepted.numel()` requests."""
+                   out_kept=None, debug_processed=None, stream=None, overlap_previous=False):
+    """Verify the drafts of `out_num_accepted.numel()` requests
+    (overlap_previous sets SS_VERIFY_OVERLAP_PREVIOUS, see include/ss.h)."""
     a = _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
-                     out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed)
+                     out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed,
+                     SS_VERIFY_OVERLAP_PREVIOUS if overlap_previous else 0)
     _check(load().ss_spec_verify(C.byref(a), C.c_void_p(workspace.data_ptr()),
                                  workspace.numel() * workspace.element_size(), _stream_handle(stream)))
 
@@ -577,7 +582,8 @@ def alloc_outputs(dw, device="cuda", debug=False):
 
 def run(dw, o, stream=None, debug=False, overlap_previous=False):
     """One library call on a device workload `dw` into outputs `o`
-    (overlap_previous: see ss_process_sample; sampling only)."""
+    (overlap_previous: see ss_process_sample; sampling and linear
+    verification)."""
     params = {k: dw.get(k) for k in PARAM_FIELDS}
     params["bitmask_stride"] = dw.get("bitmask_stride", 0)
     dbg = o.get("processed") if debug else None
@@ -595,4 +601,5 @@ def run(dw, o, stream=None, debug=False, overlap_previous=False):
         ss_spec_verify(dw["target_logits"], dw["draft_offsets"], dw["draft_tokens"], dw["draft_probs"], params,
                        o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],
                        max_draft=dw["max_draft"], dtype=dw["dtype"], row_stride=dw["row_stride"],
-                       draft_stride=dw["draft_stride"], out_kept=o["kept"], debug_processed=dbg, stream=stream)
+                       draft_stride=dw["draft_stride"], out_kept=o["kept"], debug_processed=dbg, stream=stream,
+                       overlap_previous=overlap_previous)

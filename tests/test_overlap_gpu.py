@@ -1,7 +1,8 @@
-"""Back-to-back sampling calls that overlap (SS_SAMPLE_OVERLAP_PREVIOUS,
-programmatic dependent launch): every call's results equal those of the same
-call made alone, including when consecutive calls write the same output
-buffers (the later call's writes land last) and inside a CUDA graph."""
+"""Back-to-back calls that overlap (SS_SAMPLE_OVERLAP_PREVIOUS /
+SS_VERIFY_OVERLAP_PREVIOUS, programmatic dependent launch): every call's
+results equal those of the same call made alone, including when consecutive
+calls write the same output buffers (the later call's writes land last), when
+verification calls share one workspace, and inside a CUDA graph."""
 import numpy as np
 import pytest
 
@@ -107,3 +108,59 @@ def test_overlap_flag_on_fp32_and_verification_is_harmless(ss):
     for k in KEYS:
         assert torch.equal(a[k], b[k]), k
     assert np.all(a["status"].cpu().numpy() == 0)
+
+
+VKEYS = ("out_tokens", "num_accepted", "status", "kept")
+
+
+def _vsets(ss, n):
+    return [ss.to_device(W.make(4, requests=16, k=4, vocab=128256, seed=70 + i)) for i in range(n)]
+
+
+def test_overlapped_verification_with_one_workspace(ss):
+    # consecutive verification calls share the outputs and the workspace: a
+    # call may start early but uses the workspace only after the one before
+    sets = _vsets(ss, 4)
+    ref = []
+    for dw in sets:
+        o = ss.alloc_outputs(dw)
+        ss.run(dw, o)
+        torch.cuda.synchronize()
+        ref.append({k: o[k].clone() for k in VKEYS})
+    o = ss.alloc_outputs(sets[0])
+    for rep in range(3):
+        for dw in sets:
+            ss.run(dw, o, overlap_previous=True)
+        torch.cuda.synchronize()
+        for k in VKEYS:
+            assert torch.equal(ref[-1][k], o[k]), (rep, k)
+    # each call's own outputs, overlapped, into separate buffers (one workspace each)
+    sep = [ss.alloc_outputs(dw) for dw in sets]
+    for dw, oo in zip(sets, sep):
+        ss.run(dw, oo, overlap_previous=True)
+    torch.cuda.synchronize()
+    for r, oo in zip(ref, sep):
+        for k in VKEYS:
+            assert torch.equal(r[k], oo[k]), k
+
+
+def test_overlapped_sampling_after_verification(ss):
+    # a sampling call overlapping the verification call before it
+    v = _vsets(ss, 1)[0]
+    s_sets = _sets(ss, 2)
+    ref_s = _alone(ss, s_sets)
+    ov = ss.alloc_outputs(v)
+    ss.run(v, ov)
+    torch.cuda.synchronize()
+    ref_v = {k: ov[k].clone() for k in VKEYS}
+    o2 = ss.alloc_outputs(v)
+    so = [ss.alloc_outputs(dw) for dw in s_sets]
+    ss.run(v, o2, overlap_previous=True)
+    for dw, oo in zip(s_sets, so):
+        ss.run(dw, oo, overlap_previous=True)
+    torch.cuda.synchronize()
+    for k in VKEYS:
+        assert torch.equal(ref_v[k], o2[k]), k
+    for r, oo in zip(ref_s, so):
+        for k in KEYS:
+            assert torch.equal(r[k], oo[k]), k
