@@ -2202,7 +2202,9 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     const int32_t t = hkey[s];
     float y = ninf();
     if (t >= 0) {
-      const uint32_t raw = hraw[s] | reinterpret_cast<const uint16_t*>(g_dyn)[t - lo];
+      uint16_t* staged = reinterpret_cast<uint16_t*>(g_dyn) + (t - lo);
+      const uint32_t raw = hraw[s] | *staged;
+      *staged = 0xff80u;  // the staged copy is excluded: the token is an entry
       float z = bf16_to_f(raw & 0xffffu);
       const int32_t hc = hcnt[s];
       const int32_t cnt = hc & ~kBiasFlag;
@@ -2236,13 +2238,9 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
     }
   }
   __syncthreads();
-  // fix-up: the patched tokens' staged copies are excluded (they are
-  // entries now), then the bounds of their 16-token pairs are recomputed
+  // fix-up: the bounds of the patched tokens' 16-token pairs are recomputed
+  // (their staged copies were excluded above)
   if (c.npatch) {
-    uint16_t* d16 = reinterpret_cast<uint16_t*>(g_dyn);
-    for (int s = tid; s < kHashCap; s += kThreads)
-      if (hkey[s] >= 0) d16[hkey[s] - lo] = 0xff80u;
-    __syncthreads();
     for (int s = tid; s < kHashCap; s += kThreads)
       if (hkey[s] >= 0) {
         const int pr = (hkey[s] - lo) >> 4;
@@ -2601,12 +2599,15 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
           const int grp = tid >> 3, sub = tid & 7;  // 8 threads per group
           uint32_t cnt = 0;
           unsigned long long mass = 0;
-          for (int s = g_gb[grp] + sub; s < g_gb[grp + 1]; s += 8) {
+          const float m = c.m;
+          const int s_end = g_gb[grp + 1];
+          // no branch on empty slots (their mass term is 0): unrolled, the
+          // iterations' loads and exponentials overlap
+#pragma unroll 4
+          for (int s = g_gb[grp] + sub; s < s_end; s += 8) {
             const uint32_t h = (hist[s >> 1] >> ((s & 1) << 4)) & 0xffffu;
-            if (h) {
-              cnt += h;
-              mass += static_cast<unsigned long long>(h) * fmass(slot_y(s), c.m);
-            }
+            cnt += h;
+            mass += static_cast<unsigned long long>(h) * fmass(slot_y(s), m);
           }
 #pragma unroll
           for (int o = 1; o < 8; o <<= 1) {
