@@ -595,13 +595,13 @@ def run_tree(args, ss, rank, dev, stream):
     with torch.cuda.stream(stream):
         ss.ss_workspace_init(out["workspace"], stream=stream)
         for dw in ring:
-            ss.run(dw, out, stream=stream)
+            ss.run(dw, out, stream=stream, overlap_previous=not args.no_overlap)
     stream.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
             for dw in ring:
-                ss.run(dw, out, stream=stream)
+                ss.run(dw, out, stream=stream, overlap_previous=not args.no_overlap)
     reps = max(1, args.tree_steps // len(ring))
     for _ in range(3):
         g.replay()
@@ -620,7 +620,7 @@ def run_tree(args, ss, rank, dev, stream):
     return {"workload": TREE_WORKLOAD, "node_rows_per_s": rows * reps / (ms / 1e3),
             "requests_per_s": 32 * calls / (ms / 1e3), "ms_per_call": ms / calls, "calls": calls,
             "mean_nodes_per_request": rows / (32.0 * len(ring)),
-            "logits_GBps": alg * reps / (ms / 1e3) / 1e9}
+            "logits_GBps": alg * reps / (ms / 1e3) / 1e9, "consecutive_calls_overlap": not args.no_overlap}
 
 
 def run_sharded(args, ss, rank, dev, stream, parts=4):

@@ -145,6 +145,7 @@ typedef struct {
 /* ss_sample_args.flags / ss_verify_args.flags (0 = none). */
 #define SS_SAMPLE_OVERLAP_PREVIOUS 1 /* the call may overlap the call before it (below) */
 #define SS_VERIFY_OVERLAP_PREVIOUS 1 /* the same for ss_spec_verify / ss_spec_verify_noalloc */
+#define SS_TREE_OVERLAP_PREVIOUS 1   /* the same for ss_tree_verify (ss_tree_args.flags) */
 
 /* ss_process_sample: one token per row.  Row r is logits + r * row_stride. */
 typedef struct {
@@ -337,6 +338,14 @@ typedef struct {
   int32_t* out_status;          /* [R]                                            */
   int32_t* out_kept;            /* [sum n_i] |K| per node row, or NULL            */
   float* debug_processed;       /* [sum n_i, V], or NULL                          */
+  int32_t flags;                /* 0, or SS_TREE_OVERLAP_PREVIOUS: the call may
+                                   begin while the kernel before it on the stream
+                                   -- a tree verification call of this library --
+                                   is still running (programmatic dependent
+                                   launch); its outputs, debug rows and workspace
+                                   are written only once that call has finished.
+                                   Set it only when no input of this call is an
+                                   output of that call.  Other bits are invalid. */
 } ss_tree_args;
 
 ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t workspace_bytes, ss_stream_t stream);

@@ -262,6 +262,7 @@ struct KArgs {
   // row_is_heavy), the others are left to a concurrent launch of the other
   // class; 3: every task, costliest first (see ordered_task)
   int32_t row_class;
+  int32_t overlap;  // trees: launched to overlap the call before it (writes wait for it)
   Layout L;
 };
 
@@ -1878,6 +1879,13 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   const int rank = static_cast<int>(cl.block_rank());
   const int ncta = static_cast<int>(cl.num_blocks());
   const Layout& L = a.L;
+  // Programmatic dependent launch (tree calls with SS_TREE_OVERLAP_PREVIOUS):
+  // a next call may start its CTAs once every CTA of this one has started;
+  // this call's own global writes wait for the grid before it (no-ops in a
+  // launch without the attribute).  Debug rows are written throughout, so a
+  // call that writes them waits at once.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (a.debug_processed) asm volatile("griddepcontrol.wait;" ::: "memory");
   int task = static_cast<int>(blockIdx.x) / ncta;
   if (a.row_class != 0) {
     task = ordered_task(a, task, reinterpret_cast<int32_t*>(smem_raw + L.red_off));
@@ -2470,6 +2478,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
 
   // ------------------------------------------------------------- outputs
   if (rank == 0 && tid == 0) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous call has finished
     if (status != SS_ROW_OK) {
       token = -1;
       kept = 0;
@@ -2870,13 +2879,15 @@ static cudaError_t launch(const KArgs& ka, int cs, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = ka.L.total;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = ka.overlap ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, ss_row_kernel<DT>, ka);
 }
 
@@ -3243,6 +3254,7 @@ ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t works
   if (A.num_requests < 0 || A.vocab < 1 || A.max_nodes < 1 || A.max_nodes > SS_TREE_MAX_NODES)
     return SS_ERR_INVALID_ARG;
   if (A.dtype != SS_DTYPE_F32 && A.dtype != SS_DTYPE_BF16) return SS_ERR_INVALID_ARG;
+  if (A.flags & ~SS_TREE_OVERLAP_PREVIOUS) return SS_ERR_INVALID_ARG;
   if (A.num_requests == 0) return SS_OK;
   const int es = (A.dtype == SS_DTYPE_BF16) ? 2 : 4;
   if (!A.target_logits || (reinterpret_cast<uintptr_t>(A.target_logits) % es) != 0 || !A.node_offsets ||
@@ -3280,6 +3292,7 @@ ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t works
   k.debug_processed = A.debug_processed;
   k.ws_results = reinterpret_cast<int4*>(workspace);
   k.ws_counters = counters_at_end(workspace, workspace_bytes, A.num_requests);
+  k.overlap = (A.flags & SS_TREE_OVERLAP_PREVIOUS) ? 1 : 0;
   if (tasks >= 16 && tasks <= kMaxOrderedTasks) k.row_class = 3;
   return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -84,6 +84,7 @@ class ss_sample_args(C.Structure):
 
 SS_SAMPLE_OVERLAP_PREVIOUS = 1
 SS_VERIFY_OVERLAP_PREVIOUS = 1
+SS_TREE_OVERLAP_PREVIOUS = 1
 
 
 class ss_verify_args(C.Structure):
@@ -128,6 +129,7 @@ class ss_tree_args(C.Structure):
         ("out_status", C.c_void_p),
         ("out_kept", C.c_void_p),
         ("debug_processed", C.c_void_p),
+        ("flags", C.c_int32),
     ]
 
 
@@ -415,9 +417,12 @@ def ss_spec_verify_noalloc(target_logits, draft_offsets, draft_tokens, draft_pro
 
 def ss_tree_verify(target_logits, node_offsets, parents, node_tokens, draft_probs, params, out_tokens,
                    out_num_accepted, out_status, workspace, *, vocab, max_nodes, dtype, row_stride=None,
-                   draft_stride=None, out_path=None, out_kept=None, debug_processed=None, stream=None):
-    """Verify the draft trees of `out_num_accepted.numel()` requests."""
+                   draft_stride=None, out_path=None, out_kept=None, debug_processed=None, stream=None,
+                   overlap_previous=False):
+    """Verify the draft trees of `out_num_accepted.numel()` requests
+    (overlap_previous sets SS_TREE_OVERLAP_PREVIOUS, see include/ss.h)."""
     a = ss_tree_args()
+    a.flags = SS_TREE_OVERLAP_PREVIOUS if overlap_previous else 0
     a.num_requests = int(out_num_accepted.numel())
     a.vocab = int(vocab)
     a.max_nodes = int(max_nodes)
@@ -582,8 +587,7 @@ def alloc_outputs(dw, device="cuda", debug=False):
 
 def run(dw, o, stream=None, debug=False, overlap_previous=False):
     """One library call on a device workload `dw` into outputs `o`
-    (overlap_previous: see ss_process_sample; sampling and linear
-    verification)."""
+    (overlap_previous: see ss_process_sample; every kind of call)."""
     params = {k: dw.get(k) for k in PARAM_FIELDS}
     params["bitmask_stride"] = dw.get("bitmask_stride", 0)
     dbg = o.get("processed") if debug else None
@@ -596,7 +600,7 @@ def run(dw, o, stream=None, debug=False, overlap_previous=False):
                        params, o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],
                        max_nodes=dw["max_nodes"], dtype=dw["dtype"], row_stride=dw["row_stride"],
                        draft_stride=dw["draft_stride"], out_path=o["out_path"], out_kept=o["kept"],
-                       debug_processed=dbg, stream=stream)
+                       debug_processed=dbg, stream=stream, overlap_previous=overlap_previous)
     else:
         ss_spec_verify(dw["target_logits"], dw["draft_offsets"], dw["draft_tokens"], dw["draft_probs"], params,
                        o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],

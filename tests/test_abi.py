@@ -101,6 +101,13 @@ def test_host_side_argument_errors_launch_nothing(lib):
     assert lib.ss_spec_verify(C.byref(v), C.c_void_p(256), 8, None) == 4  # too small
     v.row_stride = 63  # stride < vocab
     assert lib.ss_spec_verify(C.byref(v), C.c_void_p(256), 1 << 20, None) == 1
+    t = ss.ss_tree_args()
+    t.num_requests, t.vocab, t.max_nodes, t.dtype = 0, 100, 4, 1
+    assert lib.ss_tree_verify(C.byref(t), None, 0, None) == 0  # no requests: nothing to do
+    t.flags = 2  # an unknown flag bit
+    assert lib.ss_tree_verify(C.byref(t), None, 0, None) == 1
+    t.flags = ss.SS_TREE_OVERLAP_PREVIOUS
+    assert lib.ss_tree_verify(C.byref(t), None, 0, None) == 0
 
 
 def test_shard_entry_points_reject_bad_arguments(lib):

@@ -1,5 +1,6 @@
-"""Back-to-back calls that overlap (SS_SAMPLE_OVERLAP_PREVIOUS /
-SS_VERIFY_OVERLAP_PREVIOUS, programmatic dependent launch): every call's
+"""Back-to-back calls that overlap (SS_SAMPLE_OVERLAP_PREVIOUS,
+SS_VERIFY_OVERLAP_PREVIOUS, SS_TREE_OVERLAP_PREVIOUS: programmatic dependent
+launch): every call's
 results equal those of the same call made alone, including when consecutive
 calls write the same output buffers (the later call's writes land last), when
 verification calls share one workspace, and inside a CUDA graph."""
@@ -164,3 +165,43 @@ def test_overlapped_sampling_after_verification(ss):
     for r, oo in zip(ref_s, so):
         for k in KEYS:
             assert torch.equal(r[k], oo[k]), k
+
+
+TKEYS = ("out_tokens", "out_path", "num_accepted", "status")
+
+
+def test_overlapped_tree_verification_with_one_workspace(ss):
+    # draft trees of different shapes, back to back, into shared outputs and
+    # one workspace, then each into its own, alone and in a graph
+    hosts = [W.tree(seed=300 + i, requests=24, vocab=128256, max_nodes=16) for i in range(4)]
+    sets = [ss.to_device(w) for w in hosts]
+    rows = [int(w["node_offsets"][-1]) for w in hosts]
+    ref = []
+    for dw in sets:
+        o = ss.alloc_outputs(dw)
+        ss.run(dw, o)
+        torch.cuda.synchronize()
+        ref.append({k: o[k].clone() for k in TKEYS + ("kept",)})
+    big = max(range(len(sets)), key=lambda i: rows[i])
+    o = ss.alloc_outputs(sets[big])
+    for rep in range(3):
+        for dw in sets:
+            ss.run(dw, o, overlap_previous=True)
+        torch.cuda.synchronize()
+        for k in TKEYS:
+            assert torch.equal(ref[-1][k], o[k]), (rep, k)
+        assert torch.equal(ref[-1]["kept"], o["kept"][:rows[-1]]), rep
+    sep = [ss.alloc_outputs(dw) for dw in sets]
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for dw, oo in zip(sets, sep):
+                ss.run(dw, oo, stream=stream, overlap_previous=True)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for r, oo in zip(ref, sep):
+        for k in TKEYS + ("kept",):
+            assert torch.equal(r[k], oo[k]), k
+    assert any(int(r["num_accepted"].sum()) > 0 for r in ref)
