@@ -511,6 +511,22 @@ def run_e2e(args, ss, ring_host, dev, stream, rows_per_call, dist):
             "pipeline": "one packed copy per step, back to back on a copy stream, overlapped with the previous step's sampling; read-backs on a third stream"}
 
 
+def graph_of_calls(ss, ring, out, stream, overlap, min_calls=16):
+    """A CUDA graph of consecutive calls cycling through the input sets of
+    `ring` (whole passes, at least `min_calls` calls), so that consecutive
+    calls may overlap inside it as in a serving loop; returns the graph and
+    its number of calls."""
+    import torch
+    inner = max(1, -(-min_calls // len(ring)))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(inner):
+                for dw in ring:
+                    ss.run(dw, out, stream=stream, overlap_previous=overlap)
+    return g, inner * len(ring)
+
+
 def run_spec(args, ss, rank, dev, stream):
     """Verification throughput on the linear-draft workload (32 requests, k=4)."""
     import torch
@@ -523,16 +539,12 @@ def run_spec(args, ss, rank, dev, stream):
         for i in range(len(ring)):
             ss.run(ring[i], out, stream=stream, overlap_previous=not args.no_overlap)
     stream.synchronize()
-    n = args.spec_steps
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(len(ring)):
-                ss.run(ring[i], out, stream=stream, overlap_previous=not args.no_overlap)
-    reps = max(1, n // len(ring))
-    for _ in range(3):
-        g.replay()
-    stream.synchronize()
+    g, per_graph = graph_of_calls(ss, ring, out, stream, not args.no_overlap)
+    reps = max(1, args.spec_steps // per_graph)
+    with torch.cuda.stream(stream):  # warm-up on the timed stream, finished before t0
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -542,7 +554,7 @@ def run_spec(args, ss, rank, dev, stream):
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
-    calls = reps * len(ring)
+    calls = reps * per_graph
     # the step after verification (tokens placed for the next step on the
     # device), timed on its own
     R, width = out["out_tokens"].shape
@@ -577,7 +589,7 @@ def run_spec(args, ss, rank, dev, stream):
             "requests_per_s": int(ring_host[0]["num_requests"]) * calls / (ms / 1e3),
             "ms_per_call": ms / calls, "calls": calls,
             "logits_GBps": W.algorithmic_bytes(ring_host[0]) * calls / (ms / 1e3) / 1e9,
-            "consecutive_calls_overlap": not args.no_overlap}
+            "consecutive_calls_overlap": not args.no_overlap, "calls_per_graph": per_graph}
 
 
 TREE_WORKLOAD = "tree verify R=32 trees of 1-16 nodes V=128256 bf16"
@@ -597,15 +609,12 @@ def run_tree(args, ss, rank, dev, stream):
         for dw in ring:
             ss.run(dw, out, stream=stream, overlap_previous=not args.no_overlap)
     stream.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(g, stream=stream):
-            for dw in ring:
-                ss.run(dw, out, stream=stream, overlap_previous=not args.no_overlap)
-    reps = max(1, args.tree_steps // len(ring))
-    for _ in range(3):
-        g.replay()
-    stream.synchronize()
+    g, per_graph = graph_of_calls(ss, ring, out, stream, not args.no_overlap)
+    reps = max(1, args.tree_steps // per_graph)
+    with torch.cuda.stream(stream):  # warm-up on the timed stream, finished before t0
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -615,12 +624,14 @@ def run_tree(args, ss, rank, dev, stream):
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
-    calls = reps * len(ring)
+    calls = reps * per_graph
+    passes = calls // len(ring)  # whole passes over the ring
     alg = sum(W.algorithmic_bytes(w) for w in ring_host)
-    return {"workload": TREE_WORKLOAD, "node_rows_per_s": rows * reps / (ms / 1e3),
+    return {"workload": TREE_WORKLOAD, "node_rows_per_s": rows * passes / (ms / 1e3),
             "requests_per_s": 32 * calls / (ms / 1e3), "ms_per_call": ms / calls, "calls": calls,
             "mean_nodes_per_request": rows / (32.0 * len(ring)),
-            "logits_GBps": alg * reps / (ms / 1e3) / 1e9, "consecutive_calls_overlap": not args.no_overlap}
+            "logits_GBps": alg * passes / (ms / 1e3) / 1e9, "consecutive_calls_overlap": not args.no_overlap,
+            "calls_per_graph": per_graph}
 
 
 def run_sharded(args, ss, rank, dev, stream, parts=4):
@@ -691,9 +702,10 @@ def run_sharded(args, ss, rank, dev, stream, parts=4):
             for dw in ring:
                 call(dw)
     reps = max(1, args.shard_steps // len(ring))
-    for _ in range(3):
-        g.replay()
-    stream.synchronize()
+    with torch.cuda.stream(stream):  # warm-up on the timed stream, finished before t0
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -790,15 +802,12 @@ def run_config_block(args, ss, cfg, rank, dev, stream, peak, ring_n, calls_wante
         for dw in ring:
             ss.run(dw, out, stream=stream, overlap_previous=overlap)
     stream.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(g, stream=stream):
-            for dw in ring:
-                ss.run(dw, out, stream=stream, overlap_previous=overlap)
-    reps = max(1, calls_wanted // ring_n)
-    for _ in range(3):
-        g.replay()
-    stream.synchronize()
+    g, per_graph = graph_of_calls(ss, ring, out, stream, overlap, min_calls=min(16, calls_wanted))
+    reps = max(1, calls_wanted // per_graph)
+    with torch.cuda.stream(stream):  # warm-up on the timed stream, finished before t0
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -808,7 +817,7 @@ def run_config_block(args, ss, cfg, rank, dev, stream, peak, ring_n, calls_wante
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
-    calls = reps * ring_n
+    calls = reps * per_graph
     per_call_s = ms / 1e3 / calls
     achieved = alg / per_call_s / 1e9
     # untimed: one more call on the first set, for the check
@@ -827,6 +836,7 @@ def run_config_block(args, ss, cfg, rank, dev, stream, peak, ring_n, calls_wante
         "l2": "ring of %d input set(s), %.0f MB%s" % (ring_n, ring_n * alg / 1e6,
                                                        " > 2x L2" if ring_n * alg > 2 * L2_BYTES else " > L2"),
         "consecutive_calls_overlap": overlap,
+        "calls_per_graph": per_graph,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "algorithmic_bytes_per_launch": alg, "traffic": recorded_traffic(W.CONFIG_NAMES[cfg], kernel),
                      "kernel": kernel, "kernel_sha256": kernel_source_hash(kernel)},
