@@ -222,7 +222,7 @@ def run_ours(args, rank, world, dist):
     overlap = ring_host[0]["kind"] == "sample" and not args.no_overlap
 
     def call(i, ov=overlap):
-        ss.run(ring[i % args.ring], out, stream=stream, overlap_previous=ov)
+        ss.run(ring[i % args.ring], out, stream=stream, overlap_previous=ov, target_rows=True)
 
     # graphs: one of `per_graph` calls (replayed), one for the remainder
     per_graph = min(args.steps, args.ring * 8)
@@ -323,7 +323,7 @@ def run_ours(args, rank, world, dist):
     # untimed: the GPU's outputs on the first input set, checked against the
     # oracle (all rows)
     chk = ss.alloc_outputs(ring[0], dev)
-    ss.run(ring[0], chk, stream=stream)
+    ss.run(ring[0], chk, stream=stream, target_rows=True)
     stream.synchronize()
     gpu0 = {k: v.cpu().numpy() for k, v in chk.items() if k not in ("workspace", "processed")}
     n_check = int(ring_host[0]["num_rows"]) if ring_host[0]["kind"] == "sample" else int(ring_host[0]["num_requests"])
@@ -514,8 +514,9 @@ def run_e2e(args, ss, ring_host, dev, stream, rows_per_call, dist):
 def graph_of_calls(ss, ring, out, stream, overlap, min_calls=16):
     """A CUDA graph of consecutive calls cycling through the input sets of
     `ring` (whole passes, at least `min_calls` calls), so that consecutive
-    calls may overlap inside it as in a serving loop; returns the graph and
-    its number of calls."""
+    calls may overlap inside it as in a serving loop; verification calls
+    state their number of target rows.  Returns the graph and its number of
+    calls."""
     import torch
     inner = max(1, -(-min_calls // len(ring)))
     g = torch.cuda.CUDAGraph()
@@ -523,7 +524,7 @@ def graph_of_calls(ss, ring, out, stream, overlap, min_calls=16):
         with torch.cuda.graph(g, stream=stream):
             for _ in range(inner):
                 for dw in ring:
-                    ss.run(dw, out, stream=stream, overlap_previous=overlap)
+                    ss.run(dw, out, stream=stream, overlap_previous=overlap, target_rows=True)
     return g, inner * len(ring)
 
 
@@ -537,7 +538,7 @@ def run_spec(args, ss, rank, dev, stream):
     with torch.cuda.stream(stream):
         ss.ss_workspace_init(out["workspace"], stream=stream)
         for i in range(len(ring)):
-            ss.run(ring[i], out, stream=stream, overlap_previous=not args.no_overlap)
+            ss.run(ring[i], out, stream=stream, overlap_previous=not args.no_overlap, target_rows=True)
     stream.synchronize()
     g, per_graph = graph_of_calls(ss, ring, out, stream, not args.no_overlap)
     reps = max(1, args.spec_steps // per_graph)
@@ -800,7 +801,7 @@ def run_config_block(args, ss, cfg, rank, dev, stream, peak, ring_n, calls_wante
         if "workspace" in out:
             ss.ss_workspace_init(out["workspace"], stream=stream)
         for dw in ring:
-            ss.run(dw, out, stream=stream, overlap_previous=overlap)
+            ss.run(dw, out, stream=stream, overlap_previous=overlap, target_rows=True)
     stream.synchronize()
     g, per_graph = graph_of_calls(ss, ring, out, stream, overlap, min_calls=min(16, calls_wanted))
     reps = max(1, calls_wanted // per_graph)
@@ -822,7 +823,7 @@ def run_config_block(args, ss, cfg, rank, dev, stream, peak, ring_n, calls_wante
     achieved = alg / per_call_s / 1e9
     # untimed: one more call on the first set, for the check
     chk = ss.alloc_outputs(ring[0], dev)
-    ss.run(ring[0], chk, stream=stream)
+    ss.run(ring[0], chk, stream=stream, target_rows=True)
     stream.synchronize()
     gpu = {k: v.cpu().numpy() for k, v in chk.items() if k not in ("workspace", "processed")}
     kernel = kernel_for(w0)
@@ -837,6 +838,7 @@ def run_config_block(args, ss, cfg, rank, dev, stream, peak, ring_n, calls_wante
                                                        " > 2x L2" if ring_n * alg > 2 * L2_BYTES else " > L2"),
         "consecutive_calls_overlap": overlap,
         "calls_per_graph": per_graph,
+        "target_rows_stated": w0["kind"] == "verify",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "algorithmic_bytes_per_launch": alg, "traffic": recorded_traffic(W.CONFIG_NAMES[cfg], kernel),
                      "kernel": kernel, "kernel_sha256": kernel_source_hash(kernel)},

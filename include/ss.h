@@ -208,6 +208,22 @@ typedef struct {
                                    call is an output of that call.  Other bits
                                    are invalid; ss_spec_verify_noalloc ignores
                                    it (it clears its scratch before the launch). */
+  int32_t num_target_rows;      /* 0, or the number of target rows, sum(k_i + 1)
+                                   with a k_i outside [0, max_draft] counted as
+                                   0.  On bf16 logits the launch may then have
+                                   one cluster per target row instead of one per
+                                   (request, position up to max_draft): the
+                                   library takes it when the full launch's idle
+                                   clusters (positions past a request's drafts)
+                                   would outnumber the rows past position 0,
+                                   whose clusters find their request and
+                                   position from draft_offsets.  Must be 0 or in
+                                   [num_requests, num_requests * (max_draft +
+                                   1)], else SS_ERR_INVALID_ARG; on bf16 logits a
+                                   value in that range that is not the sum makes
+                                   every request report SS_ROW_BAD_PARAM (tokens
+                                   -1, none accepted), whichever launch is
+                                   taken.  The fp32 path ignores it. */
 } ss_verify_args;
 
 /* Bytes of caller-owned device workspace ss_spec_verify needs for up to

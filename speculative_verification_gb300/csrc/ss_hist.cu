@@ -282,6 +282,11 @@ struct HArgs {
   int32_t mode;  // 0 sampling, 1 verification
   int32_t num_tasks;
   int32_t vocab, max_draft;
+  // verification: the number of requests; the caller's count of target rows
+  // (0: none; checked against the offsets when given); compact: the launch
+  // has one cluster per target row (num_tasks = target_rows), else one per
+  // (request, position up to max_draft)
+  int32_t nreq, target_rows, compact;
   int64_t row_stride;
   const uint16_t* logits;
   const int32_t* draft_offsets;
@@ -395,6 +400,7 @@ __shared__ uint32_t g_rtie[kMaxCluster];
 __shared__ uint32_t g_cert[kCertBins / 2];  // two 16-bit bin counts per word
 __shared__ int32_t g_tietok[kTieEnt];
 __shared__ uint32_t g_prm[32];           // the request's parameter words
+__shared__ int32_t g_loc[3];             // compact verification: request, position, count matches
 __shared__ uint32_t g_dscore;            // the draw's best score so far (order key; 0: none)
 __shared__ int32_t g_dtok;               // the lowest token holding it
 __shared__ int32_t g_fpos[3];            // short path: first failing positions (top-p, min-p), draft position
@@ -651,7 +657,7 @@ __device__ void coarse_locate(int by_mass, unsigned long long target) {
 
 // Thread 0: the task's row, its slice, and the bulk copies (issued first, so
 // that they overlap everything else of the set-up); then the parameters.
-__device__ void decode_and_copy(const HArgs& a, int task, int rank) {
+__device__ void decode_and_copy(const HArgs& a, int req, int j, int rank) {
   Ctx& c = g;
   c.valid = 1;
   c.bad_k = 0;
@@ -666,15 +672,10 @@ __device__ void decode_and_copy(const HArgs& a, int task, int rank) {
   c.x = -1;
   c.drow = -1;
   c.d0 = 0;
-  int req = task, j = 0, k = 0;
-  int64_t row = task;
+  int k = 0;
+  int64_t row = req;
   if (a.mode == 1) {
-    // position-major: every request's position 0 first, so that later
-    // positions tend to start after the earlier ones have decided
-    const int nreq = a.num_tasks / (a.max_draft + 1);
-    c.nreq = nreq;
-    j = task / nreq;
-    req = task - j * nreq;
+    c.nreq = a.nreq;
     c.d0 = a.draft_offsets[req];
     k = a.draft_offsets[req + 1] - c.d0;
     if (k < 0 || k > a.max_draft) {
@@ -718,19 +719,15 @@ __device__ void decode_and_copy(const HArgs& a, int task, int rank) {
   }
 }
 
-__device__ void read_params(const HArgs& a, int task);
+__device__ void read_params(const HArgs& a, int j);
 
 // Warp 1: the request's parameter words, one global load per lane (all in
 // flight at once), into g_prm; then its lane 0 checks them (read_params),
 // while thread 0 issues the bulk copies.
-__device__ void load_params(const HArgs& a, int task) {
+__device__ void load_params(const HArgs& a, int req, int j) {
   const ss_params& p = a.p;
   const int lane = threadIdx.x & 31;
-  int i = task;
-  if (a.mode == 1) {
-    const int nreq = a.num_tasks / (a.max_draft + 1);
-    i = task - (task / nreq) * nreq;
-  }
+  const int i = req;
   uint32_t v = 0;
   switch (lane) {
     case 0: v = __float_as_uint(p.temperature[i]); break;
@@ -758,21 +755,86 @@ __device__ void load_params(const HArgs& a, int task) {
   asm volatile("bar.arrive 1, 64;" ::: "memory");
   if (lane < 19) g_prm[lane] = v;
   __syncwarp();
-  if (lane == 0) read_params(a, task);
+  if (lane == 0) read_params(a, j);
+}
+
+// Compact verification launches (the caller gave the number of target
+// rows): one cluster per target row, in the order of the full launch --
+// position-major, every request's position 0 first, then position 1 of the
+// requests that have one, and so on.  A request's draft count k_i counts as 0
+// when it lies outside [0, max_draft] (such a request has position 0 only,
+// which reports it).
+__device__ __forceinline__ int drafts_of(const HArgs& a, int i) {
+  const int32_t k = __ldg(a.draft_offsets + i + 1) - __ldg(a.draft_offsets + i);
+  return (k < 0 || k > a.max_draft) ? 0 : k;
+}
+
+// Warp-wide: the sum over requests of min(k_i, cap), in every lane.
+__device__ long long sum_min_drafts(const HArgs& a, int cap) {
+  const int lane = threadIdx.x & 31;
+  long long s = 0;
+  for (int i = lane; i < a.nreq; i += 32) s += min(drafts_of(a, i), cap);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
+
+// Warp 0 of the CTAs with launch index nreq + t: the task's request and
+// position (g_loc[0], g_loc[1]) and whether the caller's count equals the
+// offsets' sum (g_loc[2]; on a mismatch the request is -1).
+__device__ void locate_position(const HArgs& a, long long t) {
+  const int lane = threadIdx.x & 31;
+  const long long past0 = sum_min_drafts(a, a.max_draft);
+  const bool ok = a.nreq + past0 == a.target_rows;
+  int req = -1, j = 0;
+  if (ok && t < past0) {
+    // the smallest position j with more than t tasks at positions 1..j
+    int lo = 1, hi = a.max_draft;
+    while (lo < hi) {
+      const int mid = lo + (hi - lo) / 2;
+      if (sum_min_drafts(a, mid) > t)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    j = lo;
+    long long idx = (j == 1) ? t : t - sum_min_drafts(a, j - 1);
+    // the idx-th request, in request order, with at least j drafts
+    for (int base = 0; base < a.nreq; base += 32) {
+      const int i = base + lane;
+      const bool has = i < a.nreq && drafts_of(a, i) >= j;
+      const unsigned m = __ballot_sync(0xffffffffu, has);
+      const int n = __popc(m);
+      if (idx < n) {
+        const int before = __popc(m & ((1u << lane) - 1u));
+        const unsigned pick = __ballot_sync(0xffffffffu, has && before == idx);
+        req = base + __ffs(pick) - 1;
+        break;
+      }
+      idx -= n;
+    }
+  }
+  if (lane == 0) {
+    g_loc[0] = req;
+    g_loc[1] = j;
+    g_loc[2] = ok ? 1 : 0;
+  }
+}
+
+// Warp 2 of the other CTAs of a launch with a count, beside the parameter
+// loads: whether the caller's count equals the offsets' sum (g_loc[2]).
+__device__ void check_row_count(const HArgs& a) {
+  const long long past0 = sum_min_drafts(a, a.max_draft);
+  if ((threadIdx.x & 31) == 0) g_loc[2] = (a.nreq + past0 == a.target_rows) ? 1 : 0;
 }
 
 // Lane 0 of warp 1, after load_params: the parameters, checked (the status
 // they give goes to c.pstatus; decode_and_copy runs meanwhile).
-__device__ void read_params(const HArgs& a, int task) {
+__device__ void read_params(const HArgs& a, int j) {
   Ctx& c = g;
   int st = SS_ROW_OK;
-  int j = 0;
   int32_t k = 0;
-  if (a.mode == 1) {
-    const int nreq = a.num_tasks / (a.max_draft + 1);
-    j = task / nreq;
-    k = static_cast<int32_t>(g_prm[18]) - static_cast<int32_t>(g_prm[17]);
-  }
+  if (a.mode == 1) k = static_cast<int32_t>(g_prm[18]) - static_cast<int32_t>(g_prm[17]);
   const float T = __uint_as_float(g_prm[0]);
   c.T = T;
   c.top_k = static_cast<int32_t>(g_prm[1]);
@@ -1958,7 +2020,7 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   const int tid = threadIdx.x;
   const int C = static_cast<int>(cl.num_blocks());
   const int rank = static_cast<int>(cl.block_rank());
-  const int task = static_cast<int>(blockIdx.x) / C;
+  const int launch_task = static_cast<int>(blockIdx.x) / C;
   uint4* data = reinterpret_cast<uint4*>(g_dyn);
   uint16_t* vb = reinterpret_cast<uint16_t*>(g_dyn + a.o_vb);
   uint32_t* hist = reinterpret_cast<uint32_t*>(g_dyn + a.o_hist);
@@ -1980,16 +2042,54 @@ __global__ void __launch_bounds__(kThreads, 2) ss_hist_kernel(const HArgs a) {
   // verification, its use of the workspace wait for this grid
   // (griddepcontrol.wait; a no-op in a launch without the attribute).
   grid_launch_dependents();
+  // the task's request and position: position-major over (position, request)
+  // -- every request's position 0 first, so that later positions tend to
+  // start after the earlier ones have decided -- or, in a compact launch,
+  // over the target rows that exist
+  int req = launch_task, j = 0;
+  if (a.mode == 1) {
+    if (a.compact && launch_task >= a.nreq) {
+      if (tid < 32) locate_position(a, static_cast<long long>(launch_task) - a.nreq);
+      __syncthreads();
+      req = g_loc[0];
+      j = g_loc[1];
+    } else {
+      j = launch_task / a.nreq;
+      req = launch_task - j * a.nreq;
+    }
+  }
   // the parameter loads go out before the bulk copies (a global load issued
   // after 16 KB copies of every CTA waits behind them)
-  if (tid < 32) {
-    asm volatile("bar.sync 1, 64;" ::: "memory");
-    if (tid == 0) decode_and_copy(a, task, rank);
-  } else if (tid < 64) {
-    load_params(a, task);
+  if (req >= 0) {
+    if (tid < 32) {
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+      if (tid == 0) decode_and_copy(a, req, j, rank);
+    } else if (tid < 64) {
+      load_params(a, req, j);
+    } else if (tid < 96 && a.target_rows > 0 && !(a.compact && launch_task >= a.nreq)) {
+      check_row_count(a);
+    }
   }
   __syncthreads();
   SS_STAMP(17);
+  if (a.target_rows > 0 && (req < 0 || !g_loc[2])) {
+    // the caller's count of target rows is not the offsets' sum: nothing is
+    // verified, and the launch's first cluster reports it on every request
+    // (a position-0 CTA first waits for the copies it has issued)
+    if (req >= 0 && tid == 0)
+      for (int q = 0; q < c.nch; ++q) mbar_wait_bounded(mbar + q, 0, kWaitPolls);
+    if (launch_task == 0 && rank == 0) {
+      grid_dependency_wait();
+      const int width = a.max_draft + 1;
+      for (int64_t e = tid; e < static_cast<int64_t>(a.nreq) * width; e += kThreads) a.out_token[e] = -1;
+      for (int i = tid; i < a.nreq; i += kThreads) {
+        a.out_num_accepted[i] = 0;
+        a.out_status[i] = SS_ROW_BAD_PARAM;
+      }
+    }
+    __syncthreads();
+    return;
+  }
   if (!c.valid) return;  // the same for the whole cluster
   if (c.bad_k) {
     // a draft count outside [0, max_draft]: the request's outputs, from its
@@ -3026,7 +3126,15 @@ ss_status hist_sample(const ss_sample_args& A, cudaStream_t stream, uint32_t sta
 ss_status hist_verify(const ss_verify_args& A, int4* results, int32_t* counters, cudaStream_t stream) {
   hist::HArgs a{};
   a.mode = 1;
-  a.num_tasks = A.num_requests * (A.max_draft + 1);
+  a.nreq = A.num_requests;
+  a.target_rows = A.num_target_rows;
+  // one cluster per target row when the idle clusters of the full launch
+  // (positions past a request's drafts) would outnumber the rows past
+  // position 0, whose clusters then search the offsets for their position
+  const int64_t full = static_cast<int64_t>(A.num_requests) * (A.max_draft + 1);
+  const int64_t rows = A.num_target_rows;
+  a.compact = (rows > 0 && full - rows > rows - A.num_requests) ? 1 : 0;
+  a.num_tasks = a.compact ? A.num_target_rows : static_cast<int32_t>(full);
   a.vocab = A.vocab;
   a.max_draft = A.max_draft;
   a.row_stride = A.row_stride;

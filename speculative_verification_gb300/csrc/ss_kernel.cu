@@ -2996,6 +2996,10 @@ static ss_status check_verify(const ss_verify_args* args) {
   if (A.num_requests < 0 || A.vocab < 1 || A.max_draft < 0 || A.max_draft > kMaxDraft) return SS_ERR_INVALID_ARG;
   if (A.dtype != SS_DTYPE_F32 && A.dtype != SS_DTYPE_BF16) return SS_ERR_INVALID_ARG;
   if (A.flags & ~SS_VERIFY_OVERLAP_PREVIOUS) return SS_ERR_INVALID_ARG;
+  if (A.num_target_rows != 0 &&
+      (A.num_target_rows < A.num_requests ||
+       A.num_target_rows > static_cast<int64_t>(A.num_requests) * (static_cast<int64_t>(A.max_draft) + 1)))
+    return SS_ERR_INVALID_ARG;
   if (A.num_requests == 0) return SS_OK;
   const int es = (A.dtype == SS_DTYPE_BF16) ? 2 : 4;
   if (!A.target_logits || (reinterpret_cast<uintptr_t>(A.target_logits) % es) != 0 || !A.draft_offsets)

@@ -106,6 +106,7 @@ class ss_verify_args(C.Structure):
         ("out_kept", C.c_void_p),
         ("debug_processed", C.c_void_p),
         ("flags", C.c_int32),
+        ("num_target_rows", C.c_int32),
     ]
 
 
@@ -371,9 +372,11 @@ def ss_merge_round(records, params, state, out_token, out_status, *, round, voca
 
 
 def _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
-                 out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed, flags=0):
+                 out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed, flags=0,
+                 num_target_rows=0):
     a = ss_verify_args()
     a.flags = int(flags)
+    a.num_target_rows = int(num_target_rows)
     a.num_requests = int(out_num_accepted.numel())
     a.vocab = int(vocab)
     a.max_draft = int(max_draft)
@@ -395,23 +398,25 @@ def _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params
 
 def ss_spec_verify(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
                    out_status, workspace, *, vocab, max_draft, dtype, row_stride=None, draft_stride=None,
-                   out_kept=None, debug_processed=None, stream=None, overlap_previous=False):
+                   out_kept=None, debug_processed=None, stream=None, overlap_previous=False, num_target_rows=0):
     """Verify the drafts of `out_num_accepted.numel()` requests
-    (overlap_previous sets SS_VERIFY_OVERLAP_PREVIOUS, see include/ss.h)."""
+    (overlap_previous sets SS_VERIFY_OVERLAP_PREVIOUS; num_target_rows is
+    ss_verify_args.num_target_rows: see include/ss.h)."""
     a = _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
                      out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed,
-                     SS_VERIFY_OVERLAP_PREVIOUS if overlap_previous else 0)
+                     SS_VERIFY_OVERLAP_PREVIOUS if overlap_previous else 0, num_target_rows)
     _check(load().ss_spec_verify(C.byref(a), C.c_void_p(workspace.data_ptr()),
                                  workspace.numel() * workspace.element_size(), _stream_handle(stream)))
 
 
 def ss_spec_verify_noalloc(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens,
                            out_num_accepted, out_status, *, vocab, max_draft, dtype, row_stride=None,
-                           draft_stride=None, out_kept=None, debug_processed=None, stream=None):
+                           draft_stride=None, out_kept=None, debug_processed=None, stream=None, num_target_rows=0):
     """ss_spec_verify with the library's static device scratch instead of a
     caller workspace (for callers that cannot allocate device memory)."""
     a = _verify_args(target_logits, draft_offsets, draft_tokens, draft_probs, params, out_tokens, out_num_accepted,
-                     out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed)
+                     out_status, vocab, max_draft, dtype, row_stride, draft_stride, out_kept, debug_processed,
+                     0, num_target_rows)
     _check(load().ss_spec_verify_noalloc(C.byref(a), _stream_handle(stream)))
 
 
@@ -585,9 +590,11 @@ def alloc_outputs(dw, device="cuda", debug=False):
     return o
 
 
-def run(dw, o, stream=None, debug=False, overlap_previous=False):
+def run(dw, o, stream=None, debug=False, overlap_previous=False, target_rows=False):
     """One library call on a device workload `dw` into outputs `o`
-    (overlap_previous: see ss_process_sample; every kind of call)."""
+    (overlap_previous: see ss_process_sample; every kind of call).  With
+    target_rows, a linear verification call states its number of target rows
+    (the rows of dw["target_logits"]; ss_verify_args.num_target_rows)."""
     params = {k: dw.get(k) for k in PARAM_FIELDS}
     params["bitmask_stride"] = dw.get("bitmask_stride", 0)
     dbg = o.get("processed") if debug else None
@@ -606,4 +613,5 @@ def run(dw, o, stream=None, debug=False, overlap_previous=False):
                        o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],
                        max_draft=dw["max_draft"], dtype=dw["dtype"], row_stride=dw["row_stride"],
                        draft_stride=dw["draft_stride"], out_kept=o["kept"], debug_processed=dbg, stream=stream,
-                       overlap_previous=overlap_previous)
+                       overlap_previous=overlap_previous,
+                       num_target_rows=int(dw["target_logits"].shape[0]) if target_rows else 0)

@@ -101,6 +101,12 @@ def test_host_side_argument_errors_launch_nothing(lib):
     assert lib.ss_spec_verify(C.byref(v), C.c_void_p(256), 8, None) == 4  # too small
     v.row_stride = 63  # stride < vocab
     assert lib.ss_spec_verify(C.byref(v), C.c_void_p(256), 1 << 20, None) == 1
+    v.row_stride = 64
+    for rows in (-1, 1, 7):  # outside [R, R * (max_draft + 1)] = [2, 6]
+        v.num_target_rows = rows
+        assert lib.ss_spec_verify(C.byref(v), C.c_void_p(256), 1 << 20, None) == 1, rows
+        assert lib.ss_spec_verify_noalloc(C.byref(v), None) == 1, rows
+    v.num_target_rows = 0
     t = ss.ss_tree_args()
     t.num_requests, t.vocab, t.max_nodes, t.dtype = 0, 100, 4, 1
     assert lib.ss_tree_verify(C.byref(t), None, 0, None) == 0  # no requests: nothing to do
@@ -159,3 +165,18 @@ def test_tree_entry_point_rejects_bad_arguments(lib):
     assert lib.ss_tree_verify(ss.C.byref(a), None, 0, None) == 1
     a.max_nodes, a.num_requests = 4, 0  # nothing to do
     assert lib.ss_tree_verify(ss.C.byref(a), None, 0, None) == 0
+
+
+def test_argument_structs_match_the_header():
+    """The binding's ctypes structs list the header's fields, in order."""
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "ss.h")).read(), flags=re.S)
+    structs = re.findall(r"typedef struct \{(.*?)\}\s*(\w+);", text, flags=re.S)
+    assert len(structs) >= 5
+    for body, name in structs:
+        fields = []
+        for decl in (d.strip() for d in body.split(";")):
+            if decl:
+                first, *more = decl.split(",")  # "int32_t a, b, c"
+                fields += [re.split(r"[\s*]+", first.strip())[-1]] + [m.strip(" *") for m in more]
+        cls = getattr(ss, name)
+        assert [f[0] for f in cls._fields_] == fields, name
