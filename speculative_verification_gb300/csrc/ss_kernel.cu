@@ -3382,6 +3382,6 @@ const char* ss_status_string(ss_status status) {
   return "unknown status";
 }
 
-const char* ss_version(void) { return "ss 0.2.0 (sm_103a)"; }
+const char* ss_version(void) { return "ss 0.3.0 (sm_103a)"; }
 
 }  // extern "C"
