@@ -216,10 +216,11 @@ def run_ours(args, rank, world, dist):
     out = ss.alloc_outputs(ring[0], dev)
     stream = torch.cuda.Stream(device=dev)
 
-    # consecutive sampling calls over independent batches may overlap (a
-    # call's first rows start on the SMs the previous call's last rows leave:
-    # SS_SAMPLE_OVERLAP_PREVIOUS); no call reads another's outputs here
-    overlap = ring_host[0]["kind"] == "sample" and not args.no_overlap
+    # consecutive calls over independent batches may overlap (a call's first
+    # rows start on the SMs the previous call's last rows leave:
+    # SS_SAMPLE_OVERLAP_PREVIOUS / SS_VERIFY_OVERLAP_PREVIOUS); no call reads
+    # another's outputs here
+    overlap = ring_host[0]["kind"] in ("sample", "verify") and not args.no_overlap
 
     def call(i, ov=overlap):
         ss.run(ring[i % args.ring], out, stream=stream, overlap_previous=ov, target_rows=True)
@@ -375,7 +376,8 @@ def run_ours(args, rank, world, dist):
             "input_dtype": ring_host[0]["dtype"],
             "l2": "ring of %d input sets, %.0f MB > 2x L2" % (args.ring, args.ring * bytes_per_call / 1e6),
             "launch": ("CUDA graph of %d calls, replayed; consecutive calls overlap (programmatic dependent "
-                       "launch, SS_SAMPLE_OVERLAP_PREVIOUS)" % per_graph) if overlap else (
+                       "launch, %s)" % (per_graph, "SS_SAMPLE_OVERLAP_PREVIOUS" if ring_host[0]["kind"] == "sample"
+                                        else "SS_VERIFY_OVERLAP_PREVIOUS")) if overlap else (
                            "CUDA graph of %d calls, replayed" % per_graph),
             "parallelism": "dp%d replicas" % world,
             "cluster_ctas_per_row": cs,
