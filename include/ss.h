@@ -222,8 +222,9 @@ typedef struct {
                                    1)], else SS_ERR_INVALID_ARG; on bf16 logits a
                                    value in that range that is not the sum makes
                                    every request report SS_ROW_BAD_PARAM (tokens
-                                   -1, none accepted), whichever launch is
-                                   taken.  The fp32 path ignores it. */
+                                   -1, none accepted; out_kept and
+                                   debug_processed are not written), whichever
+                                   launch is taken.  The fp32 path ignores it. */
 } ss_verify_args;
 
 /* Bytes of caller-owned device workspace ss_spec_verify needs for up to
