@@ -363,6 +363,20 @@ typedef struct {
                                    are written only once that call has finished.
                                    Set it only when no input of this call is an
                                    output of that call.  Other bits are invalid. */
+  int32_t num_nodes_total;      /* 0, or the number of target rows, sum n_i
+                                   (node_offsets[R]) with an n_i outside [1,
+                                   max_nodes] counted as 1.  When the launch
+                                   orders its node slots, costliest first (16 to
+                                   4096 slots, R * max_nodes), it then stops at
+                                   that many clusters instead of one per slot:
+                                   the slots without a node come last in that
+                                   order.  Must be 0 or in [num_requests,
+                                   num_requests * max_nodes], else
+                                   SS_ERR_INVALID_ARG; a value in that range
+                                   that is not the sum makes every request
+                                   report SS_ROW_BAD_PARAM (tokens and path -1,
+                                   none accepted; out_kept and debug_processed
+                                   are not written), whatever the launch. */
 } ss_tree_args;
 
 ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t workspace_bytes, ss_stream_t stream);

@@ -263,6 +263,10 @@ struct KArgs {
   // class; 3: every task, costliest first (see ordered_task)
   int32_t row_class;
   int32_t overlap;  // trees: launched to overlap the call before it (writes wait for it)
+  // trees: the caller's count of tasks (nodes, a request with a bad node
+  // count as one; 0: none), checked against the offsets; clusters launched
+  // (0: num_tasks; an ordered launch may stop at the stated count)
+  int32_t stated_tasks, grid_tasks;
   Layout L;
 };
 
@@ -305,8 +309,9 @@ static_assert(2 + kCostLevels + kWarps <= kLevelCacheOff, "ordering scratch over
 // past its request's drafts has no work and is left out; one of a request with
 // a bad draft count only reports the status (cheapest level).  Every thread of
 // the CTA calls it; every CTA of the cluster gets the same answer.  Returns the
-// task, or -1.  sm: kRedBytes of shared memory.
-__device__ int ordered_task(const KArgs& a, int i, int32_t* sm) {
+// task, or -1, and in *total the number of tasks with work.  sm: kRedBytes of
+// shared memory.
+__device__ int ordered_task(const KArgs& a, int i, int32_t* sm, int* total) {
   const ss_params& p = a.p;
   const int n = a.num_tasks;
   auto level = [&](int task) -> int {
@@ -340,6 +345,9 @@ __device__ int ordered_task(const KArgs& a, int i, int32_t* sm) {
     if (l >= 0) atomicAdd(&cnt[l], 1);
   }
   __syncthreads();
+  int all = 0;
+  for (int l = 0; l < kCostLevels; ++l) all += cnt[l];
+  *total = all;
   int lv = kCostLevels - 1, t = i;
   while (lv >= 0 && t >= cnt[lv]) t -= cnt[lv--];
   if (lv < 0) return -1;
@@ -363,6 +371,44 @@ __device__ int ordered_task(const KArgs& a, int i, int32_t* sm) {
     if (base > t) break;  // the same for every thread
   }
   return sm[0];
+}
+
+// Tree calls with a stated node count, launches without the ordering: the
+// number of tasks with work (a request's nodes, or one for a request with a
+// node count outside [1, max_nodes]), summed over the block.  sm[1] is
+// scratch.  Every thread calls it.
+__device__ int tree_task_count(const KArgs& a, int32_t* sm) {
+  const int width = a.max_draft + 1;
+  const int R = a.num_tasks / width;
+  if (threadIdx.x == 0) sm[1] = 0;
+  __syncthreads();
+  int s = 0;
+  for (int i = threadIdx.x; i < R; i += kThreads) {
+    const int32_t k = a.draft_offsets[i + 1] - a.draft_offsets[i] - 1;
+    s += (k < 0 || k > a.max_draft) ? 1 : k + 1;
+  }
+  if (s) atomicAdd(sm + 1, s);
+  __syncthreads();
+  const int total = sm[1];
+  __syncthreads();
+  return total;
+}
+
+// A stated node count that is not the offsets' sum: every request reports
+// SS_ROW_BAD_PARAM (tokens and path -1, none accepted).  The first cluster's
+// rank 0 alone, every thread; nothing else of the call runs.
+__device__ void report_bad_tree_count(const KArgs& a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous call has finished
+  const int width = a.max_draft + 1;
+  const int R = a.num_tasks / width;
+  for (int64_t e = threadIdx.x; e < static_cast<int64_t>(R) * width; e += kThreads) {
+    a.out_token[e] = -1;
+    if (a.out_path) a.out_path[e] = -1;
+  }
+  for (int i = threadIdx.x; i < R; i += kThreads) {
+    a.out_num_accepted[i] = 0;
+    a.out_status[i] = SS_ROW_BAD_PARAM;
+  }
 }
 
 // Head of a row's shard record (followed by shard_cap (y, token) entries).
@@ -1887,10 +1933,18 @@ __global__ void __launch_bounds__(kThreads, 2) ss_row_kernel(const KArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (a.debug_processed) asm volatile("griddepcontrol.wait;" ::: "memory");
   int task = static_cast<int>(blockIdx.x) / ncta;
+  int with_work = -1;
   if (a.row_class != 0) {
-    task = ordered_task(a, task, reinterpret_cast<int32_t*>(smem_raw + L.red_off));
-    if (task < 0) return;  // the whole cluster: no task left for it
+    task = ordered_task(a, task, reinterpret_cast<int32_t*>(smem_raw + L.red_off), &with_work);
+  } else if (a.stated_tasks > 0) {
+    with_work = tree_task_count(a, reinterpret_cast<int32_t*>(smem_raw + L.red_off));
   }
+  if (a.stated_tasks > 0 && with_work != a.stated_tasks) {
+    // the same in every CTA: the call verifies nothing
+    if (blockIdx.x < static_cast<unsigned>(ncta) && rank == 0) report_bad_tree_count(a);
+    return;
+  }
+  if (task < 0) return;  // the whole cluster: no task left for it
   Ctx& c = g;
   const int tid = threadIdx.x;
   const int V_ = a.vocab;
@@ -2875,7 +2929,7 @@ static cudaError_t launch(const KArgs& ka, int cs, cudaStream_t stream) {
   e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(ka.num_tasks) * cs, 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(ka.grid_tasks > 0 ? ka.grid_tasks : ka.num_tasks) * cs, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = ka.L.total;
   cfg.stream = stream;
@@ -3259,6 +3313,10 @@ ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t works
     return SS_ERR_INVALID_ARG;
   if (A.dtype != SS_DTYPE_F32 && A.dtype != SS_DTYPE_BF16) return SS_ERR_INVALID_ARG;
   if (A.flags & ~SS_TREE_OVERLAP_PREVIOUS) return SS_ERR_INVALID_ARG;
+  if (A.num_nodes_total != 0 &&
+      (A.num_nodes_total < A.num_requests ||
+       A.num_nodes_total > static_cast<int64_t>(A.num_requests) * A.max_nodes))
+    return SS_ERR_INVALID_ARG;
   if (A.num_requests == 0) return SS_OK;
   const int es = (A.dtype == SS_DTYPE_BF16) ? 2 : 4;
   if (!A.target_logits || (reinterpret_cast<uintptr_t>(A.target_logits) % es) != 0 || !A.node_offsets ||
@@ -3297,7 +3355,12 @@ ss_status ss_tree_verify(const ss_tree_args* args, void* workspace, size_t works
   k.ws_results = reinterpret_cast<int4*>(workspace);
   k.ws_counters = counters_at_end(workspace, workspace_bytes, A.num_requests);
   k.overlap = (A.flags & SS_TREE_OVERLAP_PREVIOUS) ? 1 : 0;
-  if (tasks >= 16 && tasks <= kMaxOrderedTasks) k.row_class = 3;
+  k.stated_tasks = A.num_nodes_total;
+  if (tasks >= 16 && tasks <= kMaxOrderedTasks) {
+    k.row_class = 3;
+    // the ordering puts the node slots without work last: stop before them
+    if (A.num_nodes_total > 0) k.grid_tasks = A.num_nodes_total;
+  }
   return run(k, A.dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -3382,6 +3445,6 @@ const char* ss_status_string(ss_status status) {
   return "unknown status";
 }
 
-const char* ss_version(void) { return "ss 0.3.0 (sm_103a)"; }
+const char* ss_version(void) { return "ss 0.4.0 (sm_103a)"; }
 
 }  // extern "C"

@@ -131,6 +131,7 @@ class ss_tree_args(C.Structure):
         ("out_kept", C.c_void_p),
         ("debug_processed", C.c_void_p),
         ("flags", C.c_int32),
+        ("num_nodes_total", C.c_int32),
     ]
 
 
@@ -423,11 +424,13 @@ def ss_spec_verify_noalloc(target_logits, draft_offsets, draft_tokens, draft_pro
 def ss_tree_verify(target_logits, node_offsets, parents, node_tokens, draft_probs, params, out_tokens,
                    out_num_accepted, out_status, workspace, *, vocab, max_nodes, dtype, row_stride=None,
                    draft_stride=None, out_path=None, out_kept=None, debug_processed=None, stream=None,
-                   overlap_previous=False):
+                   overlap_previous=False, num_nodes_total=0):
     """Verify the draft trees of `out_num_accepted.numel()` requests
-    (overlap_previous sets SS_TREE_OVERLAP_PREVIOUS, see include/ss.h)."""
+    (overlap_previous sets SS_TREE_OVERLAP_PREVIOUS; num_nodes_total is
+    ss_tree_args.num_nodes_total: see include/ss.h)."""
     a = ss_tree_args()
     a.flags = SS_TREE_OVERLAP_PREVIOUS if overlap_previous else 0
+    a.num_nodes_total = int(num_nodes_total)
     a.num_requests = int(out_num_accepted.numel())
     a.vocab = int(vocab)
     a.max_nodes = int(max_nodes)
@@ -593,8 +596,9 @@ def alloc_outputs(dw, device="cuda", debug=False):
 def run(dw, o, stream=None, debug=False, overlap_previous=False, target_rows=False):
     """One library call on a device workload `dw` into outputs `o`
     (overlap_previous: see ss_process_sample; every kind of call).  With
-    target_rows, a linear verification call states its number of target rows
-    (the rows of dw["target_logits"]; ss_verify_args.num_target_rows)."""
+    target_rows, a verification call states its number of target rows (the
+    rows of dw["target_logits"]: ss_verify_args.num_target_rows,
+    ss_tree_args.num_nodes_total)."""
     params = {k: dw.get(k) for k in PARAM_FIELDS}
     params["bitmask_stride"] = dw.get("bitmask_stride", 0)
     dbg = o.get("processed") if debug else None
@@ -607,7 +611,8 @@ def run(dw, o, stream=None, debug=False, overlap_previous=False, target_rows=Fal
                        params, o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],
                        max_nodes=dw["max_nodes"], dtype=dw["dtype"], row_stride=dw["row_stride"],
                        draft_stride=dw["draft_stride"], out_path=o["out_path"], out_kept=o["kept"],
-                       debug_processed=dbg, stream=stream, overlap_previous=overlap_previous)
+                       debug_processed=dbg, stream=stream, overlap_previous=overlap_previous,
+                       num_nodes_total=int(dw["target_logits"].shape[0]) if target_rows else 0)
     else:
         ss_spec_verify(dw["target_logits"], dw["draft_offsets"], dw["draft_tokens"], dw["draft_probs"], params,
                        o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],

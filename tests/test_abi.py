@@ -114,6 +114,10 @@ def test_host_side_argument_errors_launch_nothing(lib):
     assert lib.ss_tree_verify(C.byref(t), None, 0, None) == 1
     t.flags = ss.SS_TREE_OVERLAP_PREVIOUS
     assert lib.ss_tree_verify(C.byref(t), None, 0, None) == 0
+    t.num_requests = 2
+    for nodes in (-1, 1, 9):  # outside [R, R * max_nodes] = [2, 8]
+        t.num_nodes_total = nodes
+        assert lib.ss_tree_verify(C.byref(t), None, 0, None) == 1, nodes
 
 
 def test_shard_entry_points_reject_bad_arguments(lib):

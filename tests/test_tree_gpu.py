@@ -136,3 +136,75 @@ def test_tree_requests_split_with_row_ids(ss):
     b = run_gpu(ss, parity.subset_tree(w, list(range(9, 18))))
     for key in ("out_tokens", "out_path", "num_accepted", "status"):
         assert np.array_equal(np.concatenate([a[key], b[key]]), whole[key]), key
+
+
+TREE_KEYS = ("out_tokens", "out_path", "num_accepted", "status", "kept")
+
+
+def _tree_outputs(ss, dw, count, **kw):
+    o = ss.alloc_outputs(dw)
+    params = {k: dw.get(k) for k in ss.PARAM_FIELDS}
+    params["bitmask_stride"] = dw.get("bitmask_stride", 0)
+    ss.ss_tree_verify(dw["target_logits"], dw["node_offsets"], dw["parents"], dw["node_tokens"], dw["draft_probs"],
+                      params, o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],
+                      max_nodes=dw["max_nodes"], dtype=dw["dtype"], row_stride=dw["row_stride"],
+                      draft_stride=dw["draft_stride"], out_path=o["out_path"], out_kept=o["kept"],
+                      num_nodes_total=count, **kw)
+    torch.cuda.synchronize()
+    return o
+
+
+@pytest.mark.parametrize("requests,max_nodes", [(32, 16), (3, 4)])  # ordered launch; one without the ordering
+def test_tree_node_count_keeps_the_outputs(ss, requests, max_nodes):
+    w = W.tree(seed=40 + requests, requests=requests, vocab=9001, max_nodes=max_nodes)
+    dw = ss.to_device(w)
+    nodes = int(w["node_offsets"][-1])
+    full = _tree_outputs(ss, dw, 0)
+    counted = _tree_outputs(ss, dw, nodes)
+    for key in TREE_KEYS:
+        assert torch.equal(full[key], counted[key]), key
+    assert (full["status"].cpu().numpy() == 0).all()
+
+
+@pytest.mark.parametrize("requests,max_nodes", [(32, 16), (3, 4)])
+@pytest.mark.parametrize("delta", [-1, 1])
+def test_tree_wrong_node_count_reports_bad_param(ss, requests, max_nodes, delta):
+    w = W.tree(seed=50 + requests, requests=requests, vocab=5003, max_nodes=max_nodes)
+    dw = ss.to_device(w)
+    nodes = int(w["node_offsets"][-1])
+    if not (requests <= nodes + delta <= requests * max_nodes):
+        pytest.skip("count outside the accepted range")
+    ref = _tree_outputs(ss, dw, 0)
+    o = _tree_outputs(ss, dw, nodes + delta)
+    assert (o["status"].cpu().numpy() == 4).all()  # SS_ROW_BAD_PARAM
+    assert (o["num_accepted"].cpu().numpy() == 0).all()
+    assert (o["out_tokens"].cpu().numpy() == -1).all() and (o["out_path"].cpu().numpy() == -1).all()
+    # the workspace is untouched: a correct call on it gives the reference
+    params = {k: dw.get(k) for k in ss.PARAM_FIELDS}
+    params["bitmask_stride"] = dw.get("bitmask_stride", 0)
+    ss.ss_tree_verify(dw["target_logits"], dw["node_offsets"], dw["parents"], dw["node_tokens"], dw["draft_probs"],
+                      params, o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],
+                      max_nodes=dw["max_nodes"], dtype=dw["dtype"], row_stride=dw["row_stride"],
+                      draft_stride=dw["draft_stride"], out_path=o["out_path"], out_kept=o["kept"],
+                      num_nodes_total=nodes)
+    torch.cuda.synchronize()
+    for key in TREE_KEYS:
+        assert torch.equal(ref[key], o[key]), key
+
+
+def test_tree_node_count_overlapped_in_a_graph(ss):
+    sets = [ss.to_device(W.tree(seed=70 + i, requests=24, vocab=128256, max_nodes=16)) for i in range(3)]
+    ref = [_tree_outputs(ss, dw, 0) for dw in sets]
+    outs = [ss.alloc_outputs(dw) for dw in sets]
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for dw, o in zip(sets, outs):
+                ss.run(dw, o, stream=stream, overlap_previous=True, target_rows=True)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for r, o in zip(ref, outs):
+        for key in TREE_KEYS:
+            assert torch.equal(r[key], o[key]), key
