@@ -592,7 +592,8 @@ def run_spec(args, ss, rank, dev, stream):
             "requests_per_s": int(ring_host[0]["num_requests"]) * calls / (ms / 1e3),
             "ms_per_call": ms / calls, "calls": calls,
             "logits_GBps": W.algorithmic_bytes(ring_host[0]) * calls / (ms / 1e3) / 1e9,
-            "consecutive_calls_overlap": not args.no_overlap, "calls_per_graph": per_graph}
+            "consecutive_calls_overlap": not args.no_overlap, "calls_per_graph": per_graph,
+            "target_rows_stated": True}
 
 
 TREE_WORKLOAD = "tree verify R=32 trees of 1-16 nodes V=128256 bf16"
@@ -634,7 +635,7 @@ def run_tree(args, ss, rank, dev, stream):
             "requests_per_s": 32 * calls / (ms / 1e3), "ms_per_call": ms / calls, "calls": calls,
             "mean_nodes_per_request": rows / (32.0 * len(ring)),
             "logits_GBps": alg * passes / (ms / 1e3) / 1e9, "consecutive_calls_overlap": not args.no_overlap,
-            "calls_per_graph": per_graph}
+            "calls_per_graph": per_graph, "target_rows_stated": True}
 
 
 def run_sharded(args, ss, rank, dev, stream, parts=4):
