@@ -173,3 +173,28 @@ def test_noalloc_with_a_count(ss):
                               draft_stride=dw["draft_stride"], out_kept=o["kept"], num_target_rows=_rows(w))
     torch.cuda.synchronize()
     _same(ref, {k: o[k].cpu().numpy() for k in KEYS})
+
+
+def test_compact_launch_debug_rows_and_row_ids(ss):
+    # the processed rows written by the compact launch and caller-given row
+    # ids: equal to the full launch's, row for row
+    w = W.make(5, requests=36, vocab=7001, seed=31, plain_top_k_max=800)
+    w["row_id"] = np.random.default_rng(5).integers(0, 2**32, 36, dtype=np.uint64).astype(np.uint32)
+    dw = ss.to_device(w)
+    res = []
+    for rows in (0, _rows(w)):
+        o = ss.alloc_outputs(dw, debug=True)
+        o["processed"].fill_(-123.0)
+        params = {k: dw.get(k) for k in ss.PARAM_FIELDS}
+        params["bitmask_stride"] = dw.get("bitmask_stride", 0)
+        ss.ss_spec_verify(dw["target_logits"], dw["draft_offsets"], dw["draft_tokens"], dw["draft_probs"], params,
+                          o["out_tokens"], o["num_accepted"], o["status"], o["workspace"], vocab=dw["vocab"],
+                          max_draft=dw["max_draft"], dtype=dw["dtype"], row_stride=dw["row_stride"],
+                          draft_stride=dw["draft_stride"], out_kept=o["kept"], debug_processed=o["processed"],
+                          num_target_rows=rows)
+        torch.cuda.synchronize()
+        res.append({k: o[k].cpu().numpy() for k in KEYS + ("processed",)})
+    for k in KEYS:
+        assert np.array_equal(res[0][k], res[1][k]), k
+    assert np.array_equal(res[0]["processed"].view(np.uint32), res[1]["processed"].view(np.uint32))
+    assert not (res[1]["processed"] == -123.0).all(axis=1).any()  # every target row written
